@@ -1,0 +1,8 @@
+"""Float64 CPU oracle for LRKV (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path
+(``rank_kv_attention_gb300``) never imports, links or calls it, and this
+package imports nothing from the product path.
+"""
+from .lrkv_oracle import *  # noqa: F401,F403
