@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""LRKV decode benchmark on GB300.
+
+One step = one decode step of one layer for a batch of requests, through the
+C ABI: lrkv_append writes each request's new row (shared + private
+projections) at position T-1, then lrkv_decode attends over the T cached
+rows (factored scores, one online softmax, shared + private value
+reductions, expansion by B_V^T).  Inputs are seeded synthetic tensors of the
+workload's shape, resident in HBM when the timed region starts.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LRKV decode tokens/s and achieved HBM GB/s (% of roofline) at 1 GB300"
+L2_BYTES = 129 * 10 ** 6
+NORTH_STAR_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "decode_T4096": "B=16 requests, d=2048, H=16, d_h=128, r=48, history T=4096 (current row "
+                    "included), bf16 cache, fp32 accumulation, contiguous 64-token pages",
+    "decode_T32768": "B=4, d=4096, H=32, d_h=128, r=32, T=32768, bf16 cache, fp32 accumulation",
+    "ragged_paged": "B=64, lengths uniform on [256, 8192], 64-token pages shuffled in one pool, "
+                    "H=16, d_h=128, r=56, d=2048 for the append, bf16",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode_T4096", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-pairs", type=int, default=1024,
+                    help="(request, head) pairs of the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_shape(name):
+    import lrkv_inputs as I
+    c = dict(I.CONFIGS[name])
+    c.setdefault("d", 2048)
+    return c
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        rows = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            rows = [r for r in out.strip().splitlines() if r.strip()]
+        after = False
+        if not rows:  # timed region shorter than one sampling period
+            try:
+                out = subprocess.run(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=10).stdout
+                rows = [r for r in out.strip().splitlines() if r.strip()]
+                after = True
+            except Exception:
+                rows = []
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm), "sampled_after_region": after}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh"):
+        with open(os.path.join(ROOT, "rank_kv_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary,
+    or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", f"decode_split_{config}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import ctypes
+    import numpy as np
+    import torch
+    import lrkv_inputs as I
+    import rank_kv_attention_gb300 as L
+    from rank_kv_attention_gb300 import _abi
+    from rank_kv_attention_gb300.api import PagedCache
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib = L.lib()
+
+    name = args.config
+    c = workload_shape(name)
+    case = I.config_decode_case(name)
+    Bn, H, d_h, r, d = case.B, case.H, case.d_h, case.r, c["d"]
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=1)
+    x_new = I.make_append_case([1] * Bn, case.seq_lens - 1, d, seed=2).X
+
+    def to_dev(a, kind="bf16"):
+        if kind == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    base = PagedCache(to_dev(case.S_K), to_dev(case.S_V), to_dev(case.R_K), to_dev(case.R_V))
+    cache_bytes = sum(t.numel() * 2 for t in (base.S_K, base.S_V, base.R_K, base.R_V))
+    n_copies = max(1, math.ceil(4 * L2_BYTES / cache_bytes))
+    caches = [base] + [PagedCache(*(t.clone() for t in (base.S_K, base.S_V, base.R_K, base.R_V)))
+                       for _ in range(n_copies - 1)]
+    q = to_dev(case.q)
+    BK, BV = to_dev(case.B_K), to_dev(case.B_V)
+    Wsk, Wsv, Uk, Uv = (to_dev(a) for a in (w.W_S_K, w.W_S_V, w.U_K, w.U_V))
+    X = to_dev(x_new)
+    pos = to_dev(case.seq_lens - 1, "i32")
+    sid = to_dev(np.arange(Bn), "i32")
+    seq_lens = to_dev(case.seq_lens, "i32")
+    pt = to_dev(case.page_table, "i32")
+    max_seq = int(case.seq_lens.max())
+    out = torch.empty_like(q)
+    ws = L.workspace(L.decode_workspace_bytes(Bn, H, d_h, r, max_seq), dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    descs = [cc.desc() for cc in caches]
+
+    def make_calls(X_, q_, pos_, sid_, sl_, out_):
+        calls = []
+        for dsc in descs:
+            a = (P(X_), P(pos_), P(sid_), Bn, d, P(Wsk), P(Wsv), P(Uk), P(Uv), ctypes.byref(dsc),
+                 P(pt), Bn, pt.shape[1], P(status), sp)
+            dd = (P(q_), ctypes.byref(dsc), P(BK), P(BV), P(sl_), P(pt), Bn, pt.shape[1], max_seq,
+                  P(out_), P(ws), ws.numel(), P(status), sp)
+            calls.append((a, dd))
+        return calls
+
+    calls = make_calls(X, q, pos, sid, seq_lens, out)
+    f_app, f_dec = lib.lrkv_append, lib.lrkv_decode
+
+    def step(i):
+        a, dd = calls[i % n_copies]
+        rc = f_app(*a)
+        rc2 = f_dec(*dd)
+        if rc or rc2:
+            raise RuntimeError(f"lrkv call failed: {rc} {rc2}")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident timed region
+    K, W = args.steps, args.warmup
+    for i in range(max(W, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.25)
+    ok = lib.lrkv_profile_enable(1)
+    assert ok == 0
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    tot = ctypes.c_double()
+    nl = ctypes.c_int32()
+    assert lib.lrkv_profile_read(ctypes.byref(tot), ctypes.byref(nl)) == 0
+    lib.lrkv_profile_enable(0)
+    split_ms = tot.value / max(1, nl.value)
+    st = int(status.item())
+    if st:
+        raise RuntimeError(f"device status {st}")
+
+    # ---- end to end through the C ABI with host buffers
+    Ke = args.e2e_steps or max(50, min(K, 2000))
+    pin = lambda t: t.cpu().pin_memory()
+    hX, hq, hpos, hsid, hsl = pin(X), pin(q), pin(pos), pin(sid), pin(seq_lens)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dX, dq, dpos, dsid, dsl = (torch.empty_like(t) for t in (X, q, pos, sid, seq_lens))
+    dout = torch.empty_like(out)
+    calls = make_calls(dX, dq, dpos, dsid, dsl, dout)
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hq, hpos, hsid, hsl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step(i):
+        for hsrc, ddst in ((hX, dX), (hq, dq), (hpos, dpos), (hsid, dsid), (hsl, dsl)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step(i)
+        hout.copy_(dout, non_blocking=True)
+        stream.synchronize()   # the host reads this step's result
+
+    for i in range(5):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(Ke):
+        e2e_step(i)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(g0.elapsed_time(g1))
+
+    # ---- numbers
+    ms_step = total_ms / K
+    tokens = world * Bn * K
+    value = tokens / (total_ms / 1e3)
+    seq_total = int(case.seq_lens.astype(np.int64).sum())
+    split_bytes = seq_total * 2 * (d_h + H * r) * 2          # cache rows read once
+    step_bytes = (split_bytes + 2 * H * d_h * r * 2 + 2 * Bn * H * d_h * 2   # + bases, q, out
+                  + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
+    peak, peak_kind = measured_peaks()
+    achieved = split_bytes / (split_ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: {WORKLOADS[name]}", "B": Bn, "d": d, "H": H, "d_h": d_h,
+                   "r": r, "seq_len": max_seq, "cached_rows": seq_total,
+                   "parallelism": f"replicas x{world} (requests are independent)",
+                   "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
+                         f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
+                   "step": "lrkv_append (B new rows) + lrkv_decode (B queries)"},
+        "roofline": {"kernel": "decode split (factored scores + online softmax + value reductions)",
+                     "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "frac_of_8TBs": round(achieved / NORTH_STAR_HBM_GBS, 4),
+                     "algorithmic_bytes_per_launch": split_bytes,
+                     "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
+                     "traffic": profiled_traffic(name)},
+        "step_effective_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+        "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned host inputs copied in, result copied out and synchronised every step"},
+        "gpu_launches": 4 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(name, args.cpu_pairs)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res
+
+
+def cpu_baseline(name, n_pairs):
+    from oracle.cpu_timing import time_oracle_decode
+    t = time_oracle_decode(name, n_pairs)
+    return {"value": round(t["pairs"] / t["heads"] / t["wall_s"], 3), "unit": "tokens/s",
+            "cores": t["cores"], "kind": "oracle",
+            "sample": f"{t['pairs']} random (request, head) pairs of the {name} workload "
+                      f"({t['pairs'] / t['heads']:.0f} request-steps), float64 oracle "
+                      f"(gather, materialise K_h/V_h, textbook softmax), {t['cores']} single-"
+                      f"threaded processes, {t['cpu_s']:.1f} s CPU"}
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle timed on host cores: each step is one (request, head)
+    pair of the workload; tokens/s counts H pairs as one request-step."""
+    if rank != 0:
+        return None
+    from oracle.cpu_timing import time_oracle_decode
+    import lrkv_inputs as I
+    c = workload_shape(args.config)
+    n = max(16, min(args.steps, 4096))   # bounded so the run ends within minutes
+    t = time_oracle_decode(args.config, n)
+    value = t["pairs"] / t["heads"] / t["wall_s"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t["wall_s"] / t["pairs"] * 1e3 * t["heads"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": c["B"],
+                   "H": c["H"], "d_h": c["d_h"], "r": c["r"]},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": t["cores"],
+                         "kind": "oracle",
+                         "sample": f"{t['pairs']} (request, head) pairs (steps capped at 4096)"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

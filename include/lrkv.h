@@ -1,0 +1,219 @@
+/*
+ * lrkv.h - C ABI of the GB300 (sm_103a) LRKV decode / append / prefill library.
+ *
+ * Low-Rank Key Value attention (LRKV) caches, per layer and token, one shared
+ * key row S_K and one shared value row S_V (width d_h) plus, per head h, a
+ * private key row R_K[h] and value row R_V[h] (width r).  A head's key is
+ * S_K + R_K[h] B_K[h]^T and its value S_V + R_V[h] B_V[h]^T, where B_K[h],
+ * B_V[h] (d_h x r) are layer weights (reading note "Low-Rank Key Value
+ * Attention", section 3, equations 2-5).  Decode never materialises those
+ * keys or values: it scores q.S_K + (q B_K[h]).R_K[h] (equation 6) and reduces
+ * values as a.S_V + (a.R_V[h]) B_V[h]^T (equation 7), with one softmax over
+ * both score branches and scale 1/sqrt(d_h) (section 2).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers, 16-byte aligned, row-major and
+ *    dense.  The library only reads inputs, writes only the listed outputs and
+ *    the addressed cache slots, never frees or keeps any pointer past the call,
+ *    and allocates nothing.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    A return of LRKV_OK means the work was validated and enqueued.
+ *  - Element type: every floating tensor of one call (X, Q, q, weights, bases,
+ *    cache pools, out) has the cache's dtype (LRKV_F32 or LRKV_BF16).  All
+ *    arithmetic accumulates in fp32; results are rounded once on store.
+ *  - Errors the host can see (null pointers, bad sizes, too-small workspace,
+ *    unsupported dtype) are returned as a negative LRKV_E_* code before any
+ *    work is enqueued.  Errors in device-resident metadata (a page id outside
+ *    [0, num_pages), a sequence length outside [1, max_pages*page_size], a
+ *    position or sequence id out of range) are never turned into an access:
+ *    the affected rows are skipped and the kernel ORs an LRKV_STATUS_* bit
+ *    into *dev_status (a caller-owned device int32, may be NULL; the library
+ *    never clears it).
+ */
+#ifndef LRKV_H
+#define LRKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LRKV_API __attribute__((visibility("default")))
+#else
+#define LRKV_API
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *lrkv_stream_t;
+
+typedef enum { LRKV_F32 = 0, LRKV_BF16 = 1 } lrkv_dtype_t;
+
+enum {
+    LRKV_OK = 0,
+    LRKV_E_INVALID_ARG = -1, /* null pointer, negative count, misaligned pointer */
+    LRKV_E_SHAPE = -2,       /* a dimension is zero, too large or inconsistent */
+    LRKV_E_DTYPE = -3,       /* dtype not LRKV_F32 / LRKV_BF16 */
+    LRKV_E_BOUNDS = -4,      /* host-visible bound: max_seq_len > max_pages*page_size, ... */
+    LRKV_E_WORKSPACE = -5,   /* workspace NULL, misaligned or smaller than required */
+    LRKV_E_CUDA = -6         /* a CUDA call failed; lrkv_last_cuda_error() has the code */
+};
+
+/* Bits ORed into *dev_status by the kernels. */
+#define LRKV_STATUS_BAD_PAGE 1u     /* page id outside [0, num_pages) */
+#define LRKV_STATUS_BAD_SEQLEN 2u   /* sequence length < 1 or > max_pages*page_size */
+#define LRKV_STATUS_BAD_ROW 4u      /* append: position/sequence id out of range */
+#define LRKV_STATUS_TIMEOUT 8u      /* an on-chip wait gave up (never expected) */
+
+/*
+ * Paged factored cache (section 3, after Algorithm 1: shared and private
+ * pages use one token numbering and one lifetime).  Token t of request b
+ * lives in page page_table[b*max_pages + t/page_size], slot t%page_size, and
+ * that one page id indexes all four pools:
+ *     S_K, S_V : [num_pages, page_size, d_h]
+ *     R_K, R_V : [num_pages, page_size, H, r]   (all heads of a token contiguous)
+ * Memory is caller-owned; the library never frees it.
+ * Supported: 1 <= H <= 128, 1 <= d_h <= 256, 1 <= r <= 256, page_size a
+ * multiple of 16 in [16, 1024]; with LRKV_BF16, d_h and r multiples of 8;
+ * with LRKV_F32, multiples of 4.
+ */
+typedef struct {
+    void *S_K;
+    void *S_V;
+    void *R_K;
+    void *R_V;
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t H;
+    int32_t d_h;
+    int32_t r;
+    int32_t dtype; /* lrkv_dtype_t */
+} lrkv_cache_t;
+
+/*
+ * lrkv_append - build or extend the factored cache (section 3, Algorithm 1).
+ *
+ * For each of the n new rows X[i] (request seq_ids[i], token position
+ * positions[i]):
+ *     S_K = X W_S_K,  S_V = X W_S_V,  R_K[h] = X U_K[h],  R_V[h] = X U_V[h]
+ * are computed with fp32 accumulation and stored (rounded to the cache dtype)
+ * at the row's slot.  B_K, B_V are not needed: they stay layer weights.
+ *
+ *   X          [n, d]
+ *   positions  [n] int32, device; seq_ids [n] int32, device, in [0, B)
+ *   W_S_K      [d_h, d]     weights stored output-major (like nn.Linear.weight):
+ *   W_S_V      [d_h, d]       row c holds the input weights of output column c
+ *   U_K        [H, r, d]
+ *   U_V        [H, r, d]
+ *   page_table [B, max_pages] int32, device
+ * Rows whose (seq_id, position, page id) are out of range are skipped and
+ * flag LRKV_STATUS_BAD_ROW / LRKV_STATUS_BAD_PAGE.  Two rows that address the
+ * same slot race (the caller must not do that).  n == 0 is a no-op.
+ */
+LRKV_API int lrkv_append(const void *X, const int32_t *positions, const int32_t *seq_ids,
+                int32_t n, int32_t d, const void *W_S_K, const void *W_S_V,
+                const void *U_K, const void *U_V, const lrkv_cache_t *cache,
+                const int32_t *page_table, int32_t B, int32_t max_pages,
+                int32_t *dev_status, lrkv_stream_t stream);
+
+/* Bytes of device workspace lrkv_decode needs for these sizes. */
+LRKV_API size_t lrkv_decode_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                   int32_t max_seq_len, int32_t dtype);
+
+/*
+ * lrkv_decode - one decode step read directly from the factored cache
+ * (section 3, Algorithm 2, equations 6 and 7).
+ *
+ * For request b and head h, over the seq_lens[b] cached rows j (the current
+ * token included: decode runs after its row was appended):
+ *     p        = q[b,h] B_K[h]                          (once per step)
+ *     s_j      = (q[b,h].S_K[j] + p.R_K[h,j]) / sqrt(d_h)
+ *     a        = softmax_j(s)                            (one softmax, both branches)
+ *     out[b,h] = a.S_V + (a.R_V[h]) B_V[h]^T
+ * Query projection, head concatenation and the output projection stay with
+ * the caller.
+ *
+ *   q        [B, H, d_h]         out [B, H, d_h]
+ *   B_K, B_V [H, d_h, r]
+ *   seq_lens [B] int32, device; page_table [B, max_pages] int32, device
+ *   max_seq_len  host upper bound of seq_lens (sizes the launch and workspace);
+ *                must be <= max_pages*page_size.
+ *   workspace    >= lrkv_decode_workspace_bytes(B, H, d_h, r, max_seq_len, dtype)
+ *                bytes of device memory, 256-byte aligned, caller-owned; its
+ *                contents are scratch (partial softmax states) and need no
+ *                initialisation.
+ * A request with an invalid length gets out = 0 and LRKV_STATUS_BAD_SEQLEN.
+ */
+LRKV_API int lrkv_decode(const void *q, const lrkv_cache_t *cache, const void *B_K,
+                const void *B_V, const int32_t *seq_lens, const int32_t *page_table,
+                int32_t B, int32_t max_pages, int32_t max_seq_len, void *out,
+                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                lrkv_stream_t stream);
+
+/* Bytes of device workspace lrkv_prefill needs. */
+LRKV_API size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h,
+                                    int32_t r, int32_t max_ctx, int32_t dtype);
+
+/*
+ * lrkv_prefill - append a chunk of new rows, then run causal LRKV attention
+ * for every new row (section 2: prefill builds the first cache; section 3:
+ * Algorithm 1 then equations 6-7 applied to every query row).
+ *
+ * Request b owns rows cu_rows[b] .. cu_rows[b+1]-1 of X, Q and out, at token
+ * positions start_pos[b], start_pos[b]+1, ...; rows 0..start_pos[b]-1 must
+ * already be in the cache (earlier history).  Row i at position t attends to
+ * every row of its request at positions <= t:
+ *     out[i,h] = softmax_j((Q[i,h].S_K[j] + (Q[i,h] B_K[h]).R_K[h,j]) / sqrt(d_h))
+ *                applied to  S_V[j] + R_V[h,j] B_V[h]^T
+ *
+ *   X   [n, d]    Q, out [n, H, d_h]
+ *   cu_rows [B+1] int32, device (cu_rows[0] = 0, nondecreasing, cu_rows[B] = n)
+ *   start_pos [B] int32, device
+ *   max_ctx   host upper bound of start_pos[b] + rows of b (<= max_pages*page_size)
+ *   weights as lrkv_append; B_K, B_V as lrkv_decode.
+ *   workspace >= lrkv_prefill_workspace_bytes(...) bytes, 256-byte aligned.
+ */
+LRKV_API int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows,
+                 const int32_t *start_pos, int32_t B, int32_t n, int32_t max_ctx,
+                 int32_t d, const void *W_S_K, const void *W_S_V, const void *U_K,
+                 const void *U_V, const void *B_K, const void *B_V,
+                 const lrkv_cache_t *cache, const int32_t *page_table,
+                 int32_t max_pages, void *out, void *workspace,
+                 size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream);
+
+/*
+ * Cache payload in bytes for `tokens` cached positions of one layer:
+ * tokens * 2 * (d_h + H*r) * sizeof(dtype)  (section 4, equation 9).
+ * Returns 0 for invalid arguments.
+ */
+LRKV_API size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype);
+
+/* Human-readable name of an LRKV_E_* code. */
+LRKV_API const char *lrkv_status_string(int status);
+
+/* cudaError_t of the last failed CUDA call inside the library (0 if none). */
+LRKV_API int lrkv_last_cuda_error(void);
+
+/*
+ * Instrumentation for benchmarks.  lrkv_profile_enable(1) creates a pool of
+ * CUDA events (once) and starts recording: every later lrkv_decode /
+ * lrkv_prefill brackets its split-attention kernel with an event pair on the
+ * call's stream (at most 8192 pairs are kept).  lrkv_profile_read waits for
+ * the last recorded event, returns the summed kernel time in milliseconds and
+ * the number of bracketed launches, and clears the record.  Not for use
+ * inside CUDA-graph capture.  lrkv_profile_enable(0) stops recording.
+ */
+LRKV_API int lrkv_profile_enable(int on);
+LRKV_API int lrkv_profile_read(double *total_ms, int32_t *launches);
+
+/* Library version, major*10000 + minor*100 + patch. */
+LRKV_API int lrkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRKV_H */

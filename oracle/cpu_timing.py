@@ -1,0 +1,73 @@
+"""Times the float64 oracle on host cores (test infrastructure only).
+
+Used by bench.py's CPU-baseline leg and its ``--impl reference`` arm.  The
+oracle runs as it stands: for each sampled (request, head) pair it gathers the
+request's rows from the paged pools, materialises K_h and V_h and runs
+textbook softmax attention.  Work is spread over a ``spawn`` process pool of
+single-threaded workers (BLAS threads pinned to 1), so ``cores`` is exactly
+the number of worker processes.
+"""
+from __future__ import annotations
+
+import multiprocessing as mp
+import os
+import time
+
+_CASE = None
+
+
+def _init(config):
+    global _CASE
+    import lrkv_inputs as I
+    _CASE = I.config_decode_case(config)
+
+
+def _run_pairs(pairs):
+    import numpy as np
+    import lrkv_inputs as I
+    from . import lrkv_oracle as O
+    c = _CASE
+    f = lambda a: I.to_f64(a, c.dtype)
+    t0 = time.perf_counter()
+    for b, h in pairs:
+        pages, L = c.rows(b)
+        sk = f(O.gather_rows(c.S_K, pages, L, c.page_size))
+        sv = f(O.gather_rows(c.S_V, pages, L, c.page_size))
+        rk = f(O.gather_rows(c.R_K, pages, L, c.page_size)[:, h, :])
+        rv = f(O.gather_rows(c.R_V, pages, L, c.page_size)[:, h, :])
+        K_h = O.expand_head(sk, rk, f(c.B_K[h]))
+        V_h = O.expand_head(sv, rv, f(c.B_V[h]))
+        o = O.attend(f(c.q[b, h]), K_h, V_h)
+        assert np.all(np.isfinite(o))
+    return time.perf_counter() - t0
+
+
+def time_oracle_decode(config: str, n_pairs: int, workers: int | None = None, seed: int = 0):
+    """Run the oracle on ``n_pairs`` sampled (request, head) pairs of a decode
+    workload; returns dict(wall_s, cpu_s, pairs, cores, heads)."""
+    import numpy as np
+    import lrkv_inputs as I
+    cfg = I.CONFIGS[config]
+    B, H = cfg["B"], cfg["H"]
+    workers = max(1, min(workers or os.cpu_count() or 1, n_pairs))
+    rng = np.random.default_rng(seed)
+    pairs = [(int(rng.integers(B)), int(rng.integers(H))) for _ in range(n_pairs)]
+    chunks = [pairs[i::workers] for i in range(workers)]
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                             "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers, initializer=_init, initargs=(config,)) as pool:
+            pool.map(_run_pairs, [[(0, 0)]] * workers)   # warm: imports, page-in
+            t0 = time.perf_counter()
+            cpu = pool.map(_run_pairs, chunks)
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return dict(wall_s=wall, cpu_s=float(sum(cpu)), pairs=n_pairs, cores=workers, heads=H)

@@ -1,0 +1,157 @@
+"""PyTorch-facing binding of the LRKV C ABI.
+
+Every function here only checks tensor properties, builds the C arguments
+and calls the library on the current CUDA stream; all arithmetic runs in the
+library's CUDA kernels.  Tensors must be contiguous CUDA tensors of the
+cache's dtype (torch.bfloat16 or torch.float32); integer metadata is int32.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _abi
+
+_DT = {torch.float32: _abi.LRKV_F32, torch.bfloat16: _abi.LRKV_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, device=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+@dataclass
+class PagedCache:
+    """Caller-owned paged factored cache (four pools sharing page ids).
+
+    S_K, S_V: [num_pages, page_size, d_h]; R_K, R_V: [num_pages, page_size, H, r].
+    """
+    S_K: torch.Tensor
+    S_V: torch.Tensor
+    R_K: torch.Tensor
+    R_V: torch.Tensor
+
+    @classmethod
+    def empty(cls, num_pages, page_size, H, d_h, r, dtype=torch.bfloat16, device="cuda"):
+        mk = lambda *s: torch.empty(s, dtype=dtype, device=device)
+        return cls(mk(num_pages, page_size, d_h), mk(num_pages, page_size, d_h),
+                   mk(num_pages, page_size, H, r), mk(num_pages, page_size, H, r))
+
+    @property
+    def dtype(self):
+        return self.S_K.dtype
+
+    def desc(self) -> _abi.CacheDesc:
+        for n in ("S_K", "S_V", "R_K", "R_V"):
+            _need(getattr(self, n), n, self.dtype)
+        npg, ps, d_h = self.S_K.shape
+        _, _, H, r = self.R_K.shape
+        return _abi.CacheDesc(self.S_K.data_ptr(), self.S_V.data_ptr(), self.R_K.data_ptr(),
+                              self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype])
+
+
+def cache_bytes(H, d_h, r, tokens, dtype=torch.bfloat16) -> int:
+    return int(_abi.lib().lrkv_cache_bytes(H, d_h, r, tokens, _DT[dtype]))
+
+
+def decode_workspace_bytes(B, H, d_h, r, max_seq_len, dtype=torch.bfloat16) -> int:
+    return int(_abi.lib().lrkv_decode_workspace_bytes(B, H, d_h, r, max_seq_len, _DT[dtype]))
+
+
+def prefill_workspace_bytes(B, n, H, d_h, r, max_ctx, dtype=torch.bfloat16) -> int:
+    return int(_abi.lib().lrkv_prefill_workspace_bytes(B, n, H, d_h, r, max_ctx, _DT[dtype]))
+
+
+def workspace(nbytes, device="cuda") -> torch.Tensor:
+    """A byte buffer usable as workspace (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def append(X, positions, seq_ids, W_S_K, W_S_V, U_K, U_V, cache: PagedCache, page_table,
+           status=None, stream=None):
+    """lrkv_append: project rows X and store them at (seq_ids, positions)."""
+    dt = cache.dtype
+    for n, t in (("X", X), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V)):
+        _need(t, n, dt)
+    for n, t in (("positions", positions), ("seq_ids", seq_ids), ("page_table", page_table)):
+        _need(t, n, torch.int32)
+    if status is not None:
+        _need(status, "status", torch.int32)
+    n, d = X.shape
+    B, max_pages = page_table.shape
+    desc = cache.desc()
+    code = _abi.lib().lrkv_append(_ptr(X), _ptr(positions), _ptr(seq_ids), n, d, _ptr(W_S_K),
+                                  _ptr(W_S_V), _ptr(U_K), _ptr(U_V), ctypes.byref(desc),
+                                  _ptr(page_table), B, max_pages, _ptr(status), _stream(stream))
+    _abi.check("lrkv_append", code)
+
+
+def decode(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_len, out=None,
+           ws=None, status=None, stream=None):
+    """lrkv_decode: per-head attention output [B, H, d_h] of one decode step."""
+    dt = cache.dtype
+    for n, t in (("q", q), ("B_K", B_K), ("B_V", B_V)):
+        _need(t, n, dt)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(page_table, "page_table", torch.int32)
+    B, H, d_h = q.shape
+    r = cache.R_K.shape[3]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dt)
+    need = decode_workspace_bytes(B, H, d_h, r, max_seq_len, dt)
+    if ws is None:
+        ws = workspace(need, q.device)
+    _need(ws, "ws", torch.uint8)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_decode(_ptr(q), ctypes.byref(desc), _ptr(B_K), _ptr(B_V),
+                                  _ptr(seq_lens), _ptr(page_table), B, page_table.shape[1],
+                                  max_seq_len, _ptr(out), _ptr(ws), ws.numel(), _ptr(status),
+                                  _stream(stream))
+    _abi.check("lrkv_decode", code)
+    return out
+
+
+def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
+            cache: PagedCache, page_table, out=None, ws=None, status=None, stream=None):
+    """lrkv_prefill: append the chunk X, then causal attention for each row's Q."""
+    dt = cache.dtype
+    for n, t in (("X", X), ("Q", Q), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K),
+                 ("U_V", U_V), ("B_K", B_K), ("B_V", B_V)):
+        _need(t, n, dt)
+    for n, t in (("cu_rows", cu_rows), ("start_pos", start_pos), ("page_table", page_table)):
+        _need(t, n, torch.int32)
+    n, d = X.shape
+    _, H, d_h = Q.shape
+    r = cache.R_K.shape[3]
+    B = start_pos.shape[0]
+    if out is None:
+        out = torch.empty_like(Q)
+    need = prefill_workspace_bytes(B, n, H, d_h, r, max_ctx, dt)
+    if ws is None:
+        ws = workspace(need, X.device)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_prefill(_ptr(X), _ptr(Q), _ptr(cu_rows), _ptr(start_pos), B, n,
+                                   max_ctx, d, _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K), _ptr(U_V),
+                                   _ptr(B_K), _ptr(B_V), ctypes.byref(desc), _ptr(page_table),
+                                   page_table.shape[1], _ptr(out), _ptr(ws), ws.numel(),
+                                   _ptr(status), _stream(stream))
+    _abi.check("lrkv_prefill", code)
+    return out

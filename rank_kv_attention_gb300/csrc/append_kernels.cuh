@@ -1,0 +1,33 @@
+// Internal interface between the C-ABI layer and the append kernels.
+#pragma once
+
+#include "lrkv_common.cuh"
+
+namespace lrkv {
+
+template <typename T>
+struct AppendArgsT {
+    const T *X;
+    const int32_t *positions;
+    const int32_t *seq_ids;
+    int n, d;
+    const T *W_S_K, *W_S_V, *U_K, *U_V;
+    T *S_K, *S_V, *R_K, *R_V;
+    const int32_t *page_table;
+    int B, max_pages, num_pages, page_size, H, d_h, r;
+    int32_t *status;
+    cudaStream_t stream;
+};
+
+template <typename T>
+cudaError_t launch_append_generic(const AppendArgsT<T> &a);
+
+// Tensor-core append (bf16): covered shapes and launcher.
+bool tc_append_supported(int n, int d, int d_h, int H, int r);
+cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);
+
+cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
+                                int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
+                                int32_t *req_row, int32_t *status, cudaStream_t s);
+
+}  // namespace lrkv

@@ -1,0 +1,40 @@
+// Internal interface between the C-ABI layer and the decode kernels.
+#pragma once
+
+#include "lrkv_common.cuh"
+
+namespace lrkv {
+
+struct DecodeArgs {
+    const void *q;
+    lrkv_cache_t cache;
+    const void *B_K;
+    const void *B_V;
+    const int32_t *seq_lens;
+    const int32_t *page_table;
+    const int32_t *req_row;  // page-table row of request b (NULL: row b)
+    int B;
+    int max_pages;
+    int max_seq_len;
+    void *out;
+    int32_t *status;
+    cudaStream_t stream;
+};
+
+template <typename T>
+cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align);
+template <typename T>
+cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G);
+template <typename T>
+cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws);
+
+// Tensor-core split kernel (bf16, d_h = 128, page_size % 16 == 0, selected
+// (H, r) pairs).  `fast_decode_supported` says whether a shape is covered;
+// `fast_decode_grid` is its CTA count on this device.
+bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype);
+int fast_decode_grid(int H, int r);
+cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G);
+
+int device_sm_count();
+
+}  // namespace lrkv

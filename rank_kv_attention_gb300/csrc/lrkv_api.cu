@@ -1,0 +1,378 @@
+// C-ABI entry points of the LRKV library: argument validation on the host,
+// workspace layout, and dispatch to the kernels.  Nothing here allocates.
+#include <math.h>
+#include <algorithm>
+#include <string.h>
+
+#include "append_kernels.cuh"
+#include "decode_kernels.cuh"
+
+namespace lrkv {
+
+static thread_local int g_last_cuda_error = 0;
+
+static int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return LRKV_E_CUDA;
+}
+
+// Event pairs bracketing split-kernel launches (benchmark instrumentation).
+struct Profiler {
+    static const int kCap = 8192;
+    bool on = false, created = false;
+    int n = 0;
+    cudaEvent_t ev[2 * kCap];
+};
+static Profiler g_prof;
+
+static void prof_before(cudaStream_t s) {
+    if (g_prof.on && g_prof.n < Profiler::kCap) cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+}
+static void prof_after(cudaStream_t s) {
+    if (g_prof.on && g_prof.n < Profiler::kCap) {
+        cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
+        ++g_prof.n;
+    }
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 160;  // no device visible (sizing queries only): an upper bound
+    }
+    return n;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+static int elem_bytes(int dtype) { return dtype == LRKV_BF16 ? 2 : 4; }
+
+static int check_dims(int H, int d_h, int r, int dtype) {
+    if (dtype != LRKV_F32 && dtype != LRKV_BF16) return LRKV_E_DTYPE;
+    if (H < 1 || H > 128 || d_h < 1 || d_h > 256 || r < 1 || r > 256) return LRKV_E_SHAPE;
+    const int mult = dtype == LRKV_BF16 ? 8 : 4;
+    if (d_h % mult || r % mult) return LRKV_E_SHAPE;
+    return LRKV_OK;
+}
+
+static int check_cache(const lrkv_cache_t *c) {
+    if (!c) return LRKV_E_INVALID_ARG;
+    int st = check_dims(c->H, c->d_h, c->r, c->dtype);
+    if (st) return st;
+    if (!c->S_K || !c->S_V || !c->R_K || !c->R_V) return LRKV_E_INVALID_ARG;
+    if (!aligned16(c->S_K) || !aligned16(c->S_V) || !aligned16(c->R_K) || !aligned16(c->R_V))
+        return LRKV_E_INVALID_ARG;
+    if (c->num_pages < 1 || c->page_size < 16 || c->page_size > 1024 || c->page_size % 16)
+        return LRKV_E_SHAPE;
+    if ((int64_t)c->num_pages * c->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    return LRKV_OK;
+}
+
+// Decode launch geometry.  The workspace always reserves slots for the larger
+// of the two paths' grids so that its size does not depend on the path.
+struct DecodeGeom {
+    int G_fast, G_gen, G_ws;
+};
+
+static DecodeGeom decode_geom(int B, int max_seq_len) {
+    const int sm = device_sm_count();
+    const int64_t rows = (int64_t)B * max_seq_len;
+    DecodeGeom g;
+    g.G_fast = (int)std::max<int64_t>(1, std::min<int64_t>(sm, (rows + 63) / 64));
+    g.G_gen = (int)std::max<int64_t>(1, std::min<int64_t>(2 * sm, (rows + 255) / 256));
+    g.G_ws = std::max(g.G_fast, g.G_gen);
+    return g;
+}
+
+static size_t decode_ws_bytes(int B, int H, int d_h, int r, int max_seq_len) {
+    DecodeGeom g = decode_geom(B, max_seq_len);
+    return decode_ws_layout(nullptr, B, H, d_h, r, g.G_ws).bytes;
+}
+
+static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
+    const auto &c = a.cache;
+    DecodeGeom geo = decode_geom(a.B, a.max_seq_len);
+    DecodeWs ws = decode_ws_layout(workspace, a.B, c.H, c.d_h, c.r, geo.G_ws);
+    if (ws_bytes < ws.bytes) return LRKV_E_WORKSPACE;
+    const bool fast = fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype);
+    const int G = fast ? geo.G_fast : geo.G_gen;
+    cudaError_t e;
+    if (c.dtype == LRKV_BF16) {
+        e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign);
+        if (e == cudaSuccess) {
+            prof_before(a.stream);
+            e = fast ? launch_split_fast(a, ws, G) : launch_split_generic<__nv_bfloat16>(a, ws, G);
+            prof_after(a.stream);
+        }
+        if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws);
+    } else {
+        e = launch_prologue<float>(a, ws, G, kPlanTileAlign);
+        if (e == cudaSuccess) {
+            prof_before(a.stream);
+            e = launch_split_generic<float>(a, ws, G);
+            prof_after(a.stream);
+        }
+        if (e == cudaSuccess) e = launch_combine<float>(a, ws);
+    }
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+}
+
+template <typename T>
+static AppendArgsT<T> make_append_args(const void *X, const int32_t *positions,
+                                       const int32_t *seq_ids, int n, int d, const void *W_S_K,
+                                       const void *W_S_V, const void *U_K, const void *U_V,
+                                       const lrkv_cache_t *c, const int32_t *page_table, int B,
+                                       int max_pages, int32_t *status, cudaStream_t s) {
+    AppendArgsT<T> a;
+    a.X = static_cast<const T *>(X);
+    a.positions = positions;
+    a.seq_ids = seq_ids;
+    a.n = n;
+    a.d = d;
+    a.W_S_K = static_cast<const T *>(W_S_K);
+    a.W_S_V = static_cast<const T *>(W_S_V);
+    a.U_K = static_cast<const T *>(U_K);
+    a.U_V = static_cast<const T *>(U_V);
+    a.S_K = static_cast<T *>(c->S_K);
+    a.S_V = static_cast<T *>(c->S_V);
+    a.R_K = static_cast<T *>(c->R_K);
+    a.R_V = static_cast<T *>(c->R_V);
+    a.page_table = page_table;
+    a.B = B;
+    a.max_pages = max_pages;
+    a.num_pages = c->num_pages;
+    a.page_size = c->page_size;
+    a.H = c->H;
+    a.d_h = c->d_h;
+    a.r = c->r;
+    a.status = status;
+    a.stream = s;
+    return a;
+}
+
+static int check_append(const void *X, const int32_t *positions, const int32_t *seq_ids, int n,
+                        int d, const void *W_S_K, const void *W_S_V, const void *U_K,
+                        const void *U_V, const lrkv_cache_t *cache, const int32_t *page_table,
+                        int B, int max_pages) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if (n < 0 || B < 1 || max_pages < 1) return LRKV_E_SHAPE;
+    if (d < 1 || d > 65536 || d % (cache->dtype == LRKV_BF16 ? 8 : 4)) return LRKV_E_SHAPE;
+    if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (n == 0) return LRKV_OK;
+    if (!X || !positions || !seq_ids || !W_S_K || !W_S_V || !U_K || !U_V || !page_table)
+        return LRKV_E_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W_S_K) || !aligned16(W_S_V) || !aligned16(U_K) ||
+        !aligned16(U_V))
+        return LRKV_E_INVALID_ARG;
+    return LRKV_OK;
+}
+
+static int run_append(const void *X, const int32_t *positions, const int32_t *seq_ids, int n,
+                      int d, const void *W_S_K, const void *W_S_V, const void *U_K,
+                      const void *U_V, const lrkv_cache_t *c, const int32_t *page_table, int B,
+                      int max_pages, int32_t *status, cudaStream_t s) {
+    if (n == 0) return LRKV_OK;
+    cudaError_t e;
+    if (c->dtype == LRKV_BF16) {
+        auto a = make_append_args<__nv_bfloat16>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K,
+                                                 U_V, c, page_table, B, max_pages, status, s);
+        e = tc_append_supported(n, d, c->d_h, c->H, c->r) ? launch_append_tc(a)
+                                                           : launch_append_generic(a);
+    } else {
+        auto a = make_append_args<float>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K, U_V, c,
+                                         page_table, B, max_pages, status, s);
+        e = launch_append_generic(a);
+    }
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+}
+
+// Prefill workspace: per-row metadata (4 int32 arrays of n) then the decode
+// workspace of the n virtual one-query requests.
+struct PrefillWs {
+    int32_t *pos, *sid, *vlen, *req_row;
+    void *dec;
+    size_t dec_bytes, bytes;
+};
+
+static PrefillWs prefill_ws_layout(void *base, int n, int H, int d_h, int r, int max_ctx) {
+    PrefillWs w;
+    char *p = static_cast<char *>(base);
+    size_t o = 0;
+    const size_t arr = align256(sizeof(int32_t) * (size_t)std::max(n, 1));
+    w.pos = reinterpret_cast<int32_t *>(p + o); o += arr;
+    w.sid = reinterpret_cast<int32_t *>(p + o); o += arr;
+    w.vlen = reinterpret_cast<int32_t *>(p + o); o += arr;
+    w.req_row = reinterpret_cast<int32_t *>(p + o); o += arr;
+    w.dec = p + o;
+    w.dec_bytes = decode_ws_bytes(std::max(n, 1), H, d_h, r, std::max(max_ctx, 1));
+    o += w.dec_bytes;
+    w.bytes = o;
+    return w;
+}
+
+}  // namespace lrkv
+
+using namespace lrkv;
+
+extern "C" {
+
+int lrkv_version(void) { return 100; }
+
+int lrkv_profile_enable(int on) {
+    if (on && !g_prof.created) {
+        for (int i = 0; i < 2 * Profiler::kCap; ++i) {
+            cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+            if (e != cudaSuccess) {
+                for (int k = 0; k < i; ++k) cudaEventDestroy(g_prof.ev[k]);
+                return cuda_fail(e);
+            }
+        }
+        g_prof.created = true;
+    }
+    g_prof.on = on != 0;
+    g_prof.n = 0;
+    return LRKV_OK;
+}
+
+int lrkv_profile_read(double *total_ms, int32_t *launches) {
+    if (!total_ms || !launches) return LRKV_E_INVALID_ARG;
+    *total_ms = 0.0;
+    *launches = g_prof.n;
+    if (g_prof.n > 0) {
+        cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * g_prof.n - 1]);
+        if (e != cudaSuccess) return cuda_fail(e);
+        for (int i = 0; i < g_prof.n; ++i) {
+            float ms = 0.f;
+            e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+            if (e != cudaSuccess) return cuda_fail(e);
+            *total_ms += ms;
+        }
+    }
+    g_prof.n = 0;
+    return LRKV_OK;
+}
+
+int lrkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char *lrkv_status_string(int status) {
+    switch (status) {
+        case LRKV_OK: return "ok";
+        case LRKV_E_INVALID_ARG: return "invalid argument";
+        case LRKV_E_SHAPE: return "unsupported or inconsistent shape";
+        case LRKV_E_DTYPE: return "unsupported dtype";
+        case LRKV_E_BOUNDS: return "bound violated";
+        case LRKV_E_WORKSPACE: return "workspace missing, misaligned or too small";
+        case LRKV_E_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || tokens < 0) return 0;
+    return (size_t)tokens * 2 * ((size_t)d_h + (size_t)H * r) * elem_bytes(dtype);
+}
+
+size_t lrkv_decode_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                   int32_t max_seq_len, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || B < 1 || max_seq_len < 1) return 0;
+    return decode_ws_bytes(B, H, d_h, r, max_seq_len);
+}
+
+int lrkv_append(const void *X, const int32_t *positions, const int32_t *seq_ids, int32_t n,
+                int32_t d, const void *W_S_K, const void *W_S_V, const void *U_K, const void *U_V,
+                const lrkv_cache_t *cache, const int32_t *page_table, int32_t B, int32_t max_pages,
+                int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_append(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table,
+                          B, max_pages);
+    if (st) return st;
+    return run_append(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B,
+                      max_pages, dev_status, (cudaStream_t)stream);
+}
+
+int lrkv_decode(const void *q, const lrkv_cache_t *cache, const void *B_K, const void *B_V,
+                const int32_t *seq_lens, const int32_t *page_table, int32_t B, int32_t max_pages,
+                int32_t max_seq_len, void *out, void *workspace, size_t workspace_bytes,
+                int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if (B < 1 || max_pages < 1 || max_seq_len < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * cache->page_size) return LRKV_E_BOUNDS;
+    if ((int64_t)B * max_seq_len > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (!q || !B_K || !B_V || !seq_lens || !page_table || !out) return LRKV_E_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(B_K) || !aligned16(B_V) || !aligned16(out))
+        return LRKV_E_INVALID_ARG;
+    if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    DecodeArgs a;
+    a.q = q;
+    a.cache = *cache;
+    a.B_K = B_K;
+    a.B_V = B_V;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.req_row = nullptr;
+    a.B = B;
+    a.max_pages = max_pages;
+    a.max_seq_len = max_seq_len;
+    a.out = out;
+    a.status = dev_status;
+    a.stream = (cudaStream_t)stream;
+    return run_decode(a, workspace, workspace_bytes);
+}
+
+size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h, int32_t r,
+                                    int32_t max_ctx, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || B < 1 || n < 0 || max_ctx < 1) return 0;
+    return prefill_ws_layout(nullptr, n, H, d_h, r, max_ctx).bytes;
+}
+
+int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int32_t *start_pos,
+                 int32_t B, int32_t n, int32_t max_ctx, int32_t d, const void *W_S_K,
+                 const void *W_S_V, const void *U_K, const void *U_V, const void *B_K,
+                 const void *B_V, const lrkv_cache_t *cache, const int32_t *page_table,
+                 int32_t max_pages, void *out, void *workspace, size_t workspace_bytes,
+                 int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_append(X, cu_rows, start_pos, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table,
+                          B, max_pages);
+    if (st) return st;
+    if (max_ctx < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_ctx > (int64_t)max_pages * cache->page_size) return LRKV_E_BOUNDS;
+    if (n == 0) return LRKV_OK;
+    if ((int64_t)n * max_ctx > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (!Q || !B_K || !B_V || !out || !aligned16(Q) || !aligned16(B_K) || !aligned16(B_V) ||
+        !aligned16(out))
+        return LRKV_E_INVALID_ARG;
+    if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    PrefillWs w = prefill_ws_layout(workspace, n, cache->H, cache->d_h, cache->r, max_ctx);
+    if (workspace_bytes < w.bytes) return LRKV_E_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_prefill_rows(cu_rows, start_pos, B, n, max_pages * cache->page_size,
+                                        w.pos, w.sid, w.vlen, w.req_row, dev_status, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = run_append(X, w.pos, w.sid, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
+                    dev_status, s);
+    if (st) return st;
+    // Causal attention: row i is a one-query decode over its request's rows
+    // 0..pos_i, reading the page-table row of its request.
+    DecodeArgs a;
+    a.q = Q;
+    a.cache = *cache;
+    a.B_K = B_K;
+    a.B_V = B_V;
+    a.seq_lens = w.vlen;
+    a.page_table = page_table;
+    a.req_row = w.req_row;
+    a.B = n;
+    a.max_pages = max_pages;
+    a.max_seq_len = max_ctx;
+    a.out = out;
+    a.status = dev_status;
+    a.stream = s;
+    return run_decode(a, w.dec, w.dec_bytes);
+}
+
+}  // extern "C"

@@ -1,0 +1,207 @@
+// Shared device helpers for the LRKV kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lrkv.h"
+
+namespace lrkv {
+
+// ---------------------------------------------------------------------------
+// Launch plan shared by the decode kernels.
+//
+// Decode work is balanced over a fixed grid of G CTAs: the visible rows of
+// all requests are laid end to end (request b occupies [off[b], off[b+1])),
+// and CTA g takes the contiguous range [g*chunk, (g+1)*chunk).  A CTA's range
+// can cut several requests; each (request, CTA) piece is a "segment" whose
+// partial softmax state goes to slot b + g (unique among the segments that
+// exist, so B + G slots suffice).
+// ---------------------------------------------------------------------------
+struct DecodePlan {
+    int32_t total;   // sum of the (validated) sequence lengths
+    int32_t chunk;   // rows per CTA (multiple of the tile size)
+    int32_t pad[2];
+    // int32_t off[B + 1] follows
+};
+
+constexpr int kPlanTileAlign = 16;
+
+// Workspace layout of lrkv_decode (all offsets 256-byte aligned):
+//   [plan header + off[B+1]] [p: B*H*r f32] [ml: slots*H*2 f32] [acc: slots*H*(d_h+r) f32]
+struct DecodeWs {
+    DecodePlan *plan;
+    int32_t *off;
+    float *p;
+    float *ml;
+    float *acc;
+    size_t bytes;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, int d_h, int r,
+                                                     int G) {
+    DecodeWs w;
+    char *p = static_cast<char *>(base);
+    size_t o = 0;
+    w.plan = reinterpret_cast<DecodePlan *>(p + o);
+    w.off = reinterpret_cast<int32_t *>(p + o + sizeof(DecodePlan));
+    o += align256(sizeof(DecodePlan) + sizeof(int32_t) * (size_t)(B + 1));
+    w.p = reinterpret_cast<float *>(p + o);
+    o += align256(sizeof(float) * (size_t)B * H * r);
+    size_t slots = (size_t)B + G;
+    w.ml = reinterpret_cast<float *>(p + o);
+    o += align256(sizeof(float) * slots * H * 2);
+    w.acc = reinterpret_cast<float *>(p + o);
+    o += align256(sizeof(float) * slots * H * (size_t)(d_h + r));
+    w.bytes = o;
+    return w;
+}
+
+// ---------------------------------------------------------------------------
+// Element conversion
+// ---------------------------------------------------------------------------
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    __device__ static float load(const float *p) { return *p; }
+    __device__ static void store(float *p, float v) { *p = v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    __device__ static float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+    __device__ static void store(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void status_or(int32_t *st, uint32_t bits) {
+    if (st) atomicOr(reinterpret_cast<unsigned int *>(st), bits);
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory / mbarrier / bulk-copy wrappers (PTX ISA, sm_90+)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the phase did not
+// complete within ~2 s of wall time (the caller then records
+// LRKV_STATUS_TIMEOUT and leaves its loop instead of spinning forever).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    uint32_t ok = 0;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 255u) == 255u && globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
+// 2-D tiled TMA load: box at (x, y) of the tensor map into shared memory,
+// completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Plain contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core fragments (m16n8k16, bf16 in, fp32 accumulate)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                            uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                                  uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4],
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile
+// written by TMA with CU_TENSOR_MAP_SWIZZLE_128B (rows of 128 bytes; the
+// chunk index is XORed with the row index modulo 8).
+__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
+    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+}  // namespace lrkv

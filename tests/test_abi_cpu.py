@@ -1,0 +1,115 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every
+function include/lrkv.h declares, and its host-only entry points (sizes,
+status strings, argument validation that rejects before any CUDA work)
+behave as documented.  No call here touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from rank_kv_attention_gb300 import _abi
+from rank_kv_attention_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _abi.lib()
+
+
+def header_functions():
+    txt = open(os.path.join(ROOT, "include", "lrkv.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"LRKV_API\s+[\w\s\*]*?\b(lrkv_\w+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_abi.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_strings(lib):
+    assert lib.lrkv_version() >= 100
+    assert lib.lrkv_status_string(0) == b"ok"
+    assert b"workspace" in lib.lrkv_status_string(_abi.LRKV_E_WORKSPACE)
+
+
+@pytest.mark.parametrize("H,d_h,r,T,dt,eb", [(16, 128, 48, 4096, 1, 2), (32, 128, 32, 32768, 1, 2),
+                                             (4, 16, 4, 65, 0, 4), (18, 128, 56, 2048, 1, 2)])
+def test_cache_bytes_is_equation_9(lib, H, d_h, r, T, dt, eb):
+    got = lib.lrkv_cache_bytes(H, d_h, r, T, dt)
+    assert got == oracle.lrkv_payload(eb, 1, 1, T, H, d_h, r)
+
+
+def test_cache_bytes_rejects_bad_shapes(lib):
+    assert lib.lrkv_cache_bytes(0, 128, 48, 10, 1) == 0
+    assert lib.lrkv_cache_bytes(16, 130, 48, 10, 1) == 0   # bf16 needs d_h % 8 == 0
+    assert lib.lrkv_cache_bytes(16, 128, 48, 10, 7) == 0   # bad dtype
+
+
+def test_workspace_sizes_positive_and_monotone(lib):
+    a = lib.lrkv_decode_workspace_bytes(16, 16, 128, 48, 4096, 1)
+    b = lib.lrkv_decode_workspace_bytes(64, 16, 128, 48, 4096, 1)
+    assert 0 < a < b
+    assert lib.lrkv_decode_workspace_bytes(0, 16, 128, 48, 4096, 1) == 0
+    assert lib.lrkv_prefill_workspace_bytes(8, 16384, 16, 128, 48, 2048, 1) > 0
+
+
+def _cache(dtype=1, **kw):
+    c = _abi.CacheDesc(16, 16, 16, 16, 4, 64, 16, 128, 48, dtype)  # fake aligned addresses
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_decode_rejects_on_host(lib):
+    ws = ctypes.c_void_p(256)
+    good = dict(q=16, BK=16, BV=16, sl=16, pt=16, B=2, mp=4, msl=100, out=16, ws=ws, wsb=1 << 30)
+
+    def call(cache, **over):
+        a = dict(good, **over)
+        return lib.lrkv_decode(a["q"], ctypes.byref(cache), a["BK"], a["BV"], a["sl"], a["pt"], a["B"],
+                               a["mp"], a["msl"], a["out"], a["ws"], a["wsb"], None, None)
+    assert call(_cache(), q=None) == _abi.LRKV_E_INVALID_ARG
+    assert call(_cache(), q=8) == _abi.LRKV_E_INVALID_ARG           # misaligned
+    assert call(_cache(dtype=5)) == _abi.LRKV_E_DTYPE
+    assert call(_cache(d_h=130)) == _abi.LRKV_E_SHAPE
+    assert call(_cache(page_size=40)) == _abi.LRKV_E_SHAPE
+    assert call(_cache(), msl=4 * 64 + 1) == _abi.LRKV_E_BOUNDS     # beyond max_pages * page_size
+    assert call(_cache(), B=0) == _abi.LRKV_E_SHAPE
+    assert call(_cache(), ws=None) == _abi.LRKV_E_WORKSPACE
+    assert call(_cache(), ws=ctypes.c_void_p(16)) == _abi.LRKV_E_WORKSPACE   # not 256-aligned
+    assert call(_cache(), wsb=16) == _abi.LRKV_E_WORKSPACE
+    assert lib.lrkv_decode(16, None, 16, 16, 16, 16, 2, 4, 100, 16, ws, 1 << 30, None, None) \
+        == _abi.LRKV_E_INVALID_ARG
+
+
+def test_append_rejects_on_host(lib):
+    c = _cache()
+    ok_args = [16, 16, 16, 5, 2048, 16, 16, 16, 16, ctypes.byref(c), 16, 2, 4, None, None]
+    a = list(ok_args); a[0] = None
+    assert lib.lrkv_append(*a) == _abi.LRKV_E_INVALID_ARG
+    a = list(ok_args); a[4] = 2047          # d not a multiple of 8 for bf16
+    assert lib.lrkv_append(*a) == _abi.LRKV_E_SHAPE
+    a = list(ok_args); a[3] = -1
+    assert lib.lrkv_append(*a) == _abi.LRKV_E_SHAPE
+    a = list(ok_args); a[3] = 0             # n == 0 is a no-op, even with null rows
+    a[0] = None
+    assert lib.lrkv_append(*a) == _abi.LRKV_OK
+
+
+def test_prefill_rejects_on_host(lib):
+    c = _cache()
+    args = [16, 16, 16, 16, 2, 10, 300, 2048, 16, 16, 16, 16, 16, 16, ctypes.byref(c), 16, 4, 16,
+            ctypes.c_void_p(256), 1 << 30, None, None]
+    assert lib.lrkv_prefill(*args) == _abi.LRKV_E_BOUNDS   # max_ctx 300 > 4 pages * 64
+    args[6] = 200
+    args[18] = None
+    assert lib.lrkv_prefill(*args) == _abi.LRKV_E_WORKSPACE
