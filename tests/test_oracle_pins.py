@@ -448,3 +448,11 @@ def test_mutation_transposed_base(monkeypatch):
     monkeypatch.setattr(O, "expand_head",
                         lambda S, R, B: np.asarray(S, float) + (np.asarray(R) @ np.asarray(B).T[::-1, ::-1]))
     _must_fail(check_bruteforce)
+
+
+def test_decode_flop_model_matches_arithmetic_ratio():
+    """The flop model divided by the dense-MHA flops of the same step is the
+    section 4 decode arithmetic ratio 1 + r/d_h + r/T (one request)."""
+    for T, H, d_h, r in [(4096, 16, 128, 48), (32768, 32, 128, 32), (7, 3, 16, 4)]:
+        dense = 2 * (T * H * 2 * d_h)
+        assert Fraction(O.decode_flops([T], H, d_h, r), dense) == O.decode_arith_ratio(d_h, r, T)
