@@ -153,6 +153,38 @@ LRKV_API int lrkv_decode(const void *q, const lrkv_cache_t *cache, const void *B
                 void *workspace, size_t workspace_bytes, int32_t *dev_status,
                 lrkv_stream_t stream);
 
+/*
+ * lrkv_decode_noalloc - the same decode step as lrkv_decode, for callers that
+ * cannot allocate device memory.  (Library plumbing: the paper has no
+ * counterpart.)
+ *
+ * Some hosts own every byte of device memory: a serving engine that reserves
+ * HBM up front for its own pool, or a plugin hook whose contract forbids
+ * allocating.  There, cudaMalloc either fails or stalls the whole device in
+ * the middle of a latency-critical step, so such a caller cannot provide the
+ * workspace lrkv_decode asks for.  This entry point takes the same arguments
+ * minus the workspace and keeps its scratch (launch plan, private queries,
+ * per-segment softmax partials) in a device array built into the library:
+ *   - the array is LRKV_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU that loads
+ *     the library, held until the process exits;
+ *   - sizes whose lrkv_decode_workspace_bytes(B, H, d_h, r, max_seq_len,
+ *     dtype) exceeds that are rejected with LRKV_E_WORKSPACE before any work;
+ *   - the first call on each device looks up the array's device address with
+ *     that device current (set-up done once per device); make that first call
+ *     before any stream capture;
+ *   - every call on a device shares the one array and leaves its scratch
+ *     behind; nothing in it needs clearing (each call writes every value before
+ *     reading it), but two calls that can run at the same time on the GPU
+ *     (different streams, or threads) race: the caller must serialise them.
+ * It allocates nothing and calls no allocating routine.
+ */
+#define LRKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+LRKV_API int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const void *B_K,
+                                 const void *B_V, const int32_t *seq_lens,
+                                 const int32_t *page_table, int32_t B, int32_t max_pages,
+                                 int32_t max_seq_len, void *out, int32_t *dev_status,
+                                 lrkv_stream_t stream);
+
 /* Bytes of device workspace lrkv_prefill needs. */
 LRKV_API size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h,
                                     int32_t r, int32_t max_ctx, int32_t dtype);

@@ -22,6 +22,8 @@ LRKV_E_BOUNDS = -4
 LRKV_E_WORKSPACE = -5
 LRKV_E_CUDA = -6
 
+LRKV_NOALLOC_SCRATCH_BYTES = 16 << 20
+
 LRKV_STATUS_BAD_PAGE = 1
 LRKV_STATUS_BAD_SEQLEN = 2
 LRKV_STATUS_BAD_ROW = 4
@@ -61,6 +63,7 @@ SIGNATURES = {
     "lrkv_append": (ctypes.c_int, [P, P, P, I32, I32, P, P, P, P, CACHE_P, P, I32, I32, P, P]),
     "lrkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "lrkv_decode": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, P, SZ, P, P]),
+    "lrkv_decode_noalloc": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, P, P]),
     "lrkv_prefill_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),

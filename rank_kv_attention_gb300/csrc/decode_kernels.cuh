@@ -37,4 +37,8 @@ cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G);
 
 int device_sm_count();
 
+// Device address of the built-in scratch array used by lrkv_decode_noalloc on
+// the current device (nullptr and *err set on failure).
+void *noalloc_scratch_address(cudaError_t *err);
+
 }  // namespace lrkv

@@ -324,6 +324,44 @@ int lrkv_decode(const void *q, const lrkv_cache_t *cache, const void *B_K, const
     return run_decode(a, workspace, workspace_bytes);
 }
 
+int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const void *B_K,
+                        const void *B_V, const int32_t *seq_lens, const int32_t *page_table,
+                        int32_t B, int32_t max_pages, int32_t max_seq_len, void *out,
+                        int32_t *dev_status, lrkv_stream_t stream) {
+    // Same host checks as lrkv_decode, then the built-in scratch array stands
+    // in for the caller's workspace.
+    int st = check_cache(cache);
+    if (st) return st;
+    if (B < 1 || max_pages < 1 || max_seq_len < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * cache->page_size) return LRKV_E_BOUNDS;
+    if ((int64_t)B * max_seq_len > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (!q || !B_K || !B_V || !seq_lens || !page_table || !out) return LRKV_E_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(B_K) || !aligned16(B_V) || !aligned16(out))
+        return LRKV_E_INVALID_ARG;
+    if (decode_ws_bytes(B, cache->H, cache->d_h, cache->r, max_seq_len) >
+        (size_t)LRKV_NOALLOC_SCRATCH_BYTES)
+        return LRKV_E_WORKSPACE;
+    cudaError_t e;
+    void *scratch = noalloc_scratch_address(&e);
+    if (!scratch) return cuda_fail(e);
+    DecodeArgs a;
+    a.q = q;
+    a.cache = *cache;
+    a.B_K = B_K;
+    a.B_V = B_V;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.req_row = nullptr;
+    a.B = B;
+    a.max_pages = max_pages;
+    a.max_seq_len = max_seq_len;
+    a.out = out;
+    a.status = dev_status;
+    a.stream = (cudaStream_t)stream;
+    return run_decode(a, scratch, (size_t)LRKV_NOALLOC_SCRATCH_BYTES);
+}
+
 size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h, int32_t r,
                                     int32_t max_ctx, int32_t dtype) {
     if (check_dims(H, d_h, r, dtype) || B < 1 || n < 0 || max_ctx < 1) return 0;
