@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) append_generic_kernel(AppendArgsT<T> a) {
     __shared__ float Xs[kAK][kAM + 1];
     __shared__ float Ws[kAK][kAN + 1];
     __shared__ int64_t dst_row[kAM];
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const int c0 = blockIdx.x * kAN, i0 = blockIdx.y * kAM;
     const int d_h = a.d_h, Hr = a.H * a.r;
@@ -103,12 +105,274 @@ template <typename T>
 cudaError_t launch_append_generic(const AppendArgsT<T> &a) {
     const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
     dim3 grid((Ntot + kAN - 1) / kAN, (a.n + kAM - 1) / kAM);
-    append_generic_kernel<T><<<grid, 256, 0, a.stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(append_generic_kernel<T>, grid, dim3(256), 0, a.stream, a);
 }
 
 template cudaError_t launch_append_generic<float>(const AppendArgsT<float> &);
 template cudaError_t launch_append_generic<__nv_bfloat16>(const AppendArgsT<__nv_bfloat16> &);
+
+// ---------------------------------------------------------------------------
+// Few-row append (one new row per request in a decode step).  The work is a
+// skinny X[n x d] . W^T product bound by reading W once: a block holds up to
+// 16 rows of X in shared memory and each warp streams two weight rows with
+// 16-byte coalesced loads, accumulating in fp32.
+// ---------------------------------------------------------------------------
+constexpr int kSkRows = 16, kSkWarps = 4, kSkCols = 4;  // rows per block, warps, columns per warp
+
+template <typename T>
+__device__ __forceinline__ const T *weight_row(const AppendArgsT<T> &a, int c) {
+    const int d_h = a.d_h, Hr = a.H * a.r;
+    if (c < d_h) return a.W_S_K + (size_t)c * a.d;
+    if (c < 2 * d_h) return a.W_S_V + (size_t)(c - d_h) * a.d;
+    if (c < 2 * d_h + Hr) return a.U_K + (size_t)(c - 2 * d_h) * a.d;
+    return a.U_V + (size_t)(c - 2 * d_h - Hr) * a.d;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSkWarps * 32) append_rows_kernel(AppendArgsT<T> a) {
+    constexpr int V = Vec16<T>::N;  // elements per 16-byte chunk
+    extern __shared__ __align__(16) unsigned char sk_raw[];
+    T *xs = reinterpret_cast<T *>(sk_raw);  // [kSkRows][d]
+    __shared__ int64_t dst_row[kSkRows];
+    __shared__ __align__(8) uint64_t xbar;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int i0 = blockIdx.y * kSkRows;
+    const int nr = min(kSkRows, a.n - i0);
+    const int d = a.d;
+    const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
+    const int c0 = (blockIdx.x * kSkWarps + warp) * kSkCols;  // this warp's first output column
+    const T *wrow[kSkCols];
+#pragma unroll
+    for (int cc = 0; cc < kSkCols; ++cc) wrow[cc] = weight_row(a, min(c0 + cc, Ntot - 1));
+    const int nchunk = d / V;
+
+    // the block's rows of X (contiguous) arrive by one bulk copy while the
+    // first weight chunks are loaded
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+        const uint32_t bytes = (uint32_t)(nr * d * sizeof(T));
+        mbar_arrive_expect_tx(&xbar, bytes);
+        bulk_load(xs, a.X + (size_t)i0 * d, bytes, &xbar);
+    }
+    uint4 wn[kSkCols];
+#pragma unroll
+    for (int cc = 0; cc < kSkCols; ++cc)
+        if (lane < nchunk) wn[cc] = *reinterpret_cast<const uint4 *>(wrow[cc] + (size_t)lane * V);
+    if (tid < kSkRows)
+        dst_row[tid] = (tid < nr) ? append_dest_row(a.positions, a.seq_ids, i0 + tid, a.page_table,
+                                                    a.B, a.max_pages, a.num_pages, a.page_size,
+                                                    a.status)
+                                  : -1;
+    __syncthreads();
+    if (!mbar_wait(&xbar, 0)) {
+        status_or(a.status, LRKV_STATUS_TIMEOUT);
+        return;
+    }
+
+    float acc[kSkCols][kSkRows];
+#pragma unroll
+    for (int cc = 0; cc < kSkCols; ++cc)
+#pragma unroll
+        for (int r = 0; r < kSkRows; ++r) acc[cc][r] = 0.f;
+    for (int q = lane; q < nchunk; q += 32) {
+        float w[kSkCols][V];
+#pragma unroll
+        for (int cc = 0; cc < kSkCols; ++cc) Vec16<T>::load(reinterpret_cast<const T *>(&wn[cc]), w[cc]);
+        // prefetch the next chunks of the weight rows
+        if (q + 32 < nchunk) {
+#pragma unroll
+            for (int cc = 0; cc < kSkCols; ++cc)
+                wn[cc] = *reinterpret_cast<const uint4 *>(wrow[cc] + (size_t)(q + 32) * V);
+        }
+#pragma unroll
+        for (int r = 0; r < kSkRows; ++r) {
+            if (r < nr) {
+                float x[V];
+                Vec16<T>::load(xs + (size_t)r * d + (size_t)q * V, x);
+#pragma unroll
+                for (int cc = 0; cc < kSkCols; ++cc)
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[cc][r] = fmaf(w[cc][e], x[e], acc[cc][r]);
+            }
+        }
+    }
+    const int d_h = a.d_h, Hr = a.H * a.r;
+#pragma unroll
+    for (int cc = 0; cc < kSkCols; ++cc) {
+        float mine = 0.f;
+#pragma unroll
+        for (int r = 0; r < kSkRows; ++r) {
+            float v = acc[cc][r];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == r) mine = v;
+        }
+        const int c = c0 + cc;
+        if (c >= Ntot || lane >= nr) continue;
+        const int64_t row = dst_row[lane];
+        if (row < 0) continue;
+        T *dst;
+        if (c < d_h) dst = a.S_K + row * d_h + c;
+        else if (c < 2 * d_h) dst = a.S_V + row * d_h + (c - d_h);
+        else if (c < 2 * d_h + Hr) dst = a.R_K + row * Hr + (c - 2 * d_h);
+        else dst = a.R_V + row * Hr + (c - 2 * d_h - Hr);
+        Elem<T>::store(dst, mine);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Few-row append on tensor cores (bf16).  A block holds 16 rows of X in
+// shared memory (rows padded by 16 bytes so ldmatrix is conflict-free) and
+// produces 16 output columns; its 4 warps split the contraction d, each
+// running mma.m16n8k16 (rows of X = M, output columns = N) with the weight
+// fragments read straight from global memory, then the partial sums meet in
+// shared memory and are scattered to the cache.
+// ---------------------------------------------------------------------------
+constexpr int kTcRows = 16, kTcCols = 16, kTcWarps = 4, kTcBatch = 8;
+
+__global__ void __launch_bounds__(kTcWarps * 32) append_rows_mma_kernel(AppendArgsT<__nv_bfloat16> a) {
+    extern __shared__ __align__(16) unsigned char tc_raw[];
+    const int d = a.d;
+    const int xstride = d * 2 + 16;                    // bytes per padded row of X
+    unsigned char *xs = tc_raw;                         // [16][xstride]
+    float *part = reinterpret_cast<float *>(tc_raw + kTcRows * xstride);  // [warps][16][16]
+    __shared__ int64_t dst_row[kTcRows];
+    __shared__ __align__(8) uint64_t xbar;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int i0 = blockIdx.y * kTcRows;
+    const int nr = min(kTcRows, a.n - i0);
+    const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
+    const int c0 = blockIdx.x * kTcCols;
+
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&xbar, (uint32_t)(nr * d * 2));
+        for (int r = 0; r < nr; ++r)
+            bulk_load(xs + r * xstride, a.X + (size_t)(i0 + r) * d, (uint32_t)(d * 2), &xbar);
+    }
+    for (int r = nr; r < kTcRows; ++r)
+        for (int e = tid; e < d / 8; e += blockDim.x)
+            reinterpret_cast<uint4 *>(xs + r * xstride)[e] = make_uint4(0, 0, 0, 0);
+    if (tid < kTcRows)
+        dst_row[tid] = (tid < nr) ? append_dest_row(a.positions, a.seq_ids, i0 + tid, a.page_table,
+                                                    a.B, a.max_pages, a.num_pages, a.page_size,
+                                                    a.status)
+                                  : -1;
+    const __nv_bfloat16 *w0 = weight_row(a, min(c0 + gq, Ntot - 1));
+    const __nv_bfloat16 *w1 = weight_row(a, min(c0 + 8 + gq, Ntot - 1));
+    const int nks = d / 16, per = nks / kTcWarps;      // k-steps per warp (d % 64 == 0)
+    const int ks0 = warp * per;
+    __syncthreads();
+    if (!mbar_wait(&xbar, 0)) {
+        status_or(a.status, LRKV_STATUS_TIMEOUT);
+        return;
+    }
+
+    float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const uint32_t xb = smem_u32(xs);
+    const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
+    for (int ks = ks0; ks < ks0 + per; ks += kTcBatch) {
+        uint32_t b[kTcBatch][4];
+#pragma unroll
+        for (int u = 0; u < kTcBatch; ++u) {
+            if (ks + u < ks0 + per) {
+                const int k = (ks + u) * 16 + 2 * tq;
+                b[u][0] = *reinterpret_cast<const uint32_t *>(w0 + k);
+                b[u][1] = *reinterpret_cast<const uint32_t *>(w0 + k + 8);
+                b[u][2] = *reinterpret_cast<const uint32_t *>(w1 + k);
+                b[u][3] = *reinterpret_cast<const uint32_t *>(w1 + k + 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kTcBatch; ++u) {
+            if (ks + u < ks0 + per) {
+                uint32_t av[4];
+                ldmatrix_x4(xb + arow * xstride + (2 * (ks + u) + (lane >> 4)) * 16, av[0], av[1], av[2], av[3]);
+                mma_bf16_16816(c[0], av, b[u][0], b[u][1]);
+                mma_bf16_16816(c[1], av, b[u][2], b[u][3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+        float *pw = part + warp * kTcRows * kTcCols;
+        const int col = nb * 8 + 2 * tq;
+        pw[gq * kTcCols + col] = c[nb][0];
+        pw[gq * kTcCols + col + 1] = c[nb][1];
+        pw[(gq + 8) * kTcCols + col] = c[nb][2];
+        pw[(gq + 8) * kTcCols + col + 1] = c[nb][3];
+    }
+    __syncthreads();
+    const int d_h = a.d_h, Hr = a.H * a.r;
+    for (int o = tid; o < kTcRows * kTcCols; o += blockDim.x) {
+        const int row = o / kTcCols, cidx = c0 + o % kTcCols;
+        if (row >= nr || cidx >= Ntot) continue;
+        const int64_t dr = dst_row[row];
+        if (dr < 0) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTcWarps; ++w) v += part[(w * kTcRows + row) * kTcCols + o % kTcCols];
+        __nv_bfloat16 *dst;
+        if (cidx < d_h) dst = a.S_K + dr * d_h + cidx;
+        else if (cidx < 2 * d_h) dst = a.S_V + dr * d_h + (cidx - d_h);
+        else if (cidx < 2 * d_h + Hr) dst = a.R_K + dr * Hr + (cidx - 2 * d_h);
+        else dst = a.R_V + dr * Hr + (cidx - 2 * d_h - Hr);
+        *dst = __float2bfloat16_rn(v);
+    }
+}
+
+bool rows_mma_append_fits(const AppendArgsT<__nv_bfloat16> &a) {
+    return a.n <= 4 * kTcRows && a.d % 64 == 0 &&
+           (size_t)kTcRows * (a.d * 2 + 16) + kTcWarps * kTcRows * kTcCols * 4 <= 200 * 1024;
+}
+
+cudaError_t launch_append_rows_mma(const AppendArgsT<__nv_bfloat16> &a) {
+    const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
+    dim3 grid((Ntot + kTcCols - 1) / kTcCols, (a.n + kTcRows - 1) / kTcRows);
+    const size_t sm = (size_t)kTcRows * (a.d * 2 + 16) + kTcWarps * kTcRows * kTcCols * 4;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(append_rows_mma_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_pdl(append_rows_mma_kernel, grid, dim3(kTcWarps * 32), sm, a.stream, a);
+}
+
+template <typename T>
+bool rows_append_fits(const AppendArgsT<T> &a) {
+    return a.n <= 4 * kSkRows && (size_t)kSkRows * a.d * sizeof(T) <= 160 * 1024 &&
+           a.d % Vec16<T>::N == 0;
+}
+
+template <typename T>
+cudaError_t launch_append_rows(const AppendArgsT<T> &a) {
+    const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
+    const int cols_per_block = kSkWarps * kSkCols;
+    dim3 grid((Ntot + cols_per_block - 1) / cols_per_block, (a.n + kSkRows - 1) / kSkRows);
+    const size_t sm = (size_t)kSkRows * a.d * sizeof(T);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(append_rows_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_pdl(append_rows_kernel<T>, grid, dim3(kSkWarps * 32), sm, a.stream, a);
+}
+
+template bool rows_append_fits<float>(const AppendArgsT<float> &);
+template bool rows_append_fits<__nv_bfloat16>(const AppendArgsT<__nv_bfloat16> &);
+template cudaError_t launch_append_rows<float>(const AppendArgsT<float> &);
+template cudaError_t launch_append_rows<__nv_bfloat16>(const AppendArgsT<__nv_bfloat16> &);
 
 // ---------------------------------------------------------------------------
 // Prefill set-up: per new row, its request, position, visible length and the
@@ -118,6 +382,8 @@ __global__ void prefill_rows_kernel(const int32_t *__restrict__ cu_rows,
                                     const int32_t *__restrict__ start_pos, int B, int n,
                                     int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                     int32_t *req_row, int32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     // request b with cu_rows[b] <= i < cu_rows[b+1]
@@ -142,9 +408,8 @@ cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    prefill_rows_kernel<<<(n + 255) / 256, 256, 0, s>>>(cu_rows, start_pos, B, n, max_len, pos, sid,
-                                                         vlen, req_row, status);
-    return cudaGetLastError();
+    return launch_pdl(prefill_rows_kernel, dim3((n + 255) / 256), dim3(256), 0, s, cu_rows,
+                      start_pos, B, n, max_len, pos, sid, vlen, req_row, status);
 }
 
 }  // namespace lrkv

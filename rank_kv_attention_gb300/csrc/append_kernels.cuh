@@ -22,6 +22,16 @@ struct AppendArgsT {
 template <typename T>
 cudaError_t launch_append_generic(const AppendArgsT<T> &a);
 
+// Few-row append (decode step): whether the shape fits, and the launcher.
+template <typename T>
+bool rows_append_fits(const AppendArgsT<T> &a);
+template <typename T>
+cudaError_t launch_append_rows(const AppendArgsT<T> &a);
+
+// Few-row append on tensor cores (bf16): whether the shape fits, launcher.
+bool rows_mma_append_fits(const AppendArgsT<__nv_bfloat16> &a);
+cudaError_t launch_append_rows_mma(const AppendArgsT<__nv_bfloat16> &a);
+
 // Tensor-core append (bf16): covered shapes and launcher.
 bool tc_append_supported(int n, int d, int d_h, int H, int r);
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);

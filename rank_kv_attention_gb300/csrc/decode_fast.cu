@@ -3,72 +3,69 @@
 // Reading note "Low-Rank Key Value Attention": section 3, Algorithm 2 and
 // equations 6-7, fused as the note describes after Algorithm 2 (running max,
 // exp-sum, a shared and a private value accumulator, both rescaled by the
-// same factor when the max moves); section 4 on why the shared tile must be
-// reused by all heads for the byte savings to show.
+// same factor when the max moves); section 4 on why one shared tile must be
+// reused by every head for the byte savings to show.
 //
-// One CTA streams a contiguous range of cache rows (possibly spanning
-// several requests, see DecodePlan) for ALL H heads:
-//   * a producer warp stages 16-row tiles into a ring of shared-memory stages:
-//     S_K / S_V rows through 2-D TMA with 128-byte swizzle (read from HBM once
-//     and reused by every head), and the tile's R_K / R_V rows (all heads
-//     contiguous) through plain bulk copies; completion is tracked by
-//     mbarriers;
-//   * eight consumer warps score the tile: the shared part Q[H x 128] .
-//     S_K^T[128 x 16] on tensor cores (mma.m16n8k16, bf16 in, fp32 acc), the
-//     private part p_h . R_K[h, j] (rank r) with fp32 FMAs, one thread per
-//     (head, row); one online softmax per head over the merged score; then
-//     the shared value contraction P[H x 16] . S_V[16 x 128] on tensor cores
-//     (P split into bf16 hi + lo so the weights keep ~16 mantissa bits) and
-//     the private reduction a . R_V[h] with FMAs.
+// One CTA (8 warps) streams a contiguous range of cache rows, possibly
+// spanning several requests (see DecodePlan), for ALL H heads:
+//   * 16-row tiles are staged by TMA (cp.async.bulk.tensor, 128-byte swizzle)
+//     into a ring of shared-memory stages: the shared S_K / S_V rows (read from
+//     HBM once, used by every head) and the private R_K / R_V rows of all
+//     heads; completion is tracked by one mbarrier per stage;
+//   * every warp owns H/8 heads end to end, so no CTA-wide barrier is needed
+//     per tile.  All four contractions run on tensor cores (mma.m16n8k16, bf16
+//     in, fp32 accumulate), with the tile rows or the value columns as M and
+//     the warp's heads as N:
+//       scores  = S_K[16 x 128] . Q^T  +  R_K[16 x (H/8) r] . blockdiag(p)^T
+//       values += S_V^T . P^T           and  R_V^T . P^T  (private reduction)
+//     where blockdiag(p) puts each head's private query p_h = q_h B_K[h] on
+//     that head's own r columns of the tile, so the private score of head h
+//     only ever meets R_K[h]; p and the softmax weights P enter as bf16
+//     hi + lo halves, which keeps ~16 significant bits;
+//   * the online softmax runs inside half-warps (lane = (head, row)); the
+//     running maximum is only moved when the tile maximum exceeds it by more
+//     than 2^8, so accumulators are rarely rescaled (the result is the same:
+//     numerator and denominator share the reference);
+//   * a stage is refilled by the last warp that finishes it (shared counter),
+//     so the copy of tile k+STAGES starts as soon as tile k is free.
 // Each (request, CTA) segment writes (m, l, accS, accR) to its partial slot;
 // the combine kernel merges segments and expands accR by B_V^T once.
+// Kernels of one decode are launched with programmatic dependent launch:
+// each waits (griddepcontrol.wait) for its predecessor before reading its
+// results, so only launch latency overlaps.
 #include "decode_kernels.cuh"
 
 namespace lrkv {
-
-constexpr int cgcd(int a, int b) { return b == 0 ? a : cgcd(b, a % b); }
 
 template <int H_, int R_, int STAGES_>
 struct FastCfg {
     static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_;
     static constexpr int DH = 128;
-    static constexpr int NCW = 8, NC = NCW * 32, NT = NC;
-    static constexpr int MT = H / 16;        // m16 tiles of heads
-    static constexpr int NB = TS / 8;        // n8 blocks of rows in the score mma
-    static constexpr int RC = R / 8;         // 16-byte chunks in one private row
-    static constexpr int S_BOX = TS * 128;   // one 64-column half of a 16-row S tile
-    static constexpr int S_BYTES = 2 * S_BOX;
-    static constexpr int R_BYTES = TS * H * R * 2;
-    static constexpr int OFF_SK = 0, OFF_SV = S_BYTES, OFF_RK = 2 * S_BYTES,
-                         OFF_RV = 2 * S_BYTES + R_BYTES;
-    static constexpr int STAGE = 2 * S_BYTES + 2 * R_BYTES;
-    static constexpr int PAIRS = TS * H / NC;  // (row, head) pairs per thread per tile
-    static constexpr int HPT = NC / H;         // threads sharing one head
-    static constexpr int PST = TS + 8;         // padded row of the bf16 weight tile
-    static constexpr int DISTINCT = 8 / cgcd(RC, 8);
-    // shared-memory map after the stages
-    static constexpr int OFF_BAR = STAGES * STAGE;
-    static constexpr int OFF_SCS = OFF_BAR + 64;
-    static constexpr int OFF_SCP = OFF_SCS + H * TS * 4;
-    static constexpr int OFF_P32 = OFF_SCP + H * TS * 4;
-    static constexpr int OFF_PB = OFF_P32 + H * TS * 4;
-    static constexpr int OFF_M = OFF_PB + 2 * H * PST * 2;
-    static constexpr int OFF_L = OFF_M + H * 4;
-    static constexpr int OFF_A = OFF_L + H * 4;
-    static constexpr int OFF_RED = OFF_A + H * 4;
-    static constexpr int SMEM = OFF_RED + H * R * 4 + 1024;  // + alignment slack
+    static constexpr int NCW = 8, NT = NCW * 32;
+    static constexpr int HPW = H / NCW;      // heads per warp (2 or 4)
+    static constexpr int NH = HPW / 2;       // head slots per thread
+    static constexpr int RC = R / 8;         // 16-byte chunks per private row
+    static constexpr int BOX = TS * 128;     // one 64-column, 16-row swizzled box
+    static constexpr int NBOX_R = H * R / 64;
+    static constexpr int R_BYTES = NBOX_R * BOX;
+    static constexpr int OFF_SK = 0, OFF_SV = 2 * BOX, OFF_RK = 4 * BOX, OFF_RV = 4 * BOX + R_BYTES;
+    static constexpr int STAGE = 4 * BOX + 2 * R_BYTES;
+    static constexpr int KSP = HPW * R / 16;  // k-steps (and m-tiles) of a warp's private columns
+    static constexpr int OFF_BAR = STAGES * STAGE;   // full[STAGES]
+    static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
+    static constexpr int OFF_OK = OFF_CNT + 64;      // per-stage "page id valid" flags
+    static constexpr int OFF_CUR = OFF_OK + 64;      // issue cursor
+    static constexpr int SMEM = OFF_CUR + 64 + 1024;  // + alignment slack
 
-    static_assert(H % 16 == 0 && NC % H == 0 && (TS * H) % NC == 0, "head mapping");
-    static_assert(R % 8 == 0, "private rows are read in 16-byte chunks");
-    static_assert(STAGE % 1024 == 0 && S_BOX % 1024 == 0, "128B-swizzle tiles need 1 KB alignment");
-    static_assert(MT * NB <= NCW, "score tiles per warp");
+    static_assert(H == 16 || H == 32, "two or four heads per warp");
+    static_assert(R % 8 == 0 && (H * R) % 64 == 0, "private rows tile into 64-column boxes");
+    static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
+    static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct FastParams {
     const __nv_bfloat16 *q;
-    const __nv_bfloat16 *R_K;
-    const __nv_bfloat16 *R_V;
     const int32_t *page_table;
     const int32_t *req_row;
     int max_pages, num_pages, page_size, B;
@@ -77,19 +74,20 @@ struct FastParams {
     int32_t *status;
 };
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+struct FastMaps {
+    CUtensorMap sk, sv, rk, rv;
+};
 
-// Barrier over the 256 consumer threads that also ORs a flag across them.
-__device__ __forceinline__ bool consumer_sync_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{ .reg .pred p, q; setp.ne.u32 q, %1, 0; barrier.cta.red.or.pred p, 1, 256, q; "
-        "selp.u32 %0, 1, 0, p; }"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
+// Copy-issue cursor over the CTA's tile sequence (segments in order, 16-row
+// tiles inside a segment).  Lives in shared memory; only the warp that
+// releases a stage last touches it, and releases happen in tile order.
+struct IssueCursor {
+    int b;
+    int32_t start;
+    int t, t_b;
+    int done, issued;
+    int page_key, page_id;  // last page looked up: (request, page index) -> id
+};
 
 __device__ __forceinline__ int find_request_fast(const int32_t *off, int B, int32_t x) {
     int lo = 0, hi = B - 1;
@@ -101,390 +99,391 @@ __device__ __forceinline__ int find_request_fast(const int32_t *off, int B, int3
     return lo;
 }
 
+__device__ __forceinline__ const int32_t *page_row(const FastParams &P, int b) {
+    return P.page_table + (size_t)(P.req_row ? P.req_row[b] : b) * P.max_pages;
+}
+
+template <class C>
+__device__ __forceinline__ void cursor_begin_segment(IssueCursor *cur, const FastParams &P,
+                                                     int32_t end) {
+    int b = cur->b;
+    while (P.ws.off[b + 1] <= cur->start) ++b;
+    const int32_t base = P.ws.off[b];
+    cur->b = b;
+    cur->t = (cur->start - base) / C::TS * C::TS;
+    cur->t_b = min(end, P.ws.off[b + 1]) - base;
+}
+
+// Issue the copies of the cursor's next tile into its stage.
+template <class C>
+__device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
+                           uint8_t *smem, uint64_t *full, int *okf, int32_t end) {
+    if (cur->done) return;
+    const int it = cur->issued;
+    const int s = it % C::STAGES;
+    // one page-table read per page (a page holds several 16-row tiles); the
+    // next page's entry is prefetched into L2 when its first tile is near
+    const int pidx = cur->t / P.page_size;
+    const int key = cur->b * P.max_pages + pidx;
+    int32_t page;
+    if (key == cur->page_key) {
+        page = cur->page_id;
+    } else {
+        const int32_t *row_pt = page_row(P, cur->b);
+        page = row_pt[pidx];
+        cur->page_key = key;
+        cur->page_id = page;
+        if (pidx + 1 < P.max_pages)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row_pt + pidx + 1));
+    }
+    const bool ok = page >= 0 && page < P.num_pages;
+    if (!ok) {
+        status_or(P.status, LRKV_STATUS_BAD_PAGE);
+        page = 0;  // consumers mask the tile
+    }
+    okf[s] = ok;  // published to the consumers by the mbarrier phase
+    const int row = page * P.page_size + cur->t % P.page_size;
+    uint8_t *st = smem + s * C::STAGE;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&full[s], C::STAGE);
+    // each map is 3-D (64 columns, rows, 64-column block) with a box of
+    // 64 x 16 x all blocks, so one copy lands the whole 16-row tile as
+    // consecutive 16-row x 128-byte swizzled boxes
+    // the cache streams through once per step: evict it from L2 first
+    const uint64_t pol = l2_evict_first_policy();
+    tma_load_3d_hint(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s], pol);
+    tma_load_3d_hint(st + C::OFF_SV, &M.sv, 0, row, 0, &full[s], pol);
+    tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, 0, &full[s], pol);
+    tma_load_3d_hint(st + C::OFF_RV, &M.rv, 0, row, 0, &full[s], pol);
+    cur->issued = it + 1;
+    cur->t += C::TS;
+    if (cur->t >= cur->t_b) {
+        cur->start = P.ws.off[cur->b] + cur->t_b;
+        if (cur->start >= end) cur->done = 1;
+        else cursor_begin_segment<C>(cur, P, end);
+    }
+}
+
+// The running maximum (log2 units) only moves when a tile exceeds it by this
+// much; weights stay below 2^kLazyMax, far inside fp32 range.
+constexpr float kLazyMax = 8.f;
+
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
 }
 
-// Walks the CTA's tile sequence (segments in order, 16-row tiles within a
-// segment) ahead of the consumers and issues each tile's copies.  Only thread 0
-// uses it.
-template <class C>
-struct TileIssuer {
-    int b;
-    int32_t start, end;
-    int t, t_b;
-    const int32_t *pt;
-    bool done;
-
-    __device__ void begin_segment(const FastParams &P) {
-        while (P.ws.off[b + 1] <= start) ++b;
-        const int32_t base = P.ws.off[b];
-        const int32_t seg_end = min(end, P.ws.off[b + 1]);
-        t = (start - base) / C::TS * C::TS;
-        t_b = seg_end - base;
-        pt = P.page_table + (size_t)(P.req_row ? P.req_row[b] : b) * P.max_pages;
-    }
-
-    __device__ void init(const FastParams &P, int b0, int32_t s0, int32_t e) {
-        b = b0;
-        start = s0;
-        end = e;
-        done = start >= end;
-        if (!done) begin_segment(P);
-    }
-
-    // Issue the next tile into `stage`; returns false once the sequence is over.
-    __device__ bool issue(const FastParams &P, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                          uint8_t *smem, uint64_t *full, int stage) {
-        if (done) return false;
-        int32_t page = pt[t / P.page_size];
-        if (page < 0 || page >= P.num_pages) page = 0;  // consumers mask the tile
-        const int row = page * P.page_size + t % P.page_size;
-        uint8_t *st = smem + stage * C::STAGE;
-        mbar_arrive_expect_tx(&full[stage], C::STAGE);
-        tma_load_2d(st + C::OFF_SK, tmK, 0, row, &full[stage]);
-        tma_load_2d(st + C::OFF_SK + C::S_BOX, tmK, 64, row, &full[stage]);
-        tma_load_2d(st + C::OFF_SV, tmV, 0, row, &full[stage]);
-        tma_load_2d(st + C::OFF_SV + C::S_BOX, tmV, 64, row, &full[stage]);
-        const size_t roff = (size_t)row * C::H * C::R;
-        bulk_load(st + C::OFF_RK, P.R_K + roff, C::R_BYTES, &full[stage]);
-        bulk_load(st + C::OFF_RV, P.R_V + roff, C::R_BYTES, &full[stage]);
-        t += C::TS;
-        if (t >= t_b) {  // next segment
-            start = P.ws.off[b] + t_b;
-            if (start >= end) done = true;
-            else begin_segment(P);
-        }
-        return true;
-    }
-};
+// Byte offset, inside a stage region made of 64-column swizzled boxes, of the
+// 16-byte chunk `cc` (counted along the row) of tile row `j`.
+__device__ __forceinline__ uint32_t box_chunk(int j, int cc) {
+    return (uint32_t)((cc >> 3) * (16 * 128)) + swz128(j, cc & 7);
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::NT, 1)
-    decode_split_fast_kernel(const __grid_constant__ CUtensorMap tmK,
-                             const __grid_constant__ CUtensorMap tmV, const FastParams P) {
+    decode_split_fast_kernel(const __grid_constant__ FastMaps M, const FastParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    float *sc_sh = reinterpret_cast<float *>(smem + C::OFF_SCS);
-    float *sc_pr = reinterpret_cast<float *>(smem + C::OFF_SCP);
-    float *p32 = reinterpret_cast<float *>(smem + C::OFF_P32);
-    __nv_bfloat16 *pb = reinterpret_cast<__nv_bfloat16 *>(smem + C::OFF_PB);
-    float *m_s = reinterpret_cast<float *>(smem + C::OFF_M);
-    float *l_s = reinterpret_cast<float *>(smem + C::OFF_L);
-    float *a_s = reinterpret_cast<float *>(smem + C::OFF_A);
-    float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
+    int *cnt = reinterpret_cast<int *>(smem + C::OFF_CNT);
+    int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
+    IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x;
     const DecodeWs &ws = P.ws;
 
+    pdl_wait();  // the plan and private queries come from the prologue kernel
+    pdl_launch_dependents();
     const int32_t total = ws.plan->total, chunk = ws.plan->chunk;
     const int32_t start0 = g * chunk;
     const int32_t end = min(total, start0 + chunk);
     if (start0 >= end) return;
     const int b0 = find_request_fast(ws.off, P.B, start0);
 
-    // Thread 0 owns the barriers and the copy issue; it fills every stage up
-    // front and then refills stage (k-1) % STAGES once the consumer barrier
-    // after tile k's scores proves all warps are done with tile k-1.
-    TileIssuer<C> issuer;
-    uint32_t issued = 0;
     if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            cnt[s] = 0;
+        }
         fence_barrier_init();
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
-        issuer.init(P, b0, start0, end);
-        for (int s = 0; s < C::STAGES; ++s)
-            if (issuer.issue(P, &tmK, &tmV, smem, full, s)) ++issued;
+        prefetch_tensormap(&M.sk);
+        prefetch_tensormap(&M.sv);
+        prefetch_tensormap(&M.rk);
+        prefetch_tensormap(&M.rv);
+        cur->b = b0;
+        cur->start = start0;
+        cur->done = 0;
+        cur->issued = 0;
+        cur->page_key = -1;
+        cur->page_id = 0;
+        cursor_begin_segment<C>(cur, P, end);
+        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, smem, full, okf, end);
     }
     __syncthreads();
-    const int ps = P.page_size;
 
-    // ------------------------------------------------------------------ consumers
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
-    const int h_pr = tid % C::H;              // head of this thread's private work
-    const int jj0 = tid / C::H;
-    const int rot = ((tid & 7) / C::DISTINCT) % C::RC;  // bank-conflict-free chunk order
-    const bool score_warp = warp < C::MT * C::NB;
-    const int mt_s = warp / C::NB, nb_s = warp % C::NB;
+    const int hl = lane >> 4, j = lane & 15;  // this lane's (head slot, tile row)
+    int hd[C::NH];                            // heads of this lane's slots
+#pragma unroll
+    for (int i = 0; i < C::NH; ++i) hd[i] = warp * C::HPW + hl + 2 * i;
 
-    float p_rot[C::R];
-    float accR[C::R];
-    float accS[C::MT][2][4];
-    uint32_t qf[8][4];
+    float accS[8][4], accR[C::KSP][4];
+    float m[C::NH], l[C::NH];
+    uint32_t qb[8][2];            // Q^T fragments (shared scores)
+    uint32_t pbh[C::KSP][2], pbl[C::KSP][2];  // blockdiag(p)^T fragments, hi and lo halves
+    bool timed_out = false;
 
     uint32_t it = 0;
     int b = b0;
     int32_t start = start0;
-    while (start < end) {
+    while (start < end && !timed_out) {
         while (ws.off[b + 1] <= start) ++b;
         const int32_t base = ws.off[b];
         const int32_t seg_end = min(end, ws.off[b + 1]);
         const int t_a = start - base, t_b = seg_end - base;
-        const int32_t *pt = P.page_table + (size_t)(P.req_row ? P.req_row[b] : b) * P.max_pages;
 
-        // -------- segment set-up
-        if (tid < C::H) {
-            m_s[tid] = -INFINITY;
-            l_s[tid] = 0.f;
+        // -------- segment set-up: query fragments, private-query fragments, state
+#pragma unroll
+        for (int i = 0; i < C::NH; ++i) {
+            m[i] = -INFINITY;
+            l[i] = 0.f;
         }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accS[mt][e] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < C::KSP; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accR[mt][e] = 0.f;
         {
-            const float *pp = ws.p + ((size_t)b * C::H + h_pr) * C::R;
-#pragma unroll
-            for (int c = 0; c < C::RC; ++c) {
-                int ch = c + rot;
-                if (ch >= C::RC) ch -= C::RC;
-                const float4 v0 = *reinterpret_cast<const float4 *>(pp + ch * 8);
-                const float4 v1 = *reinterpret_cast<const float4 *>(pp + ch * 8 + 4);
-                p_rot[c * 8 + 0] = v0.x; p_rot[c * 8 + 1] = v0.y;
-                p_rot[c * 8 + 2] = v0.z; p_rot[c * 8 + 3] = v0.w;
-                p_rot[c * 8 + 4] = v1.x; p_rot[c * 8 + 5] = v1.y;
-                p_rot[c * 8 + 6] = v1.z; p_rot[c * 8 + 7] = v1.w;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < C::R; ++k) accR[k] = 0.f;
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accS[mt][n][e] = 0.f;
-        if (score_warp) {
-            const __nv_bfloat16 *q0 = P.q + ((size_t)b * C::H + mt_s * 16 + gq) * C::DH + 2 * tq;
-            const __nv_bfloat16 *q8 = q0 + 8 * C::DH;
+            // B fragments of Q^T: column n = head warp*HPW + n (n < HPW), else 0
+            const bool own = gq < C::HPW;
+            const __nv_bfloat16 *qrow = P.q + ((size_t)b * C::H + warp * C::HPW + (own ? gq : 0)) * C::DH;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                qf[ks][0] = ld_u32(q0 + ks * 16);
-                qf[ks][1] = ld_u32(q8 + ks * 16);
-                qf[ks][2] = ld_u32(q0 + ks * 16 + 8);
-                qf[ks][3] = ld_u32(q8 + ks * 16 + 8);
+                qb[ks][0] = own ? ld_u32(qrow + ks * 16 + 2 * tq) : 0u;
+                qb[ks][1] = own ? ld_u32(qrow + ks * 16 + 2 * tq + 8) : 0u;
+            }
+            // B fragments of blockdiag(p)^T over the warp's HPW*R private
+            // columns: entry (k, n) is p[head n][k - n R] when k falls in head
+            // n's columns, else 0
+            const float *pw = ws.p + ((size_t)b * C::H + warp * C::HPW) * C::R;
+#pragma unroll
+            for (int ks = 0; ks < C::KSP; ++ks) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = ks * 16 + 2 * tq + (e & 1) + (e >> 1) * 8;
+                    v[e] = (own && k / C::R == gq) ? pw[k] : 0.f;  // pw[k] = p[head k/R][k%R]
+                }
+                float hv[4], lv[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    hv[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+                    lv[e] = v[e] - hv[e];
+                }
+                pbh[ks][0] = pack_bf16(hv[0], hv[1]);
+                pbh[ks][1] = pack_bf16(hv[2], hv[3]);
+                pbl[ks][0] = pack_bf16(lv[0], lv[1]);
+                pbl[ks][1] = pack_bf16(lv[2], lv[3]);
             }
         }
 
         // -------- stream the segment's tiles
         for (int t = t_a / C::TS * C::TS; t < t_b; t += C::TS, ++it) {
             const int s = it % C::STAGES;
-            const bool got = mbar_wait(&full[s], (it / C::STAGES) & 1);
-            const int32_t page = pt[t / ps];
-            const bool page_ok = page >= 0 && page < P.num_pages;
-            if (!page_ok && tid == 0) status_or(P.status, LRKV_STATUS_BAD_PAGE);
-            const uint8_t *st = smem + s * C::STAGE;
+            if (!mbar_wait(&full[s], (it / C::STAGES) & 1)) {
+                if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
+                timed_out = true;
+                break;
+            }
+            const bool page_ok = okf[s] != 0;
             const bool partial = !page_ok || t < t_a || t + C::TS > t_b;
+            const bool valid = page_ok && t + j >= t_a && t + j < t_b;
+            const uint8_t *st = smem + s * C::STAGE;
+            const int mi = lane >> 3;
 
-            if (got && partial) {
-                // zero the S_V rows that are not visible so 0-weight x garbage
-                // cannot reach the tensor-core accumulation
-                const int row = tid >> 4, ch = tid & 15;
-                const int tok = t + row;
-                if (!(page_ok && tok >= t_a && tok < t_b)) {
-                    uint8_t *dst = const_cast<uint8_t *>(st) + C::OFF_SV + (ch >> 3) * C::S_BOX +
-                                   row * 128 + (ch & 7) * 16;
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                }
-            }
-
-            // A1: shared scores on tensor cores
-            if (got && score_warp) {
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
+            // scores: D[row x head] = S_K . Q^T + R_K(warp columns) . blockdiag(p)^T
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            {
                 const uint32_t skb = smem_u32(st + C::OFF_SK);
-                const int mi = lane >> 3, rr = lane & 7;
-                const int tok = nb_s * 8 + rr;
+                const uint32_t rkb = smem_u32(st + C::OFF_RK);
+                const int rr = (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                    const int ch = 4 * k2 + mi;
-                    uint32_t b0r, b1r, b2r, b3r;
-                    ldmatrix_x4(skb + (ch >> 3) * C::S_BOX + swz128(tok, ch & 7), b0r, b1r, b2r, b3r);
-                    mma_bf16_16816(c, qf[2 * k2], b0r, b1r);
-                    mma_bf16_16816(c, qf[2 * k2 + 1], b2r, b3r);
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t a[4];
+                    ldmatrix_x4(skb + box_chunk(rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
                 }
-                const int h0 = mt_s * 16 + gq, j0 = nb_s * 8 + 2 * tq;
-                *reinterpret_cast<float2 *>(&sc_sh[h0 * C::TS + j0]) = make_float2(c[0], c[1]);
-                *reinterpret_cast<float2 *>(&sc_sh[(h0 + 8) * C::TS + j0]) = make_float2(c[2], c[3]);
+                const int cw = warp * (C::HPW * C::R / 8);  // first 16-byte chunk of the warp's columns
+#pragma unroll
+                for (int ks = 0; ks < C::KSP; ++ks) {
+                    uint32_t a[4];
+                    ldmatrix_x4(rkb + box_chunk(rr, cw + 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    mma_bf16_16816(c, a, pbh[ks][0], pbh[ks][1]);
+                    mma_bf16_16816(c, a, pbl[ks][0], pbl[ks][1]);
+                }
             }
-            // A2: private scores p_h . R_K[h, j]
+
+            // softmax per (head slot, row) lane; lazy reference maximum
+            float pe[C::NH], al[C::NH];
+            bool rescale = false;
 #pragma unroll
-            for (int i = 0; i < C::PAIRS; ++i) {
-                const int j = jj0 + i * C::HPT;
-                const int tok = t + j;
-                float acc = 0.f;
-                if (got && page_ok && tok >= t_a && tok < t_b) {
-                    const uint8_t *rk = st + C::OFF_RK + (j * C::H + h_pr) * (C::R * 2);
+            for (int i = 0; i < C::NH; ++i) {
+                // D[row j][head n = hl + 2i] sits in lane (j % 8) * 4 + i, register hl + 2 (j / 8)
+                const int src = (j & 7) * 4 + i;
+                const float v0 = __shfl_sync(0xffffffffu, c[0], src);
+                const float v1 = __shfl_sync(0xffffffffu, c[1], src);
+                const float v2 = __shfl_sync(0xffffffffu, c[2], src);
+                const float v3 = __shfl_sync(0xffffffffu, c[3], src);
+                const float lo = hl ? v1 : v0, hi = hl ? v3 : v2;
+                const float sc = valid ? ((j < 8) ? lo : hi) * P.scale_log2 : -INFINITY;
+                float mx = sc;
 #pragma unroll
-                    for (int c = 0; c < C::RC; ++c) {
-                        int ch = c + rot;
-                        if (ch >= C::RC) ch -= C::RC;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(rk + ch * 16);
-                        acc = fmaf(p_rot[c * 8 + 0], bf16lo(v.x), acc);
-                        acc = fmaf(p_rot[c * 8 + 1], bf16hi(v.x), acc);
-                        acc = fmaf(p_rot[c * 8 + 2], bf16lo(v.y), acc);
-                        acc = fmaf(p_rot[c * 8 + 3], bf16hi(v.y), acc);
-                        acc = fmaf(p_rot[c * 8 + 4], bf16lo(v.z), acc);
-                        acc = fmaf(p_rot[c * 8 + 5], bf16hi(v.z), acc);
-                        acc = fmaf(p_rot[c * 8 + 6], bf16lo(v.w), acc);
-                        acc = fmaf(p_rot[c * 8 + 7], bf16hi(v.w), acc);
+                for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float m_old = m[i];
+                const float m_new = (mx > m_old + kLazyMax) ? mx : m_old;
+                const float alpha = (m_new == m_old) ? 1.f : exp2f(m_old - m_new);
+                const float e = (valid && m_new != -INFINITY) ? exp2f(sc - m_new) : 0.f;
+                float sum = e;
+#pragma unroll
+                for (int o = 8; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                l[i] = l[i] * alpha + sum;
+                m[i] = m_new;
+                pe[i] = e;
+                al[i] = alpha;
+                rescale |= alpha != 1.f;
+            }
+
+            // values: accS += S_V^T . P^T, accR += R_V^T(warp columns) . P^T
+            {
+                // B fragment: column n = gq (< HPW) holds P of head slot (n & 1, n >> 1)
+                // at rows 2tq, 2tq+1 and 2tq+8, 2tq+9
+                const int sl = (gq & 1) * 16 + 2 * tq;
+                float w0 = 0.f, w1 = 0.f, w8 = 0.f, w9 = 0.f;
+#pragma unroll
+                for (int i = 0; i < C::NH; ++i) {
+                    const float x0 = __shfl_sync(0xffffffffu, pe[i], sl);
+                    const float x1 = __shfl_sync(0xffffffffu, pe[i], sl + 1);
+                    const float x8 = __shfl_sync(0xffffffffu, pe[i], sl + 8);
+                    const float x9 = __shfl_sync(0xffffffffu, pe[i], sl + 9);
+                    if ((gq >> 1) == i) { w0 = x0; w1 = x1; w8 = x8; w9 = x9; }
+                }
+                if (gq >= C::HPW) w0 = w1 = w8 = w9 = 0.f;
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(w0), h1 = __float2bfloat16_rn(w1);
+                const __nv_bfloat16 h8 = __float2bfloat16_rn(w8), h9 = __float2bfloat16_rn(w9);
+                const uint32_t bh0 = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
+                const uint32_t bh1 = pack_bf16(__bfloat162float(h8), __bfloat162float(h9));
+                const uint32_t bl0 = pack_bf16(w0 - __bfloat162float(h0), w1 - __bfloat162float(h1));
+                const uint32_t bl1 = pack_bf16(w8 - __bfloat162float(h8), w9 - __bfloat162float(h9));
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // factors of columns 2tq and 2tq+1 (head slot tq of lanes 0 and 16)
+                    float a0 = 1.f, a1 = 1.f;
+#pragma unroll
+                    for (int i = 0; i < C::NH; ++i) {
+                        const float y0 = __shfl_sync(0xffffffffu, al[i], 0);
+                        const float y1 = __shfl_sync(0xffffffffu, al[i], 16);
+                        if (tq == i) { a0 = y0; a1 = y1; }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        accS[mt][0] *= a0; accS[mt][1] *= a1;
+                        accS[mt][2] *= a0; accS[mt][3] *= a1;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < C::KSP; ++mt) {
+                        accR[mt][0] *= a0; accR[mt][1] *= a1;
+                        accR[mt][2] *= a0; accR[mt][3] *= a1;
                     }
                 }
-                sc_pr[h_pr * C::TS + j] = acc;
-            }
-            if (consumer_sync_or(!got)) {
-                if (tid == 0) {
-                    status_or(P.status, LRKV_STATUS_TIMEOUT);
-                    // never leave with copies in flight into this CTA's shared memory
-                    for (uint32_t k = it + 1; k < issued; ++k)
-                        mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
+                uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+                if (partial) {
+                    auto ok = [&](int r) { return page_ok && t + r >= t_a && t + r < t_b; };
+                    m01 = (ok(2 * tq) ? 0x0000ffffu : 0u) | (ok(2 * tq + 1) ? 0xffff0000u : 0u);
+                    m89 = (ok(2 * tq + 8) ? 0x0000ffffu : 0u) | (ok(2 * tq + 9) ? 0xffff0000u : 0u);
                 }
-                return;
-            }
-            // every warp has finished tile it-1: refill its stage
-            if (tid == 0 && it > 0 && issuer.issue(P, &tmK, &tmV, smem, full, (it - 1) % C::STAGES))
-                ++issued;
-
-            // B: merged score, online softmax per head (16 lanes per head)
-#pragma unroll
-            for (int i = 0; i < C::PAIRS; ++i) {
-                const int e = tid + i * C::NC;
-                const int h = e / C::TS, j = e % C::TS;
-                const int tok = t + j;
-                const bool v = page_ok && tok >= t_a && tok < t_b;
-                const float sv = v ? (sc_sh[h * C::TS + j] + sc_pr[h * C::TS + j]) * P.scale_log2
-                                   : -INFINITY;
-                float mx = sv;
-#pragma unroll
-                for (int o = C::TS / 2; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float m_old = m_s[h];
-                const float m_new = fmaxf(m_old, mx);
-                float alpha = 1.f, pe = 0.f;
-                if (m_new != -INFINITY) {
-                    alpha = exp2f(m_old - m_new);
-                    pe = v ? exp2f(sv - m_new) : 0.f;
-                }
-                float sum = pe;
-#pragma unroll
-                for (int o = C::TS / 2; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                p32[h * C::TS + j] = pe;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(pe);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(pe - __bfloat162float(hi));
-                pb[h * C::PST + j] = hi;
-                pb[C::H * C::PST + h * C::PST + j] = lo;
-                if (j == 0) {
-                    m_s[h] = m_new;
-                    l_s[h] = l_s[h] * alpha + sum;
-                    a_s[h] = alpha;
-                }
-            }
-            consumer_sync();
-
-            // C1: shared value accumulation on tensor cores
-            {
+                const int rr = (mi >> 1) * 8 + (lane & 7);
                 const uint32_t svb = smem_u32(st + C::OFF_SV);
-                const int mi = lane >> 3, rr = lane & 7;
-                const int tok = (mi & 1) * 8 + rr;
-                const int ch = 2 * warp + (mi >> 1);
-                uint32_t b00, b01, b10, b11;
-                ldmatrix_x4_trans(svb + (ch >> 3) * C::S_BOX + swz128(tok, ch & 7), b00, b01, b10, b11);
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                    const int h0 = mt * 16 + gq;
-                    const float al0 = a_s[h0], al8 = a_s[h0 + 8];
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(svb + box_chunk(rr, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+                    mma_bf16_16816(accS[mt], a, bh0, bh1);
+                    mma_bf16_16816(accS[mt], a, bl0, bl1);
+                }
+                const uint32_t rvb = smem_u32(st + C::OFF_RV);
+                const int cw = warp * (C::HPW * C::R / 8);
 #pragma unroll
-                    for (int n = 0; n < 2; ++n) {
-                        accS[mt][n][0] *= al0; accS[mt][n][1] *= al0;
-                        accS[mt][n][2] *= al8; accS[mt][n][3] *= al8;
-                    }
-                    uint32_t ah[4], alw[4];
-                    const __nv_bfloat16 *ph = pb + h0 * C::PST + 2 * tq;
-                    const __nv_bfloat16 *pl = ph + C::H * C::PST;
-                    ah[0] = ld_u32(ph);                 ah[1] = ld_u32(ph + 8 * C::PST);
-                    ah[2] = ld_u32(ph + 8);             ah[3] = ld_u32(ph + 8 * C::PST + 8);
-                    alw[0] = ld_u32(pl);                alw[1] = ld_u32(pl + 8 * C::PST);
-                    alw[2] = ld_u32(pl + 8);            alw[3] = ld_u32(pl + 8 * C::PST + 8);
-                    mma_bf16_16816(accS[mt][0], ah, b00, b01);
-                    mma_bf16_16816(accS[mt][0], alw, b00, b01);
-                    mma_bf16_16816(accS[mt][1], ah, b10, b11);
-                    mma_bf16_16816(accS[mt][1], alw, b10, b11);
+                for (int mt = 0; mt < C::KSP; ++mt) {
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(rvb + box_chunk(rr, cw + 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+                    mma_bf16_16816(accR[mt], a, bh0, bh1);
+                    mma_bf16_16816(accR[mt], a, bl0, bl1);
                 }
             }
-            // C2: private value accumulation a . R_V[h]
-            {
-                const float al = a_s[h_pr];
-#pragma unroll
-                for (int k = 0; k < C::R; ++k) accR[k] *= al;
-#pragma unroll
-                for (int i = 0; i < C::PAIRS; ++i) {
-                    const int j = jj0 + i * C::HPT;
-                    const int tok = t + j;
-                    if (page_ok && tok >= t_a && tok < t_b) {
-                        const float pj = p32[h_pr * C::TS + j];
-                        const uint8_t *rv = st + C::OFF_RV + (j * C::H + h_pr) * (C::R * 2);
-#pragma unroll
-                        for (int c = 0; c < C::RC; ++c) {
-                            int ch = c + rot;
-                            if (ch >= C::RC) ch -= C::RC;
-                            const uint4 v = *reinterpret_cast<const uint4 *>(rv + ch * 16);
-                            accR[c * 8 + 0] = fmaf(pj, bf16lo(v.x), accR[c * 8 + 0]);
-                            accR[c * 8 + 1] = fmaf(pj, bf16hi(v.x), accR[c * 8 + 1]);
-                            accR[c * 8 + 2] = fmaf(pj, bf16lo(v.y), accR[c * 8 + 2]);
-                            accR[c * 8 + 3] = fmaf(pj, bf16hi(v.y), accR[c * 8 + 3]);
-                            accR[c * 8 + 4] = fmaf(pj, bf16lo(v.z), accR[c * 8 + 4]);
-                            accR[c * 8 + 5] = fmaf(pj, bf16hi(v.z), accR[c * 8 + 5]);
-                            accR[c * 8 + 6] = fmaf(pj, bf16lo(v.w), accR[c * 8 + 6]);
-                            accR[c * 8 + 7] = fmaf(pj, bf16hi(v.w), accR[c * 8 + 7]);
-                        }
-                    }
-                }
-            }
-        }
 
-        // -------- segment end: write the partial state of slot b + g
-        consumer_sync();
+            // release the stage; the last warp out refills it
+            __syncwarp();
+            if (lane == 0) {
+                int prev;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;"
+                             : "=r"(prev)
+                             : "r"(smem_u32(&cnt[s]))
+                             : "memory");
+                if (prev == C::NCW - 1) {
+                    cnt[s] = 0;
+                    issue_next<C>(cur, P, M, smem, full, okf, end);
+                }
+            }
+            __syncwarp();
+        }
+        if (timed_out) break;
+
+        // -------- segment end: this warp's heads of partial slot b + g
         const size_t slot = (size_t)b + g;
         const size_t W = C::DH + C::R;
-        if (tid < C::H) {
-            ws.ml[(slot * C::H + tid) * 2 + 0] = m_s[tid];
-            ws.ml[(slot * C::H + tid) * 2 + 1] = l_s[tid];
-        }
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt)
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const int h0 = mt * 16 + gq;
-                const int d = 16 * warp + 8 * n + 2 * tq;
-                *reinterpret_cast<float2 *>(&ws.acc[(slot * C::H + h0) * W + d]) =
-                    make_float2(accS[mt][n][0], accS[mt][n][1]);
-                *reinterpret_cast<float2 *>(&ws.acc[(slot * C::H + h0 + 8) * W + d]) =
-                    make_float2(accS[mt][n][2], accS[mt][n][3]);
+        for (int i = 0; i < C::NH; ++i) {
+            if (j == 0) {
+                ws.ml[(slot * C::H + hd[i]) * 2 + 0] = m[i];
+                ws.ml[(slot * C::H + hd[i]) * 2 + 1] = l[i];
             }
-        // private accumulators: threads sharing a head are summed in a fixed order
-        if (C::H == 16) {
-#pragma unroll
-            for (int k = 0; k < C::R; ++k) accR[k] += __shfl_xor_sync(0xffffffffu, accR[k], 16);
         }
-        for (int w = 0; w < C::NCW; ++w) {
-            if (warp == w && lane < C::H) {
+        if (2 * tq < C::HPW) {
+            const int h0 = warp * C::HPW + 2 * tq;
 #pragma unroll
-                for (int c = 0; c < C::RC; ++c) {
-                    int ch = c + rot;
-                    if (ch >= C::RC) ch -= C::RC;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        float *dst = &red[h_pr * C::R + ch * 8 + e];
-                        *dst = (w == 0) ? accR[c * 8 + e] : *dst + accR[c * 8 + e];
-                    }
-                }
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d = mt * 16 + gq;
+                ws.acc[(slot * C::H + h0) * W + d] = accS[mt][0];
+                ws.acc[(slot * C::H + h0 + 1) * W + d] = accS[mt][1];
+                ws.acc[(slot * C::H + h0) * W + d + 8] = accS[mt][2];
+                ws.acc[(slot * C::H + h0 + 1) * W + d + 8] = accS[mt][3];
             }
-            consumer_sync();
         }
-        for (int i = tid; i < C::H * C::R; i += C::NC) {
-            const int h = i / C::R, k = i % C::R;
-            ws.acc[(slot * C::H + h) * W + C::DH + k] = red[i];
-        }
-        consumer_sync();
+        // private reduction: accumulator row mm (a private column of the
+        // warp) is useful in column n = mm / R (its own head)
+#pragma unroll
+        for (int mt = 0; mt < C::KSP; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int mm = mt * 16 + gq + (e >> 1) * 8;
+                const int n = 2 * tq + (e & 1);
+                if (n < C::HPW && mm / C::R == n)
+                    ws.acc[(slot * C::H + warp * C::HPW + n) * W + C::DH + (mm - n * C::R)] = accR[mt][e];
+            }
         start = seg_end;
+    }
+
+    // Never leave with copies in flight into this CTA's shared memory (only
+    // possible after a timeout: normally every issued tile was consumed).
+    __syncthreads();
+    if (tid == 0) {
+        const int issued = cur->issued;
+        for (int k = (int)it; k < issued; ++k) mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
     }
 }
 
@@ -511,16 +510,18 @@ static EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// 2-D map over an S pool viewed as [rows, 128] bf16; box = 16 rows x 64 columns,
-// 128-byte swizzle (matches swz128 on the device side).
-static bool make_s_map(CUtensorMap *map, const void *pool, int64_t rows) {
+// Map over a pool viewed as [rows, cols] bf16, as three dimensions
+// (64 columns, rows, cols / 64 blocks of columns) with strides (2 B, cols*2 B,
+// 128 B).  A box of 64 x 16 x (cols/64) with 128-byte swizzle lands a 16-row
+// tile as cols/64 consecutive 16-row x 128-byte boxes (matches box_chunk).
+static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
-    cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {128 * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    cuuint32_t box[3] = {64, 16, (cuuint32_t)(cols / 64)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -540,9 +541,10 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     using C = typename Pick<H, R>::Cfg;
     static_assert(Pick<H, R>::STAGES >= 2, "at least double buffering");
     const auto &c = a.cache;
-    CUtensorMap mk, mv;
+    FastMaps maps;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    if (!make_s_map(&mk, c.S_K, rows) || !make_s_map(&mv, c.S_V, rows))
+    if (!make_map(&maps.sk, c.S_K, rows, 128) || !make_map(&maps.sv, c.S_V, rows, 128) ||
+        !make_map(&maps.rk, c.R_K, rows, H * R) || !make_map(&maps.rv, c.R_V, rows, H * R))
         return cudaErrorInvalidValue;
     auto kern = decode_split_fast_kernel<C>;
     static bool attr_set = false;
@@ -553,8 +555,6 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     }
     FastParams P;
     P.q = static_cast<const __nv_bfloat16 *>(a.q);
-    P.R_K = static_cast<const __nv_bfloat16 *>(c.R_K);
-    P.R_V = static_cast<const __nv_bfloat16 *>(c.R_V);
     P.page_table = a.page_table;
     P.req_row = a.req_row;
     P.max_pages = a.max_pages;
@@ -564,8 +564,7 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     P.scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     P.ws = ws;
     P.status = a.status;
-    kern<<<G, C::NT, C::SMEM, a.stream>>>(mk, mv, P);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(G), dim3(C::NT), C::SMEM, a.stream, maps, P);
 }
 
 #define LRKV_FAST_SHAPES(X) X(16, 16) X(16, 32) X(16, 48) X(16, 56) X(16, 64) X(32, 16) X(32, 32)

@@ -12,17 +12,47 @@
 namespace lrkv {
 
 // ---------------------------------------------------------------------------
-// Prologue: blocks [0, B*H) form p[b,h,:] = q[b,h,:] B_K[h]; the last block
-// validates sequence lengths and writes the balanced plan (row offsets and
-// the per-CTA chunk).
+// Prologue: block (x = h < H, y) forms p[b, h, :] = q[b, h, :] B_K[h] for the
+// requests b of row group y, with B_K[h] staged in shared memory; block
+// (x = H, y = 0) validates sequence lengths and writes the balanced plan (row
+// offsets and rows per CTA).
 // ---------------------------------------------------------------------------
+constexpr int kProRows = 8;  // requests per prologue block
+constexpr size_t kStageFloats = 40 * 1024;  // largest B_K / B_V head staged in shared memory
+
 template <typename T>
 __global__ void __launch_bounds__(256) decode_prologue_kernel(
     const T *__restrict__ q, const T *__restrict__ B_K, const int32_t *__restrict__ seq_lens,
-    int B, int H, int d_h, int r, int max_len, int G, int tile_align, DecodeWs ws,
+    T *__restrict__ out,
+    int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, DecodeWs ws,
     int32_t *status) {
     const int tid = threadIdx.x;
-    if (blockIdx.x == (unsigned)(B * H)) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == (unsigned)H) {
+        // completion counters of this row group's requests start at zero, and
+        // requests with an invalid length get a zero output (no segment
+        // will ever write it)
+        for (int i = tid; i < kProRows * kHeadGroups; i += blockDim.x) {
+            const int b = blockIdx.y * kProRows + i / kHeadGroups;
+            if (b < B) ws.done[(size_t)b * kHeadGroups + i % kHeadGroups] = 0;
+        }
+        __shared__ int bad_len[kProRows];
+        if (tid < kProRows) {
+            const int b = blockIdx.y * kProRows + tid;
+            int bad = 0;
+            if (b < B) {
+                const int32_t L = seq_lens[b];
+                bad = (L < 1 || L > max_len);
+            }
+            bad_len[tid] = bad;
+        }
+        __syncthreads();
+        for (int bb = 0; bb < kProRows; ++bb)
+            if (bad_len[bb])
+                for (int i = tid; i < H * d_h; i += blockDim.x)
+                    Elem<T>::store(out + (size_t)(blockIdx.y * kProRows + bb) * H * d_h + i, 0.f);
+        if (blockIdx.y != 0) return;
         // --- plan: exclusive scan of validated lengths ---
         __shared__ int32_t part[256];
         const int per = (B + blockDim.x - 1) / blockDim.x;
@@ -35,19 +65,27 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
         }
         part[tid] = s;
         __syncthreads();
-        if (tid == 0) {
-            int32_t run = 0;
-            for (int i = 0; i < (int)blockDim.x; ++i) {
-                int32_t v = part[i];
-                part[i] = run;
-                run += v;
+        if (tid < 32) {  // warp scan of the 256 partial sums (8 per lane)
+            int32_t v[8], run = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { v[i] = part[tid * 8 + i]; run += v[i]; }
+            int32_t incl = run;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
             }
-            ws.plan->total = run;
-            int32_t chunk = (run + G - 1) / G;
-            chunk = max(chunk, tile_align);
-            chunk = (chunk + tile_align - 1) / tile_align * tile_align;
-            ws.plan->chunk = chunk;
-            ws.off[B] = run;
+            int32_t ex = incl - run;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { part[tid * 8 + i] = ex; ex += v[i]; }
+            if (tid == 31) {
+                ws.plan->total = incl;
+                int32_t chunk = (incl + G - 1) / G;
+                chunk = max(chunk, tile_align);
+                chunk = (chunk + tile_align - 1) / tile_align * tile_align;
+                ws.plan->chunk = chunk;
+                ws.off[B] = incl;
+            }
         }
         __syncthreads();
         int32_t run = part[tid];
@@ -64,17 +102,45 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
         if (bad) status_or(status, LRKV_STATUS_BAD_SEQLEN);
         return;
     }
-    // --- private query ---
-    const int b = blockIdx.x / H, h = blockIdx.x % H;
-    extern __shared__ float qs[];
-    const T *qp = q + ((size_t)b * H + h) * d_h;
-    for (int d = tid; d < d_h; d += blockDim.x) qs[d] = Elem<T>::load(qp + d);
+    // --- private queries of up to kProRows requests for head h ---
+    const int h = blockIdx.x, b0 = blockIdx.y * kProRows;
+    const int nb = min(kProRows, B - b0);
+    extern __shared__ float sm[];
+    float *bk = sm;                               // [d_h][r] when staged
+    float *qs = bk + (staged ? d_h * r : 0);      // [kProRows][d_h]
+    const T *src = B_K + (size_t)h * d_h * r;
+    // query rows (one 16-byte vector per thread in flight) overlap the B_K staging
+    constexpr int V = Vec16<T>::N;
+    const int qv_row = d_h / V, nqv = nb * qv_row;
+    float qv[V];
+    const bool has_q = tid < nqv;
+    if (has_q) Vec16<T>::load(q + ((size_t)(b0 + tid / qv_row) * H + h) * d_h + (tid % qv_row) * V, qv);
+    if (staged) stage_f32(bk, src, d_h * r);
+    if (has_q)
+#pragma unroll
+        for (int e = 0; e < V; ++e) qs[tid * V + e] = qv[e];
+    for (int i = tid + blockDim.x; i < nqv; i += blockDim.x) {
+        float v[V];
+        Vec16<T>::load(q + ((size_t)(b0 + i / qv_row) * H + h) * d_h + (i % qv_row) * V, v);
+#pragma unroll
+        for (int e = 0; e < V; ++e) qs[i * V + e] = v[e];
+    }
     __syncthreads();
-    const T *bk = B_K + (size_t)h * d_h * r;
-    for (int k = tid; k < r; k += blockDim.x) {
-        float acc = 0.f;
-        for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], Elem<T>::load(bk + (size_t)d * r + k), acc);
-        ws.p[((size_t)b * H + h) * r + k] = acc;
+    for (int o = tid; o < nb * r; o += blockDim.x) {
+        const int bb = o / r, k = o % r;
+        const float *qq = qs + bb * d_h;
+        float a0 = 0.f, a1 = 0.f;
+        if (staged) {
+            int d = 0;
+            for (; d + 1 < d_h; d += 2) {
+                a0 = fmaf(qq[d], bk[d * r + k], a0);
+                a1 = fmaf(qq[d + 1], bk[(d + 1) * r + k], a1);
+            }
+            if (d < d_h) a0 = fmaf(qq[d], bk[d * r + k], a0);
+        } else {
+            for (int d = 0; d < d_h; ++d) a0 = fmaf(qq[d], Elem<T>::load(src + (size_t)d * r + k), a0);
+        }
+        ws.p[((size_t)(b0 + bb) * H + h) * r + k] = a0 + a1;
     }
 }
 
@@ -111,6 +177,8 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.x, h = blockIdx.y;
+    pdl_wait();
+    pdl_launch_dependents();
     const int32_t total = ws.plan->total, chunk = ws.plan->chunk;
     int32_t start = g * chunk;
     const int32_t end = min(total, start + chunk);
@@ -217,14 +285,21 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Combine: grid (H, B).  Log-sum-exp merge of the request's segments, then
-// out = accS / L + (accR / L) B_V[h]^T  (equation 7, expansion done once).
+// Combine: grid (H, B), one block per (request, head).  Log-sum-exp merge of
+// the request's segments, then out = accS / L + (accR / L) B_V[h]^T
+// (equation 7, expansion done once).  All global reads (B_V[h], the
+// segments' (m, l) and accumulators) are issued before the merge needs them.
 // ---------------------------------------------------------------------------
+constexpr int kCombSeg = 16;  // segments whose partials a thread keeps in flight
+
 template <typename T>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const T *__restrict__ B_V,
+__global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict__ B_V,
                                                              int B, int H, int d_h, int r,
-                                                             DecodeWs ws, T *__restrict__ out) {
-    extern __shared__ float cr[];  // r (normalised private reduction)
+                                                             bool staged, DecodeWs ws,
+                                                             T *__restrict__ out) {
+    extern __shared__ __align__(16) float cs[];
+    pdl_wait();
+    pdl_launch_dependents();
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
     const int32_t o0 = ws.off[b], o1 = ws.off[b + 1];
     T *dst = out + ((size_t)b * H + h) * d_h;
@@ -233,37 +308,106 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const T *__restrict
         return;
     }
     const int32_t chunk = ws.plan->chunk;
-    const int g_lo = o0 / chunk, g_hi = (o1 - 1) / chunk;
-    float M = -INFINITY;
-    for (int g = g_lo; g <= g_hi; ++g) M = fmaxf(M, ws.ml[(((size_t)b + g) * H + h) * 2]);
-    float L = 0.f;
-    for (int g = g_lo; g <= g_hi; ++g) {
-        const float *ml = ws.ml + (((size_t)b + g) * H + h) * 2;
-        if (ml[0] != -INFINITY) L += exp2f(ml[0] - M) * ml[1];
-    }
-    const float invL = (L > 0.f) ? 1.f / L : 0.f;
+    const int g_lo = o0 / chunk, nseg = (o1 - 1) / chunk - g_lo + 1;
     const int W = d_h + r;
-    for (int k = tid; k < r; k += blockDim.x) {
-        float a = 0.f;
-        for (int g = g_lo; g <= g_hi; ++g) {
-            const size_t s = ((size_t)b + g) * H + h;
-            const float m = ws.ml[s * 2];
-            if (m != -INFINITY) a = fmaf(exp2f(m - M), ws.acc[s * W + d_h + k], a);
+    const size_t s0 = ((size_t)b + g_lo) * H + h;  // slot of segment g: s0 + g H
+    T *bv = reinterpret_cast<T *>(cs);                                   // [d_h][r] when staged
+    float *cr = cs + (staged ? ((size_t)d_h * r * sizeof(T) + 15) / 16 * 4 : 0);  // [r]
+    float *w = cr + r;                                                    // [nseg]
+    __shared__ float red[2][8];
+    const int nthr = blockDim.x, nwarp = nthr >> 5;
+    const T *src = B_V + (size_t)h * d_h * r;
+    // 1. B_V[h] as raw 16-byte vectors, the segments' (m, l), first accumulators
+    if (staged) {
+        const int nv = d_h * r * (int)sizeof(T) / 16;
+        const uint4 *s16 = reinterpret_cast<const uint4 *>(src);
+        uint4 *d16 = reinterpret_cast<uint4 *>(bv);
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (tid + u * nthr < nv) v[u] = s16[tid + u * nthr];
+        for (int base = tid; base < nv; base += 4 * nthr) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (base + u * nthr < nv) d16[base + u * nthr] = v[u];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (base + (4 + u) * nthr < nv) v[u] = s16[base + (4 + u) * nthr];
         }
-        cr[k] = a * invL;
     }
+    // this thread's columns: c0 = tid, c1 = tid + blockDim.x (W <= 2 blockDim.x)
+    const int c0 = tid, c1 = tid + nthr;
+    float m_my = -INFINITY, l_my = 0.f;
+    if (tid < nseg) {
+        const float2 ml = *reinterpret_cast<const float2 *>(ws.ml + (s0 + (size_t)tid * H) * 2);
+        m_my = ml.x;
+        l_my = ml.y;
+    }
+    float a0 = 0.f, a1 = 0.f;
+    float v0[kCombSeg], v1[kCombSeg];
+#pragma unroll
+    for (int g = 0; g < kCombSeg; ++g) {
+        v0[g] = (g < nseg && c0 < W) ? ws.acc[(s0 + (size_t)g * H) * W + c0] : 0.f;
+        v1[g] = (g < nseg && c1 < W) ? ws.acc[(s0 + (size_t)g * H) * W + c1] : 0.f;
+    }
+    // 2. merge weights
+    float mx = m_my;
+    for (int k = tid + nthr; k < nseg; k += nthr) mx = fmaxf(mx, ws.ml[(s0 + (size_t)k * H) * 2]);
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((tid & 31) == 0) red[0][tid >> 5] = mx;
     __syncthreads();
-    const T *bv = B_V + (size_t)h * d_h * r;
-    for (int d = tid; d < d_h; d += blockDim.x) {
-        float a = 0.f;
-        for (int g = g_lo; g <= g_hi; ++g) {
-            const size_t s = ((size_t)b + g) * H + h;
-            const float m = ws.ml[s * 2];
-            if (m != -INFINITY) a = fmaf(exp2f(m - M), ws.acc[s * W + d], a);
+    float M = red[0][0];
+    for (int i = 1; i < nwarp; ++i) M = fmaxf(M, red[0][i]);
+    for (int k = tid; k < nseg; k += blockDim.x) {
+        const float mk = (k == tid) ? m_my : ws.ml[(s0 + (size_t)k * H) * 2];
+        w[k] = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
+    }
+    float ls = (tid < nseg && m_my != -INFINITY) ? exp2f(m_my - M) * l_my : 0.f;
+    for (int k = tid + nthr; k < nseg; k += blockDim.x) {
+        const float2 ml = *reinterpret_cast<const float2 *>(ws.ml + (s0 + (size_t)k * H) * 2);
+        if (ml.x != -INFINITY) ls = fmaf(exp2f(ml.x - M), ml.y, ls);
+    }
+    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if ((tid & 31) == 0) red[1][tid >> 5] = ls;
+    __syncthreads();
+    float L = 0.f;
+    for (int i = 0; i < nwarp; ++i) L += red[1][i];
+    const float invL = (L > 0.f) ? 1.f / L : 0.f;
+    // 3. weighted sums over segments
+#pragma unroll
+    for (int g = 0; g < kCombSeg; ++g) {
+        if (g < nseg) {
+            a0 = fmaf(w[g], v0[g], a0);
+            a1 = fmaf(w[g], v1[g], a1);
         }
-        float o = a * invL;
-        const T *row = bv + (size_t)d * r;
-        for (int k = 0; k < r; ++k) o = fmaf(cr[k], Elem<T>::load(row + k), o);
+    }
+    for (int g = kCombSeg; g < nseg; ++g) {
+        const float *acc = ws.acc + (s0 + (size_t)g * H) * W;
+        if (c0 < W) a0 = fmaf(w[g], acc[c0], a0);
+        if (c1 < W) a1 = fmaf(w[g], acc[c1], a1);
+    }
+    a0 *= invL;
+    a1 *= invL;
+    // private part of the columns goes to shared memory for the expansion
+    if (c0 >= d_h && c0 < W) cr[c0 - d_h] = a0;
+    if (c1 >= d_h && c1 < W) cr[c1 - d_h] = a1;
+    __syncthreads();
+    // 4. out[d] = accS[d] / L + sum_k (accR[k] / L) B_V[h][d][k]
+    for (int d = tid; d < d_h; d += blockDim.x) {
+        float o = (d == c0) ? a0 : (d == c1) ? a1 : 0.f;
+        if (staged) {
+            const T *row = bv + (size_t)d * r;
+            constexpr int V = Vec16<T>::N;
+            for (int k = 0; k < r; k += V) {
+                float x[V];
+                Vec16<T>::load(row + k, x);
+#pragma unroll
+                for (int e = 0; e < V; ++e) o = fmaf(cr[k + e], x[e], o);
+            }
+        } else {
+            const T *row = src + (size_t)d * r;
+            for (int k = 0; k < r; ++k) o = fmaf(cr[k], Elem<T>::load(row + k), o);
+        }
         Elem<T>::store(dst + d, o);
     }
 }
@@ -273,12 +417,21 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const T *__restrict
 // ---------------------------------------------------------------------------
 template <typename T>
 cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align) {
-    const int blocks = a.B * a.cache.H + 1;
-    const size_t sm = sizeof(float) * a.cache.d_h;
-    decode_prologue_kernel<T><<<blocks, 256, sm, a.stream>>>(
-        static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens, a.B, a.cache.H,
-        a.cache.d_h, a.cache.r, a.max_pages * a.cache.page_size, G, tile_align, ws, a.status);
-    return cudaGetLastError();
+    const auto &c = a.cache;
+    dim3 grid(c.H + 1, (a.B + kProRows - 1) / kProRows);
+    const bool staged = (size_t)c.d_h * c.r <= kStageFloats;
+    const size_t sm = sizeof(float) * ((staged ? (size_t)c.d_h * c.r : 0) + (size_t)kProRows * c.d_h);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_pdl(decode_prologue_kernel<T>, grid, dim3(256), sm, a.stream,
+                      static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
+                      static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
+                      a.max_pages * a.cache.page_size, G, tile_align, staged, ws, a.status);
 }
 
 template <typename T>
@@ -286,28 +439,38 @@ cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G)
     const auto &c = a.cache;
     const size_t sm = sizeof(float) * (c.d_h + c.r + kGenTile) + sizeof(int32_t) * kGenTile;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)c.d_h);
-    dim3 grid(G, c.H);
-    decode_split_generic_kernel<T><<<grid, kGenTile, sm, a.stream>>>(
-        static_cast<const T *>(a.q), static_cast<const T *>(c.S_K), static_cast<const T *>(c.S_V),
-        static_cast<const T *>(c.R_K), static_cast<const T *>(c.R_V), a.page_table, a.req_row, a.max_pages,
-        c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r, scale_log2, ws, a.status);
-    return cudaGetLastError();
+    return launch_pdl(decode_split_generic_kernel<T>, dim3(G, c.H), dim3(kGenTile), sm, a.stream,
+                      static_cast<const T *>(a.q), static_cast<const T *>(c.S_K),
+                      static_cast<const T *>(c.S_V), static_cast<const T *>(c.R_K),
+                      static_cast<const T *>(c.R_V), a.page_table, a.req_row, a.max_pages,
+                      c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r, scale_log2, ws, a.status);
 }
 
 template <typename T>
-cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws) {
+cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G) {
     dim3 grid(a.cache.H, a.B);
-    decode_combine_kernel<T><<<grid, 128, sizeof(float) * a.cache.r, a.stream>>>(
-        static_cast<const T *>(a.B_V), a.B, a.cache.H, a.cache.d_h, a.cache.r, ws,
-        static_cast<T *>(a.out));
-    return cudaGetLastError();
+    // d_h <= 256 columns of accS plus r <= 256 of accR: two columns per thread
+    const bool staged = (size_t)a.cache.d_h * a.cache.r <= kStageFloats;
+    const size_t bv_bytes = staged ? ((size_t)a.cache.d_h * a.cache.r * sizeof(T) + 15) / 16 * 16 : 0;
+    const size_t sm = bv_bytes + sizeof(float) * ((size_t)a.cache.r + G);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int nthr = (a.cache.d_h + a.cache.r <= 256) ? 128 : 256;
+    return launch_pdl(decode_combine_kernel<T>, grid, dim3(nthr), sm, a.stream,
+                      static_cast<const T *>(a.B_V), a.B, a.cache.H, a.cache.d_h, a.cache.r,
+                      staged, ws, static_cast<T *>(a.out));
 }
 
 template cudaError_t launch_prologue<float>(const DecodeArgs &, const DecodeWs &, int, int);
 template cudaError_t launch_prologue<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int, int);
 template cudaError_t launch_split_generic<float>(const DecodeArgs &, const DecodeWs &, int);
 template cudaError_t launch_split_generic<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int);
-template cudaError_t launch_combine<float>(const DecodeArgs &, const DecodeWs &);
-template cudaError_t launch_combine<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &);
+template cudaError_t launch_combine<float>(const DecodeArgs &, const DecodeWs &, int);
+template cudaError_t launch_combine<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int);
 
 }  // namespace lrkv

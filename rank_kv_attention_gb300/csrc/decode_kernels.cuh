@@ -26,7 +26,7 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
 template <typename T>
 cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G);
 template <typename T>
-cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws);
+cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G);
 
 // Tensor-core split kernel (bf16, d_h = 128, page_size % 16 == 0, selected
 // (H, r) pairs).  `fast_decode_supported` says whether a shape is covered;

@@ -107,7 +107,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
             e = fast ? launch_split_fast(a, ws, G) : launch_split_generic<__nv_bfloat16>(a, ws, G);
             prof_after(a.stream);
         }
-        if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws);
+        if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws, G);
     } else {
         e = launch_prologue<float>(a, ws, G, kPlanTileAlign);
         if (e == cudaSuccess) {
@@ -115,7 +115,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
             e = launch_split_generic<float>(a, ws, G);
             prof_after(a.stream);
         }
-        if (e == cudaSuccess) e = launch_combine<float>(a, ws);
+        if (e == cudaSuccess) e = launch_combine<float>(a, ws, G);
     }
     return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }
@@ -180,12 +180,14 @@ static int run_append(const void *X, const int32_t *positions, const int32_t *se
     if (c->dtype == LRKV_BF16) {
         auto a = make_append_args<__nv_bfloat16>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K,
                                                  U_V, c, page_table, B, max_pages, status, s);
-        e = tc_append_supported(n, d, c->d_h, c->H, c->r) ? launch_append_tc(a)
-                                                           : launch_append_generic(a);
+        if (rows_mma_append_fits(a)) e = launch_append_rows_mma(a);
+        else if (rows_append_fits(a)) e = launch_append_rows(a);
+        else if (tc_append_supported(n, d, c->d_h, c->H, c->r)) e = launch_append_tc(a);
+        else e = launch_append_generic(a);
     } else {
         auto a = make_append_args<float>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K, U_V, c,
                                          page_table, B, max_pages, status, s);
-        e = launch_append_generic(a);
+        e = rows_append_fits(a) ? launch_append_rows(a) : launch_append_generic(a);
     }
     return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }

@@ -30,13 +30,17 @@ struct DecodePlan {
 constexpr int kPlanTileAlign = 16;
 
 // Workspace layout of lrkv_decode (all offsets 256-byte aligned):
-//   [plan header + off[B+1]] [p: B*H*r f32] [ml: slots*H*2 f32] [acc: slots*H*(d_h+r) f32]
+//   [plan header + off[B+1]] [p: B*H*r f32] [ml: slots*H*2 f32]
+//   [acc: slots*H*(d_h+r) f32] [done: B*kHeadGroups int32]
+constexpr int kHeadGroups = 16;  // completion counters per request (one per head group)
+
 struct DecodeWs {
     DecodePlan *plan;
     int32_t *off;
     float *p;
     float *ml;
     float *acc;
+    int32_t *done;
     size_t bytes;
 };
 
@@ -57,6 +61,8 @@ __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, i
     o += align256(sizeof(float) * slots * H * 2);
     w.acc = reinterpret_cast<float *>(p + o);
     o += align256(sizeof(float) * slots * H * (size_t)(d_h + r));
+    w.done = reinterpret_cast<int32_t *>(p + o);
+    o += align256(sizeof(int32_t) * (size_t)B * kHeadGroups);
     w.bytes = o;
     return w;
 }
@@ -80,6 +86,46 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 16-byte vector of T widened to floats (8 bf16 or 4 fp32 elements).
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const __nv_bfloat16 *p, float (&v)[8]) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        v[0] = __uint_as_float(u.x << 16); v[1] = __uint_as_float(u.x & 0xffff0000u);
+        v[2] = __uint_as_float(u.y << 16); v[3] = __uint_as_float(u.y & 0xffff0000u);
+        v[4] = __uint_as_float(u.z << 16); v[5] = __uint_as_float(u.z & 0xffff0000u);
+        v[6] = __uint_as_float(u.w << 16); v[7] = __uint_as_float(u.w & 0xffff0000u);
+    }
+};
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const float *p, float (&v)[4]) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    }
+};
+
+// Block-cooperative copy of n elements (n a multiple of Vec16<T>::N, src
+// 16-byte aligned) into fp32 shared memory, several vectors in flight per
+// thread.
+template <typename T>
+__device__ __forceinline__ void stage_f32(float *dst, const T *src, int n) {
+    constexpr int V = Vec16<T>::N, U = 4;
+    const int nv = n / V, step = blockDim.x * U;
+    for (int base = threadIdx.x; base < nv; base += step) {
+        float v[U][V];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * (int)blockDim.x < nv) Vec16<T>::load(src + (size_t)(base + u * blockDim.x) * V, v[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * (int)blockDim.x < nv)
+#pragma unroll
+                for (int e = 0; e < V; ++e) dst[(base + u * blockDim.x) * V + e] = v[u][e];
+    }
 }
 
 __device__ __forceinline__ void status_or(int32_t *st, uint32_t bits) {
@@ -157,6 +203,34 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 3-D tiled TMA load: box at (x, y, z) of the tensor map.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Same, with an L2 cache-eviction policy (see l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 int z, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Policy marking streamed data as first to leave L2, so that small tensors
+// reused every step (weights, bases, partials) stay resident.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Plain contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
@@ -166,6 +240,13 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// preamble, and wait for the previous kernel's completion and memory.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -202,6 +283,25 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
 // chunk index is XORed with the row index modulo 8).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may be
+// scheduled while its predecessor in the stream drains; every kernel of this
+// library starts with pdl_wait(), so stream order is kept for its reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
 }  // namespace lrkv
