@@ -264,6 +264,19 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = max_over_ranks(e0.elapsed_time(e1))
 
+    # ---- live breakdown: the same K steps with only one of the two calls
+    def timed(fn):
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(K):
+            fn(i)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / K
+    append_ms = timed(lambda i: f_app(*calls[i % n_copies][0]))
+    decode_ms = timed(lambda i: f_dec(*calls[i % n_copies][1]))
+
     # ---- the split kernel's own duration: the library brackets each launch
     # with CUDA events on its stream (a second pass over K steps, so those
     # events do not perturb the step timing above)
@@ -342,6 +355,8 @@ def run_ours(args, rank, world, local_rank):
                      "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
                      "traffic": profiled_traffic(name)},
         "step_effective_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+        "breakdown_ms": {"append_alone": round(append_ms, 5), "decode_alone": round(decode_ms, 5),
+                         "split_kernel": round(split_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host inputs copied in, result copied out and synchronised every step"},

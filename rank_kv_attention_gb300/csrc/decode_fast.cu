@@ -55,7 +55,8 @@ struct FastCfg {
     static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
     static constexpr int OFF_OK = OFF_CNT + 64;      // per-stage "page id valid" flags
     static constexpr int OFF_CUR = OFF_OK + 64;      // issue cursor
-    static constexpr int SMEM = OFF_CUR + 64 + 1024;  // + alignment slack
+    static constexpr int OFF_PLAN = OFF_CUR + 64;    // local plan: scan scratch + request offsets
+    static constexpr int SMEM = OFF_PLAN + 512 + 1024;  // + alignment slack
 
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R) % 64 == 0, "private rows tile into 64-column boxes");
@@ -66,6 +67,7 @@ struct FastCfg {
 
 struct FastParams {
     const __nv_bfloat16 *q;
+    const int32_t *seq_lens;
     const int32_t *page_table;
     const int32_t *req_row;
     int max_pages, num_pages, page_size, B;
@@ -86,43 +88,33 @@ struct IssueCursor {
     int32_t start;
     int t, t_b;
     int done, issued;
-    int page_key, page_id;  // last page looked up: (request, page index) -> id
+    int page_key, page_id;  // page of the last issued tile: (request, page index) -> id
 };
-
-__device__ __forceinline__ int find_request_fast(const int32_t *off, int B, int32_t x) {
-    int lo = 0, hi = B - 1;
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if (off[mid + 1] > x) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo;
-}
 
 __device__ __forceinline__ const int32_t *page_row(const FastParams &P, int b) {
     return P.page_table + (size_t)(P.req_row ? P.req_row[b] : b) * P.max_pages;
 }
 
 template <class C>
-__device__ __forceinline__ void cursor_begin_segment(IssueCursor *cur, const FastParams &P,
+__device__ __forceinline__ void cursor_begin_segment(IssueCursor *cur, const int32_t *off,
                                                      int32_t end) {
     int b = cur->b;
-    while (P.ws.off[b + 1] <= cur->start) ++b;
-    const int32_t base = P.ws.off[b];
+    while (off[b + 1] <= cur->start) ++b;
+    const int32_t base = off[b];
     cur->b = b;
     cur->t = (cur->start - base) / C::TS * C::TS;
-    cur->t_b = min(end, P.ws.off[b + 1]) - base;
+    cur->t_b = min(end, off[b + 1]) - base;
 }
 
 // Issue the copies of the cursor's next tile into its stage.
 template <class C>
 __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
-                           uint8_t *smem, uint64_t *full, int *okf, int32_t end) {
+                           const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
+                           int32_t end) {
     if (cur->done) return;
     const int it = cur->issued;
     const int s = it % C::STAGES;
-    // one page-table read per page (a page holds several 16-row tiles); the
-    // next page's entry is prefetched into L2 when its first tile is near
+    // one page-table read per page (a page holds several 16-row tiles)
     const int pidx = cur->t / P.page_size;
     const int key = cur->b * P.max_pages + pidx;
     int32_t page;
@@ -158,9 +150,9 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
     cur->issued = it + 1;
     cur->t += C::TS;
     if (cur->t >= cur->t_b) {
-        cur->start = P.ws.off[cur->b] + cur->t_b;
+        cur->start = off[cur->b] + cur->t_b;
         if (cur->start >= end) cur->done = 1;
-        else cursor_begin_segment<C>(cur, P, end);
+        else cursor_begin_segment<C>(cur, off, end);
     }
 }
 
@@ -193,13 +185,71 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int g = blockIdx.x;
     const DecodeWs &ws = P.ws;
 
-    pdl_wait();  // the plan and private queries come from the prologue kernel
-    pdl_launch_dependents();
-    const int32_t total = ws.plan->total, chunk = ws.plan->chunk;
+    // ---- Local launch plan.  It reads only caller inputs (sequence lengths,
+    // page table, cache), which were complete before the prologue kernel got
+    // past its own wait and let this grid launch, so the first tiles can be
+    // requested while the prologue is still computing the private queries.
+    // The same validated lengths and chunk formula as the prologue's plan.
+    int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);  // [0] b0 [1] b_last [2..9] warp sums [16..] offsets
+    constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kLocalReq]
+    const int Bn = P.B;
+    const int max_len = P.max_pages * P.page_size;
+    const int per = (Bn + C::NT - 1) / C::NT;
+    const int lo = min(Bn, tid * per), hi = min(Bn, lo + per);
+    auto len_of = [&](int bb) {
+        const int32_t L = P.seq_lens[bb];
+        return (L < 1 || L > max_len) ? 0 : L;
+    };
+    int32_t mysum = 0;
+    for (int bb = lo; bb < hi; ++bb) mysum += len_of(bb);
+    int32_t incl = mysum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) pl[2 + warp] = incl;
+    __syncthreads();
+    int32_t wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < C::NCW; ++w) {
+        const int32_t v = pl[2 + w];
+        if (w < warp) wbase += v;
+        total += v;
+    }
+    const int32_t base_t = wbase + incl - mysum;  // offset of request lo
+    int32_t chunk = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    chunk = max(chunk, kPlanTileAlign);
+    chunk = (chunk + kPlanTileAlign - 1) / kPlanTileAlign * kPlanTileAlign;
     const int32_t start0 = g * chunk;
     const int32_t end = min(total, start0 + chunk);
-    if (start0 >= end) return;
-    const int b0 = find_request_fast(ws.off, P.B, start0);
+    if (start0 >= end) {
+        pdl_wait();
+        return;
+    }
+    {
+        int32_t o = base_t;
+        for (int bb = lo; bb < hi; ++bb) {
+            const int32_t L = len_of(bb);
+            if (L > 0 && o <= start0 && start0 < o + L) pl[0] = bb;
+            if (L > 0 && o < end && end <= o + L) pl[1] = bb;
+            o += L;
+        }
+    }
+    __syncthreads();
+    const int b0 = pl[0];
+    const bool local = pl[1] + 1 - b0 <= kLocalReq;
+    if (local) {
+        int32_t o = base_t;
+        for (int bb = lo; bb < hi; ++bb) {
+            if (bb >= b0 && bb - b0 <= kLocalReq) pl[16 + bb - b0] = o;
+            o += len_of(bb);
+        }
+        if (hi == Bn && Bn - b0 <= kLocalReq) pl[16 + Bn - b0] = o;  // off[B] = total
+    }
+    __syncthreads();
+    const int32_t *off = local ? pl + 16 - b0 : ws.off;  // off[b] for this CTA's requests
+    if (!local) pdl_wait();  // fall back to the prologue's offsets
 
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -217,10 +267,12 @@ __global__ void __launch_bounds__(C::NT, 1)
         cur->issued = 0;
         cur->page_key = -1;
         cur->page_id = 0;
-        cursor_begin_segment<C>(cur, P, end);
-        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, smem, full, okf, end);
+        cursor_begin_segment<C>(cur, off, end);
+        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, off, smem, full, okf, end);
     }
     __syncthreads();
+    if (local) pdl_wait();  // the private queries come from the prologue kernel
+    pdl_launch_dependents();
 
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
     const int hl = lane >> 4, j = lane & 15;  // this lane's (head slot, tile row)
@@ -238,9 +290,9 @@ __global__ void __launch_bounds__(C::NT, 1)
     int b = b0;
     int32_t start = start0;
     while (start < end && !timed_out) {
-        while (ws.off[b + 1] <= start) ++b;
-        const int32_t base = ws.off[b];
-        const int32_t seg_end = min(end, ws.off[b + 1]);
+        while (off[b + 1] <= start) ++b;
+        const int32_t base = off[b];
+        const int32_t seg_end = min(end, off[b + 1]);
         const int t_a = start - base, t_b = seg_end - base;
 
         // -------- segment set-up: query fragments, private-query fragments, state
@@ -305,9 +357,13 @@ __global__ void __launch_bounds__(C::NT, 1)
             const uint8_t *st = smem + s * C::STAGE;
             const int mi = lane >> 3;
 
-            // scores: D[row x head] = S_K . Q^T + R_K(warp columns) . blockdiag(p)^T
+            // scores: D[row x head] = S_K . Q^T + R_K(warp columns) . blockdiag(p)^T,
+            // accumulated in four independent chains (shared even/odd k-steps,
+            // private hi/lo halves) so the tensor-core latency overlaps
             float c[4] = {0.f, 0.f, 0.f, 0.f};
             {
+                float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+                float c3[4] = {0.f, 0.f, 0.f, 0.f};
                 const uint32_t skb = smem_u32(st + C::OFF_SK);
                 const uint32_t rkb = smem_u32(st + C::OFF_RK);
                 const int rr = (mi & 1) * 8 + (lane & 7);
@@ -315,16 +371,19 @@ __global__ void __launch_bounds__(C::NT, 1)
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a[4];
                     ldmatrix_x4(skb + box_chunk(rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
-                    mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
+                    if (ks & 1) mma_bf16_16816(c1, a, qb[ks][0], qb[ks][1]);
+                    else mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
                 }
                 const int cw = warp * (C::HPW * C::R / 8);  // first 16-byte chunk of the warp's columns
 #pragma unroll
                 for (int ks = 0; ks < C::KSP; ++ks) {
                     uint32_t a[4];
                     ldmatrix_x4(rkb + box_chunk(rr, cw + 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
-                    mma_bf16_16816(c, a, pbh[ks][0], pbh[ks][1]);
-                    mma_bf16_16816(c, a, pbl[ks][0], pbl[ks][1]);
+                    mma_bf16_16816(c2, a, pbh[ks][0], pbh[ks][1]);
+                    mma_bf16_16816(c3, a, pbl[ks][0], pbl[ks][1]);
                 }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c[e] = (c[e] + c1[e]) + (c2[e] + c3[e]);
             }
 
             // softmax per (head slot, row) lane; lazy reference maximum
@@ -436,7 +495,7 @@ __global__ void __launch_bounds__(C::NT, 1)
                              : "memory");
                 if (prev == C::NCW - 1) {
                     cnt[s] = 0;
-                    issue_next<C>(cur, P, M, smem, full, okf, end);
+                    issue_next<C>(cur, P, M, off, smem, full, okf, end);
                 }
             }
             __syncwarp();
@@ -532,7 +591,10 @@ struct Pick {
     static constexpr int stage = FastCfg<H, R, 1>::STAGE;
     static constexpr int misc = FastCfg<H, R, 1>::SMEM - FastCfg<H, R, 1>::OFF_BAR;
     static constexpr int fit = (227 * 1024 - misc) / stage;
-    static constexpr int STAGES = fit > 4 ? 4 : fit;
+    // deeper rings of large stages measured slower (more DRAM queueing for
+    // the same consumption rate): 3 stages of >= 48 KB, else up to 4
+    static constexpr int cap = stage >= 48 * 1024 ? 3 : 4;
+    static constexpr int STAGES = fit > cap ? cap : fit;
     using Cfg = FastCfg<H, R, STAGES>;
 };
 
@@ -555,6 +617,7 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     }
     FastParams P;
     P.q = static_cast<const __nv_bfloat16 *>(a.q);
+    P.seq_lens = a.seq_lens;
     P.page_table = a.page_table;
     P.req_row = a.req_row;
     P.max_pages = a.max_pages;

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/lrkv.h"
+#include "lrkv.h"
 
 namespace lrkv {
 
