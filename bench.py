@@ -35,6 +35,8 @@ WORKLOADS = {
     "decode_T32768": "B=4, d=4096, H=32, d_h=128, r=32, T=32768, bf16 cache, fp32 accumulation",
     "ragged_paged": "B=64, lengths uniform on [256, 8192], 64-token pages shuffled in one pool, "
                     "H=16, d_h=128, r=56, d=2048 for the append, bf16",
+    "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
+                    "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
 
 
@@ -57,13 +59,13 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
 
 
 def workload_shape(name):
@@ -287,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     tot = ctypes.c_double()
     nl = ctypes.c_int32()
-    assert lib.lrkv_profile_read(ctypes.byref(tot), ctypes.byref(nl)) == 0
+    assert lib.lrkv_profile_read(0, ctypes.byref(tot), ctypes.byref(nl)) == 0
     lib.lrkv_profile_enable(0)
     split_ms = tot.value / max(1, nl.value)
     st = int(status.item())
@@ -409,11 +411,104 @@ def run_reference(args, rank, world):
     }
 
 
+def run_prefill(args, rank, world, local_rank):
+    """Prefill of fresh prompts: one step = lrkv_prefill over the whole batch."""
+    import ctypes
+    import numpy as np
+    import torch
+    import lrkv_inputs as I
+    import rank_kv_attention_gb300 as L
+    from rank_kv_attention_gb300.api import PagedCache
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib = L.lib()
+    c = I.CONFIGS[args.config]
+    Bq, d, H, d_h, r, T = c["B"], c["d"], c["H"], c["d_h"], c["r"], c["T"]
+    n = Bq * T
+    ac = I.make_append_case([T] * Bq, [0] * Bq, d, dtype="bf16", seed=c["seed"], shuffle=True)
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=c["seed"])
+    rng = np.random.default_rng(99)
+    Q = I.f32_to_bf16_bits(rng.standard_normal((n, H, d_h)).astype(np.float32))
+
+    def to_dev(a, kind="bf16"):
+        if kind == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    cache = PagedCache.empty(ac.num_pages, 64, H, d_h, r, torch.bfloat16, dev)
+    X, Qd = to_dev(ac.X), to_dev(Q)
+    Wt = [to_dev(a) for a in (w.W_S_K, w.W_S_V, w.U_K, w.U_V, w.B_K, w.B_V)]
+    cu = to_dev(np.arange(0, n + 1, T), "i32")
+    sp = to_dev(np.zeros(Bq), "i32")
+    pt = to_dev(ac.page_table, "i32")
+    out = torch.empty_like(Qd)
+    ws = L.workspace(L.prefill_workspace_bytes(Bq, n, H, d_h, r, T), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        L.prefill(X, Qd, cu, sp, T, *Wt, cache, pt, out=out, ws=ws, stream=stream)
+
+    K, W = args.steps, args.warmup
+    for _ in range(max(W, 3)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.25)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = e0.elapsed_time(e1)
+    assert lib.lrkv_profile_enable(1) == 0
+    for _ in range(K):
+        step()
+    torch.cuda.synchronize()
+    res_k = {}
+    for which, name in ((0, "attention"), (1, "projection")):
+        tot, nl = ctypes.c_double(), ctypes.c_int32()
+        assert lib.lrkv_profile_read(which, ctypes.byref(tot), ctypes.byref(nl)) == 0
+        res_k[name] = tot.value / max(1, nl.value)
+    lib.lrkv_profile_enable(0)
+    ms = total_ms / K
+    Ntot = 2 * d_h + 2 * H * r
+    proj_flops = 2 * n * d * Ntot
+    peak, kind = measured_peaks("bf16_tflops", 1900.0)
+    achieved = proj_flops / (res_k["projection"] / 1e3) / 1e12
+    attn_flops = 2 * 2 * (Bq * T * (T + 1) // 2) * H * (d_h + r)   # scores + values, causal
+    return {
+        "metric": "LRKV prefill tokens/s", "value": round(n / (ms / 1e3), 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": Bq, "d": d, "H": H,
+                   "d_h": d_h, "r": r, "seq_len": T, "rows": n},
+        "roofline": {"kernel": "append projection GEMM (tcgen05)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{kind} bf16 GEMM (burst)",
+                     "flops_per_launch": proj_flops, "avg_launch_ms": round(res_k["projection"], 4),
+                     "traffic": None},
+        "breakdown_ms": {"projection": round(res_k["projection"], 4),
+                         "attention": round(res_k["attention"], 4)},
+        "attention_tflops": round(attn_flops / (res_k["attention"] / 1e3) / 1e12, 1),
+        "clocks": clk,
+    }
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
+    elif args.config == "prefill_2048":
+        res = run_prefill(args, rank, world, local_rank)
     else:
         res = run_ours(args, rank, world, local_rank)
     if rank == 0 and res is not None:

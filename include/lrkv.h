@@ -230,16 +230,21 @@ LRKV_API const char *lrkv_status_string(int status);
 LRKV_API int lrkv_last_cuda_error(void);
 
 /*
- * Instrumentation for benchmarks.  lrkv_profile_enable(1) creates a pool of
- * CUDA events (once) and starts recording: every later lrkv_decode /
- * lrkv_prefill brackets its split-attention kernel with an event pair on the
- * call's stream (at most 8192 pairs are kept).  lrkv_profile_read waits for
- * the last recorded event, returns the summed kernel time in milliseconds and
- * the number of bracketed launches, and clears the record.  Not for use
- * inside CUDA-graph capture.  lrkv_profile_enable(0) stops recording.
+ * Instrumentation for benchmarks.  lrkv_profile_enable(1) creates pools of
+ * CUDA events (once) and starts recording: every later call brackets its
+ * dominant kernel with an event pair on the call's stream -- the
+ * split-attention kernel of lrkv_decode / lrkv_prefill (LRKV_PROFILE_ATTENTION)
+ * and the projection kernel of lrkv_append / lrkv_prefill
+ * (LRKV_PROFILE_PROJECTION); at most 8192 pairs are kept of each.
+ * lrkv_profile_read(which, ...) waits for that kind's last event, returns its
+ * summed kernel time in milliseconds and the number of bracketed launches,
+ * and clears that record.  Not for use inside CUDA-graph capture.
+ * lrkv_profile_enable(0) stops recording.
  */
+#define LRKV_PROFILE_ATTENTION 0
+#define LRKV_PROFILE_PROJECTION 1
 LRKV_API int lrkv_profile_enable(int on);
-LRKV_API int lrkv_profile_read(double *total_ms, int32_t *launches);
+LRKV_API int lrkv_profile_read(int32_t which, double *total_ms, int32_t *launches);
 
 /* Library version, major*10000 + minor*100 + patch. */
 LRKV_API int lrkv_version(void);

@@ -24,6 +24,9 @@ LRKV_E_CUDA = -6
 
 LRKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
+LRKV_PROFILE_ATTENTION = 0
+LRKV_PROFILE_PROJECTION = 1
+
 LRKV_STATUS_BAD_PAGE = 1
 LRKV_STATUS_BAD_SEQLEN = 2
 LRKV_STATUS_BAD_ROW = 4
@@ -72,7 +75,7 @@ SIGNATURES = {
     "lrkv_last_cuda_error": (ctypes.c_int, []),
     "lrkv_version": (ctypes.c_int, []),
     "lrkv_profile_enable": (ctypes.c_int, [ctypes.c_int]),
-    "lrkv_profile_read": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I32)]),
+    "lrkv_profile_read": (ctypes.c_int, [I32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I32)]),
 }
 
 

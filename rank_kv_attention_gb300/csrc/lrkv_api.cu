@@ -16,22 +16,26 @@ static int cuda_fail(cudaError_t e) {
     return LRKV_E_CUDA;
 }
 
-// Event pairs bracketing split-kernel launches (benchmark instrumentation).
+// Event pairs bracketing the dominant kernel of each call (benchmark
+// instrumentation), one pool per kind.
 struct Profiler {
     static const int kCap = 8192;
-    bool on = false, created = false;
+    bool created = false;
     int n = 0;
     cudaEvent_t ev[2 * kCap];
 };
-static Profiler g_prof;
+static bool g_prof_on = false;
+static Profiler g_prof[2];
 
-static void prof_before(cudaStream_t s) {
-    if (g_prof.on && g_prof.n < Profiler::kCap) cudaEventRecord(g_prof.ev[2 * g_prof.n], s);
+static void prof_before(int kind, cudaStream_t s) {
+    Profiler &p = g_prof[kind];
+    if (g_prof_on && p.n < Profiler::kCap) cudaEventRecord(p.ev[2 * p.n], s);
 }
-static void prof_after(cudaStream_t s) {
-    if (g_prof.on && g_prof.n < Profiler::kCap) {
-        cudaEventRecord(g_prof.ev[2 * g_prof.n + 1], s);
-        ++g_prof.n;
+static void prof_after(int kind, cudaStream_t s) {
+    Profiler &p = g_prof[kind];
+    if (g_prof_on && p.n < Profiler::kCap) {
+        cudaEventRecord(p.ev[2 * p.n + 1], s);
+        ++p.n;
     }
 }
 
@@ -103,17 +107,17 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     if (c.dtype == LRKV_BF16) {
         e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign);
         if (e == cudaSuccess) {
-            prof_before(a.stream);
+            prof_before(LRKV_PROFILE_ATTENTION, a.stream);
             e = fast ? launch_split_fast(a, ws, G) : launch_split_generic<__nv_bfloat16>(a, ws, G);
-            prof_after(a.stream);
+            prof_after(LRKV_PROFILE_ATTENTION, a.stream);
         }
         if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws, G);
     } else {
         e = launch_prologue<float>(a, ws, G, kPlanTileAlign);
         if (e == cudaSuccess) {
-            prof_before(a.stream);
+            prof_before(LRKV_PROFILE_ATTENTION, a.stream);
             e = launch_split_generic<float>(a, ws, G);
-            prof_after(a.stream);
+            prof_after(LRKV_PROFILE_ATTENTION, a.stream);
         }
         if (e == cudaSuccess) e = launch_combine<float>(a, ws, G);
     }
@@ -177,6 +181,7 @@ static int run_append(const void *X, const int32_t *positions, const int32_t *se
                       int max_pages, int32_t *status, cudaStream_t s) {
     if (n == 0) return LRKV_OK;
     cudaError_t e;
+    prof_before(LRKV_PROFILE_PROJECTION, s);
     if (c->dtype == LRKV_BF16) {
         auto a = make_append_args<__nv_bfloat16>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K,
                                                  U_V, c, page_table, B, max_pages, status, s);
@@ -189,6 +194,7 @@ static int run_append(const void *X, const int32_t *positions, const int32_t *se
                                          page_table, B, max_pages, status, s);
         e = rows_append_fits(a) ? launch_append_rows(a) : launch_append_generic(a);
     }
+    prof_after(LRKV_PROFILE_PROJECTION, s);
     return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }
 
@@ -225,36 +231,39 @@ extern "C" {
 int lrkv_version(void) { return 100; }
 
 int lrkv_profile_enable(int on) {
-    if (on && !g_prof.created) {
+    for (int k = 0; k < 2 && on; ++k) {
+        Profiler &p = g_prof[k];
+        if (p.created) continue;
         for (int i = 0; i < 2 * Profiler::kCap; ++i) {
-            cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+            cudaError_t e = cudaEventCreate(&p.ev[i]);
             if (e != cudaSuccess) {
-                for (int k = 0; k < i; ++k) cudaEventDestroy(g_prof.ev[k]);
+                for (int j = 0; j < i; ++j) cudaEventDestroy(p.ev[j]);
                 return cuda_fail(e);
             }
         }
-        g_prof.created = true;
+        p.created = true;
     }
-    g_prof.on = on != 0;
-    g_prof.n = 0;
+    g_prof_on = on != 0;
+    g_prof[0].n = g_prof[1].n = 0;
     return LRKV_OK;
 }
 
-int lrkv_profile_read(double *total_ms, int32_t *launches) {
-    if (!total_ms || !launches) return LRKV_E_INVALID_ARG;
+int lrkv_profile_read(int32_t which, double *total_ms, int32_t *launches) {
+    if (!total_ms || !launches || which < 0 || which > 1) return LRKV_E_INVALID_ARG;
+    Profiler &p = g_prof[which];
     *total_ms = 0.0;
-    *launches = g_prof.n;
-    if (g_prof.n > 0) {
-        cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * g_prof.n - 1]);
+    *launches = p.n;
+    if (p.n > 0) {
+        cudaError_t e = cudaEventSynchronize(p.ev[2 * p.n - 1]);
         if (e != cudaSuccess) return cuda_fail(e);
-        for (int i = 0; i < g_prof.n; ++i) {
+        for (int i = 0; i < p.n; ++i) {
             float ms = 0.f;
-            e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+            e = cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]);
             if (e != cudaSuccess) return cuda_fail(e);
             *total_ms += ms;
         }
     }
-    g_prof.n = 0;
+    p.n = 0;
     return LRKV_OK;
 }
 

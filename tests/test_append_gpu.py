@@ -69,7 +69,8 @@ def test_append_exact_values_and_placement(dtype):
 
 
 @pytest.mark.parametrize("H,d_h,r,d,dtype", [(16, 128, 48, 2048, "bf16"), (32, 128, 32, 512, "bf16"),
-                                              (4, 16, 4, 64, "f32"), (8, 64, 24, 136, "bf16")])
+                                              (4, 16, 4, 64, "f32"), (8, 64, 24, 136, "bf16"),
+                                              (8, 64, 24, 192, "bf16")])
 def test_append_random_values(H, d_h, r, d, dtype):
     ac = I.make_append_case([100, 3, 77], [10, 0, 200], d, dtype=dtype, seed=H + r,
                             shuffle=True, interleave=True)
