@@ -40,4 +40,21 @@ cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s);
 
+// Causal prefill attention on tensor cores (bf16, d_h = 128, r % 8 == 0,
+// r <= 64, page_size % 64 == 0).  Returns 0 when launched, 1 when the shape
+// is not covered (nothing enqueued), or -cudaError_t on a launch failure.
+struct PrefillTcArgs {
+    const void *Q;
+    const int32_t *cu_rows, *start_pos;
+    int B, n, max_ctx;
+    const void *B_K, *B_V;
+    lrkv_cache_t cache;
+    const int32_t *page_table;
+    int max_pages;
+    void *out;
+    int32_t *status;
+    cudaStream_t stream;
+};
+int launch_prefill_tc(const PrefillTcArgs &p);
+
 }  // namespace lrkv

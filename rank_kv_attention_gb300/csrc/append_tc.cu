@@ -16,6 +16,7 @@
 //     its page slot.
 // Weights are stored output-major ([columns][d]), so both operands are K-major.
 #include "append_kernels.cuh"
+#include "tc_common.cuh"
 
 namespace lrkv {
 
@@ -38,77 +39,6 @@ struct TcTiles {
     int first[5];  // first output-column tile of each segment; first[4] = total tiles
     int width[4];  // columns of each segment
 };
-
-// ---- tcgen05 / TMEM wrappers (PTX ISA 8.6+, sm_100a family) ----------------
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// D[tmem] (+)= A[smem desc] . B[smem desc]^T, one instruction of K = 16
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// arrive on an mbarrier when all previously issued tcgen05.mma of this thread complete
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-        "%28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with
-// 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row atoms 1024 bytes
-// apart (stride byte offset), descriptor version 1, layout "SWIZZLE_128B".
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFF);         // start address
-    d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
-    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;                          // descriptor version
-    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N) {
-    return (1u << 4)                          // D format: f32
-           | (1u << 7)                        // A format: bf16
-           | (1u << 10)                       // B format: bf16
-           | ((uint32_t)(N >> 3) << 17)       // N / 8
-           | ((uint32_t)(M >> 4) << 24);      // M / 16
-}
 
 __global__ void __launch_bounds__(128, 1)
     append_tc_kernel(const __grid_constant__ TcMaps maps, const AppendArgsT<__nv_bfloat16> a,
@@ -243,26 +173,6 @@ __global__ void __launch_bounds__(128, 1)
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*TcEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                               const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                               CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static TcEncodeFn tc_encode() {
-    static TcEncodeFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<TcEncodeFn>(p);
-    }
-    return fn;
-}
-
 // [rows, d] bf16, K (= d) innermost; box 64 x 128 with 128-byte swizzle.
 // Rows beyond `rows` read as zeros.
 static bool tc_map(CUtensorMap *m, const void *base, int64_t rows, int d) {

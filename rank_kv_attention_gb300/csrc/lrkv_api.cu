@@ -405,7 +405,30 @@ int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int
     st = run_append(X, w.pos, w.sid, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
                     dev_status, s);
     if (st) return st;
-    // Causal attention: row i is a one-query decode over its request's rows
+    {
+        // Causal attention on tensor cores (query tiles of 128 rows per head).
+        PrefillTcArgs p;
+        p.Q = Q;
+        p.cu_rows = cu_rows;
+        p.start_pos = start_pos;
+        p.B = B;
+        p.n = n;
+        p.max_ctx = max_ctx;
+        p.B_K = B_K;
+        p.B_V = B_V;
+        p.cache = *cache;
+        p.page_table = page_table;
+        p.max_pages = max_pages;
+        p.out = out;
+        p.status = dev_status;
+        p.stream = s;
+        prof_before(LRKV_PROFILE_ATTENTION, s);
+        const int rc = launch_prefill_tc(p);
+        if (rc == 0) prof_after(LRKV_PROFILE_ATTENTION, s);
+        if (rc < 0) return cuda_fail((cudaError_t)(-rc));
+        if (rc == 0) return LRKV_OK;
+    }
+    // Other shapes: row i is a one-query decode over its request's rows
     // 0..pos_i, reading the page-table row of its request.
     DecodeArgs a;
     a.q = Q;
