@@ -217,6 +217,20 @@ LRKV_API int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows,
                  size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream);
 
 /*
+ * Which attention kernel lrkv_prefill runs for this cache (host-only query):
+ *   LRKV_PREFILL_TILED   - 128-row query tiles on the tensor cores, keys in
+ *                          tiles of 64; taken for bf16 caches with d_h = 128,
+ *                          r a multiple of 8 up to 64 and page_size a
+ *                          multiple of 64, when tensor maps can be encoded;
+ *   LRKV_PREFILL_PER_ROW - every query row as a one-query decode (any shape).
+ * Both compute the same function.  Returns a negative LRKV_E_* code for an
+ * invalid descriptor.
+ */
+#define LRKV_PREFILL_PER_ROW 0
+#define LRKV_PREFILL_TILED 1
+LRKV_API int lrkv_prefill_kernel_kind(const lrkv_cache_t *cache);
+
+/*
  * Cache payload in bytes for `tokens` cached positions of one layer:
  * tokens * 2 * (d_h + H*r) * sizeof(dtype)  (section 4, equation 9).
  * Returns 0 for invalid arguments.

@@ -9,11 +9,13 @@ does, and raises if the library has not been built (see ``build.build``).
 from ._abi import (LRKV_BF16, LRKV_F32, LRKV_OK, LRKV_E_INVALID_ARG, LRKV_E_SHAPE,
                    LRKV_E_DTYPE, LRKV_E_BOUNDS, LRKV_E_WORKSPACE, LRKV_E_CUDA,
                    LRKV_STATUS_BAD_PAGE, LRKV_STATUS_BAD_SEQLEN, LRKV_STATUS_BAD_ROW,
-                   LRKV_STATUS_TIMEOUT, CacheDesc, LrkvError, lib)
+                   LRKV_STATUS_TIMEOUT, LRKV_PREFILL_PER_ROW, LRKV_PREFILL_TILED, CacheDesc,
+                   LrkvError, lib)
 
 __all__ = [
     "lib", "CacheDesc", "LrkvError", "PagedCache", "append", "decode", "prefill",
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
+    "prefill_kernel_kind",
 ]
 
 
@@ -21,7 +23,7 @@ def __getattr__(name):
     # torch-facing helpers are imported lazily so that the ctypes layer works
     # without importing torch
     if name in ("PagedCache", "append", "decode", "prefill", "decode_workspace_bytes",
-                "prefill_workspace_bytes", "cache_bytes", "workspace"):
+                "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -24,6 +24,9 @@ LRKV_E_CUDA = -6
 
 LRKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
+LRKV_PREFILL_PER_ROW = 0
+LRKV_PREFILL_TILED = 1
+
 LRKV_PROFILE_ATTENTION = 0
 LRKV_PROFILE_PROJECTION = 1
 
@@ -70,6 +73,7 @@ SIGNATURES = {
     "lrkv_prefill_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),
+    "lrkv_prefill_kernel_kind": (ctypes.c_int, [CACHE_P]),
     "lrkv_cache_bytes": (SZ, [I32, I32, I32, ctypes.c_int64, I32]),
     "lrkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lrkv_last_cuda_error": (ctypes.c_int, []),

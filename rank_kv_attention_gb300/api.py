@@ -67,6 +67,16 @@ class PagedCache:
                               self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype])
 
 
+def prefill_kernel_kind(cache: PagedCache) -> int:
+    """LRKV_PREFILL_TILED or LRKV_PREFILL_PER_ROW: the attention kernel
+    lrkv_prefill runs for this cache."""
+    L = _abi.lib()
+    st = L.lrkv_prefill_kernel_kind(ctypes.byref(cache.desc()))
+    if st < 0:
+        raise _abi.LrkvError("lrkv_prefill_kernel_kind", st, L)
+    return st
+
+
 def cache_bytes(H, d_h, r, tokens, dtype=torch.bfloat16) -> int:
     return int(_abi.lib().lrkv_cache_bytes(H, d_h, r, tokens, _DT[dtype]))
 

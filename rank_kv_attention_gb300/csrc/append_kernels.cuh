@@ -56,5 +56,7 @@ struct PrefillTcArgs {
     cudaStream_t stream;
 };
 int launch_prefill_tc(const PrefillTcArgs &p);
+// Whether lrkv_prefill runs the tensor-core attention kernel for this cache.
+bool prefill_tc_covers(const lrkv_cache_t &cache);
 
 }  // namespace lrkv

@@ -282,6 +282,13 @@ const char *lrkv_status_string(int status) {
     }
 }
 
+int lrkv_prefill_kernel_kind(const lrkv_cache_t *cache) {
+    if (!cache) return LRKV_E_INVALID_ARG;
+    const int st = check_cache(cache);
+    if (st) return st;
+    return prefill_tc_covers(*cache) ? LRKV_PREFILL_TILED : LRKV_PREFILL_PER_ROW;
+}
+
 size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype) {
     if (check_dims(H, d_h, r, dtype) || tokens < 0) return 0;
     return (size_t)tokens * 2 * ((size_t)d_h + (size_t)H * r) * elem_bytes(dtype);

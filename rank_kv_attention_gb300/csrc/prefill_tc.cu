@@ -501,18 +501,17 @@ cudaError_t launch_r16(const PfMaps &maps, const PfArgs &a, dim3 grid, cudaStrea
 
 }  // namespace
 
-int launch_prefill_tc(const PrefillTcArgs &p) {
+// Shape checks and tensor maps of one call; false when the shape is not covered.
+static bool prefill_tc_plan(const PrefillTcArgs &p, PfMaps &maps, int &n_qtiles) {
     const lrkv_cache_t &c = p.cache;
     if (c.dtype != LRKV_BF16 || c.d_h != 128 || c.r < 8 || c.r > 64 || c.r % 8 != 0 ||
-        c.page_size % PF_BN != 0 || c.H > 65535 || p.B > 65535 || p.n < 1)
-        return 1;
+        c.page_size % PF_BN != 0 || c.H > 65535 || p.B > 65535 || p.n < 1 || p.max_ctx < 1)
+        return false;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
     const int64_t max_len = (int64_t)p.max_pages * c.page_size;
-    if (rows + PF_BN >= INT32_MAX || max_len >= INT32_MAX || (int64_t)c.H * 128 >= INT32_MAX)
-        return 1;
-    const int n_qtiles = (std::min(p.n, p.max_ctx) + PF_BM - 1) / PF_BM;
-    if (n_qtiles > 65535) return 1;
-    PfMaps maps;
+    if (rows + PF_BN >= INT32_MAX || max_len >= INT32_MAX) return false;
+    n_qtiles = (std::min(p.n, p.max_ctx) + PF_BM - 1) / PF_BM;
+    if (n_qtiles > 65535) return false;
     const uint64_t Hr = (uint64_t)c.H * c.r;
     const uint64_t qdims[3] = {128, (uint64_t)c.H, (uint64_t)p.n};
     const uint64_t qstr[2] = {256, (uint64_t)c.H * 256};
@@ -521,14 +520,33 @@ int launch_prefill_tc(const PrefillTcArgs &p) {
     const uint64_t r_dims[2] = {Hr, (uint64_t)rows}, r_str[1] = {Hr * 2};
     const uint64_t b_dims[2] = {(uint64_t)c.r, (uint64_t)c.H * 128}, b_str[1] = {(uint64_t)c.r * 2};
     const uint32_t box[2] = {64, 64};
-    if (!tma_map_bf16(&maps.q, p.Q, 3, qdims, qstr, qbox) ||
-        !tma_map_bf16(&maps.sk, c.S_K, 2, kv_dims, kv_str, box) ||
-        !tma_map_bf16(&maps.sv, c.S_V, 2, kv_dims, kv_str, box) ||
-        !tma_map_bf16(&maps.rk, c.R_K, 2, r_dims, r_str, box) ||
-        !tma_map_bf16(&maps.rv, c.R_V, 2, r_dims, r_str, box) ||
-        !tma_map_bf16(&maps.bk, p.B_K, 2, b_dims, b_str, box) ||
-        !tma_map_bf16(&maps.bv, p.B_V, 2, b_dims, b_str, box))
-        return 1;
+    return tma_map_bf16(&maps.q, p.Q, 3, qdims, qstr, qbox) &&
+           tma_map_bf16(&maps.sk, c.S_K, 2, kv_dims, kv_str, box) &&
+           tma_map_bf16(&maps.sv, c.S_V, 2, kv_dims, kv_str, box) &&
+           tma_map_bf16(&maps.rk, c.R_K, 2, r_dims, r_str, box) &&
+           tma_map_bf16(&maps.rv, c.R_V, 2, r_dims, r_str, box) &&
+           tma_map_bf16(&maps.bk, p.B_K, 2, b_dims, b_str, box) &&
+           tma_map_bf16(&maps.bv, p.B_V, 2, b_dims, b_str, box);
+}
+
+bool prefill_tc_covers(const lrkv_cache_t &cache) {
+    PrefillTcArgs p = {};
+    p.cache = cache;
+    p.Q = p.B_K = p.B_V = cache.S_K;  // any 16-byte aligned device address
+    p.B = 1;
+    p.n = 1;
+    p.max_ctx = 1;
+    p.max_pages = 1;
+    PfMaps maps;
+    int nq = 0;
+    return prefill_tc_plan(p, maps, nq);
+}
+
+int launch_prefill_tc(const PrefillTcArgs &p) {
+    const lrkv_cache_t &c = p.cache;
+    PfMaps maps;
+    int n_qtiles = 0;
+    if (!prefill_tc_plan(p, maps, n_qtiles)) return 1;
     PfArgs a;
     a.cu_rows = p.cu_rows;
     a.start_pos = p.start_pos;
@@ -542,7 +560,7 @@ int launch_prefill_tc(const PrefillTcArgs &p) {
     a.page_size = c.page_size;
     a.max_pages = p.max_pages;
     a.num_pages = c.num_pages;
-    a.max_len = (int)max_len;
+    a.max_len = p.max_pages * c.page_size;
     a.n_qtiles = n_qtiles;
     a.scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     // heaviest query tiles (most keys) first: blockIdx.z counts tiles from the end

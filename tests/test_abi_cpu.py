@@ -113,3 +113,18 @@ def test_prefill_rejects_on_host(lib):
     args[6] = 200
     args[18] = None
     assert lib.lrkv_prefill(*args) == _abi.LRKV_E_WORKSPACE
+
+
+def test_prefill_kernel_kind_host_checks(lib):
+    assert lib.lrkv_prefill_kernel_kind(None) == _abi.LRKV_E_INVALID_ARG
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(dtype=5))) == _abi.LRKV_E_DTYPE
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(d_h=130))) == _abi.LRKV_E_SHAPE
+    # shapes outside the tiled kernel always take the per-row path
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(d_h=64))) == _abi.LRKV_PREFILL_PER_ROW
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(r=72))) == _abi.LRKV_PREFILL_PER_ROW
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(page_size=32))) == \
+        _abi.LRKV_PREFILL_PER_ROW
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache(dtype=0))) == _abi.LRKV_PREFILL_PER_ROW
+    # covered shape: tiled wherever the driver can encode tensor maps
+    assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache())) in (
+        _abi.LRKV_PREFILL_PER_ROW, _abi.LRKV_PREFILL_TILED)

@@ -118,3 +118,93 @@ def test_prefill_2048_sampled():
                              rows_wanted=want_rows, heads_wanted=heads)
         for i in want_rows:
             assert_close(got[rows[i]][heads], ref[i][heads], "bf16", f"req {b} row {i}")
+
+
+# --------------------------------------------------------------------------
+# Tiled tensor-core attention: shapes, tails, history, bad pages
+# --------------------------------------------------------------------------
+def _history_then_prefill(H, r, page_size, hist, new, seed, d=64, d_h=128, bad_page=None):
+    """Append each request's history with lrkv_append, then lrkv_prefill the
+    new rows.  Returns (device out, status, float64 oracle out, per-row
+    request ids, per-row positions, cache)."""
+    import rank_kv_attention_gb300 as L
+    from rank_kv_attention_gb300.api import PagedCache
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    caps = [a + b for a, b in zip(hist, new)]
+    pt, num_pages = I.make_page_table(caps, page_size, True, rng, 2)
+    pools = I.empty_pools(num_pages, page_size, H, d_h, r, "bf16", canary=True)
+    cache = PagedCache(*[dev(p, "bf16") for p in pools])
+    assert L.prefill_kernel_kind(cache) == L.LRKV_PREFILL_TILED
+    draw = lambda s: I.f32_to_bf16_bits((rng.standard_normal(s) / np.sqrt(d)).astype(np.float32))
+    Xh = [draw((k, d)) for k in hist]
+    if sum(hist):
+        pos = np.concatenate([np.arange(k) for k in hist]).astype(np.int32)
+        sid = np.concatenate([np.full(k, b) for b, k in enumerate(hist)]).astype(np.int32)
+        L.append(dev(np.concatenate(Xh), "bf16"), dev(pos, "i32"), dev(sid, "i32"),
+                 dev(w.W_S_K, "bf16"), dev(w.W_S_V, "bf16"), dev(w.U_K, "bf16"),
+                 dev(w.U_V, "bf16"), cache, dev(pt, "i32"))
+    if bad_page is not None:
+        b, k = bad_page
+        pt = pt.copy()
+        pt[b, k] = num_pages + 7
+    Xn = draw((sum(new), d))
+    Qn = I.f32_to_bf16_bits(rng.standard_normal((sum(new), H, d_h)).astype(np.float32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    max_ctx = int(max(caps))
+    out = L.prefill(dev(Xn, "bf16"), dev(Qn, "bf16"), dev(cu, "i32"), dev(np.array(hist), "i32"),
+                    max_ctx, dev(w.W_S_K, "bf16"), dev(w.W_S_V, "bf16"), dev(w.U_K, "bf16"),
+                    dev(w.U_V, "bf16"), dev(w.B_K, "bf16"), dev(w.B_V, "bf16"), cache,
+                    dev(pt, "i32"), status=status)
+    f = lambda a: I.to_f64(a, "bf16")
+    history = {b: oracle.project(f(Xh[b]), f(w.W_S_K), f(w.W_S_V), f(w.U_K), f(w.U_V))
+               for b in range(len(hist)) if hist[b]}
+    pos = np.concatenate([np.arange(hist[b], hist[b] + new[b]) for b in range(len(new))])
+    sid = np.concatenate([np.full(new[b], b) for b in range(len(new))])
+    ref = oracle.prefill(f(Qn), f(Xn), pos, sid, f(w.W_S_K), f(w.W_S_V), f(w.U_K), f(w.U_V),
+                         f(w.B_K), f(w.B_V), history=history)
+    return out, int(status.item()), ref, sid, pos, cache
+
+
+# (H, r, page_size, history, new rows): several query tiles per request,
+# ragged last tiles and key tiles, an empty request, r not a multiple of 16,
+# r = 8 and 64, H r below one 64-column box, 128-row pages.
+TILED = [
+    (16, 48, 64, [0, 77, 200], [300, 1, 129]),
+    (8, 8, 64, [5, 0], [140, 64]),
+    (4, 16, 128, [130, 0, 64], [70, 200, 0]),
+    (32, 32, 64, [64, 1], [64, 255]),
+    (16, 56, 64, [10, 300], [90, 40]),
+    (2, 64, 128, [0], [257]),
+    (16, 40, 64, [33], [200]),
+    (1, 48, 64, [0], [100]),
+]
+
+
+@pytest.mark.parametrize("H,r,page_size,hist,new", TILED)
+def test_tiled_prefill_parity(H, r, page_size, hist, new):
+    out, st, ref, _, _, _ = _history_then_prefill(H, r, page_size, hist, new, seed=H * 7 + r)
+    assert st == 0
+    assert_close(host(out, "bf16"), ref, "bf16", f"H={H} r={r} page={page_size}")
+
+
+def test_tiled_prefill_deterministic():
+    a, _, _, _, _, _ = _history_then_prefill(16, 48, 64, [40], [300], seed=3)
+    b, _, _, _, _, _ = _history_then_prefill(16, 48, 64, [40], [300], seed=3)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_tiled_prefill_bad_page_flagged():
+    """Request 1's second page id is outside the pool: append and attention
+    skip it and flag LRKV_STATUS_BAD_PAGE; request 0 and request 1's rows
+    that see only its first page still match the oracle; all outputs stay
+    finite."""
+    import rank_kv_attention_gb300 as L
+    out, st, ref, sid, pos, _ = _history_then_prefill(16, 48, 64, [0, 0], [100, 150], seed=12,
+                                                      bad_page=(1, 1))
+    got = host(out, "bf16")
+    assert st & L.LRKV_STATUS_BAD_PAGE
+    assert np.all(np.isfinite(got))
+    keep = (sid == 0) | (pos < 64)
+    assert_close(got[keep], ref[keep], "bf16", "rows unaffected by the bad page")
