@@ -192,6 +192,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     }
 }
 
+// Bounded wait that suspends the thread in hardware between polls (PTX
+// try_wait with a suspend-time hint of `hint_ns`) instead of re-polling the
+// barrier word: waiting warps then leave shared-memory bandwidth to the
+// tensor cores.  Same 2 s bound and return value as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                uint32_t hint_ns = 20000) {
+    const uint32_t a = smem_u32(bar);
+    uint32_t ok = 0;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+            "selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(a), "r"(parity), "r"(hint_ns)
+            : "memory");
+        if (ok) return true;
+        // the clock is read only once the phase was found incomplete
+        if (it == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
 // 2-D tiled TMA load: box at (x, y) of the tensor map into shared memory,
 // completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,

@@ -31,6 +31,16 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] . B[smem desc]^T: A (M x 16, 16-bit) read from tensor
+// memory, lane = row, each 32-bit column two consecutive K elements.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // arrive on an mbarrier when all previously issued tcgen05.mma of this thread complete
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
     asm volatile(
@@ -101,6 +111,32 @@ __device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t 
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Shared-memory descriptors split into 32-bit words: every 128-byte-swizzle
+// descriptor used here has the same upper word (stride byte offset 1024,
+// version 1, layout SWIZZLE_128B); the lower word holds the start address and
+// the leading byte offset, so a K step is a 32-bit add on the lower word.
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr >> 4) & 0x3FFF) | ((lbo >> 4) << 16);
+}
+// tc_mma_f16 / tc_mma_f16_ts with descriptors given by their lower words.
+__device__ __forceinline__ void tc_mma_lo(uint32_t d_tmem, uint32_t alo, uint32_t blo, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; .reg .b64 da, db; setp.ne.u32 p, %4, 0; mov.b64 da, {%1, %5}; "
+        "mov.b64 db, {%2, %5}; tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p; }" ::"r"(d_tmem),
+        "r"(alo), "r"(blo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; .reg .b64 db; setp.ne.u32 p, %4, 0; mov.b64 db, {%2, %5}; "
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(blo), "r"(idesc), "r"(accumulate), "r"(kSw128DescHi)
+        : "memory");
 }
 
 // kind::f16 instruction descriptor with a K-major A and an MN-major B.
