@@ -246,6 +246,24 @@ __device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3-D tiled TMA store of a shared-memory box to (x, y, z) of the tensor map,
+// tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z,
+                                             const void *src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the bulk stores of this thread have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Policy marking streamed data as first to leave L2, so that small tensors
 // reused every step (weights, bases, partials) stay resident.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
