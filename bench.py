@@ -135,18 +135,23 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def kernel_source_hash():
+DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
+PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
+
+
+def kernel_source_hash(files=DECODE_SPLIT_SOURCES):
     h = hashlib.sha256()
-    for f in ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "rank_kv_attention_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config):
-    """DRAM bytes per launch of the split kernel from the committed ncu summary,
-    or None if absent or taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", f"decode_split_{config}.md")
+def profiled_traffic(config, name="decode_split", files=DECODE_SPLIT_SOURCES):
+    """DRAM bytes per launch of a kernel from its committed ncu summary
+    (profiles/<name>_<config>.md), or None if absent or taken on a different
+    kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{name}_{config}.md")
     if not os.path.exists(path):
         return None
     vals = {}
@@ -154,7 +159,7 @@ def profiled_traffic(config):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash(files):
         return None
     try:
         return float(vals["dram_bytes_per_full_launch"])
@@ -481,23 +486,30 @@ def run_prefill(args, rank, world, local_rank):
     Ntot = 2 * d_h + 2 * H * r
     proj_flops = 2 * n * d * Ntot
     peak, kind = measured_peaks("bf16_tflops", 1900.0)
-    achieved = proj_flops / (res_k["projection"] / 1e3) / 1e12
-    attn_flops = 2 * 2 * (Bq * T * (T + 1) // 2) * H * (d_h + r)   # scores + values, causal
+    # attention: per (row, head) with v visible keys, scores and values cost
+    # 2 v (d_h + r) each; p = q B_K[h] and the B_V[h] expansion 2 d_h r each
+    visible = Bq * T * (T + 1) // 2
+    attn_flops = H * (4 * visible * (d_h + r) + 4 * n * d_h * r)
+    attn_tf = attn_flops / (res_k["attention"] / 1e3) / 1e12
+    proj_tf = proj_flops / (res_k["projection"] / 1e3) / 1e12
     return {
         "metric": "LRKV prefill tokens/s", "value": round(n / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": Bq, "d": d, "H": H,
-                   "d_h": d_h, "r": r, "seq_len": T, "rows": n},
-        "roofline": {"kernel": "append projection GEMM (tcgen05)", "bound": "tensor",
-                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "peak_source": f"{kind} bf16 GEMM (burst)",
-                     "flops_per_launch": proj_flops, "avg_launch_ms": round(res_k["projection"], 4),
-                     "traffic": None},
+                   "d_h": d_h, "r": r, "seq_len": T, "rows": n,
+                   "l2": "no flush: one step's working set (~0.3 GB) exceeds L2"},
+        "roofline": {"kernel": "prefill_tc_kernel (causal attention, tcgen05)", "bound": "tensor",
+                     "achieved": round(attn_tf, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(attn_tf / peak, 4), "peak_source": f"{kind} bf16 GEMM (burst)",
+                     "flops_per_launch": attn_flops, "avg_launch_ms": round(res_k["attention"], 4),
+                     "traffic": profiled_traffic(args.config, "prefill_attention", PREFILL_SOURCES)},
+        "projection": {"kernel": "append_tc_kernel (X.[W_S_K|W_S_V|U_K|U_V], tcgen05)",
+                       "achieved": round(proj_tf, 1), "unit": "TFLOP/s", "frac": round(proj_tf / peak, 4),
+                       "flops_per_launch": proj_flops, "avg_launch_ms": round(res_k["projection"], 4)},
         "breakdown_ms": {"projection": round(res_k["projection"], 4),
                          "attention": round(res_k["attention"], 4)},
-        "attention_tflops": round(attn_flops / (res_k["attention"] / 1e3) / 1e12, 1),
         "clocks": clk,
     }
 
