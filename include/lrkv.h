@@ -185,6 +185,39 @@ LRKV_API int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const
                                  int32_t max_seq_len, void *out, int32_t *dev_status,
                                  lrkv_stream_t stream);
 
+/*
+ * lrkv_decode_step - one decode step together with the append of its new
+ * rows (section 3: Algorithm 1 for the new row, then Algorithm 2 with
+ * equations 6 and 7).  Request b's new row X[b] is projected and written at
+ * position seq_lens[b] - 1, exactly where lrkv_append would put it, and
+ * request b is decoded over its seq_lens[b] rows, that new one included, as
+ * lrkv_decode would:
+ *
+ *   X [B, d]   one new row per request      q, out [B, H, d_h]
+ *   W_S_K, W_S_V, U_K, U_V as lrkv_append; B_K, B_V, page_table and
+ *   max_seq_len as lrkv_decode; seq_lens [B] counts the new row.
+ *   workspace >= lrkv_decode_step_workspace_bytes(B, H, d_h, r, max_seq_len,
+ *                dtype) bytes, 256-byte aligned, caller-owned scratch.
+ *
+ * Same result as lrkv_append (positions seq_lens[b] - 1, sequence ids b)
+ * followed by lrkv_decode, up to floating-point rounding order.  For bf16
+ * caches with d_h = 128, d % 128 == 0 and a (H, r) that the tensor-core decode
+ * covers, the decode's split kernel itself projects and writes the new rows
+ * while it streams the older ones, and the combine folds each new row in as
+ * one more key; other shapes run the append and the decode kernels in turn.
+ * A request with an invalid length gets no new row, out = 0 and
+ * LRKV_STATUS_BAD_SEQLEN; a new row on an invalid page is skipped (not
+ * attended) and flagged LRKV_STATUS_BAD_PAGE.
+ */
+LRKV_API size_t lrkv_decode_step_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                                 int32_t max_seq_len, int32_t dtype);
+LRKV_API int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_S_V,
+                              const void *U_K, const void *U_V, const void *q,
+                              const lrkv_cache_t *cache, const void *B_K, const void *B_V,
+                              const int32_t *seq_lens, const int32_t *page_table, int32_t B,
+                              int32_t max_pages, int32_t max_seq_len, void *out, void *workspace,
+                              size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream);
+
 /* Bytes of device workspace lrkv_prefill needs. */
 LRKV_API size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h,
                                     int32_t r, int32_t max_ctx, int32_t dtype);

@@ -15,7 +15,7 @@ from ._abi import (LRKV_BF16, LRKV_F32, LRKV_OK, LRKV_E_INVALID_ARG, LRKV_E_SHAP
 __all__ = [
     "lib", "CacheDesc", "LrkvError", "PagedCache", "append", "decode", "prefill",
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
-    "prefill_kernel_kind",
+    "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes",
 ]
 
 
@@ -23,7 +23,8 @@ def __getattr__(name):
     # torch-facing helpers are imported lazily so that the ctypes layer works
     # without importing torch
     if name in ("PagedCache", "append", "decode", "prefill", "decode_workspace_bytes",
-                "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind"):
+                "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind",
+                "decode_step", "decode_step_workspace_bytes"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -70,6 +70,9 @@ SIGNATURES = {
     "lrkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "lrkv_decode": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, P, SZ, P, P]),
     "lrkv_decode_noalloc": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, P, P]),
+    "lrkv_decode_step_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
+    "lrkv_decode_step": (ctypes.c_int, [P, I32, P, P, P, P, P, CACHE_P, P, P, P, P, I32, I32, I32, P,
+                                        P, SZ, P, P]),
     "lrkv_prefill_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),

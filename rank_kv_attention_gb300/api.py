@@ -139,6 +139,39 @@ def decode(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_len, ou
     return out
 
 
+def decode_step_workspace_bytes(B, H, d_h, r, max_seq_len, dtype=torch.bfloat16) -> int:
+    return _abi.lib().lrkv_decode_step_workspace_bytes(B, H, d_h, r, max_seq_len, _DT[dtype])
+
+
+def decode_step(X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_lens, page_table,
+                max_seq_len, out=None, ws=None, status=None, stream=None):
+    """lrkv_decode_step: append each request's new row X[b] at position
+    seq_lens[b] - 1, then decode; returns out [B, H, d_h]."""
+    dt = cache.dtype
+    for n, t in (("X", X), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V),
+                 ("q", q), ("B_K", B_K), ("B_V", B_V)):
+        _need(t, n, dt)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(page_table, "page_table", torch.int32)
+    B, H, d_h = q.shape
+    r = cache.R_K.shape[3]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dt)
+    need = decode_step_workspace_bytes(B, H, d_h, r, max_seq_len, dt)
+    if ws is None:
+        ws = workspace(need, q.device)
+    _need(ws, "ws", torch.uint8)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_decode_step(_ptr(X), X.shape[1], _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K),
+                                       _ptr(U_V), _ptr(q), ctypes.byref(desc), _ptr(B_K), _ptr(B_V),
+                                       _ptr(seq_lens), _ptr(page_table), B, page_table.shape[1],
+                                       max_seq_len, _ptr(out), _ptr(ws), ws.numel(), _ptr(status),
+                                       _stream(stream))
+    _abi.check("lrkv_decode_step", code)
+    return out
+
+
 def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
             cache: PagedCache, page_table, out=None, ws=None, status=None, stream=None):
     """lrkv_prefill: append the chunk X, then causal attention for each row's Q."""

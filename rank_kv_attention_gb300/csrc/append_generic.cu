@@ -404,6 +404,26 @@ __global__ void prefill_rows_kernel(const int32_t *__restrict__ cu_rows,
     req_row[i] = ok ? b : 0;
 }
 
+// Decode step through the separate append: request b's new row sits at
+// position seq_lens[b] - 1 (an invalid length gives position -1, which the
+// append skips and flags).
+__global__ void step_rows_kernel(const int32_t *__restrict__ seq_lens, int B, int max_len,
+                                 int32_t *pos, int32_t *sid) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int32_t L = seq_lens[b];
+    pos[b] = (L < 1 || L > max_len) ? -1 : L - 1;
+    sid[b] = b;
+}
+
+cudaError_t launch_step_rows(const int32_t *seq_lens, int B, int max_len, int32_t *pos,
+                             int32_t *sid, cudaStream_t s) {
+    return launch_pdl(step_rows_kernel, dim3((B + 255) / 256), dim3(256), 0, s, seq_lens, B,
+                      max_len, pos, sid);
+}
+
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s) {

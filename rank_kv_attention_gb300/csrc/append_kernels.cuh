@@ -36,6 +36,8 @@ cudaError_t launch_append_rows_mma(const AppendArgsT<__nv_bfloat16> &a);
 bool tc_append_supported(int n, int d, int d_h, int H, int r);
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);
 
+cudaError_t launch_step_rows(const int32_t *seq_lens, int B, int max_len, int32_t *pos,
+                             int32_t *sid, cudaStream_t s);
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s);

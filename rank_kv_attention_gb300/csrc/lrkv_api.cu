@@ -380,6 +380,79 @@ int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const void *B_
     return run_decode(a, scratch, (size_t)LRKV_NOALLOC_SCRATCH_BYTES);
 }
 
+// Decode-step workspace: the decode workspace, then positions and ids of the
+// new rows for shapes that run the separate append.
+static size_t step_ws_bytes(int B, int H, int d_h, int r, int max_seq_len, size_t *dec_bytes) {
+    const size_t dec = align256(decode_ws_bytes(B, H, d_h, r, max_seq_len));
+    if (dec_bytes) *dec_bytes = dec;
+    return dec + 2 * align256(sizeof(int32_t) * (size_t)B);
+}
+
+size_t lrkv_decode_step_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                        int32_t max_seq_len, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || B < 1 || max_seq_len < 1) return 0;
+    return step_ws_bytes(B, H, d_h, r, max_seq_len, nullptr);
+}
+
+int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_S_V,
+                     const void *U_K, const void *U_V, const void *q, const lrkv_cache_t *cache,
+                     const void *B_K, const void *B_V, const int32_t *seq_lens,
+                     const int32_t *page_table, int32_t B, int32_t max_pages,
+                     int32_t max_seq_len, void *out, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, lrkv_stream_t stream) {
+    // the append's checks (positions and ids are derived here, so any
+    // non-null stand-in passes) and the decode's
+    int st = check_append(X, seq_lens, seq_lens, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table,
+                          B, max_pages);
+    if (st) return st;
+    if (max_seq_len < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * cache->page_size) return LRKV_E_BOUNDS;
+    if ((int64_t)B * max_seq_len > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (!q || !B_K || !B_V || !out) return LRKV_E_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(B_K) || !aligned16(B_V) || !aligned16(out))
+        return LRKV_E_INVALID_ARG;
+    if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    size_t dec_bytes = 0;
+    if (workspace_bytes < step_ws_bytes(B, cache->H, cache->d_h, cache->r, max_seq_len, &dec_bytes))
+        return LRKV_E_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    DecodeArgs a;
+    a.q = q;
+    a.cache = *cache;
+    a.B_K = B_K;
+    a.B_V = B_V;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.req_row = nullptr;
+    a.B = B;
+    a.max_pages = max_pages;
+    a.max_seq_len = max_seq_len;
+    a.out = out;
+    a.status = dev_status;
+    a.stream = s;
+    const bool fused = cache->dtype == LRKV_BF16 && d % 128 == 0 && B <= kFusedStepMaxRows &&
+                       fast_decode_supported(cache->H, cache->d_h, cache->r, cache->page_size,
+                                             cache->dtype) &&
+                       fast_decode_step_fits(cache->H, cache->r, d);
+    if (fused) {
+        a.X = X;
+        a.W[0] = W_S_K;
+        a.W[1] = W_S_V;
+        a.W[2] = U_K;
+        a.W[3] = U_V;
+        a.d = d;
+        return run_decode(a, workspace, dec_bytes);
+    }
+    int32_t *pos = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + dec_bytes);
+    int32_t *sid = pos + align256(sizeof(int32_t) * (size_t)B) / sizeof(int32_t);
+    cudaError_t e = launch_step_rows(seq_lens, B, max_pages * cache->page_size, pos, sid, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = run_append(X, pos, sid, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
+                    dev_status, s);
+    if (st) return st;
+    return run_decode(a, workspace, dec_bytes);
+}
+
 size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h, int32_t r,
                                     int32_t max_ctx, int32_t dtype) {
     if (check_dims(H, d_h, r, dtype) || B < 1 || n < 0 || max_ctx < 1) return 0;

@@ -272,6 +272,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+// Policy marking data reused every step (weights) as last to leave L2.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 32-bit global load carrying an L2 cache policy.
+__device__ __forceinline__ uint32_t ld_u32_hint(const void *ptr, uint64_t policy) {
+    uint32_t v;
+    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(ptr), "l"(policy));
+    return v;
+}
+
 // Plain contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
@@ -279,6 +293,16 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The same bulk copy with an L2 cache policy on the source reads.
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes,
+                                               uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

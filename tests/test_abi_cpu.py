@@ -128,3 +128,27 @@ def test_prefill_kernel_kind_host_checks(lib):
     # covered shape: tiled wherever the driver can encode tensor maps
     assert lib.lrkv_prefill_kernel_kind(ctypes.byref(_cache())) in (
         _abi.LRKV_PREFILL_PER_ROW, _abi.LRKV_PREFILL_TILED)
+
+
+def test_decode_step_rejects_on_host(lib):
+    ws = ctypes.c_void_p(256)
+
+    def call(**over):
+        a = dict(X=16, d=2048, W=16, q=16, c=_cache(), BK=16, BV=16, sl=16, pt=16, B=2, mp=4,
+                 msl=100, out=16, ws=ws, wsb=1 << 30)
+        a.update(over)
+        return lib.lrkv_decode_step(a["X"], a["d"], a["W"], a["W"], a["W"], a["W"], a["q"],
+                                    ctypes.byref(a["c"]), a["BK"], a["BV"], a["sl"], a["pt"],
+                                    a["B"], a["mp"], a["msl"], a["out"], a["ws"], a["wsb"], None,
+                                    None)
+    assert call(X=None) == _abi.LRKV_E_INVALID_ARG
+    assert call(W=None) == _abi.LRKV_E_INVALID_ARG
+    assert call(q=None) == _abi.LRKV_E_INVALID_ARG
+    assert call(d=2047) == _abi.LRKV_E_SHAPE             # bf16 rows need d % 8 == 0
+    assert call(c=_cache(dtype=3)) == _abi.LRKV_E_DTYPE
+    assert call(msl=4 * 64 + 1) == _abi.LRKV_E_BOUNDS     # beyond max_pages * page_size
+    assert call(ws=None) == _abi.LRKV_E_WORKSPACE
+    assert call(wsb=64) == _abi.LRKV_E_WORKSPACE
+    a = lib.lrkv_decode_step_workspace_bytes(16, 16, 128, 48, 4096, 1)
+    assert a >= lib.lrkv_decode_workspace_bytes(16, 16, 128, 48, 4096, 1) > 0
+    assert lib.lrkv_decode_step_workspace_bytes(0, 16, 128, 48, 4096, 1) == 0
