@@ -6,3 +6,4 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 package imports nothing from the product path.
 """
 from .lrkv_oracle import *  # noqa: F401,F403
+from . import fp8  # noqa: F401  (8-bit cache storage)
