@@ -50,13 +50,21 @@ extern "C" {
 /* Same object as cudaStream_t. */
 typedef struct CUstream_st *lrkv_stream_t;
 
-typedef enum { LRKV_F32 = 0, LRKV_BF16 = 1 } lrkv_dtype_t;
+/*
+ * Element types.  LRKV_F32 and LRKV_BF16 apply to every floating tensor of a
+ * call.  LRKV_FP8_E4M3 stores the four cache pools as 8-bit E4M3 codes (OCP
+ * 8-bit floating point: sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, largest finite 448), each pool with its own scale
+ * (lrkv_cache_t.scale); every other floating tensor of the call (X, weights,
+ * q, Q, B_K, B_V, out) is bf16.  It halves the cache payload of equation 9.
+ */
+typedef enum { LRKV_F32 = 0, LRKV_BF16 = 1, LRKV_FP8_E4M3 = 2 } lrkv_dtype_t;
 
 enum {
     LRKV_OK = 0,
     LRKV_E_INVALID_ARG = -1, /* null pointer, negative count, misaligned pointer */
     LRKV_E_SHAPE = -2,       /* a dimension is zero, too large or inconsistent */
-    LRKV_E_DTYPE = -3,       /* dtype not LRKV_F32 / LRKV_BF16 */
+    LRKV_E_DTYPE = -3,       /* dtype not an lrkv_dtype_t, or a scale not positive finite */
     LRKV_E_BOUNDS = -4,      /* host-visible bound: max_seq_len > max_pages*page_size, ... */
     LRKV_E_WORKSPACE = -5,   /* workspace NULL, misaligned or smaller than required */
     LRKV_E_CUDA = -6         /* a CUDA call failed; lrkv_last_cuda_error() has the code */
@@ -78,7 +86,12 @@ enum {
  * Memory is caller-owned; the library never frees it.
  * Supported: 1 <= H <= 128, 1 <= d_h <= 256, 1 <= r <= 256, page_size a
  * multiple of 16 in [16, 1024]; with LRKV_BF16, d_h and r multiples of 8;
- * with LRKV_F32, multiples of 4.
+ * with LRKV_F32, multiples of 4; with LRKV_FP8_E4M3, d_h a multiple of 16, r
+ * of 8 and H*r of 16.
+ * With LRKV_FP8_E4M3 a pool with scale s stores, for a value x, the code of
+ * x / s rounded to the nearest E4M3 value (ties to even, finite values beyond
+ * +-448 saturating), and reads back decode(code) * s; scale[] is ignored for
+ * the other dtypes.
  */
 typedef struct {
     void *S_K;
@@ -90,7 +103,8 @@ typedef struct {
     int32_t H;
     int32_t d_h;
     int32_t r;
-    int32_t dtype; /* lrkv_dtype_t */
+    int32_t dtype;  /* lrkv_dtype_t */
+    float scale[4]; /* LRKV_FP8_E4M3: scale of S_K, S_V, R_K, R_V (positive, finite) */
 } lrkv_cache_t;
 
 /*

@@ -32,6 +32,8 @@ import numpy as np
 PAGE_SIZE = 64
 BF16_NAN_BITS = np.uint16(0x7FC1)  # canary for never-written cache slots
 F32_NAN_CANARY = np.float32(np.nan)
+FP8_NAN_CODE = np.uint8(0x7F)      # the same for 8-bit (E4M3) pools
+FP8_SCALE = 2.0 ** -5              # pool scale of the 8-bit cases: N(0,1) values use codes up to ~160
 
 
 # ----------------------------------------------------------------------------
@@ -56,6 +58,23 @@ def bf16_bits_to_f64(b) -> np.ndarray:
     return bf16_bits_to_f32(b).astype(np.float64)
 
 
+# ----------------------------------------------------------------------------
+# 8-bit (E4M3) codes (storage format only; the values they stand for are
+# defined by the oracle)
+# ----------------------------------------------------------------------------
+def f32_to_e4m3_codes(x) -> np.ndarray:
+    """Codes of float32 values (torch's float8_e4m3fn conversion), clamped to
+    the finite range first."""
+    import torch
+    v = np.clip(np.ascontiguousarray(x, dtype=np.float32), -448.0, 448.0)
+    return torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def act_dtype(dtype: str) -> str:
+    """Element type of the non-cache tensors used with a cache of this type."""
+    return "bf16" if dtype == "fp8" else dtype
+
+
 def to_f64(a, dtype: str) -> np.ndarray:
     """Exact float64 view of a stored tensor ('bf16' bits or 'f32')."""
     if dtype == "bf16":
@@ -63,24 +82,27 @@ def to_f64(a, dtype: str) -> np.ndarray:
     return np.asarray(a, dtype=np.float32).astype(np.float64)
 
 
-def _draw(rng: np.random.Generator, shape, std: float, dtype: str) -> np.ndarray:
+def _draw(rng: np.random.Generator, shape, std: float, dtype: str, scale: float = 1.0) -> np.ndarray:
     x = rng.standard_normal(size=shape, dtype=np.float32)
     if std != 1.0:
         x *= np.float32(std)
+    if dtype == "fp8":
+        return f32_to_e4m3_codes(x / np.float32(scale))
     return f32_to_bf16_bits(x) if dtype == "bf16" else x
 
 
-def _draw_chunked(rng, shape, std, dtype, chunk_elems=1 << 24):
+def _draw_chunked(rng, shape, std, dtype, chunk_elems=1 << 24, scale=1.0):
     """Like _draw but bounds the float32 temporary for very large pools."""
     shape = tuple(int(s) for s in shape)
     lead = shape[0]
     inner = int(np.prod(shape[1:])) if len(shape) > 1 else 1
-    out = np.empty(shape, dtype=np.uint16 if dtype == "bf16" else np.float32)
+    kind = {"bf16": np.uint16, "fp8": np.uint8}.get(dtype, np.float32)
+    out = np.empty(shape, dtype=kind)
     flat = out.reshape(lead, inner)
     step = max(1, chunk_elems // max(1, inner))
     for s in range(0, lead, step):
         e = min(lead, s + step)
-        flat[s:e] = _draw(rng, (e - s, inner), std, dtype)
+        flat[s:e] = _draw(rng, (e - s, inner), std, dtype, scale)
     return out
 
 
@@ -117,7 +139,7 @@ def make_page_table(seq_caps, page_size=PAGE_SIZE, shuffle=False, rng=None,
 
 def poison_tail_slots(pool, page_table, seq_lens, page_size, dtype):
     """Write the NaN canary into every slot at or beyond seq_len of each request."""
-    canary = BF16_NAN_BITS if dtype == "bf16" else F32_NAN_CANARY
+    canary = {"bf16": BF16_NAN_BITS, "fp8": FP8_NAN_CODE}.get(dtype, F32_NAN_CANARY)
     for b, L in enumerate(np.asarray(seq_lens)):
         L = int(L)
         n_pages = (L + page_size - 1) // page_size
@@ -149,6 +171,11 @@ class DecodeCase:
     R_V: np.ndarray
     B_K: np.ndarray            # [H, d_h, r]
     B_V: np.ndarray
+    scale: tuple = (1.0, 1.0, 1.0, 1.0)  # pool scales of an 8-bit ("fp8") cache
+
+    @property
+    def act_dtype(self):
+        return act_dtype(self.dtype)
 
     @property
     def max_pages(self):
@@ -168,7 +195,8 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
     """Decode inputs: a filled paged cache plus one query row per request.
 
     Queries and cache rows ~ N(0, q_std^2 / cache_std^2); bases ~ N(0, 1/r)
-    unless ``base_std`` is given.
+    unless ``base_std`` is given.  With dtype "fp8" the pools hold 8-bit codes
+    of value / FP8_SCALE and the queries and bases are bf16.
     """
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(B)
@@ -177,17 +205,19 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
     num_pages = max(num_pages, 1)
     if base_std is None:
         base_std = 1.0 / np.sqrt(r)
-    q = _draw(rng, (B, H, d_h), q_std, dtype)
-    B_K = _draw(rng, (H, d_h, r), base_std, dtype)
-    B_V = _draw(rng, (H, d_h, r), base_std, dtype)
-    S_K = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype)
-    S_V = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype)
-    R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype)
-    R_V = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype)
+    adt = act_dtype(dtype)
+    sc = FP8_SCALE if dtype == "fp8" else 1.0
+    q = _draw(rng, (B, H, d_h), q_std, adt)
+    B_K = _draw(rng, (H, d_h, r), base_std, adt)
+    B_V = _draw(rng, (H, d_h, r), base_std, adt)
+    S_K = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc)
+    S_V = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc)
+    R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc)
+    R_V = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc)
     for pool in (S_K, S_V, R_K, R_V):
         poison_tail_slots(pool, pt, seq_lens, page_size, dtype)
     return DecodeCase(B, H, d_h, r, dtype, page_size, seq_lens, pt, num_pages,
-                      q, S_K, S_V, R_K, R_V, B_K, B_V)
+                      q, S_K, S_V, R_K, R_V, B_K, B_V, (sc,) * 4)
 
 
 def ragged_lengths(B, lo, hi, seed):
@@ -271,6 +301,9 @@ def empty_pools(num_pages, page_size, H, d_h, r, dtype, canary=True):
     if dtype == "bf16":
         fill = BF16_NAN_BITS if canary else np.uint16(0)
         mk = lambda shape: np.full(shape, fill, dtype=np.uint16)
+    elif dtype == "fp8":
+        fill = FP8_NAN_CODE if canary else np.uint8(0)
+        mk = lambda shape: np.full(shape, fill, dtype=np.uint8)
     else:
         fill = F32_NAN_CANARY if canary else np.float32(0)
         mk = lambda shape: np.full(shape, fill, dtype=np.float32)

@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(HERE, "liblrkv.so")
 
 LRKV_F32 = 0
 LRKV_BF16 = 1
+LRKV_FP8_E4M3 = 2
 
 LRKV_OK = 0
 LRKV_E_INVALID_ARG = -1
@@ -43,7 +44,7 @@ class CacheDesc(ctypes.Structure):
         ("R_K", ctypes.c_void_p), ("R_V", ctypes.c_void_p),
         ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
         ("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32),
-        ("dtype", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("scale", ctypes.c_float * 4),
     ]
 
 

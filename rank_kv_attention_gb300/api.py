@@ -14,7 +14,8 @@ import torch
 
 from . import _abi
 
-_DT = {torch.float32: _abi.LRKV_F32, torch.bfloat16: _abi.LRKV_BF16}
+_DT = {torch.float32: _abi.LRKV_F32, torch.bfloat16: _abi.LRKV_BF16,
+       torch.float8_e4m3fn: _abi.LRKV_FP8_E4M3}
 
 
 def _ptr(t):
@@ -42,11 +43,15 @@ class PagedCache:
     """Caller-owned paged factored cache (four pools sharing page ids).
 
     S_K, S_V: [num_pages, page_size, d_h]; R_K, R_V: [num_pages, page_size, H, r].
+    Pools of torch.float8_e4m3fn hold 8-bit codes whose values are the codes
+    times ``scale`` (one scale per pool: S_K, S_V, R_K, R_V); the activations
+    used with such a cache are bf16.
     """
     S_K: torch.Tensor
     S_V: torch.Tensor
     R_K: torch.Tensor
     R_V: torch.Tensor
+    scale: tuple = (1.0, 1.0, 1.0, 1.0)
 
     @classmethod
     def empty(cls, num_pages, page_size, H, d_h, r, dtype=torch.bfloat16, device="cuda"):
@@ -58,13 +63,19 @@ class PagedCache:
     def dtype(self):
         return self.S_K.dtype
 
+    @property
+    def act_dtype(self):
+        """dtype of every other floating tensor used with this cache."""
+        return torch.bfloat16 if self.dtype == torch.float8_e4m3fn else self.dtype
+
     def desc(self) -> _abi.CacheDesc:
         for n in ("S_K", "S_V", "R_K", "R_V"):
             _need(getattr(self, n), n, self.dtype)
         npg, ps, d_h = self.S_K.shape
         _, _, H, r = self.R_K.shape
         return _abi.CacheDesc(self.S_K.data_ptr(), self.S_V.data_ptr(), self.R_K.data_ptr(),
-                              self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype])
+                              self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype],
+                              (ctypes.c_float * 4)(*[float(x) for x in self.scale]))
 
 
 def prefill_kernel_kind(cache: PagedCache) -> int:
@@ -97,7 +108,7 @@ def workspace(nbytes, device="cuda") -> torch.Tensor:
 def append(X, positions, seq_ids, W_S_K, W_S_V, U_K, U_V, cache: PagedCache, page_table,
            status=None, stream=None):
     """lrkv_append: project rows X and store them at (seq_ids, positions)."""
-    dt = cache.dtype
+    dt = cache.act_dtype
     for n, t in (("X", X), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V)):
         _need(t, n, dt)
     for n, t in (("positions", positions), ("seq_ids", seq_ids), ("page_table", page_table)):
@@ -116,7 +127,7 @@ def append(X, positions, seq_ids, W_S_K, W_S_V, U_K, U_V, cache: PagedCache, pag
 def decode(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_len, out=None,
            ws=None, status=None, stream=None):
     """lrkv_decode: per-head attention output [B, H, d_h] of one decode step."""
-    dt = cache.dtype
+    dt = cache.act_dtype
     for n, t in (("q", q), ("B_K", B_K), ("B_V", B_V)):
         _need(t, n, dt)
     _need(seq_lens, "seq_lens", torch.int32)
@@ -147,7 +158,7 @@ def decode_step(X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_l
                 max_seq_len, out=None, ws=None, status=None, stream=None):
     """lrkv_decode_step: append each request's new row X[b] at position
     seq_lens[b] - 1, then decode; returns out [B, H, d_h]."""
-    dt = cache.dtype
+    dt = cache.act_dtype
     for n, t in (("X", X), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V),
                  ("q", q), ("B_K", B_K), ("B_V", B_V)):
         _need(t, n, dt)
@@ -175,7 +186,7 @@ def decode_step(X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_l
 def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
             cache: PagedCache, page_table, out=None, ws=None, status=None, stream=None):
     """lrkv_prefill: append the chunk X, then causal attention for each row's Q."""
-    dt = cache.dtype
+    dt = cache.act_dtype
     for n, t in (("X", X), ("Q", Q), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K),
                  ("U_V", U_V), ("B_K", B_K), ("B_V", B_V)):
         _need(t, n, dt)

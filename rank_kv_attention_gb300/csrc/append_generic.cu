@@ -91,12 +91,7 @@ __global__ void __launch_bounds__(256) append_generic_kernel(AppendArgsT<T> a) {
         for (int q = 0; q < 4; ++q) {
             const int c = c0 + tx * 4 + q;
             if (c >= Ntot) continue;
-            T *dst;
-            if (c < d_h) dst = a.S_K + row * d_h + c;
-            else if (c < 2 * d_h) dst = a.S_V + row * d_h + (c - d_h);
-            else if (c < 2 * d_h + Hr) dst = a.R_K + row * Hr + (c - 2 * d_h);
-            else dst = a.R_V + row * Hr + (c - 2 * d_h - Hr);
-            Elem<T>::store(dst, acc[rr][q]);
+            store_projected(a, (size_t)row, c, acc[rr][q]);
         }
     }
 }
@@ -214,12 +209,7 @@ __global__ void __launch_bounds__(kSkWarps * 32) append_rows_kernel(AppendArgsT<
         if (c >= Ntot || lane >= nr) continue;
         const int64_t row = dst_row[lane];
         if (row < 0) continue;
-        T *dst;
-        if (c < d_h) dst = a.S_K + row * d_h + c;
-        else if (c < 2 * d_h) dst = a.S_V + row * d_h + (c - d_h);
-        else if (c < 2 * d_h + Hr) dst = a.R_K + row * Hr + (c - 2 * d_h);
-        else dst = a.R_V + row * Hr + (c - 2 * d_h - Hr);
-        Elem<T>::store(dst, mine);
+        store_projected(a, (size_t)row, c, mine);
     }
 }
 
@@ -319,12 +309,7 @@ __global__ void __launch_bounds__(kTcWarps * 32) append_rows_mma_kernel(AppendAr
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < kTcWarps; ++w) v += part[(w * kTcRows + row) * kTcCols + o % kTcCols];
-        __nv_bfloat16 *dst;
-        if (cidx < d_h) dst = a.S_K + dr * d_h + cidx;
-        else if (cidx < 2 * d_h) dst = a.S_V + dr * d_h + (cidx - d_h);
-        else if (cidx < 2 * d_h + Hr) dst = a.R_K + dr * Hr + (cidx - 2 * d_h);
-        else dst = a.R_V + dr * Hr + (cidx - 2 * d_h - Hr);
-        *dst = __float2bfloat16_rn(v);
+        store_projected(a, (size_t)dr, cidx, v);
     }
 }
 

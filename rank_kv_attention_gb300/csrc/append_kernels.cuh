@@ -17,7 +17,30 @@ struct AppendArgsT {
     int B, max_pages, num_pages, page_size, H, d_h, r;
     int32_t *status;
     cudaStream_t stream;
+    // LRKV_FP8_E4M3: the pools are 8-bit codes (S_K .. R_V above unused)
+    bool fp8 = false;
+    uint8_t *q8[4] = {nullptr, nullptr, nullptr, nullptr};  // S_K, S_V, R_K, R_V codes
+    float inv_scale[4] = {1.f, 1.f, 1.f, 1.f};
 };
+
+// Store value v of packed output column c (0 .. 2 d_h + 2 H r) for pool row
+// `row`: the four pools in order S_K, S_V, R_K, R_V.
+template <typename T>
+__device__ __forceinline__ void store_projected(const AppendArgsT<T> &a, size_t row, int c, float v) {
+    const int Hr = a.H * a.r;
+    int k, col;
+    size_t width;
+    if (c < a.d_h) { k = 0; col = c; width = a.d_h; }
+    else if (c < 2 * a.d_h) { k = 1; col = c - a.d_h; width = a.d_h; }
+    else if (c < 2 * a.d_h + Hr) { k = 2; col = c - 2 * a.d_h; width = Hr; }
+    else { k = 3; col = c - 2 * a.d_h - Hr; width = Hr; }
+    if (a.fp8) {
+        a.q8[k][row * width + col] = (uint8_t)(e4m3x2_from_f32(v * a.inv_scale[k], 0.f) & 0xffu);
+    } else {
+        T *base = k == 0 ? a.S_K : k == 1 ? a.S_V : k == 2 ? a.R_K : a.R_V;
+        Elem<T>::store(base + row * width + col, v);
+    }
+}
 
 template <typename T>
 cudaError_t launch_append_generic(const AppendArgsT<T> &a);

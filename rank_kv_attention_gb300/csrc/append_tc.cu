@@ -148,6 +148,27 @@ __global__ void __launch_bounds__(128, 1)
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
             const int cc = col0 + c * 32;
             if (dr < 0 || cc >= width) continue;
+            if (a.fp8) {  // 8-bit codes of v / scale
+                uint8_t *q = a.q8[seg] + dr * rowlen + cc;
+                const float is = a.inv_scale[seg];
+                if (cc + 32 <= width) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        pk[e] = (uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e]) * is,
+                                                          __uint_as_float(v[4 * e + 1]) * is) |
+                                ((uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e + 2]) * is,
+                                                           __uint_as_float(v[4 * e + 3]) * is)
+                                 << 16);
+                    uint4 *q4 = reinterpret_cast<uint4 *>(q);
+                    q4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    q4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                } else {
+                    for (int e = 0; e < width - cc; ++e)
+                        q[e] = (uint8_t)(e4m3x2_from_f32(__uint_as_float(v[e]) * is, 0.f) & 0xffu);
+                }
+                continue;
+            }
             __nv_bfloat16 *dst = base + dr * rowlen + cc;
             if (cc + 32 <= width) {
                 uint32_t pk[16];

@@ -155,12 +155,14 @@ __device__ __forceinline__ int find_request(const int32_t *off, int B, int32_t x
 // ---------------------------------------------------------------------------
 constexpr int kGenTile = 128;
 
-template <typename T>
+// T: query element type; TC: cache element type (T, or 8-bit codes whose pool
+// scales sc = (S_K, S_V, R_K, R_V) fold into the queries and accumulators).
+template <typename T, typename TC>
 __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
-    const T *__restrict__ q, const T *__restrict__ S_K, const T *__restrict__ S_V,
-    const T *__restrict__ R_K, const T *__restrict__ R_V, const int32_t *__restrict__ page_table,
+    const T *__restrict__ q, const TC *__restrict__ S_K, const TC *__restrict__ S_V,
+    const TC *__restrict__ R_K, const TC *__restrict__ R_V, const int32_t *__restrict__ page_table,
     const int32_t *__restrict__ req_row, int max_pages, int num_pages, int page_size, int B, int H, int d_h, int r,
-    float scale_log2, DecodeWs ws, int32_t *status) {
+    float scale_log2, float4 sc, DecodeWs ws, int32_t *status) {
     extern __shared__ float sm[];
     float *qs = sm;                 // d_h
     float *ps = qs + d_h;           // r
@@ -185,8 +187,9 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
         const int t_a = start - base, t_b = seg_end - base;
 
         const int32_t *pt = page_table + (size_t)(req_row ? req_row[b] : b) * max_pages;
-        for (int d = tid; d < d_h; d += kGenTile) qs[d] = Elem<T>::load(q + ((size_t)b * H + h) * d_h + d);
-        for (int k = tid; k < r; k += kGenTile) ps[k] = ws.p[((size_t)b * H + h) * r + k];
+        for (int d = tid; d < d_h; d += kGenTile)
+            qs[d] = Elem<T>::load(q + ((size_t)b * H + h) * d_h + d) * sc.x;
+        for (int k = tid; k < r; k += kGenTile) ps[k] = ws.p[((size_t)b * H + h) * r + k] * sc.z;
         __syncthreads();
 
         float m = -INFINITY, l = 0.f;
@@ -203,11 +206,11 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     valid = false;
                 } else {
                     prow = page * page_size + j % page_size;
-                    const T *sk = S_K + (size_t)prow * d_h;
-                    const T *rk = R_K + ((size_t)prow * H + h) * r;
+                    const TC *sk = S_K + (size_t)prow * d_h;
+                    const TC *rk = R_K + ((size_t)prow * H + h) * r;
                     float acc = 0.f;
-                    for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], Elem<T>::load(sk + d), acc);
-                    for (int k = 0; k < r; ++k) acc = fmaf(ps[k], Elem<T>::load(rk + k), acc);
+                    for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], CacheLoad<TC>::load(sk + d), acc);
+                    for (int k = 0; k < r; ++k) acc = fmaf(ps[k], CacheLoad<TC>::load(rk + k), acc);
                     s = acc * scale_log2;
                 }
             }
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     float a = accS[i];
                     for (int jj = 0; jj < n; ++jj) {
                         if (row[jj] < 0) continue;
-                        a = fmaf(w[jj], Elem<T>::load(S_V + (size_t)row[jj] * d_h + d), a);
+                        a = fmaf(w[jj], CacheLoad<TC>::load(S_V + (size_t)row[jj] * d_h + d), a);
                     }
                     accS[i] = a;
                 }
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     float a = accR[i];
                     for (int jj = 0; jj < n; ++jj) {
                         if (row[jj] < 0) continue;
-                        a = fmaf(w[jj], Elem<T>::load(R_V + ((size_t)row[jj] * H + h) * r + d), a);
+                        a = fmaf(w[jj], CacheLoad<TC>::load(R_V + ((size_t)row[jj] * H + h) * r + d), a);
                     }
                     accR[i] = a;
                 }
@@ -269,8 +272,8 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int d = tid + i * kGenTile;
-            if (d < d_h) acc[d] = accS[i];
-            if (d < r) acc[d_h + d] = accR[i];
+            if (d < d_h) acc[d] = accS[i] * sc.y;
+            if (d < r) acc[d_h + d] = accR[i] * sc.w;
         }
         start = seg_end;
         __syncthreads();
@@ -479,16 +482,25 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
                       a.status);
 }
 
-template <typename T>
-cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G) {
+template <typename T, typename TC>
+static cudaError_t launch_split_generic_t(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const auto &c = a.cache;
     const size_t sm = sizeof(float) * (c.d_h + c.r + kGenTile) + sizeof(int32_t) * kGenTile;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)c.d_h);
-    return launch_pdl(decode_split_generic_kernel<T>, dim3(G, c.H), dim3(kGenTile), sm, a.stream,
-                      static_cast<const T *>(a.q), static_cast<const T *>(c.S_K),
-                      static_cast<const T *>(c.S_V), static_cast<const T *>(c.R_K),
-                      static_cast<const T *>(c.R_V), a.page_table, a.req_row, a.max_pages,
-                      c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r, scale_log2, ws, a.status);
+    const bool q8 = c.dtype == LRKV_FP8_E4M3;
+    const float4 sc = q8 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
+                         : make_float4(1.f, 1.f, 1.f, 1.f);
+    return launch_pdl(decode_split_generic_kernel<T, TC>, dim3(G, c.H), dim3(kGenTile), sm, a.stream,
+                      static_cast<const T *>(a.q), static_cast<const TC *>(c.S_K),
+                      static_cast<const TC *>(c.S_V), static_cast<const TC *>(c.R_K),
+                      static_cast<const TC *>(c.R_V), a.page_table, a.req_row, a.max_pages,
+                      c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r, scale_log2, sc, ws, a.status);
+}
+
+template <typename T>
+cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G) {
+    if (a.cache.dtype == LRKV_FP8_E4M3) return launch_split_generic_t<__nv_bfloat16, uint8_t>(a, ws, G);
+    return launch_split_generic_t<T, T>(a, ws, G);
 }
 
 template <typename T>

@@ -2,6 +2,7 @@
 // workspace layout, and dispatch to the kernels.  Nothing here allocates.
 #include <math.h>
 #include <algorithm>
+#include <cmath>
 #include <string.h>
 
 #include "append_kernels.cuh"
@@ -52,11 +53,16 @@ int device_sm_count() {
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
-static int elem_bytes(int dtype) { return dtype == LRKV_BF16 ? 2 : 4; }
+// Bytes of one cache element (the pools); activations of an 8-bit cache are bf16.
+static int elem_bytes(int dtype) { return dtype == LRKV_F32 ? 4 : dtype == LRKV_BF16 ? 2 : 1; }
 
 static int check_dims(int H, int d_h, int r, int dtype) {
-    if (dtype != LRKV_F32 && dtype != LRKV_BF16) return LRKV_E_DTYPE;
+    if (dtype != LRKV_F32 && dtype != LRKV_BF16 && dtype != LRKV_FP8_E4M3) return LRKV_E_DTYPE;
     if (H < 1 || H > 128 || d_h < 1 || d_h > 256 || r < 1 || r > 256) return LRKV_E_SHAPE;
+    if (dtype == LRKV_FP8_E4M3) {  // 16-byte rows of codes; bf16 activations
+        if (d_h % 16 || r % 8 || (H * r) % 16) return LRKV_E_SHAPE;
+        return LRKV_OK;
+    }
     const int mult = dtype == LRKV_BF16 ? 8 : 4;
     if (d_h % mult || r % mult) return LRKV_E_SHAPE;
     return LRKV_OK;
@@ -72,6 +78,10 @@ static int check_cache(const lrkv_cache_t *c) {
     if (c->num_pages < 1 || c->page_size < 16 || c->page_size > 1024 || c->page_size % 16)
         return LRKV_E_SHAPE;
     if ((int64_t)c->num_pages * c->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (c->dtype == LRKV_FP8_E4M3)
+        for (int k = 0; k < 4; ++k)
+            if (!(c->scale[k] > 0.f) || !std::isfinite(c->scale[k]) || !std::isfinite(1.f / c->scale[k]))
+                return LRKV_E_DTYPE;
     return LRKV_OK;
 }
 
@@ -104,7 +114,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     const bool fast = fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype);
     const int G = fast ? geo.G_fast : geo.G_gen;
     cudaError_t e;
-    if (c.dtype == LRKV_BF16) {
+    if (c.dtype != LRKV_F32) {  // bf16 activations (bf16 or 8-bit cache)
         e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign);
         if (e == cudaSuccess) {
             prof_before(LRKV_PROFILE_ATTENTION, a.stream);
@@ -154,6 +164,15 @@ static AppendArgsT<T> make_append_args(const void *X, const int32_t *positions,
     a.r = c->r;
     a.status = status;
     a.stream = s;
+    if (c->dtype == LRKV_FP8_E4M3) {
+        a.fp8 = true;
+        void *pools[4] = {c->S_K, c->S_V, c->R_K, c->R_V};
+        for (int k = 0; k < 4; ++k) {
+            a.q8[k] = static_cast<uint8_t *>(pools[k]);
+            a.inv_scale[k] = 1.f / c->scale[k];
+        }
+        a.S_K = a.S_V = a.R_K = a.R_V = nullptr;
+    }
     return a;
 }
 
@@ -164,7 +183,7 @@ static int check_append(const void *X, const int32_t *positions, const int32_t *
     int st = check_cache(cache);
     if (st) return st;
     if (n < 0 || B < 1 || max_pages < 1) return LRKV_E_SHAPE;
-    if (d < 1 || d > 65536 || d % (cache->dtype == LRKV_BF16 ? 8 : 4)) return LRKV_E_SHAPE;
+    if (d < 1 || d > 65536 || d % (cache->dtype == LRKV_F32 ? 4 : 8)) return LRKV_E_SHAPE;
     if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
     if (n == 0) return LRKV_OK;
     if (!X || !positions || !seq_ids || !W_S_K || !W_S_V || !U_K || !U_V || !page_table)
@@ -182,7 +201,7 @@ static int run_append(const void *X, const int32_t *positions, const int32_t *se
     if (n == 0) return LRKV_OK;
     cudaError_t e;
     prof_before(LRKV_PROFILE_PROJECTION, s);
-    if (c->dtype == LRKV_BF16) {
+    if (c->dtype != LRKV_F32) {  // bf16 rows and weights (bf16 or 8-bit cache)
         auto a = make_append_args<__nv_bfloat16>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K,
                                                  U_V, c, page_table, B, max_pages, status, s);
         if (rows_mma_append_fits(a)) e = launch_append_rows_mma(a);

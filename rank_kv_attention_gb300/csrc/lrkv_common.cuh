@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -127,6 +128,40 @@ __device__ __forceinline__ void stage_f32(float *dst, const T *src, int n) {
                 for (int e = 0; e < V; ++e) dst[(base + u * blockDim.x) * V + e] = v[u][e];
     }
 }
+
+// ---------------------------------------------------------------------------
+// 8-bit E4M3 cache codes (LRKV_FP8_E4M3)
+// ---------------------------------------------------------------------------
+// Two floats -> two codes (round to nearest even, saturating at +-448; NaN
+// stays NaN); `lo` lands in bits 0-7.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two codes -> two fp16 values (exact: every E4M3 value is an fp16 value); the
+// code in bits 0-7 lands in the low half.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint16_t codes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
+    return r;
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t code) {
+    const uint32_t h2 = f16x2_from_e4m3x2(code);
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+}
+
+// Value of one stored cache element, before its pool's scale.
+template <typename TC> struct CacheLoad;
+template <> struct CacheLoad<float> {
+    __device__ static float load(const float *p) { return *p; }
+};
+template <> struct CacheLoad<__nv_bfloat16> {
+    __device__ static float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+};
+template <> struct CacheLoad<uint8_t> {
+    __device__ static float load(const uint8_t *p) { return e4m3_to_f32(*p); }
+};
 
 __device__ __forceinline__ void status_or(int32_t *st, uint32_t bits) {
     if (st) atomicOr(reinterpret_cast<unsigned int *>(st), bits);

@@ -19,6 +19,8 @@ def dev(arr, dtype):
     """Seeded numpy array -> contiguous CUDA tensor ('bf16' bit patterns or 'f32')."""
     if dtype == "bf16":
         t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    elif dtype == "fp8":
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.uint8)).view(torch.float8_e4m3fn)
     elif dtype == "f32":
         t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
     else:
@@ -39,6 +41,8 @@ def host_bits(t):
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.view(torch.int32).numpy().view(np.uint32)
 
 
@@ -65,13 +69,13 @@ class DevDecode:
 
     def __init__(self, case):
         from rank_kv_attention_gb300.api import PagedCache
-        dt = case.dtype
+        dt, adt = case.dtype, case.act_dtype
         self.case = case
-        self.q = dev(case.q, dt)
+        self.q = dev(case.q, adt)
         self.cache = PagedCache(dev(case.S_K, dt), dev(case.S_V, dt), dev(case.R_K, dt),
-                                dev(case.R_V, dt))
-        self.B_K = dev(case.B_K, dt)
-        self.B_V = dev(case.B_V, dt)
+                                dev(case.R_V, dt), tuple(case.scale))
+        self.B_K = dev(case.B_K, adt)
+        self.B_V = dev(case.B_V, adt)
         self.seq_lens = dev(case.seq_lens, "i32")
         self.page_table = dev(case.page_table, "i32")
         self.max_seq_len = int(max(1, case.seq_lens.max()))
@@ -82,9 +86,17 @@ class DevDecode:
                         self.max_seq_len, out=out, ws=ws, status=status)
 
 
+def pools_f64(case, pools=None):
+    """float64 values of the four cache pools (8-bit codes times their scales)."""
+    import oracle
+    pools = pools if pools is not None else (case.S_K, case.S_V, case.R_K, case.R_V)
+    if case.dtype == "fp8":
+        return [oracle.fp8.dequantize(p, s) for p, s in zip(pools, case.scale)]
+    return [I.to_f64(p, case.dtype) for p in pools]
+
+
 def oracle_decode(case, pairs=None):
     import oracle
-    f = lambda a: I.to_f64(a, case.dtype)
-    return oracle.decode(f(case.q), f(case.S_K), f(case.S_V), f(case.R_K), f(case.R_V),
-                         f(case.B_K), f(case.B_V), case.page_table, case.seq_lens,
-                         case.page_size, pairs=pairs)
+    f = lambda a: I.to_f64(a, case.act_dtype)
+    return oracle.decode(f(case.q), *pools_f64(case), f(case.B_K), f(case.B_V), case.page_table,
+                         case.seq_lens, case.page_size, pairs=pairs)

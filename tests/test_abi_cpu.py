@@ -42,7 +42,8 @@ def test_version_and_strings(lib):
 
 
 @pytest.mark.parametrize("H,d_h,r,T,dt,eb", [(16, 128, 48, 4096, 1, 2), (32, 128, 32, 32768, 1, 2),
-                                             (4, 16, 4, 65, 0, 4), (18, 128, 56, 2048, 1, 2)])
+                                             (4, 16, 4, 65, 0, 4), (18, 128, 56, 2048, 1, 2),
+                                             (16, 128, 48, 4096, 2, 1), (32, 64, 8, 100, 2, 1)])
 def test_cache_bytes_is_equation_9(lib, H, d_h, r, T, dt, eb):
     got = lib.lrkv_cache_bytes(H, d_h, r, T, dt)
     assert got == oracle.lrkv_payload(eb, 1, 1, T, H, d_h, r)
@@ -52,6 +53,22 @@ def test_cache_bytes_rejects_bad_shapes(lib):
     assert lib.lrkv_cache_bytes(0, 128, 48, 10, 1) == 0
     assert lib.lrkv_cache_bytes(16, 130, 48, 10, 1) == 0   # bf16 needs d_h % 8 == 0
     assert lib.lrkv_cache_bytes(16, 128, 48, 10, 7) == 0   # bad dtype
+    assert lib.lrkv_cache_bytes(16, 120, 48, 10, 2) == 0   # 8-bit codes need d_h % 16 == 0
+    assert lib.lrkv_cache_bytes(3, 128, 8, 10, 2) == 0     # ... and H * r % 16 == 0
+
+
+def test_fp8_cache_scales_checked_on_host(lib):
+    """An 8-bit cache needs four positive, finite scales with finite reciprocals."""
+    ws = ctypes.c_void_p(256)
+
+    def call(scale):
+        c = _cache(dtype=_abi.LRKV_FP8_E4M3)
+        c.scale = (ctypes.c_float * 4)(*scale)
+        return lib.lrkv_decode(16, ctypes.byref(c), 16, 16, 16, 16, 2, 4, 100, 16, ws, 1 << 30,
+                               None, None)
+    for bad in ((0.0, 1, 1, 1), (1, -1, 1, 1), (1, 1, float("inf"), 1), (1, 1, 1, float("nan")),
+                (1, 1, 1, 1e-45)):
+        assert call(bad) == _abi.LRKV_E_DTYPE, bad
 
 
 def test_workspace_sizes_positive_and_monotone(lib):
