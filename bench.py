@@ -35,6 +35,9 @@ WORKLOADS = {
     "decode_T32768": "B=4, d=4096, H=32, d_h=128, r=32, T=32768, bf16 cache, fp32 accumulation",
     "ragged_paged": "B=64, lengths uniform on [256, 8192], 64-token pages shuffled in one pool, "
                     "H=16, d_h=128, r=56, d=2048 for the append, bf16",
+    "decode_T4096_fp8": "decode_T4096 over an 8-bit cache: the four pools hold E4M3 codes (one "
+                        "scale per pool), q, bases and output bf16, f16 tensor-core inputs, fp32 "
+                        "accumulation",
     "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
                     "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
@@ -193,13 +196,17 @@ def run_ours(args, rank, world, local_rank):
     def to_dev(a, kind="bf16"):
         if kind == "bf16":
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        if kind == "fp8":
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).view(torch.float8_e4m3fn).to(dev)
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
-    base = PagedCache(to_dev(case.S_K), to_dev(case.S_V), to_dev(case.R_K), to_dev(case.R_V))
-    cache_bytes = sum(t.numel() * 2 for t in (base.S_K, base.S_V, base.R_K, base.R_V))
+    eb = 1 if case.dtype == "fp8" else 2   # bytes per cache element
+    base = PagedCache(*(to_dev(t, case.dtype) for t in (case.S_K, case.S_V, case.R_K, case.R_V)),
+                      tuple(case.scale))
+    cache_bytes = sum(t.numel() * eb for t in (base.S_K, base.S_V, base.R_K, base.R_V))
     n_copies = max(1, math.ceil(4 * L2_BYTES / cache_bytes))
-    caches = [base] + [PagedCache(*(t.clone() for t in (base.S_K, base.S_V, base.R_K, base.R_V)))
-                       for _ in range(n_copies - 1)]
+    caches = [base] + [PagedCache(*(t.clone() for t in (base.S_K, base.S_V, base.R_K, base.R_V)),
+                                  base.scale) for _ in range(n_copies - 1)]
     q = to_dev(case.q)
     BK, BV = to_dev(case.B_K), to_dev(case.B_V)
     Wsk, Wsv, Uk, Uv = (to_dev(a) for a in (w.W_S_K, w.W_S_V, w.U_K, w.U_V))
@@ -342,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
     tokens = world * Bn * K
     value = tokens / (total_ms / 1e3)
     seq_total = int(case.seq_lens.astype(np.int64).sum())
-    split_bytes = seq_total * 2 * (d_h + H * r) * 2          # cache rows read once
+    split_bytes = seq_total * 2 * (d_h + H * r) * eb         # cache rows read once
     step_bytes = (split_bytes + 2 * H * d_h * r * 2 + 2 * Bn * H * d_h * 2   # + bases, q, out
                   + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
     peak, peak_kind = measured_peaks()
@@ -350,7 +357,8 @@ def run_ours(args, rank, world, local_rank):
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 cache, f16 mma inputs" if eb == 1 else "bf16", "data": "synthetic",
         "config": {"workload": f"{name}: {WORKLOADS[name]}", "B": Bn, "d": d, "H": H, "d_h": d_h,
                    "r": r, "seq_len": max_seq, "cached_rows": seq_total,
                    "parallelism": f"replicas x{world} (requests are independent)",

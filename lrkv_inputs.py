@@ -191,12 +191,13 @@ class DecodeCase:
 def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
                      shuffle=False, spare_pages=0, page_size=PAGE_SIZE,
                      q_std=1.0, cache_std=1.0, base_std=None,
-                     max_pages=None) -> DecodeCase:
+                     max_pages=None, fp8_scale=None) -> DecodeCase:
     """Decode inputs: a filled paged cache plus one query row per request.
 
     Queries and cache rows ~ N(0, q_std^2 / cache_std^2); bases ~ N(0, 1/r)
     unless ``base_std`` is given.  With dtype "fp8" the pools hold 8-bit codes
-    of value / FP8_SCALE and the queries and bases are bf16.
+    of value / scale (``fp8_scale``: one scale, or one per pool S_K, S_V, R_K,
+    R_V; default FP8_SCALE) and the queries and bases are bf16.
     """
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(B)
@@ -206,18 +207,21 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
     if base_std is None:
         base_std = 1.0 / np.sqrt(r)
     adt = act_dtype(dtype)
-    sc = FP8_SCALE if dtype == "fp8" else 1.0
+    sc = (1.0,) * 4
+    if dtype == "fp8":
+        sc = fp8_scale if fp8_scale is not None else FP8_SCALE
+        sc = tuple(float(x) for x in np.broadcast_to(np.asarray(sc, np.float64), (4,)))
     q = _draw(rng, (B, H, d_h), q_std, adt)
     B_K = _draw(rng, (H, d_h, r), base_std, adt)
     B_V = _draw(rng, (H, d_h, r), base_std, adt)
-    S_K = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc)
-    S_V = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc)
-    R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc)
-    R_V = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc)
+    S_K = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc[0])
+    S_V = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc[1])
+    R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc[2])
+    R_V = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc[3])
     for pool in (S_K, S_V, R_K, R_V):
         poison_tail_slots(pool, pt, seq_lens, page_size, dtype)
     return DecodeCase(B, H, d_h, r, dtype, page_size, seq_lens, pt, num_pages,
-                      q, S_K, S_V, R_K, R_V, B_K, B_V, (sc,) * 4)
+                      q, S_K, S_V, R_K, R_V, B_K, B_V, sc)
 
 
 def ragged_lengths(B, lo, hi, seed):
@@ -325,6 +329,8 @@ CONFIGS = {
     "ragged_paged": dict(B=64, H=16, d_h=128, r=56, lo=256, hi=8192, dtype="bf16", seed=0),
     # prefill + append of 8 fresh 2048-token prompts.
     "prefill_2048": dict(B=8, d=2048, H=16, d_h=128, r=48, T=2048, dtype="bf16", seed=0),
+    # the 16 x 4096 decode over an 8-bit (E4M3) cache: same shapes, half the bytes
+    "decode_T4096_fp8": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="fp8", seed=0),
 }
 
 

@@ -26,15 +26,20 @@ def _run_pairs(pairs):
     import numpy as np
     import lrkv_inputs as I
     from . import lrkv_oracle as O
+    from . import fp8
     c = _CASE
-    f = lambda a: I.to_f64(a, c.dtype)
+    f = lambda a: I.to_f64(a, c.act_dtype)
+    if c.dtype == "fp8":  # 8-bit pools: codes times the pool's scale
+        fp = lambda a, k: fp8.dequantize(a, c.scale[k])
+    else:
+        fp = lambda a, k: I.to_f64(a, c.dtype)
     t0 = time.perf_counter()
     for b, h in pairs:
         pages, L = c.rows(b)
-        sk = f(O.gather_rows(c.S_K, pages, L, c.page_size))
-        sv = f(O.gather_rows(c.S_V, pages, L, c.page_size))
-        rk = f(O.gather_rows(c.R_K, pages, L, c.page_size)[:, h, :])
-        rv = f(O.gather_rows(c.R_V, pages, L, c.page_size)[:, h, :])
+        sk = fp(O.gather_rows(c.S_K, pages, L, c.page_size), 0)
+        sv = fp(O.gather_rows(c.S_V, pages, L, c.page_size), 1)
+        rk = fp(O.gather_rows(c.R_K, pages, L, c.page_size)[:, h, :], 2)
+        rv = fp(O.gather_rows(c.R_V, pages, L, c.page_size)[:, h, :], 3)
         K_h = O.expand_head(sk, rk, f(c.B_K[h]))
         V_h = O.expand_head(sv, rv, f(c.B_V[h]))
         o = O.attend(f(c.q[b, h]), K_h, V_h)

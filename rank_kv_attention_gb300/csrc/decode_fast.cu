@@ -37,19 +37,24 @@
 
 namespace lrkv {
 
-template <int H_, int R_, int STAGES_>
+// Q8_: the cache holds 8-bit E4M3 codes (one byte per element) instead of bf16.
+template <int H_, int R_, int STAGES_, bool Q8_ = false>
 struct FastCfg {
     static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_;
+    static constexpr bool Q8 = Q8_;
+    static constexpr int EB = Q8 ? 1 : 2;    // bytes per cache element
     static constexpr int DH = 128;
     static constexpr int NCW = 8, NT = NCW * 32;
     static constexpr int HPW = H / NCW;      // heads per warp (2 or 4)
     static constexpr int NH = HPW / 2;       // head slots per thread
     static constexpr int RC = R / 8;         // 16-byte chunks per private row
-    static constexpr int BOX = TS * 128;     // one 64-column, 16-row swizzled box
-    static constexpr int NBOX_R = H * R / 64;
-    static constexpr int R_BYTES = NBOX_R * BOX;
-    static constexpr int OFF_SK = 0, OFF_SV = 2 * BOX, OFF_RK = 4 * BOX, OFF_RV = 4 * BOX + R_BYTES;
-    static constexpr int STAGE = 4 * BOX + 2 * R_BYTES;
+    static constexpr int BOX = TS * 128;     // one 16-row x 128-byte swizzled box
+    static constexpr int NBOX_S = DH * EB / 128;
+    static constexpr int NBOX_R = H * R * EB / 128;
+    static constexpr int S_BYTES = NBOX_S * BOX, R_BYTES = NBOX_R * BOX;
+    static constexpr int OFF_SK = 0, OFF_SV = S_BYTES, OFF_RK = 2 * S_BYTES;
+    static constexpr int OFF_RV = 2 * S_BYTES + R_BYTES;
+    static constexpr int STAGE = 2 * S_BYTES + 2 * R_BYTES;
     static constexpr int KSP = HPW * R / 16;  // k-steps (and m-tiles) of a warp's private columns
     static constexpr int OFF_BAR = STAGES * STAGE;   // full[STAGES]
     static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
@@ -62,7 +67,8 @@ struct FastCfg {
     static constexpr int SMEM = OFF_ABAR + 64 + 1024;  // + alignment slack
 
     static_assert(H == 16 || H == 32, "two or four heads per warp");
-    static_assert(R % 8 == 0 && (H * R) % 64 == 0, "private rows tile into 64-column boxes");
+    static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
+    static_assert(STAGES <= 8, "barrier, counter and flag arrays hold 8 stages");
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -83,6 +89,7 @@ struct FastParams {
     const __nv_bfloat16 *W[4];
     __nv_bfloat16 *pool[4];
     int d, len_shift;
+    float4 sc;  // 8-bit cache: pool scales of S_K, S_V, R_K, R_V
 };
 
 struct FastMaps {
@@ -331,6 +338,215 @@ __device__ __forceinline__ uint32_t box_chunk(int j, int cc) {
     return (uint32_t)((cc >> 3) * (16 * 128)) + swz128(j, cc & 7);
 }
 
+// ---------------------------------------------------------------------------
+// 8-bit (E4M3) cache tiles.  A 16-row tile arrives as 128-byte swizzled boxes
+// of codes (one box for S_K or S_V, H r / 128 for R_K or R_V).  The codes are
+// widened to f16 in registers (exact: every E4M3 value is an f16 value) and
+// enter f16 mma.sync with fp32 accumulation; the pool scales multiply the
+// fp32 results.
+//   * Scores: the order of the 16 contraction indices of a k-step is free as
+//     long as both operands use the same one, so thread tq takes bytes
+//     4tq .. 4tq+3 of each 16-byte chunk (one 32-bit shared load per row) for
+//     its fragment slots 2tq, 2tq+1, 2tq+8, 2tq+9.
+//   * Values: the tile rows stay in order (they meet the softmax weights);
+//     the value columns are permuted instead: a 32-bit load at byte
+//     32u + 4gq of a row holds, in order, columns gq and gq + 8 of m-tile 2u
+//     and columns gq and gq + 8 of m-tile 2u + 1, and byte permutes pair the
+//     rows 2tq, 2tq + 1 (and 2tq + 8, 2tq + 9) of each column into one f16x2
+//     fragment register.  A trailing odd m-tile uses 16-bit loads.  Row masks
+//     (invalid rows may hold any code) are applied on partial tiles only.
+//   * q and p enter as f16 after an exact power-of-two scaling per head that
+//     brings the head's largest |value| into [2^14, 2^15); the softmax weights
+//     (at most 2^8 under the lazy maximum) enter as f16 directly.
+// ---------------------------------------------------------------------------
+
+// Shift e with 2^e * m in [2^14, 2^15) (0 for m = 0 or non-finite m).
+__device__ __forceinline__ int f16_range_shift(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 0;
+    const int ex = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
+    return max(-125, min(125, 14 - ex));
+}
+
+template <class C>
+__device__ __forceinline__ void q8_segment_setup(const FastParams &P, int b, int warp, int gq,
+                                                 int tq, uint32_t (&qb)[8][2],
+                                                 uint32_t (&pb)[C::KSP][2], float (&fS)[2],
+                                                 float (&fR)[2]) {
+    // column n = gq of the B fragments is head warp*HPW + n (n < HPW), else 0;
+    // contraction index k of k-step ks in slot order is 16 ks + 4 tq + e
+    const bool own = gq < C::HPW;
+    const __nv_bfloat16 *qrow = P.q + ((size_t)b * C::H + warp * C::HPW + (own ? gq : 0)) * C::DH;
+    float qv[8][4], pv[C::KSP][4];
+    float mq = 0.f, mp = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint2 u = own ? *reinterpret_cast<const uint2 *>(qrow + ks * 16 + 4 * tq) : make_uint2(0u, 0u);
+        qv[ks][0] = __uint_as_float(u.x << 16);
+        qv[ks][1] = __uint_as_float(u.x & 0xffff0000u);
+        qv[ks][2] = __uint_as_float(u.y << 16);
+        qv[ks][3] = __uint_as_float(u.y & 0xffff0000u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mq = fmaxf(mq, fabsf(qv[ks][e]));
+    }
+    // blockdiag(p)^T: entry (k, n) is p[head n][k - n R] when k lies in head
+    // n's columns of the warp, else 0
+    const float *pw = P.ws.p + ((size_t)b * C::H + warp * C::HPW) * C::R;
+#pragma unroll
+    for (int ks = 0; ks < C::KSP; ++ks)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k = ks * 16 + 4 * tq + e;
+            pv[ks][e] = (own && k / C::R == gq) ? pw[k] : 0.f;
+            mp = fmaxf(mp, fabsf(pv[ks][e]));
+        }
+    // the head's maxima over its four lanes (same gq)
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+    }
+    const int eq = f16_range_shift(mq), ep = f16_range_shift(mp);
+    const float uq = exp2i(eq), up = exp2i(ep);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        qb[ks][0] = pack_f16(qv[ks][0] * uq, qv[ks][1] * uq);
+        qb[ks][1] = pack_f16(qv[ks][2] * uq, qv[ks][3] * uq);
+    }
+#pragma unroll
+    for (int ks = 0; ks < C::KSP; ++ks) {
+        pb[ks][0] = pack_f16(pv[ks][0] * up, pv[ks][1] * up);
+        pb[ks][1] = pack_f16(pv[ks][2] * up, pv[ks][3] * up);
+    }
+    // factors of accumulator columns 2tq and 2tq + 1 (held by lanes 8tq, 8tq + 4)
+    const float fq = P.sc.x * exp2i(-eq), fp = P.sc.z * exp2i(-ep);
+    fS[0] = __shfl_sync(0xffffffffu, fq, 8 * tq);
+    fS[1] = __shfl_sync(0xffffffffu, fq, 8 * tq + 4);
+    fR[0] = __shfl_sync(0xffffffffu, fp, 8 * tq);
+    fR[1] = __shfl_sync(0xffffffffu, fp, 8 * tq + 4);
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t *p) {
+    return *reinterpret_cast<const uint32_t *>(p);
+}
+__device__ __forceinline__ uint32_t lds_u16(const uint8_t *p) {
+    return *reinterpret_cast<const uint16_t *>(p);
+}
+__device__ __forceinline__ uint32_t f16x2_lo(uint32_t w) { return f16x2_from_e4m3x2((uint16_t)w); }
+__device__ __forceinline__ uint32_t f16x2_hi(uint32_t w) {
+    return f16x2_from_e4m3x2((uint16_t)(w >> 16));
+}
+
+// Scores of a tile: c[row x head] = fS . (S_K . Q^T) + fR . (R_K . blockdiag(p)^T).
+template <class C>
+__device__ __forceinline__ void q8_scores(const uint8_t *st, int warp, int gq, int tq,
+                                          const uint32_t (&qb)[8][2],
+                                          const uint32_t (&pb)[C::KSP][2], const float (&fS)[2],
+                                          const float (&fR)[2], float (&c)[4]) {
+    float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint8_t *sk = st + C::OFF_SK, *rk = st + C::OFF_RK;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t w0 = lds_u32(sk + box_chunk(gq, ks) + 4 * tq);
+        const uint32_t w1 = lds_u32(sk + box_chunk(gq + 8, ks) + 4 * tq);
+        const uint32_t a[4] = {f16x2_lo(w0), f16x2_lo(w1), f16x2_hi(w0), f16x2_hi(w1)};
+        if (ks & 1) mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
+        else mma_f16_16816(c, a, qb[ks][0], qb[ks][1]);
+    }
+    const int cw = warp * (C::HPW * C::R / 16);  // first 16-byte chunk of the warp's columns
+#pragma unroll
+    for (int ks = 0; ks < C::KSP; ++ks) {
+        const uint32_t w0 = lds_u32(rk + box_chunk(gq, cw + ks) + 4 * tq);
+        const uint32_t w1 = lds_u32(rk + box_chunk(gq + 8, cw + ks) + 4 * tq);
+        const uint32_t a[4] = {f16x2_lo(w0), f16x2_lo(w1), f16x2_hi(w0), f16x2_hi(w1)};
+        if (ks & 1) mma_f16_16816(c3, a, pb[ks][0], pb[ks][1]);
+        else mma_f16_16816(c2, a, pb[ks][0], pb[ks][1]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[e] = fS[e & 1] * (c[e] + c1[e]) + fR[e & 1] * (c2[e] + c3[e]);
+}
+
+// A fragments of two value m-tiles from the 32-bit words of rows 2tq, 2tq+1,
+// 2tq+8, 2tq+9 (see the layout note above); MASK: zero invalid rows.
+template <bool MASK>
+__device__ __forceinline__ void q8_pair_frags(uint32_t w0, uint32_t w1, uint32_t w8, uint32_t w9,
+                                              uint32_t m01, uint32_t m89, uint32_t (&a)[4],
+                                              uint32_t (&b)[4]) {
+    const uint32_t x01 = prmt<0x5140>(w0, w1), y01 = prmt<0x7362>(w0, w1);
+    const uint32_t x89 = prmt<0x5140>(w8, w9), y89 = prmt<0x7362>(w8, w9);
+    a[0] = f16x2_lo(x01); a[1] = f16x2_hi(x01); a[2] = f16x2_lo(x89); a[3] = f16x2_hi(x89);
+    b[0] = f16x2_lo(y01); b[1] = f16x2_hi(y01); b[2] = f16x2_lo(y89); b[3] = f16x2_hi(y89);
+    if (MASK) {
+        a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
+        b[0] &= m01; b[1] &= m01; b[2] &= m89; b[3] &= m89;
+    }
+}
+
+// Values of a tile: accS += S_V^T . P^T, accR += R_V^T(warp columns) . P^T.
+template <class C, bool MASK>
+__device__ __forceinline__ void q8_values(const uint8_t *st, int warp, int gq, int tq, uint32_t m01,
+                                          uint32_t m89, uint32_t b0, uint32_t b1,
+                                          float (&accS)[8][4], float (&accR)[C::KSP][4]) {
+    const uint8_t *sv = st + C::OFF_SV, *rv = st + C::OFF_RV;
+    const int r0 = 2 * tq, r1 = r0 + 1, r8 = r0 + 8, r9 = r0 + 9;
+    auto pair = [&](const uint8_t *t, int cb, float (&d0)[4], float (&d1)[4]) {
+        const int ch = cb >> 4, o = cb & 15;
+        uint32_t a[4], a2[4];
+        q8_pair_frags<MASK>(lds_u32(t + box_chunk(r0, ch) + o), lds_u32(t + box_chunk(r1, ch) + o),
+                            lds_u32(t + box_chunk(r8, ch) + o), lds_u32(t + box_chunk(r9, ch) + o),
+                            m01, m89, a, a2);
+        mma_f16_16816(d0, a, b0, b1);
+        mma_f16_16816(d1, a2, b0, b1);
+    };
+#pragma unroll
+    for (int u = 0; u < 4; ++u) pair(sv, 32 * u + 4 * gq, accS[2 * u], accS[2 * u + 1]);
+    const int cwb = warp * C::HPW * C::R;  // first byte column of the warp's private columns
+#pragma unroll
+    for (int u = 0; u < C::KSP / 2; ++u) pair(rv, cwb + 32 * u + 4 * gq, accR[2 * u], accR[2 * u + 1]);
+    if constexpr (C::KSP & 1) {
+        constexpr int mt = C::KSP - 1;
+        const int cb = cwb + 16 * mt + 2 * gq, ch = cb >> 4, o = cb & 15;
+        const uint32_t h0 = lds_u16(rv + box_chunk(r0, ch) + o), h1 = lds_u16(rv + box_chunk(r1, ch) + o);
+        const uint32_t h8 = lds_u16(rv + box_chunk(r8, ch) + o), h9 = lds_u16(rv + box_chunk(r9, ch) + o);
+        const uint32_t x01 = prmt<0x5140>(h0, h1), x89 = prmt<0x5140>(h8, h9);
+        uint32_t a[4] = {f16x2_lo(x01), f16x2_hi(x01), f16x2_lo(x89), f16x2_hi(x89)};
+        if (MASK) { a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89; }
+        mma_f16_16816(accR[mt], a, b0, b1);
+    }
+}
+
+// Value column (relative to the tile's or the warp's first column) of
+// accumulator m-tile mt, element e, under the permutation of q8_values.
+template <int KSP>
+__device__ __forceinline__ int q8_value_col(int mt, int e, int gq) {
+    return (mt < (KSP & ~1)) ? 32 * (mt >> 1) + 4 * gq + 2 * (mt & 1) + (e >> 1)
+                             : 16 * mt + 2 * gq + (e >> 1);
+}
+
+template <class C>
+__device__ __forceinline__ void q8_write_partial(const FastParams &P, size_t slot, int warp, int gq,
+                                                 int tq, const float (&accS)[8][4],
+                                                 const float (&accR)[C::KSP][4]) {
+    const size_t W = C::DH + C::R;
+    float *acc = P.ws.acc;
+    if (2 * tq < C::HPW) {
+        const int h0 = warp * C::HPW + 2 * tq;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[(slot * C::H + h0 + (e & 1)) * W + q8_value_col<8>(mt, e, gq)] = accS[mt][e] * P.sc.y;
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::KSP; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int pc = q8_value_col<C::KSP>(mt, e, gq);
+            const int n = 2 * tq + (e & 1);
+            if (n < C::HPW && pc / C::R == n)
+                acc[(slot * C::H + warp * C::HPW + n) * W + C::DH + (pc - n * C::R)] = accR[mt][e] * P.sc.w;
+        }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NT, 1)
     decode_split_fast_kernel(const __grid_constant__ FastMaps M, const FastParams P) {
@@ -346,9 +562,10 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int g = blockIdx.x;
     const DecodeWs &ws = P.ws;
 
-    // fused step: the new rows' staging copies go out first and land while
-    // the plan below is computed
-    if (P.X && tid == 0) {
+    // fused step (bf16 caches): the new rows' staging copies go out first and
+    // land while the plan below is computed
+    const bool fused = !C::Q8 && P.X != nullptr;
+    if (fused && tid == 0) {
         uint64_t *abar = reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR);
         mbar_init(abar, 1);
         fence_barrier_init();
@@ -391,7 +608,7 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int32_t start0 = g * chunk;
     const int32_t end = min(total, start0 + chunk);
     if (start0 >= end) {
-        if (P.X &&
+        if (fused &&
             !append_new_rows<C>(P, smem, reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR),
                                 reinterpret_cast<float4 *>(smem + C::OFF_RED),
                                 reinterpret_cast<int64_t *>(smem + C::OFF_DST)))
@@ -424,7 +641,7 @@ __global__ void __launch_bounds__(C::NT, 1)
     if (!local) pdl_wait();  // fall back to the prologue's offsets
 
     // fused step: project and write the new rows before the ring's first copies
-    if (P.X &&
+    if (fused &&
         !append_new_rows<C>(P, smem, reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR),
                             reinterpret_cast<float4 *>(smem + C::OFF_RED),
                             reinterpret_cast<int64_t *>(smem + C::OFF_DST)))
@@ -461,7 +678,9 @@ __global__ void __launch_bounds__(C::NT, 1)
     float accS[8][4], accR[C::KSP][4];
     float m[C::NH], l[C::NH];
     uint32_t qb[8][2];            // Q^T fragments (shared scores)
-    uint32_t pbh[C::KSP][2], pbl[C::KSP][2];  // blockdiag(p)^T fragments, hi and lo halves
+    // blockdiag(p)^T fragments: hi and lo bf16 halves, or one f16 (8-bit cache)
+    uint32_t pbh[C::KSP][2], pbl[C::Q8 ? 1 : C::KSP][2];
+    float fS[2] = {1.f, 1.f}, fR[2] = {1.f, 1.f};  // 8-bit cache: score factors of columns 2tq, 2tq+1
     bool timed_out = false;
 
     uint32_t it = 0;
@@ -487,7 +706,9 @@ __global__ void __launch_bounds__(C::NT, 1)
         for (int mt = 0; mt < C::KSP; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accR[mt][e] = 0.f;
-        {
+        if constexpr (C::Q8) {
+            q8_segment_setup<C>(P, b, warp, gq, tq, qb, pbh, fS, fR);
+        } else {
             // B fragments of Q^T: column n = head warp*HPW + n (n < HPW), else 0
             const bool own = gq < C::HPW;
             const __nv_bfloat16 *qrow = P.q + ((size_t)b * C::H + warp * C::HPW + (own ? gq : 0)) * C::DH;
@@ -539,7 +760,9 @@ __global__ void __launch_bounds__(C::NT, 1)
             // accumulated in four independent chains (shared even/odd k-steps,
             // private hi/lo halves) so the tensor-core latency overlaps
             float c[4] = {0.f, 0.f, 0.f, 0.f};
-            {
+            if constexpr (C::Q8) {
+                q8_scores<C>(st, warp, gq, tq, qb, pbh, fS, fR, c);
+            } else {
                 float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
                 float c3[4] = {0.f, 0.f, 0.f, 0.f};
                 const uint32_t skb = smem_u32(st + C::OFF_SK);
@@ -609,6 +832,8 @@ __global__ void __launch_bounds__(C::NT, 1)
                     if ((gq >> 1) == i) { w0 = x0; w1 = x1; w8 = x8; w9 = x9; }
                 }
                 if (gq >= C::HPW) w0 = w1 = w8 = w9 = 0.f;
+                // 8-bit cache: one f16 per weight (11 significant bits)
+                const uint32_t fh0 = C::Q8 ? pack_f16(w0, w1) : 0u, fh1 = C::Q8 ? pack_f16(w8, w9) : 0u;
                 const __nv_bfloat16 h0 = __float2bfloat16_rn(w0), h1 = __float2bfloat16_rn(w1);
                 const __nv_bfloat16 h8 = __float2bfloat16_rn(w8), h9 = __float2bfloat16_rn(w9);
                 const uint32_t bh0 = pack_bf16(__bfloat162float(h0), __bfloat162float(h1));
@@ -641,6 +866,10 @@ __global__ void __launch_bounds__(C::NT, 1)
                     m01 = (ok(2 * tq) ? 0x0000ffffu : 0u) | (ok(2 * tq + 1) ? 0xffff0000u : 0u);
                     m89 = (ok(2 * tq + 8) ? 0x0000ffffu : 0u) | (ok(2 * tq + 9) ? 0xffff0000u : 0u);
                 }
+                if constexpr (C::Q8) {
+                    if (partial) q8_values<C, true>(st, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
+                    else q8_values<C, false>(st, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
+                } else {
                 const int rr = (mi >> 1) * 8 + (lane & 7);
                 const uint32_t svb = smem_u32(st + C::OFF_SV);
 #pragma unroll
@@ -660,6 +889,7 @@ __global__ void __launch_bounds__(C::NT, 1)
                     a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
                     mma_bf16_16816(accR[mt], a, bh0, bh1);
                     mma_bf16_16816(accR[mt], a, bl0, bl1);
+                }
                 }
             }
 
@@ -690,6 +920,9 @@ __global__ void __launch_bounds__(C::NT, 1)
                 ws.ml[(slot * C::H + hd[i]) * 2 + 1] = l[i];
             }
         }
+        if constexpr (C::Q8) {
+            q8_write_partial<C>(P, slot, warp, gq, tq, accS, accR);
+        } else {
         if (2 * tq < C::HPW) {
             const int h0 = warp * C::HPW + 2 * tq;
 #pragma unroll
@@ -712,6 +945,7 @@ __global__ void __launch_bounds__(C::NT, 1)
                 if (n < C::HPW && mm / C::R == n)
                     ws.acc[(slot * C::H + warp * C::HPW + n) * W + C::DH + (mm - n * C::R)] = accR[mt][e];
             }
+        }
         start = seg_end;
     }
 
@@ -747,44 +981,48 @@ static EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// Map over a pool viewed as [rows, cols] bf16, as three dimensions
-// (64 columns, rows, cols / 64 blocks of columns) with strides (2 B, cols*2 B,
-// 128 B).  A box of 64 x 16 x (cols/64) with 128-byte swizzle lands a 16-row
-// tile as cols/64 consecutive 16-row x 128-byte boxes (matches box_chunk).
-static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols) {
+// Map over a pool viewed as [rows, cols] elements of eb bytes (bf16 or 8-bit
+// codes), as three dimensions (128 / eb columns, rows, cols * eb / 128 blocks
+// of 128 bytes) with strides (eb, cols * eb, 128 bytes).  A box of
+// (128 / eb) x 16 x (cols * eb / 128) with 128-byte swizzle lands a 16-row
+// tile as consecutive 16-row x 128-byte boxes (matches box_chunk).
+static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols, int eb) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
-    cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
-    cuuint32_t box[3] = {64, 16, (cuuint32_t)(cols / 64)};
+    const int per = 128 / eb, blocks = cols * eb / 128;
+    cuuint64_t dims[3] = {(cuuint64_t)per, (cuuint64_t)rows, (cuuint64_t)blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * eb, 128};
+    cuuint32_t box[3] = {(cuuint32_t)per, 16, (cuuint32_t)blocks};
     cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
+    const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return enc(map, dt, 3, const_cast<void *>(pool), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int H, int R>
+template <int H, int R, bool Q8 = false>
 struct Pick {
-    static constexpr int stage = FastCfg<H, R, 1>::STAGE;
-    static constexpr int misc = FastCfg<H, R, 1>::SMEM - FastCfg<H, R, 1>::OFF_BAR;
+    static constexpr int stage = FastCfg<H, R, 1, Q8>::STAGE;
+    static constexpr int misc = FastCfg<H, R, 1, Q8>::SMEM - FastCfg<H, R, 1, Q8>::OFF_BAR;
     static constexpr int fit = (227 * 1024 - misc) / stage;
     // deeper rings of large stages measured slower (more DRAM queueing for
-    // the same consumption rate): 3 stages of >= 48 KB, else up to 4
-    static constexpr int cap = stage >= 48 * 1024 ? 3 : 4;
+    // the same consumption rate): 3 stages of >= 48 KB, else up to 4; the
+    // half-size stages of an 8-bit cache keep about as many bytes in flight
+    static constexpr int cap = Q8 ? (stage >= 24 * 1024 ? 6 : 8) : (stage >= 48 * 1024 ? 3 : 4);
     static constexpr int STAGES = fit > cap ? cap : fit;
-    using Cfg = FastCfg<H, R, STAGES>;
+    using Cfg = FastCfg<H, R, STAGES, Q8>;
 };
 
-template <int H, int R>
+template <int H, int R, bool Q8>
 static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int G) {
-    using C = typename Pick<H, R>::Cfg;
-    static_assert(Pick<H, R>::STAGES >= 2, "at least double buffering");
+    using C = typename Pick<H, R, Q8>::Cfg;
+    static_assert(Pick<H, R, Q8>::STAGES >= 2, "at least double buffering");
     const auto &c = a.cache;
     FastMaps maps;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    if (!make_map(&maps.sk, c.S_K, rows, 128) || !make_map(&maps.sv, c.S_V, rows, 128) ||
-        !make_map(&maps.rk, c.R_K, rows, H * R) || !make_map(&maps.rv, c.R_V, rows, H * R))
+    if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) || !make_map(&maps.sv, c.S_V, rows, 128, C::EB) ||
+        !make_map(&maps.rk, c.R_K, rows, H * R, C::EB) || !make_map(&maps.rv, c.R_V, rows, H * R, C::EB))
         return cudaErrorInvalidValue;
     auto kern = decode_split_fast_kernel<C>;
     static bool attr_set = false;
@@ -813,13 +1051,16 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     P.pool[3] = static_cast<__nv_bfloat16 *>(c.R_V);
     P.d = a.d;
     P.len_shift = a.X ? 1 : 0;
+    P.sc = Q8 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
+              : make_float4(1.f, 1.f, 1.f, 1.f);
     return launch_pdl(kern, dim3(G), dim3(C::NT), C::SMEM, a.stream, maps, P);
 }
 
 #define LRKV_FAST_SHAPES(X) X(16, 16) X(16, 32) X(16, 48) X(16, 56) X(16, 64) X(32, 16) X(32, 32)
 
 bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype) {
-    if (dtype != LRKV_BF16 || d_h != 128 || page_size % 16 != 0) return false;
+    if ((dtype != LRKV_BF16 && dtype != LRKV_FP8_E4M3) || d_h != 128 || page_size % 16 != 0)
+        return false;
     if (!get_encode_tiled()) return false;
 #define X(h, rr) if (H == h && r == rr) return true;
     LRKV_FAST_SHAPES(X)
@@ -841,7 +1082,10 @@ bool fast_decode_step_fits(int H, int r, int d) {
 
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const int H = a.cache.H, r = a.cache.r;
-#define X(h, rr) if (H == h && r == rr) return launch_fast_cfg<h, rr>(a, ws, G);
+    const bool q8 = a.cache.dtype == LRKV_FP8_E4M3;
+#define X(h, rr)                                                                  \
+    if (H == h && r == rr)                                                        \
+        return q8 ? launch_fast_cfg<h, rr, true>(a, ws, G) : launch_fast_cfg<h, rr, false>(a, ws, G);
     LRKV_FAST_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

@@ -32,6 +32,45 @@ def test_fp8_decode_page_sizes_and_long():
         assert_close(host(DevDecode(case).run(), "bf16"), oracle_decode(case), "bf16", f"ps={ps}")
 
 
+@pytest.mark.parametrize("H,r", [(16, 48), (32, 32), (16, 56)])
+@pytest.mark.parametrize("q_scale", [2.0 ** 20, 2.0 ** -20])
+def test_fp8_decode_query_range(H, r, q_scale):
+    """Queries far outside f16 range (and tiny ones), with the cache values
+    scaled the other way so the scores stay ordinary: the tensor-core kernel
+    rescales q and p per head by a power of two before rounding them to f16."""
+    case = I.make_decode_case(4, H, 128, r, [700, 33, 1, 260], dtype="fp8", seed=5, shuffle=True,
+                              q_std=q_scale, cache_std=1.0 / q_scale,
+                              fp8_scale=I.FP8_SCALE / q_scale)
+    got = host(DevDecode(case).run(), "bf16")
+    assert np.all(np.isfinite(got))
+    # outputs scale with the cache (1 / q_scale); compare at unit scale, where
+    # the tolerance's absolute term means what it does elsewhere (power-of-two
+    # scaling is exact on both sides)
+    assert_close(got * q_scale, oracle_decode(case) * q_scale, "bf16", f"q x {q_scale}")
+
+
+@pytest.mark.parametrize("scales", [(0.37, 1.3, 0.05, 2.1), (2.0 ** -9, 2.0 ** 3, 1.0, 0.01)])
+def test_fp8_decode_pool_scales(scales):
+    """Different, non-power-of-two scales per pool on the tensor-core shapes."""
+    for H, r in ((16, 48), (32, 16)):
+        case = I.make_decode_case(5, H, 128, r, [129, 1000, 17, 64, 5], dtype="fp8", seed=H + r,
+                                  shuffle=True, spare_pages=1, fp8_scale=scales)
+        assert_close(host(DevDecode(case).run(), "bf16"), oracle_decode(case), "bf16",
+                     f"H={H} r={r} scales={scales}")
+
+
+def test_fp8_decode_T4096_sampled():
+    """The 16 x 4096 decode workload over an 8-bit cache, on sampled
+    (request, head) outputs."""
+    case = I.config_decode_case("decode_T4096_fp8")
+    got = host(DevDecode(case).run(), "bf16")
+    rng = np.random.default_rng(3)
+    pairs = sorted({(b, int(rng.integers(case.H))) for b in range(case.B)} | {(0, 0), (15, 15)})
+    ref = oracle_decode(case, pairs=pairs)
+    idx = tuple(np.array(pairs).T)
+    assert_close(got[idx], ref[idx], "bf16", "decode_T4096_fp8")
+
+
 def _append_fp8(X, w, ac, H, d_h, r, scales):
     import rank_kv_attention_gb300 as L
     from rank_kv_attention_gb300.api import PagedCache
