@@ -562,6 +562,14 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int g = blockIdx.x;
     const DecodeWs &ws = P.ws;
 
+    // warm L2 with the page-table rows: the copy issuer reads them right
+    // after the plan below (caller inputs, complete before this grid launched)
+    if (!P.req_row) {
+        const size_t pt_bytes = (size_t)P.B * P.max_pages * sizeof(int32_t);
+        if (pt_bytes <= 64 * 1024)
+            for (size_t o = (size_t)tid * 128; o < pt_bytes; o += (size_t)C::NT * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.page_table) + o));
+    }
     // fused step (bf16 caches): the new rows' staging copies go out first and
     // land while the plan below is computed
     const bool fused = !C::Q8 && P.X != nullptr;

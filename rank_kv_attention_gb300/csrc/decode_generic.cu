@@ -306,11 +306,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
                                                              T *__restrict__ out,
                                                              const CombineStep<T> st) {
     extern __shared__ __align__(16) float cs[];
-    pdl_wait();
-    pdl_launch_dependents();
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    const int32_t o0 = ws.off[b], o1 = ws.off[b + 1];
-    T *dst = out + ((size_t)b * H + h) * d_h;
+    // Until the wait below only caller inputs are read (they were complete
+    // before the prologue got past its own wait, which precedes this grid's
+    // launch): the new row's pool slot, and B_V[h] staged in shared memory
+    // while the split kernel is still running.
     size_t nrow = 0;  // pool row of the fused step's new row
     bool has_new = false;
     if (st.on) {
@@ -321,21 +321,9 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
         has_new = page >= 0 && page < st.num_pages;  // else flagged by the split kernel
         if (has_new) nrow = (size_t)page * st.page_size + pos % st.page_size;
     }
-    if (o1 <= o0 && !has_new) {
-        for (int d = tid; d < d_h; d += blockDim.x) Elem<T>::store(dst + d, 0.f);
-        return;
-    }
-    const int32_t chunk = ws.plan->chunk;
-    const int g_lo = o1 > o0 ? o0 / chunk : 0, nseg = o1 > o0 ? (o1 - 1) / chunk - g_lo + 1 : 0;
-    const int W = d_h + r;
-    const size_t s0 = ((size_t)b + g_lo) * H + h;  // slot of segment g: s0 + g H
     T *bv = reinterpret_cast<T *>(cs);                                   // [d_h][r] when staged
-    float *cr = cs + (staged ? ((size_t)d_h * r * sizeof(T) + 15) / 16 * 4 : 0);  // [r]
-    float *w = cr + r;                                                    // [nseg]
-    __shared__ float red[2][8];
-    const int nthr = blockDim.x, nwarp = nthr >> 5;
     const T *src = B_V + (size_t)h * d_h * r;
-    // 1. B_V[h] as raw 16-byte vectors, the segments' (m, l), first accumulators
+    const int nthr = blockDim.x, nwarp = nthr >> 5;
     if (staged) {
         const int nv = d_h * r * (int)sizeof(T) / 16;
         const uint4 *s16 = reinterpret_cast<const uint4 *>(src);
@@ -353,6 +341,21 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
                 if (base + (4 + u) * nthr < nv) v[u] = s16[base + (4 + u) * nthr];
         }
     }
+    pdl_wait();
+    pdl_launch_dependents();
+    const int32_t o0 = ws.off[b], o1 = ws.off[b + 1];
+    T *dst = out + ((size_t)b * H + h) * d_h;
+    if (o1 <= o0 && !has_new) {
+        for (int d = tid; d < d_h; d += blockDim.x) Elem<T>::store(dst + d, 0.f);
+        return;
+    }
+    const int32_t chunk = ws.plan->chunk;
+    const int g_lo = o1 > o0 ? o0 / chunk : 0, nseg = o1 > o0 ? (o1 - 1) / chunk - g_lo + 1 : 0;
+    const int W = d_h + r;
+    const size_t s0 = ((size_t)b + g_lo) * H + h;  // slot of segment g: s0 + g H
+    float *cr = cs + (staged ? ((size_t)d_h * r * sizeof(T) + 15) / 16 * 4 : 0);  // [r]
+    float *w = cr + r;                                                    // [nseg]
+    __shared__ float red[2][8];
     // this thread's columns: c0 = tid, c1 = tid + blockDim.x (W <= 2 blockDim.x)
     const int c0 = tid, c1 = tid + nthr;
     float m_my = -INFINITY, l_my = 0.f;
