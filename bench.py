@@ -28,6 +28,9 @@ METRIC = "LRKV decode tokens/s and achieved HBM GB/s (% of roofline) at 1 GB300"
 L2_BYTES = 129 * 10 ** 6
 NORTH_STAR_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+# FP32 FMA peak from unit counts and the maximum SM clock: 152 SMs x 128 FP32
+# lanes x 2 flops x 2.07 GHz
+FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 WORKLOADS = {
     "decode_T4096": "B=16 requests, d=2048, H=16, d_h=128, r=48, history T=4096 (current row "
@@ -38,6 +41,10 @@ WORKLOADS = {
     "decode_T4096_fp8": "decode_T4096 over an 8-bit cache: the four pools hold E4M3 codes (one "
                         "scale per pool), q, bases and output bf16, f16 tensor-core inputs, fp32 "
                         "accumulation",
+    "decode_T4096_rope": "decode_T4096 with the exact rotary embedding (section 8): the cache keeps "
+                         "unrotated projections, every key is scored at its distance from the query "
+                         "(q D_(i-j)).S_K + ((q D_(i-j)) B_K[h]).R_K, d_h*r multiply-adds per key and "
+                         "head on CUDA cores; cos/sin table built once",
     "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
                     "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
@@ -140,6 +147,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
+ROPE_SPLIT_SOURCES = ("decode_generic.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 
 
 def kernel_source_hash(files=DECODE_SPLIT_SOURCES):
@@ -236,8 +244,16 @@ def run_ours(args, rank, world, local_rank):
             calls.append((a, dd, fs))
         return calls
 
+    rope = bool(c.get("rope"))
+    if rope:   # the cos/sin table is built once, outside every timed region
+        table = L.rope_table(d_h, max_seq, device=dev)
+        rope_args = (P(table), table.shape[0])
+
+        def dec_rope(q_, dsc, BK_, BV_, sl_, pt_, B_, mp_, msl_, out_, ws_, wsn_, st_, s_):
+            return lib.lrkv_decode_rope(q_, dsc, BK_, BV_, sl_, pt_, B_, mp_, msl_, *rope_args,
+                                        out_, ws_, wsn_, st_, s_)
     calls = make_calls(X, q, pos, sid, seq_lens, out)
-    f_app, f_dec, f_step = lib.lrkv_append, lib.lrkv_decode, lib.lrkv_decode_step
+    f_app, f_dec, f_step = lib.lrkv_append, (dec_rope if rope else lib.lrkv_decode), lib.lrkv_decode_step
 
     def step(i):
         # one decode step: append the B new rows, then decode the B queries
@@ -293,7 +309,7 @@ def run_ours(args, rank, world, local_rank):
         return a0.elapsed_time(a1) / K
     append_ms = timed(lambda i: f_app(*calls[i % n_copies][0]))
     decode_ms = timed(lambda i: f_dec(*calls[i % n_copies][1]))
-    fused_ms = timed(lambda i: f_step(*calls[i % n_copies][2]))
+    fused_ms = None if rope else timed(lambda i: f_step(*calls[i % n_copies][2]))
 
     # ---- the split kernel's own duration: the library brackets each launch
     # with CUDA events on its stream (a second pass over K steps, so those
@@ -354,6 +370,10 @@ def run_ours(args, rank, world, local_rank):
                   + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
     peak, peak_kind = measured_peaks()
     achieved = split_bytes / (split_ms / 1e3) / 1e9
+    # rotary path: bound by the d_h*r multiply-adds per key and head that form
+    # (q D_(i-j)) B_K[h] (2 d_h r flops; the d_h-wide shared term and the
+    # value reductions are not counted)
+    rope_flops = seq_total * H * 2 * d_h * r
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -365,19 +385,28 @@ def run_ours(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
                          f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
                    "step": "lrkv_append (B new rows) + lrkv_decode (B queries)"},
-        "roofline": {"kernel": "decode split (factored scores + online softmax + value reductions)",
+        "roofline": ({"kernel": "decode split with the exact rotary embedding (generic, FMA)",
+                      "bound": "alu", "achieved": round(rope_flops / (split_ms / 1e3) / 1e12, 3),
+                      "peak": round(FP32_FMA_TFLOPS, 2), "unit": "TFLOP/s",
+                      "frac": round(rope_flops / (split_ms / 1e3) / 1e12 / FP32_FMA_TFLOPS, 4),
+                      "peak_source": "FP32 FMA peak from unit counts: 152 SMs x 128 lanes x 2 x 2.07 GHz",
+                      "algorithmic_flops_per_launch": rope_flops,
+                      "hbm_gbs": round(achieved, 1),
+                      "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
+                      "traffic": profiled_traffic(name, files=ROPE_SPLIT_SOURCES)} if rope else
+                     {"kernel": "decode split (factored scores + online softmax + value reductions)",
                      "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "frac_of_8TBs": round(achieved / NORTH_STAR_HBM_GBS, 4),
                      "algorithmic_bytes_per_launch": split_bytes,
                      "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
-                     "traffic": profiled_traffic(name)},
+                     "traffic": profiled_traffic(name)}),
         "step_effective_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
         "breakdown_ms": {"split_kernel": round(split_ms, 5),
                          "lrkv_append_alone": round(append_ms, 5),
                          "lrkv_decode_alone": round(decode_ms, 5),
-                         "lrkv_decode_step": round(fused_ms, 5)},
+                         "lrkv_decode_step": None if fused_ms is None else round(fused_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host inputs copied in, result copied out and synchronised every step"},

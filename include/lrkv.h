@@ -278,6 +278,46 @@ LRKV_API int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows,
 LRKV_API int lrkv_prefill_kernel_kind(const lrkv_cache_t *cache);
 
 /*
+ * Exact rotary position embedding over the factored cache (reading note,
+ * section 8).  The cache keeps the unrotated projections S_K, S_V, R_K, R_V of
+ * lrkv_append.  With D_j the rotation that turns channel pairs (2c, 2c+1) of
+ * a row vector by j * theta_c, theta_c = base^(-2c/d_h) (all d_h channels,
+ * (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos)), head h's key at position j
+ * is (S_K[j] + R_K[h,j] B_K[h]^T) D_j and the query at position i is q D_i, so
+ *     s_j = (q D_{i-j}).S_K[j] + ((q D_{i-j}) B_K[h]).R_K[h,j]   (/ sqrt(d_h))
+ * -- the note's exact route (q~_i D_j^T B_h) z_j^T, which keeps z_j unrotated
+ * and pays d_h*r multiply-adds per key and head.  Values are not rotated.
+ * Key j of a request sits at position j; the decode query at seq_lens[b]-1,
+ * a prefill row at its own position.
+ *
+ * lrkv_rope_table fills table[dist][c] = (cos, sin)(dist * theta_c) for
+ * dist < max_pos and c < d_h/2 (float pairs, computed in double precision,
+ * rounded once): device memory of max_pos * d_h * 4 bytes, 8-byte aligned,
+ * caller-owned.  base > 1 and finite, d_h even in [2, 256], max_pos >= 1.
+ *
+ * lrkv_decode_rope / lrkv_prefill_rope take the arguments of lrkv_decode /
+ * lrkv_prefill plus that table and its max_pos, which must be >= max_seq_len
+ * (decode) or max_ctx (prefill).  d_h must be even and r <= 64.  The
+ * workspaces are those of lrkv_decode / lrkv_prefill.  Any cache dtype.
+ */
+LRKV_API int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, float *table,
+                             lrkv_stream_t stream);
+LRKV_API int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K,
+                              const void *B_V, const int32_t *seq_lens, const int32_t *page_table,
+                              int32_t B, int32_t max_pages, int32_t max_seq_len,
+                              const float *rope_table, int32_t rope_max_pos, void *out,
+                              void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                              lrkv_stream_t stream);
+LRKV_API int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_rows,
+                               const int32_t *start_pos, int32_t B, int32_t n, int32_t max_ctx,
+                               int32_t d, const void *W_S_K, const void *W_S_V, const void *U_K,
+                               const void *U_V, const void *B_K, const void *B_V,
+                               const lrkv_cache_t *cache, const int32_t *page_table,
+                               int32_t max_pages, const float *rope_table, int32_t rope_max_pos,
+                               void *out, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_status, lrkv_stream_t stream);
+
+/*
  * Cache payload in bytes for `tokens` cached positions of one layer:
  * tokens * 2 * (d_h + H*r) * sizeof(dtype)  (section 4, equation 9).
  * Returns 0 for invalid arguments.

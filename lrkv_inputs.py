@@ -331,6 +331,9 @@ CONFIGS = {
     "prefill_2048": dict(B=8, d=2048, H=16, d_h=128, r=48, T=2048, dtype="bf16", seed=0),
     # the 16 x 4096 decode over an 8-bit (E4M3) cache: same shapes, half the bytes
     "decode_T4096_fp8": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="fp8", seed=0),
+    # the 16 x 4096 decode with the exact rotary embedding (same cache)
+    "decode_T4096_rope": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="bf16", seed=0,
+                              rope=True),
 }
 
 

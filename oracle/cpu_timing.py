@@ -16,17 +16,21 @@ import time
 _CASE = None
 
 
+_ROPE = False
+
+
 def _init(config):
-    global _CASE
+    global _CASE, _ROPE
     import lrkv_inputs as I
     _CASE = I.config_decode_case(config)
+    _ROPE = bool(I.CONFIGS[config].get("rope"))
 
 
 def _run_pairs(pairs):
     import numpy as np
     import lrkv_inputs as I
     from . import lrkv_oracle as O
-    from . import fp8
+    from . import fp8, rope
     c = _CASE
     f = lambda a: I.to_f64(a, c.act_dtype)
     if c.dtype == "fp8":  # 8-bit pools: codes times the pool's scale
@@ -42,7 +46,10 @@ def _run_pairs(pairs):
         rv = fp(O.gather_rows(c.R_V, pages, L, c.page_size)[:, h, :], 3)
         K_h = O.expand_head(sk, rk, f(c.B_K[h]))
         V_h = O.expand_head(sv, rv, f(c.B_V[h]))
-        o = O.attend(f(c.q[b, h]), K_h, V_h)
+        qh = f(c.q[b, h])
+        if _ROPE:  # keys at positions 0..L-1, the query at L-1
+            K_h, qh = rope.rotate(K_h, np.arange(L)), rope.rotate(qh, L - 1)
+        o = O.attend(qh, K_h, V_h)
         assert np.all(np.isfinite(o))
     return time.perf_counter() - t0
 

@@ -15,7 +15,8 @@ from ._abi import (LRKV_BF16, LRKV_F32, LRKV_OK, LRKV_E_INVALID_ARG, LRKV_E_SHAP
 __all__ = [
     "lib", "CacheDesc", "LrkvError", "PagedCache", "append", "decode", "prefill",
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
-    "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes",
+    "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes", "rope_table",
+    "decode_rope", "prefill_rope",
 ]
 
 
@@ -24,7 +25,8 @@ def __getattr__(name):
     # without importing torch
     if name in ("PagedCache", "append", "decode", "prefill", "decode_workspace_bytes",
                 "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind",
-                "decode_step", "decode_step_workspace_bytes"):
+                "decode_step", "decode_step_workspace_bytes", "rope_table", "decode_rope",
+                "prefill_rope"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

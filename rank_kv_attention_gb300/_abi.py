@@ -78,6 +78,11 @@ SIGNATURES = {
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),
     "lrkv_prefill_kernel_kind": (ctypes.c_int, [CACHE_P]),
+    "lrkv_rope_table": (ctypes.c_int, [ctypes.c_double, I32, I32, P, P]),
+    "lrkv_decode_rope": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, I32, P, P, SZ, P,
+                                        P]),
+    "lrkv_prefill_rope": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P,
+                                         P, I32, P, I32, P, P, SZ, P, P]),
     "lrkv_cache_bytes": (SZ, [I32, I32, I32, ctypes.c_int64, I32]),
     "lrkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lrkv_last_cuda_error": (ctypes.c_int, []),

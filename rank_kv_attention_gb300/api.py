@@ -209,3 +209,72 @@ def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
                                    _ptr(status), _stream(stream))
     _abi.check("lrkv_prefill", code)
     return out
+
+
+# ----------------------------------------------------------------------------
+# Exact rotary position embedding (see include/lrkv.h)
+# ----------------------------------------------------------------------------
+def rope_table(d_h, max_pos, base=10000.0, device="cuda", stream=None) -> torch.Tensor:
+    """lrkv_rope_table: (cos, sin) of dist * base^(-2c/d_h), [max_pos, d_h/2, 2] fp32."""
+    t = torch.empty((max_pos, d_h // 2, 2), dtype=torch.float32, device=device)
+    _abi.check("lrkv_rope_table", _abi.lib().lrkv_rope_table(float(base), d_h, max_pos, _ptr(t),
+                                                             _stream(stream)))
+    return t
+
+
+def decode_rope(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_len, table,
+                out=None, ws=None, status=None, stream=None):
+    """lrkv_decode_rope: decode with the exact rotary embedding; the query of
+    request b sits at position seq_lens[b] - 1."""
+    dt = cache.act_dtype
+    for n, t in (("q", q), ("B_K", B_K), ("B_V", B_V)):
+        _need(t, n, dt)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(page_table, "page_table", torch.int32)
+    _need(table, "table", torch.float32)
+    B, H, d_h = q.shape
+    r = cache.R_K.shape[3]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", dt)
+    if ws is None:
+        ws = workspace(decode_workspace_bytes(B, H, d_h, r, max_seq_len, dt), q.device)
+    _need(ws, "ws", torch.uint8)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_decode_rope(_ptr(q), ctypes.byref(desc), _ptr(B_K), _ptr(B_V),
+                                       _ptr(seq_lens), _ptr(page_table), B, page_table.shape[1],
+                                       max_seq_len, _ptr(table), table.shape[0], _ptr(out),
+                                       _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
+    _abi.check("lrkv_decode_rope", code)
+    return out
+
+
+def prefill_rope(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
+                 cache: PagedCache, page_table, table, out=None, ws=None, status=None,
+                 stream=None):
+    """lrkv_prefill_rope: append the chunk X, then causal attention with the
+    exact rotary embedding (each row's query at its own position)."""
+    dt = cache.act_dtype
+    for n, t in (("X", X), ("Q", Q), ("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K),
+                 ("U_V", U_V), ("B_K", B_K), ("B_V", B_V)):
+        _need(t, n, dt)
+    for n, t in (("cu_rows", cu_rows), ("start_pos", start_pos), ("page_table", page_table)):
+        _need(t, n, torch.int32)
+    _need(table, "table", torch.float32)
+    n, d = X.shape
+    _, H, d_h = Q.shape
+    r = cache.R_K.shape[3]
+    B = start_pos.shape[0]
+    if out is None:
+        out = torch.empty_like(Q)
+    if ws is None:
+        ws = workspace(prefill_workspace_bytes(B, n, H, d_h, r, max_ctx, dt), X.device)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_prefill_rope(_ptr(X), _ptr(Q), _ptr(cu_rows), _ptr(start_pos), B, n,
+                                        max_ctx, d, _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K),
+                                        _ptr(U_V), _ptr(B_K), _ptr(B_V), ctypes.byref(desc),
+                                        _ptr(page_table), page_table.shape[1], _ptr(table),
+                                        table.shape[0], _ptr(out), _ptr(ws), ws.numel(),
+                                        _ptr(status), _stream(stream))
+    _abi.check("lrkv_prefill_rope", code)
+    return out

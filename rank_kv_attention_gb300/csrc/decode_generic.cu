@@ -7,6 +7,8 @@
 // online softmax (running max and exp-sum, both value accumulators rescaled
 // together when the max moves) reduces S_V and R_V[h] with the same weights;
 // the private reduction is expanded once by B_V[h]^T at the end.
+#include <algorithm>
+
 #include "decode_kernels.cuh"
 
 namespace lrkv {
@@ -155,18 +157,35 @@ __device__ __forceinline__ int find_request(const int32_t *off, int B, int32_t x
 // ---------------------------------------------------------------------------
 constexpr int kGenTile = 128;
 
+// Exact rotary position embedding (reading note, section 8).  The cache holds
+// the unrotated projections; a key at position j meets a query at position i
+// through D_i D_j^T = D_{i-j}, so with u = q D_{i-j} (channel pairs (2c, 2c+1)
+// turned by (i - j) theta_c) its score is u.s_j + (u B_K[h]).z_j -- the
+// note's (q~_i D_j^T B_h) z_j^T plus the rotated shared term.  Per (request,
+// head) the kernel forms, for channel pair c and private column k,
+//   A[c][k] = q_2c B[2c][k] + q_2c+1 B[2c+1][k],
+//   Bq[c][k] = q_2c B[2c+1][k] - q_2c+1 B[2c][k],
+// so that (u B_K[h])_k = sum_c cos(D theta_c) A[c][k] + sin(D theta_c) Bq[c][k]
+// and u.s = sum_c cos (q_2c s_2c + q_2c+1 s_2c+1) + sin (q_2c s_2c+1 - q_2c+1 s_2c).
+// cos and sin of D theta_c come from a table indexed by the distance D.
+struct RopeArgs {
+    const float2 *table;  // [max_pos][d_h / 2] (cos, sin)
+    int max_pos;
+};
+
 // T: query element type; TC: cache element type (T, or 8-bit codes whose pool
 // scales sc = (S_K, S_V, R_K, R_V) fold into the queries and accumulators).
-template <typename T, typename TC>
+// RP > 0: scores with the exact rotary embedding, private width padded to RP.
+template <typename T, typename TC, int RP = 0>
 __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
     const T *__restrict__ q, const TC *__restrict__ S_K, const TC *__restrict__ S_V,
     const TC *__restrict__ R_K, const TC *__restrict__ R_V, const int32_t *__restrict__ page_table,
     const int32_t *__restrict__ req_row, int max_pages, int num_pages, int page_size, int B, int H, int d_h, int r,
-    float scale_log2, float4 sc, DecodeWs ws, int32_t *status) {
+    float scale_log2, float4 sc, DecodeWs ws, int32_t *status, const T *__restrict__ B_K, RopeArgs rope) {
     extern __shared__ float sm[];
     float *qs = sm;                 // d_h
-    float *ps = qs + d_h;           // r
-    float *w = ps + r;              // kGenTile weights
+    float *ps = qs + d_h;           // r (plain) or A, Bq [d_h / 2][RP] each (rotary)
+    float *w = ps + (RP ? d_h * RP : r);  // kGenTile weights
     int32_t *row = reinterpret_cast<int32_t *>(w + kGenTile);  // kGenTile pool rows
     __shared__ float red[kGenTile / 32];
 
@@ -185,18 +204,43 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
         const int32_t base = ws.off[b];
         const int32_t seg_end = min(end, ws.off[b + 1]);
         const int t_a = start - base, t_b = seg_end - base;
+        const int32_t q_pos = ws.off[b + 1] - base - 1;  // rotary: the query's position
+        // rotary: a query past the end of the cos/sin table is not attended
+        // (zero output, flagged) rather than read out of bounds
+        const bool rope_ok = RP == 0 || q_pos < rope.max_pos;
+        if (!rope_ok && tid == 0 && g * chunk <= base) status_or(status, LRKV_STATUS_BAD_SEQLEN);
 
         const int32_t *pt = page_table + (size_t)(req_row ? req_row[b] : b) * max_pages;
-        for (int d = tid; d < d_h; d += kGenTile)
-            qs[d] = Elem<T>::load(q + ((size_t)b * H + h) * d_h + d) * sc.x;
-        for (int k = tid; k < r; k += kGenTile) ps[k] = ws.p[((size_t)b * H + h) * r + k] * sc.z;
+        const T *qr = q + ((size_t)b * H + h) * d_h;
+        for (int d = tid; d < d_h; d += kGenTile) qs[d] = Elem<T>::load(qr + d) * sc.x;
+        if constexpr (RP == 0) {
+            for (int k = tid; k < r; k += kGenTile) ps[k] = ws.p[((size_t)b * H + h) * r + k] * sc.z;
+        } else {
+            // A and Bq of this (request, head), zero beyond column r; the R_K
+            // pool scale folds in here
+            const T *bk = B_K + (size_t)h * d_h * r;
+            const int hc = d_h / 2;
+            for (int i = tid; i < hc * RP; i += kGenTile) {
+                const int c = i / RP, k = i % RP;
+                float a = 0.f, bq = 0.f;
+                if (k < r) {
+                    const float q0 = Elem<T>::load(qr + 2 * c), q1 = Elem<T>::load(qr + 2 * c + 1);
+                    const float b0 = Elem<T>::load(bk + (size_t)(2 * c) * r + k);
+                    const float b1 = Elem<T>::load(bk + (size_t)(2 * c + 1) * r + k);
+                    a = (q0 * b0 + q1 * b1) * sc.z;
+                    bq = (q0 * b1 - q1 * b0) * sc.z;
+                }
+                ps[c * RP + k] = a;
+                ps[hc * RP + c * RP + k] = bq;
+            }
+        }
         __syncthreads();
 
         float m = -INFINITY, l = 0.f;
         float accS[2] = {0.f, 0.f}, accR[2] = {0.f, 0.f};
         for (int t0 = t_a; t0 < t_b; t0 += kGenTile) {
             const int j = t0 + tid;
-            bool valid = j < t_b;
+            bool valid = j < t_b && rope_ok;
             float s = -INFINITY;
             int32_t prow = -1;
             if (valid) {
@@ -209,8 +253,32 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     const TC *sk = S_K + (size_t)prow * d_h;
                     const TC *rk = R_K + ((size_t)prow * H + h) * r;
                     float acc = 0.f;
-                    for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], CacheLoad<TC>::load(sk + d), acc);
-                    for (int k = 0; k < r; ++k) acc = fmaf(ps[k], CacheLoad<TC>::load(rk + k), acc);
+                    if constexpr (RP == 0) {
+                        for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], CacheLoad<TC>::load(sk + d), acc);
+                        for (int k = 0; k < r; ++k) acc = fmaf(ps[k], CacheLoad<TC>::load(rk + k), acc);
+                    } else {
+                        // distance from the query (the request's last row,
+                        // which may lie beyond this segment) to key j
+                        const float2 *cs = rope.table + (size_t)(q_pos - j) * (d_h / 2);
+                        const int hc = d_h / 2;
+                        float pk[RP];
+#pragma unroll
+                        for (int k = 0; k < RP; ++k) pk[k] = 0.f;
+                        for (int c = 0; c < hc; ++c) {
+                            const float2 e = cs[c];
+                            const float s0 = CacheLoad<TC>::load(sk + 2 * c);
+                            const float s1 = CacheLoad<TC>::load(sk + 2 * c + 1);
+                            const float q0 = qs[2 * c], q1 = qs[2 * c + 1];
+                            acc = fmaf(e.x, fmaf(q0, s0, q1 * s1), acc);
+                            acc = fmaf(e.y, fmaf(q0, s1, -q1 * s0), acc);
+                            const float *a = ps + c * RP, *bq = ps + hc * RP + c * RP;
+#pragma unroll
+                            for (int k = 0; k < RP; ++k) pk[k] = fmaf(e.x, a[k], fmaf(e.y, bq[k], pk[k]));
+                        }
+#pragma unroll
+                        for (int k = 0; k < RP; ++k)
+                            if (k < r) acc = fmaf(pk[k], CacheLoad<TC>::load(rk + k), acc);
+                    }
                     s = acc * scale_log2;
                 }
             }
@@ -485,25 +553,65 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
                       a.status);
 }
 
-template <typename T, typename TC>
+template <typename T, typename TC, int RP>
 static cudaError_t launch_split_generic_t(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const auto &c = a.cache;
-    const size_t sm = sizeof(float) * (c.d_h + c.r + kGenTile) + sizeof(int32_t) * kGenTile;
+    const size_t sm = sizeof(float) * (c.d_h + (RP ? (size_t)c.d_h * RP : c.r) + kGenTile) +
+                      sizeof(int32_t) * kGenTile;
+    auto kern = decode_split_generic_kernel<T, TC, RP>;
+    if (sm > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+    }
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)c.d_h);
     const bool q8 = c.dtype == LRKV_FP8_E4M3;
     const float4 sc = q8 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
                          : make_float4(1.f, 1.f, 1.f, 1.f);
-    return launch_pdl(decode_split_generic_kernel<T, TC>, dim3(G, c.H), dim3(kGenTile), sm, a.stream,
-                      static_cast<const T *>(a.q), static_cast<const TC *>(c.S_K),
-                      static_cast<const TC *>(c.S_V), static_cast<const TC *>(c.R_K),
-                      static_cast<const TC *>(c.R_V), a.page_table, a.req_row, a.max_pages,
-                      c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r, scale_log2, sc, ws, a.status);
+    RopeArgs rope{reinterpret_cast<const float2 *>(a.rope), a.rope_max_pos};
+    return launch_pdl(kern, dim3(G, c.H), dim3(kGenTile), sm, a.stream, static_cast<const T *>(a.q),
+                      static_cast<const TC *>(c.S_K), static_cast<const TC *>(c.S_V),
+                      static_cast<const TC *>(c.R_K), static_cast<const TC *>(c.R_V), a.page_table,
+                      a.req_row, a.max_pages, c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r,
+                      scale_log2, sc, ws, a.status, static_cast<const T *>(a.B_K), rope);
+}
+
+template <typename T, typename TC>
+static cudaError_t launch_split_generic_rp(const DecodeArgs &a, const DecodeWs &ws, int G) {
+    if (!a.rope) return launch_split_generic_t<T, TC, 0>(a, ws, G);
+    const int r = a.cache.r;  // the caller checks 1 <= r <= kRopeMaxRank
+    if (r <= 16) return launch_split_generic_t<T, TC, 16>(a, ws, G);
+    if (r <= 32) return launch_split_generic_t<T, TC, 32>(a, ws, G);
+    if (r <= 48) return launch_split_generic_t<T, TC, 48>(a, ws, G);
+    return launch_split_generic_t<T, TC, 64>(a, ws, G);
 }
 
 template <typename T>
 cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G) {
-    if (a.cache.dtype == LRKV_FP8_E4M3) return launch_split_generic_t<__nv_bfloat16, uint8_t>(a, ws, G);
-    return launch_split_generic_t<T, T>(a, ws, G);
+    if (a.cache.dtype == LRKV_FP8_E4M3) return launch_split_generic_rp<__nv_bfloat16, uint8_t>(a, ws, G);
+    return launch_split_generic_rp<T, T>(a, ws, G);
+}
+
+// cos and sin of distance x theta_c, theta_c = base^(-2c/d_h), in double
+// precision, rounded once to float.
+__global__ void rope_table_kernel(double base, int d_h, int max_pos, float2 *table) {
+    const int hc = d_h / 2;
+    const size_t n = (size_t)max_pos * hc;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % hc);
+        const double pos = (double)(i / hc);
+        const double th = pow(base, -2.0 * c / d_h);
+        double sv, cv;
+        sincos(pos * th, &sv, &cv);
+        table[i] = make_float2((float)cv, (float)sv);
+    }
+}
+
+cudaError_t launch_rope_table(double base, int d_h, int max_pos, float *table, cudaStream_t s) {
+    const size_t n = (size_t)max_pos * (d_h / 2);
+    const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+    rope_table_kernel<<<blocks, 256, 0, s>>>(base, d_h, max_pos, reinterpret_cast<float2 *>(table));
+    return cudaGetLastError();
 }
 
 template <typename T>

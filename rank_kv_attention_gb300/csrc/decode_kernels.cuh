@@ -27,7 +27,15 @@ struct DecodeArgs {
     const void *X = nullptr;
     const void *W[4] = {nullptr, nullptr, nullptr, nullptr};
     int d = 0;
+    // Exact rotary position embedding when rope != nullptr: the cos/sin table
+    // [rope_max_pos][d_h / 2] of lrkv_rope_table (generic split kernel only).
+    const float *rope = nullptr;
+    int rope_max_pos = 0;
 };
+
+// Largest private width the rotary split kernel keeps in registers.
+constexpr int kRopeMaxRank = 64;
+cudaError_t launch_rope_table(double base, int d_h, int max_pos, float *table, cudaStream_t s);
 
 // Rows the split kernels stream for a request of length L: none for an
 // invalid length, else L, minus the new row that a fused step folds in later.

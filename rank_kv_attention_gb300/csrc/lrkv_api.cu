@@ -111,7 +111,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     DecodeGeom geo = decode_geom(a.B, a.max_seq_len);
     DecodeWs ws = decode_ws_layout(workspace, a.B, c.H, c.d_h, c.r, geo.G_ws);
     if (ws_bytes < ws.bytes) return LRKV_E_WORKSPACE;
-    const bool fast = fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype);
+    const bool fast = !a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype);
     const int G = fast ? geo.G_fast : geo.G_gen;
     cudaError_t e;
     if (c.dtype != LRKV_F32) {  // bf16 activations (bf16 or 8-bit cache)
@@ -478,12 +478,13 @@ size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h
     return prefill_ws_layout(nullptr, n, H, d_h, r, max_ctx).bytes;
 }
 
-int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int32_t *start_pos,
-                 int32_t B, int32_t n, int32_t max_ctx, int32_t d, const void *W_S_K,
-                 const void *W_S_V, const void *U_K, const void *U_V, const void *B_K,
-                 const void *B_V, const lrkv_cache_t *cache, const int32_t *page_table,
-                 int32_t max_pages, void *out, void *workspace, size_t workspace_bytes,
-                 int32_t *dev_status, lrkv_stream_t stream) {
+static int prefill_impl(const void *X, const void *Q, const int32_t *cu_rows,
+                        const int32_t *start_pos, int32_t B, int32_t n, int32_t max_ctx, int32_t d,
+                        const void *W_S_K, const void *W_S_V, const void *U_K, const void *U_V,
+                        const void *B_K, const void *B_V, const lrkv_cache_t *cache,
+                        const int32_t *page_table, int32_t max_pages, const float *rope,
+                        int32_t rope_max_pos, void *out, void *workspace, size_t workspace_bytes,
+                        int32_t *dev_status, lrkv_stream_t stream) {
     int st = check_append(X, cu_rows, start_pos, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table,
                           B, max_pages);
     if (st) return st;
@@ -504,7 +505,7 @@ int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int
     st = run_append(X, w.pos, w.sid, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
                     dev_status, s);
     if (st) return st;
-    {
+    if (!rope) {
         // Causal attention on tensor cores (query tiles of 128 rows per head).
         PrefillTcArgs p;
         p.Q = Q;
@@ -543,7 +544,90 @@ int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int
     a.out = out;
     a.status = dev_status;
     a.stream = s;
+    a.rope = rope;
+    a.rope_max_pos = rope_max_pos;
     return run_decode(a, w.dec, w.dec_bytes);
+}
+
+int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int32_t *start_pos,
+                 int32_t B, int32_t n, int32_t max_ctx, int32_t d, const void *W_S_K,
+                 const void *W_S_V, const void *U_K, const void *U_V, const void *B_K,
+                 const void *B_V, const lrkv_cache_t *cache, const int32_t *page_table,
+                 int32_t max_pages, void *out, void *workspace, size_t workspace_bytes,
+                 int32_t *dev_status, lrkv_stream_t stream) {
+    return prefill_impl(X, Q, cu_rows, start_pos, B, n, max_ctx, d, W_S_K, W_S_V, U_K, U_V, B_K,
+                        B_V, cache, page_table, max_pages, nullptr, 0, out, workspace,
+                        workspace_bytes, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Exact rotary position embedding
+// ---------------------------------------------------------------------------
+static bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+static int check_rope(const lrkv_cache_t *cache, const float *table, int32_t max_pos, int32_t need) {
+    if (cache->d_h % 2 || cache->r > kRopeMaxRank) return LRKV_E_SHAPE;
+    if (!table || !aligned8(table)) return LRKV_E_INVALID_ARG;
+    if (max_pos < need) return LRKV_E_BOUNDS;
+    return LRKV_OK;
+}
+
+int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, float *table, lrkv_stream_t stream) {
+    if (!(base > 1.0) || !std::isfinite(base)) return LRKV_E_INVALID_ARG;
+    if (d_h < 2 || d_h > 256 || d_h % 2 || max_pos < 1) return LRKV_E_SHAPE;
+    if (!table || !aligned8(table)) return LRKV_E_INVALID_ARG;
+    cudaError_t e = launch_rope_table(base, d_h, max_pos, table, (cudaStream_t)stream);
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+}
+
+int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K, const void *B_V,
+                     const int32_t *seq_lens, const int32_t *page_table, int32_t B,
+                     int32_t max_pages, int32_t max_seq_len, const float *rope_table,
+                     int32_t rope_max_pos, void *out, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if (B < 1 || max_pages < 1 || max_seq_len < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * cache->page_size) return LRKV_E_BOUNDS;
+    if ((int64_t)B * max_seq_len > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (!q || !B_K || !B_V || !seq_lens || !page_table || !out) return LRKV_E_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(B_K) || !aligned16(B_V) || !aligned16(out))
+        return LRKV_E_INVALID_ARG;
+    if ((st = check_rope(cache, rope_table, rope_max_pos, max_seq_len))) return st;
+    if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    DecodeArgs a;
+    a.q = q;
+    a.cache = *cache;
+    a.B_K = B_K;
+    a.B_V = B_V;
+    a.seq_lens = seq_lens;
+    a.page_table = page_table;
+    a.req_row = nullptr;
+    a.B = B;
+    a.max_pages = max_pages;
+    a.max_seq_len = max_seq_len;
+    a.out = out;
+    a.status = dev_status;
+    a.stream = (cudaStream_t)stream;
+    a.rope = rope_table;
+    a.rope_max_pos = rope_max_pos;
+    return run_decode(a, workspace, workspace_bytes);
+}
+
+int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_rows,
+                      const int32_t *start_pos, int32_t B, int32_t n, int32_t max_ctx, int32_t d,
+                      const void *W_S_K, const void *W_S_V, const void *U_K, const void *U_V,
+                      const void *B_K, const void *B_V, const lrkv_cache_t *cache,
+                      const int32_t *page_table, int32_t max_pages, const float *rope_table,
+                      int32_t rope_max_pos, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_rope(cache, rope_table, rope_max_pos, max_ctx))) return st;
+    return prefill_impl(X, Q, cu_rows, start_pos, B, n, max_ctx, d, W_S_K, W_S_V, U_K, U_V, B_K,
+                        B_V, cache, page_table, max_pages, rope_table, rope_max_pos, out,
+                        workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -169,3 +169,28 @@ def test_decode_step_rejects_on_host(lib):
     a = lib.lrkv_decode_step_workspace_bytes(16, 16, 128, 48, 4096, 1)
     assert a >= lib.lrkv_decode_workspace_bytes(16, 16, 128, 48, 4096, 1) > 0
     assert lib.lrkv_decode_step_workspace_bytes(0, 16, 128, 48, 4096, 1) == 0
+
+
+def test_rope_host_checks(lib):
+    """Rotary entry points reject bad tables and shapes before any launch."""
+    E = _abi
+    assert lib.lrkv_rope_table(1.0, 128, 10, 256, None) == E.LRKV_E_INVALID_ARG     # base <= 1
+    assert lib.lrkv_rope_table(float("inf"), 128, 10, 256, None) == E.LRKV_E_INVALID_ARG
+    assert lib.lrkv_rope_table(1e4, 127, 10, 256, None) == E.LRKV_E_SHAPE           # odd d_h
+    assert lib.lrkv_rope_table(1e4, 128, 0, 256, None) == E.LRKV_E_SHAPE
+    assert lib.lrkv_rope_table(1e4, 128, 10, None, None) == E.LRKV_E_INVALID_ARG
+    assert lib.lrkv_rope_table(1e4, 128, 10, 4, None) == E.LRKV_E_INVALID_ARG       # misaligned
+    ws = ctypes.c_void_p(256)
+
+    def dec(cache, table=16, max_pos=100, msl=100):
+        return lib.lrkv_decode_rope(16, ctypes.byref(cache), 16, 16, 16, 16, 2, 4, msl, table,
+                                    max_pos, 16, ws, 1 << 30, None, None)
+    assert dec(_cache(), table=None) == E.LRKV_E_INVALID_ARG
+    assert dec(_cache(), table=12) == E.LRKV_E_INVALID_ARG                        # not 8-aligned
+    assert dec(_cache(), max_pos=99) == E.LRKV_E_BOUNDS                           # table too short
+    assert dec(_cache(r=72)) == E.LRKV_E_SHAPE                                    # r > 64
+    assert dec(_cache(d_h=130)) == E.LRKV_E_SHAPE
+    assert dec(_cache(dtype=5)) == E.LRKV_E_DTYPE
+    assert lib.lrkv_prefill_rope(16, 16, 16, 16, 2, 10, 100, 256, 16, 16, 16, 16, 16, 16,
+                                 ctypes.byref(_cache()), 16, 4, 16, 99, 16, ws, 1 << 30, None,
+                                 None) == E.LRKV_E_BOUNDS
