@@ -45,6 +45,9 @@ WORKLOADS = {
                          "unrotated projections, every key is scored at its distance from the query "
                          "(q D_(i-j)).S_K + ((q D_(i-j)) B_K[h]).R_K, d_h*r multiply-adds per key and "
                          "head on CUDA cores; cos/sin table built once",
+    "decode_T4096_norm": "decode_T4096 with joint key RMSNorm (section 8): a bf16 reciprocal per "
+                         "head and token multiplies each score; the step appends the rows, stores "
+                         "their reciprocals (lrkv_key_norms) and decodes",
     "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
                     "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
@@ -209,12 +212,23 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
     eb = 1 if case.dtype == "fp8" else 2   # bytes per cache element
+    norm = bool(c.get("norm"))
     base = PagedCache(*(to_dev(t, case.dtype) for t in (case.S_K, case.S_V, case.R_K, case.R_V)),
                       tuple(case.scale))
-    cache_bytes = sum(t.numel() * eb for t in (base.S_K, base.S_V, base.R_K, base.R_V))
+    if norm:   # joint key norms of every cached row, written once before timing
+        base.N_K = torch.empty((case.num_pages, case.page_size, case.H), dtype=torch.bfloat16,
+                               device=dev)
+        base.norm_eps = 1e-6
+        allpos = np.concatenate([np.arange(Lr) for Lr in case.seq_lens]).astype(np.int32)
+        allsid = np.concatenate([np.full(Lr, b) for b, Lr in enumerate(case.seq_lens)]).astype(np.int32)
+        L.key_norms(to_dev(allpos, "i32"), to_dev(allsid, "i32"), to_dev(case.B_K), base,
+                    to_dev(case.page_table, "i32"))
+    cache_bytes = sum(t.numel() * eb for t in (base.S_K, base.S_V, base.R_K, base.R_V)) + \
+        (base.N_K.numel() * 2 if norm else 0)
     n_copies = max(1, math.ceil(4 * L2_BYTES / cache_bytes))
     caches = [base] + [PagedCache(*(t.clone() for t in (base.S_K, base.S_V, base.R_K, base.R_V)),
-                                  base.scale) for _ in range(n_copies - 1)]
+                                  base.scale, base.N_K.clone() if norm else None, base.norm_eps)
+                       for _ in range(n_copies - 1)]
     q = to_dev(case.q)
     BK, BV = to_dev(case.B_K), to_dev(case.B_V)
     Wsk, Wsv, Uk, Uv = (to_dev(a) for a in (w.W_S_K, w.W_S_V, w.U_K, w.U_V))
@@ -241,7 +255,8 @@ def run_ours(args, rank, world, local_rank):
                   P(out_), P(ws), ws.numel(), P(status), sp)
             fs = (P(X_), d, P(Wsk), P(Wsv), P(Uk), P(Uv), P(q_), ctypes.byref(dsc), P(BK), P(BV),
                   P(sl_), P(pt), Bn, pt.shape[1], max_seq, P(out_), P(ws), ws.numel(), P(status), sp)
-            calls.append((a, dd, fs))
+            kn = (P(pos_), P(sid_), Bn, P(BK), ctypes.byref(dsc), P(pt), Bn, pt.shape[1], P(status), sp)
+            calls.append((a, dd, fs, kn))
         return calls
 
     rope = bool(c.get("rope"))
@@ -256,12 +271,14 @@ def run_ours(args, rank, world, local_rank):
     f_app, f_dec, f_step = lib.lrkv_append, (dec_rope if rope else lib.lrkv_decode), lib.lrkv_decode_step
 
     def step(i):
-        # one decode step: append the B new rows, then decode the B queries
-        a, dd, _ = calls[i % n_copies]
+        # one decode step: append the B new rows (and store their key norms),
+        # then decode the B queries
+        a, dd, _, kn = calls[i % n_copies]
         rc = f_app(*a)
+        rc3 = lib.lrkv_key_norms(*kn) if norm else 0
         rc2 = f_dec(*dd)
-        if rc or rc2:
-            raise RuntimeError(f"lrkv call failed: {rc} {rc2}")
+        if rc or rc2 or rc3:
+            raise RuntimeError(f"lrkv call failed: {rc} {rc3} {rc2}")
 
     def barrier():
         if world > 1:
@@ -365,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
     tokens = world * Bn * K
     value = tokens / (total_ms / 1e3)
     seq_total = int(case.seq_lens.astype(np.int64).sum())
-    split_bytes = seq_total * 2 * (d_h + H * r) * eb         # cache rows read once
+    split_bytes = seq_total * (2 * (d_h + H * r) * eb + (2 * H if norm else 0))  # cache rows read once
     step_bytes = (split_bytes + 2 * H * d_h * r * 2 + 2 * Bn * H * d_h * 2   # + bases, q, out
                   + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
     peak, peak_kind = measured_peaks()
@@ -384,7 +401,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (requests are independent)",
                    "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
                          f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
-                   "step": "lrkv_append (B new rows) + lrkv_decode (B queries)"},
+                   "step": "lrkv_append (B new rows) + " + ("lrkv_key_norms (their reciprocal key norms) + "
+                                                            if norm else "") + "lrkv_decode (B queries)"},
         "roofline": ({"kernel": "decode split with the exact rotary embedding (generic, FMA)",
                       "bound": "alu", "achieved": round(rope_flops / (split_ms / 1e3) / 1e12, 3),
                       "peak": round(FP32_FMA_TFLOPS, 2), "unit": "TFLOP/s",
@@ -410,7 +428,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host inputs copied in, result copied out and synchronised every step"},
-        "gpu_launches": 4 * K,   # per step: append, prologue, split, combine
+        "gpu_launches": (5 if norm else 4) * K,   # per step: append, [key norms,] prologue, split, combine
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

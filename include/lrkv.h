@@ -92,6 +92,17 @@ enum {
  * x / s rounded to the nearest E4M3 value (ties to even, finite values beyond
  * +-448 saturating), and reads back decode(code) * s; scale[] is ignored for
  * the other dtypes.
+ *
+ * Joint key RMSNorm (reading note, section 8): when N_K is not NULL the cache
+ * also holds, per token and head, the reciprocal root mean square of the full
+ * key,  1 / sqrt(mean_d (S_K[j] + R_K[h,j] B_K[h]^T)_d^2 + norm_eps),
+ *     N_K : [num_pages, page_size, H]   (bf16 for LRKV_BF16 and
+ *            LRKV_FP8_E4M3 caches, fp32 for LRKV_F32; 16-byte aligned)
+ * and every score is multiplied by it: s_j = (q.S_K[j] + p.R_K[h,j]) N_K[j,h]
+ * / sqrt(d_h).  The values N_K holds are written by lrkv_key_norms (and by
+ * lrkv_prefill and lrkv_decode_step for the rows they append).  A
+ * per-channel gain and the query's own normalisation belong to q.  Costs one
+ * scalar per head and token, 1/(2 d_h) of a dense K/V cache.
  */
 typedef struct {
     void *S_K;
@@ -105,6 +116,8 @@ typedef struct {
     int32_t r;
     int32_t dtype;  /* lrkv_dtype_t */
     float scale[4]; /* LRKV_FP8_E4M3: scale of S_K, S_V, R_K, R_V (positive, finite) */
+    void *N_K;      /* NULL, or the reciprocal key norms [num_pages, page_size, H] */
+    float norm_eps; /* N_K: eps of the root mean square (finite, >= 0) */
 } lrkv_cache_t;
 
 /*
@@ -276,6 +289,20 @@ LRKV_API int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows,
 #define LRKV_PREFILL_PER_ROW 0
 #define LRKV_PREFILL_TILED 1
 LRKV_API int lrkv_prefill_kernel_kind(const lrkv_cache_t *cache);
+
+/*
+ * lrkv_key_norms - store the reciprocal joint norm of the keys of n cached
+ * rows (reading note, section 8): for row i (request seq_ids[i], position
+ * positions[i], as in lrkv_append) and every head h,
+ *     N_K[row, h] = 1 / sqrt(mean_d (S_K[row] + R_K[row, h] B_K[h]^T)_d^2 + norm_eps)
+ * from the values the cache holds (call it after lrkv_append).  cache->N_K
+ * must not be NULL.  Rows out of range are skipped and flagged like
+ * lrkv_append's.  B_K [H, d_h, r] in the activation dtype.
+ */
+LRKV_API int lrkv_key_norms(const int32_t *positions, const int32_t *seq_ids, int32_t n,
+                            const void *B_K, const lrkv_cache_t *cache, const int32_t *page_table,
+                            int32_t B, int32_t max_pages, int32_t *dev_status,
+                            lrkv_stream_t stream);
 
 /*
  * Exact rotary position embedding over the factored cache (reading note,

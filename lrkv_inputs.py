@@ -334,6 +334,9 @@ CONFIGS = {
     # the 16 x 4096 decode with the exact rotary embedding (same cache)
     "decode_T4096_rope": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="bf16", seed=0,
                               rope=True),
+    # the 16 x 4096 decode with joint key RMSNorm (a reciprocal per head and token)
+    "decode_T4096_norm": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="bf16", seed=0,
+                              norm=True),
 }
 
 

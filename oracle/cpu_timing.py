@@ -17,20 +17,22 @@ _CASE = None
 
 
 _ROPE = False
+_NORM = False
 
 
 def _init(config):
-    global _CASE, _ROPE
+    global _CASE, _ROPE, _NORM
     import lrkv_inputs as I
     _CASE = I.config_decode_case(config)
     _ROPE = bool(I.CONFIGS[config].get("rope"))
+    _NORM = bool(I.CONFIGS[config].get("norm"))
 
 
 def _run_pairs(pairs):
     import numpy as np
     import lrkv_inputs as I
     from . import lrkv_oracle as O
-    from . import fp8, rope
+    from . import fp8, norm, rope
     c = _CASE
     f = lambda a: I.to_f64(a, c.act_dtype)
     if c.dtype == "fp8":  # 8-bit pools: codes times the pool's scale
@@ -47,6 +49,8 @@ def _run_pairs(pairs):
         K_h = O.expand_head(sk, rk, f(c.B_K[h]))
         V_h = O.expand_head(sv, rv, f(c.B_V[h]))
         qh = f(c.q[b, h])
+        if _NORM:  # joint key RMSNorm (eps 1e-6)
+            K_h = norm.rms_normalise(K_h, 1e-6)
         if _ROPE:  # keys at positions 0..L-1, the query at L-1
             K_h, qh = rope.rotate(K_h, np.arange(L)), rope.rotate(qh, L - 1)
         o = O.attend(qh, K_h, V_h)

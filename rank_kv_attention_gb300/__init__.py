@@ -16,7 +16,7 @@ __all__ = [
     "lib", "CacheDesc", "LrkvError", "PagedCache", "append", "decode", "prefill",
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
     "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes", "rope_table",
-    "decode_rope", "prefill_rope",
+    "decode_rope", "prefill_rope", "key_norms",
 ]
 
 
@@ -26,7 +26,7 @@ def __getattr__(name):
     if name in ("PagedCache", "append", "decode", "prefill", "decode_workspace_bytes",
                 "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind",
                 "decode_step", "decode_step_workspace_bytes", "rope_table", "decode_rope",
-                "prefill_rope"):
+                "prefill_rope", "key_norms"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

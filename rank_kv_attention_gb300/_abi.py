@@ -45,6 +45,7 @@ class CacheDesc(ctypes.Structure):
         ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
         ("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("scale", ctypes.c_float * 4),
+        ("N_K", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
     ]
 
 
@@ -79,6 +80,7 @@ SIGNATURES = {
                                     I32, P, P, SZ, P, P]),
     "lrkv_prefill_kernel_kind": (ctypes.c_int, [CACHE_P]),
     "lrkv_rope_table": (ctypes.c_int, [ctypes.c_double, I32, I32, P, P]),
+    "lrkv_key_norms": (ctypes.c_int, [P, P, I32, P, CACHE_P, P, I32, I32, P, P]),
     "lrkv_decode_rope": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, I32, P, P, SZ, P,
                                         P]),
     "lrkv_prefill_rope": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P,

@@ -45,13 +45,17 @@ class PagedCache:
     S_K, S_V: [num_pages, page_size, d_h]; R_K, R_V: [num_pages, page_size, H, r].
     Pools of torch.float8_e4m3fn hold 8-bit codes whose values are the codes
     times ``scale`` (one scale per pool: S_K, S_V, R_K, R_V); the activations
-    used with such a cache are bf16.
+    used with such a cache are bf16.  ``N_K`` ([num_pages, page_size, H] in
+    the activation dtype, or None) holds the reciprocal joint key norms with
+    ``norm_eps`` (see lrkv_key_norms).
     """
     S_K: torch.Tensor
     S_V: torch.Tensor
     R_K: torch.Tensor
     R_V: torch.Tensor
     scale: tuple = (1.0, 1.0, 1.0, 1.0)
+    N_K: "torch.Tensor | None" = None
+    norm_eps: float = 0.0
 
     @classmethod
     def empty(cls, num_pages, page_size, H, d_h, r, dtype=torch.bfloat16, device="cuda"):
@@ -73,9 +77,15 @@ class PagedCache:
             _need(getattr(self, n), n, self.dtype)
         npg, ps, d_h = self.S_K.shape
         _, _, H, r = self.R_K.shape
+        if self.N_K is not None:
+            _need(self.N_K, "N_K", self.act_dtype)
+            if tuple(self.N_K.shape) != (npg, ps, H):
+                raise ValueError(f"N_K must be [{npg}, {ps}, {H}], got {tuple(self.N_K.shape)}")
         return _abi.CacheDesc(self.S_K.data_ptr(), self.S_V.data_ptr(), self.R_K.data_ptr(),
                               self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype],
-                              (ctypes.c_float * 4)(*[float(x) for x in self.scale]))
+                              (ctypes.c_float * 4)(*[float(x) for x in self.scale]),
+                              self.N_K.data_ptr() if self.N_K is not None else None,
+                              float(self.norm_eps))
 
 
 def prefill_kernel_kind(cache: PagedCache) -> int:
@@ -278,3 +288,18 @@ def prefill_rope(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K,
                                         _ptr(status), _stream(stream))
     _abi.check("lrkv_prefill_rope", code)
     return out
+
+
+def key_norms(positions, seq_ids, B_K, cache: PagedCache, page_table, status=None, stream=None):
+    """lrkv_key_norms: store the reciprocal joint key norms of the given rows."""
+    _need(B_K, "B_K", cache.act_dtype)
+    for n, t in (("positions", positions), ("seq_ids", seq_ids), ("page_table", page_table)):
+        _need(t, n, torch.int32)
+    if cache.N_K is None:
+        raise ValueError("cache.N_K is None")
+    desc = cache.desc()
+    B, max_pages = page_table.shape
+    code = _abi.lib().lrkv_key_norms(_ptr(positions), _ptr(seq_ids), positions.shape[0], _ptr(B_K),
+                                     ctypes.byref(desc), _ptr(page_table), B, max_pages,
+                                     _ptr(status), _stream(stream))
+    _abi.check("lrkv_key_norms", code)

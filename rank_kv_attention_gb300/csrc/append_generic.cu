@@ -417,4 +417,82 @@ cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos
                       start_pos, B, n, max_len, pos, sid, vlen, req_row, status);
 }
 
+// ---------------------------------------------------------------------------
+// Joint key norms (reading note, section 8): for each appended row and head,
+// 1 / sqrt(mean_d (s + z B_K[h]^T)_d^2 + eps) of the key the cache holds.
+// One warp per (row, head): the private coordinates go to shared memory, lane
+// d expands channels d, d + 32, ... against row d of B_K[h].
+// ---------------------------------------------------------------------------
+template <typename T, typename TC>
+__global__ void __launch_bounds__(256) key_norms_kernel(
+    const int32_t *__restrict__ positions, const int32_t *__restrict__ seq_ids, int n,
+    const T *__restrict__ B_K, const TC *__restrict__ S_K, const TC *__restrict__ R_K,
+    T *__restrict__ N_K, const int32_t *__restrict__ page_table, int B, int max_pages, int num_pages,
+    int page_size, int H, int d_h, int r, float sk_scale, float rk_scale, float eps, int32_t *status) {
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ float zs[8][256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + warp;  // (row, head) pair; warp-uniform
+    if (gw >= (int64_t)n * H) return;
+    const int i = (int)(gw / H), h = (int)(gw % H);
+    const int32_t b = seq_ids[i], pos = positions[i];
+    if (b < 0 || b >= B || pos < 0 || (int64_t)pos >= (int64_t)max_pages * page_size) {
+        if (lane == 0 && h == 0) status_or(status, LRKV_STATUS_BAD_ROW);
+        return;
+    }
+    const int32_t page = page_table[(size_t)b * max_pages + pos / page_size];
+    if (page < 0 || page >= num_pages) {
+        if (lane == 0 && h == 0) status_or(status, LRKV_STATUS_BAD_PAGE);
+        return;
+    }
+    const size_t prow = (size_t)page * page_size + pos % page_size;
+    for (int k = lane; k < r; k += 32) zs[warp][k] = CacheLoad<TC>::load(R_K + (prow * H + h) * r + k) * rk_scale;
+    __syncwarp();
+    const T *bk = B_K + (size_t)h * d_h * r;
+    float ss = 0.f;
+    // rows of B_K[h] as 16-byte vectors (r is a multiple of the vector width
+    // for every supported dtype and B_K is 16-byte aligned), all in flight
+    constexpr int V = Vec16<T>::N;
+    for (int d = lane; d < d_h; d += 32) {
+        float kd = CacheLoad<TC>::load(S_K + prow * d_h + d) * sk_scale;
+        const T *row = bk + (size_t)d * r;
+        for (int k = 0; k < r; k += V) {
+            float bv[V];
+            Vec16<T>::load(row + k, bv);
+#pragma unroll
+            for (int e = 0; e < V; ++e) kd = fmaf(bv[e], zs[warp][k + e], kd);
+        }
+        ss = fmaf(kd, kd, ss);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) Elem<T>::store(N_K + prow * H + h, 1.f / sqrtf(ss / (float)d_h + eps));
+}
+
+cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, int n, const void *B_K,
+                             const lrkv_cache_t &c, const int32_t *page_table, int B, int max_pages,
+                             int32_t *status, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t warps = (int64_t)n * c.H;
+    const unsigned blocks = (unsigned)((warps + 7) / 8);
+    if (c.dtype == LRKV_F32)
+        return launch_pdl(key_norms_kernel<float, float>, dim3(blocks), dim3(256), 0, s, positions,
+                          seq_ids, n, static_cast<const float *>(B_K), static_cast<const float *>(c.S_K),
+                          static_cast<const float *>(c.R_K), static_cast<float *>(c.N_K), page_table, B,
+                          max_pages, c.num_pages, c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps,
+                          status);
+    if (c.dtype == LRKV_FP8_E4M3)
+        return launch_pdl(key_norms_kernel<__nv_bfloat16, uint8_t>, dim3(blocks), dim3(256), 0, s,
+                          positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
+                          static_cast<const uint8_t *>(c.S_K), static_cast<const uint8_t *>(c.R_K),
+                          static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
+                          c.page_size, c.H, c.d_h, c.r, c.scale[0], c.scale[2], c.norm_eps, status);
+    return launch_pdl(key_norms_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
+                      positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
+                      static_cast<const __nv_bfloat16 *>(c.S_K), static_cast<const __nv_bfloat16 *>(c.R_K),
+                      static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
+                      c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps, status);
+}
+
 }  // namespace lrkv

@@ -45,6 +45,11 @@ __device__ __forceinline__ void store_projected(const AppendArgsT<T> &a, size_t 
 template <typename T>
 cudaError_t launch_append_generic(const AppendArgsT<T> &a);
 
+// Reciprocal joint key norms of n cached rows into c.N_K (see lrkv_key_norms).
+cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, int n, const void *B_K,
+                             const lrkv_cache_t &c, const int32_t *page_table, int B, int max_pages,
+                             int32_t *status, cudaStream_t s);
+
 // Few-row append (decode step): whether the shape fits, and the launcher.
 template <typename T>
 bool rows_append_fits(const AppendArgsT<T> &a);

@@ -54,7 +54,11 @@ struct FastCfg {
     static constexpr int S_BYTES = NBOX_S * BOX, R_BYTES = NBOX_R * BOX;
     static constexpr int OFF_SK = 0, OFF_SV = S_BYTES, OFF_RK = 2 * S_BYTES;
     static constexpr int OFF_RV = 2 * S_BYTES + R_BYTES;
-    static constexpr int STAGE = 2 * S_BYTES + 2 * R_BYTES;
+    // joint key norms (optional): the tile's 16 x H bf16 reciprocals
+    static constexpr int OFF_NK = 2 * S_BYTES + 2 * R_BYTES;
+    static constexpr int NK_TX = TS * H * 2;   // bytes one copy lands
+    static constexpr int STAGE_TX = 2 * S_BYTES + 2 * R_BYTES;
+    static constexpr int STAGE = STAGE_TX + 1024;
     static constexpr int KSP = HPW * R / 16;  // k-steps (and m-tiles) of a warp's private columns
     static constexpr int OFF_BAR = STAGES * STAGE;   // full[STAGES]
     static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
@@ -69,6 +73,7 @@ struct FastCfg {
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
     static_assert(STAGES <= 8, "barrier, counter and flag arrays hold 8 stages");
+    static_assert(NK_TX <= 1024 && (H * 2) % 16 == 0, "norm rows fit their slot; 16-byte TMA rows");
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -90,10 +95,11 @@ struct FastParams {
     __nv_bfloat16 *pool[4];
     int d, len_shift;
     float4 sc;  // 8-bit cache: pool scales of S_K, S_V, R_K, R_V
+    int norm;   // the cache holds joint key norms (a fifth copy per tile)
 };
 
 struct FastMaps {
-    CUtensorMap sk, sv, rk, rv;
+    CUtensorMap sk, sv, rk, rv, nk;
 };
 
 // Copy-issue cursor over the CTA's tile sequence (segments in order, 16-row
@@ -153,7 +159,7 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
     const int row = page * P.page_size + cur->t % P.page_size;
     uint8_t *st = smem + s * C::STAGE;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&full[s], C::STAGE);
+    mbar_arrive_expect_tx(&full[s], C::STAGE_TX + (P.norm ? C::NK_TX : 0));
     // each map is 3-D (64 columns, rows, 64-column block) with a box of
     // 64 x 16 x all blocks, so one copy lands the whole 16-row tile as
     // consecutive 16-row x 128-byte swizzled boxes
@@ -163,6 +169,7 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
     tma_load_3d_hint(st + C::OFF_SV, &M.sv, 0, row, 0, &full[s], pol);
     tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, 0, &full[s], pol);
     tma_load_3d_hint(st + C::OFF_RV, &M.rv, 0, row, 0, &full[s], pol);
+    if (P.norm) tma_load_3d_hint(st + C::OFF_NK, &M.nk, 0, row, 0, &full[s], pol);
     cur->issued = it + 1;
     cur->t += C::TS;
     if (cur->t >= cur->t_b) {
@@ -664,6 +671,7 @@ __global__ void __launch_bounds__(C::NT, 1)
         prefetch_tensormap(&M.sv);
         prefetch_tensormap(&M.rk);
         prefetch_tensormap(&M.rv);
+        if (P.norm) prefetch_tensormap(&M.nk);
         cur->b = b0;
         cur->start = start0;
         cur->done = 0;
@@ -807,7 +815,10 @@ __global__ void __launch_bounds__(C::NT, 1)
                 const float v2 = __shfl_sync(0xffffffffu, c[2], src);
                 const float v3 = __shfl_sync(0xffffffffu, c[3], src);
                 const float lo = hl ? v1 : v0, hi = hl ? v3 : v2;
-                const float sc = valid ? ((j < 8) ? lo : hi) * P.scale_log2 : -INFINITY;
+                float sc = valid ? ((j < 8) ? lo : hi) * P.scale_log2 : -INFINITY;
+                if (P.norm && valid)  // joint key norm of (row j, head hd[i])
+                    sc *= __bfloat162float(
+                        reinterpret_cast<const __nv_bfloat16 *>(st + C::OFF_NK)[j * C::H + hd[i]]);
                 float mx = sc;
 #pragma unroll
                 for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -1009,6 +1020,20 @@ static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over the joint key norms [rows, H] bf16 as (H, rows, 1): a box of
+// H x 16 x 1 lands a tile's 16 rows of reciprocals, unswizzled.
+static bool make_norm_map(CUtensorMap *map, const void *nk, int64_t rows, int H) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)H * 2 * rows};
+    cuuint32_t box[3] = {(cuuint32_t)H, 16, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(nk), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int H, int R, bool Q8 = false>
 struct Pick {
     static constexpr int stage = FastCfg<H, R, 1, Q8>::STAGE;
@@ -1032,6 +1057,7 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) || !make_map(&maps.sv, c.S_V, rows, 128, C::EB) ||
         !make_map(&maps.rk, c.R_K, rows, H * R, C::EB) || !make_map(&maps.rv, c.R_V, rows, H * R, C::EB))
         return cudaErrorInvalidValue;
+    if (c.N_K && !make_norm_map(&maps.nk, c.N_K, rows, H)) return cudaErrorInvalidValue;
     auto kern = decode_split_fast_kernel<C>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -1061,6 +1087,7 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     P.len_shift = a.X ? 1 : 0;
     P.sc = Q8 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
               : make_float4(1.f, 1.f, 1.f, 1.f);
+    P.norm = c.N_K != nullptr;
     return launch_pdl(kern, dim3(G), dim3(C::NT), C::SMEM, a.stream, maps, P);
 }
 

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
     const T *__restrict__ q, const TC *__restrict__ S_K, const TC *__restrict__ S_V,
     const TC *__restrict__ R_K, const TC *__restrict__ R_V, const int32_t *__restrict__ page_table,
     const int32_t *__restrict__ req_row, int max_pages, int num_pages, int page_size, int B, int H, int d_h, int r,
-    float scale_log2, float4 sc, DecodeWs ws, int32_t *status, const T *__restrict__ B_K, RopeArgs rope) {
+    float scale_log2, float4 sc, DecodeWs ws, int32_t *status, const T *__restrict__ B_K, RopeArgs rope,
+    const T *__restrict__ N_K) {
     extern __shared__ float sm[];
     float *qs = sm;                 // d_h
     float *ps = qs + d_h;           // r (plain) or A, Bq [d_h / 2][RP] each (rotary)
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                         for (int k = 0; k < RP; ++k)
                             if (k < r) acc = fmaf(pk[k], CacheLoad<TC>::load(rk + k), acc);
                     }
+                    if (N_K) acc *= Elem<T>::load(N_K + (size_t)prow * H + h);  // joint key norm
                     s = acc * scale_log2;
                 }
             }
@@ -572,7 +574,8 @@ static cudaError_t launch_split_generic_t(const DecodeArgs &a, const DecodeWs &w
                       static_cast<const TC *>(c.S_K), static_cast<const TC *>(c.S_V),
                       static_cast<const TC *>(c.R_K), static_cast<const TC *>(c.R_V), a.page_table,
                       a.req_row, a.max_pages, c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r,
-                      scale_log2, sc, ws, a.status, static_cast<const T *>(a.B_K), rope);
+                      scale_log2, sc, ws, a.status, static_cast<const T *>(a.B_K), rope,
+                      static_cast<const T *>(c.N_K));
 }
 
 template <typename T, typename TC>

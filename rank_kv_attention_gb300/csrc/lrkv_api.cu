@@ -78,6 +78,8 @@ static int check_cache(const lrkv_cache_t *c) {
     if (c->num_pages < 1 || c->page_size < 16 || c->page_size > 1024 || c->page_size % 16)
         return LRKV_E_SHAPE;
     if ((int64_t)c->num_pages * c->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (c->N_K && (!aligned16(c->N_K) || !(c->norm_eps >= 0.f) || !std::isfinite(c->norm_eps)))
+        return LRKV_E_INVALID_ARG;
     if (c->dtype == LRKV_FP8_E4M3)
         for (int k = 0; k < 4; ++k)
             if (!(c->scale[k] > 0.f) || !std::isfinite(c->scale[k]) || !std::isfinite(1.f / c->scale[k]))
@@ -449,7 +451,7 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     a.out = out;
     a.status = dev_status;
     a.stream = s;
-    const bool fused = cache->dtype == LRKV_BF16 && d % 128 == 0 && B <= kFusedStepMaxRows &&
+    const bool fused = cache->dtype == LRKV_BF16 && !cache->N_K && d % 128 == 0 && B <= kFusedStepMaxRows &&
                        fast_decode_supported(cache->H, cache->d_h, cache->r, cache->page_size,
                                              cache->dtype) &&
                        fast_decode_step_fits(cache->H, cache->r, d);
@@ -469,6 +471,10 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     st = run_append(X, pos, sid, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
                     dev_status, s);
     if (st) return st;
+    if (cache->N_K) {
+        e = launch_key_norms(pos, sid, B, B_K, *cache, page_table, B, max_pages, dev_status, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     return run_decode(a, workspace, dec_bytes);
 }
 
@@ -505,7 +511,11 @@ static int prefill_impl(const void *X, const void *Q, const int32_t *cu_rows,
     st = run_append(X, w.pos, w.sid, n, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
                     dev_status, s);
     if (st) return st;
-    if (!rope) {
+    if (cache->N_K) {
+        e = launch_key_norms(w.pos, w.sid, n, B_K, *cache, page_table, B, max_pages, dev_status, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (!rope && !cache->N_K) {
         // Causal attention on tensor cores (query tiles of 128 rows per head).
         PrefillTcArgs p;
         p.Q = Q;
@@ -570,6 +580,21 @@ static int check_rope(const lrkv_cache_t *cache, const float *table, int32_t max
     if (!table || !aligned8(table)) return LRKV_E_INVALID_ARG;
     if (max_pos < need) return LRKV_E_BOUNDS;
     return LRKV_OK;
+}
+
+int lrkv_key_norms(const int32_t *positions, const int32_t *seq_ids, int32_t n, const void *B_K,
+                   const lrkv_cache_t *cache, const int32_t *page_table, int32_t B,
+                   int32_t max_pages, int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if (!cache->N_K) return LRKV_E_INVALID_ARG;
+    if (n < 0 || B < 1 || max_pages < 1) return LRKV_E_SHAPE;
+    if ((int64_t)max_pages * cache->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (n == 0) return LRKV_OK;
+    if (!positions || !seq_ids || !B_K || !page_table || !aligned16(B_K)) return LRKV_E_INVALID_ARG;
+    cudaError_t e = launch_key_norms(positions, seq_ids, n, B_K, *cache, page_table, B, max_pages,
+                                     dev_status, (cudaStream_t)stream);
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }
 
 int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, float *table, lrkv_stream_t stream) {

@@ -194,3 +194,25 @@ def test_rope_host_checks(lib):
     assert lib.lrkv_prefill_rope(16, 16, 16, 16, 2, 10, 100, 256, 16, 16, 16, 16, 16, 16,
                                  ctypes.byref(_cache()), 16, 4, 16, 99, 16, ws, 1 << 30, None,
                                  None) == E.LRKV_E_BOUNDS
+
+
+def test_key_norm_host_checks(lib):
+    """The joint key norm pool and eps are validated with the cache."""
+    E = _abi
+    ws = ctypes.c_void_p(256)
+
+    def dec(cache):
+        return lib.lrkv_decode(16, ctypes.byref(cache), 16, 16, 16, 16, 2, 4, 100, 16, ws, 1 << 30,
+                               None, None)
+    assert dec(_cache(N_K=8)) == E.LRKV_E_INVALID_ARG                     # misaligned
+    assert dec(_cache(N_K=16, norm_eps=-1.0)) == E.LRKV_E_INVALID_ARG
+    assert dec(_cache(N_K=16, norm_eps=float("nan"))) == E.LRKV_E_INVALID_ARG
+    # lrkv_key_norms needs the pool
+    assert lib.lrkv_key_norms(16, 16, 4, 16, ctypes.byref(_cache()), 16, 2, 4, None, None) \
+        == E.LRKV_E_INVALID_ARG
+    assert lib.lrkv_key_norms(16, 16, -1, 16, ctypes.byref(_cache(N_K=16)), 16, 2, 4, None, None) \
+        == E.LRKV_E_SHAPE
+    assert lib.lrkv_key_norms(16, 16, 0, 16, ctypes.byref(_cache(N_K=16)), 16, 2, 4, None, None) \
+        == E.LRKV_OK
+    assert lib.lrkv_key_norms(16, 16, 4, 8, ctypes.byref(_cache(N_K=16)), 16, 2, 4, None, None) \
+        == E.LRKV_E_INVALID_ARG                                             # B_K misaligned
