@@ -569,6 +569,15 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int g = blockIdx.x;
     const DecodeWs &ws = P.ws;
 
+    // fetch the tensor-map descriptors now: the first copies use them right
+    // after the plan below
+    if (tid == 32) {
+        prefetch_tensormap(&M.sk);
+        prefetch_tensormap(&M.sv);
+        prefetch_tensormap(&M.rk);
+        prefetch_tensormap(&M.rv);
+        if (P.norm) prefetch_tensormap(&M.nk);
+    }
     // warm L2 with the page-table rows: the copy issuer reads them right
     // after the plan below (caller inputs, complete before this grid launched)
     if (!P.req_row) {
@@ -599,8 +608,12 @@ __global__ void __launch_bounds__(C::NT, 1)
     const int per = (Bn + C::NT - 1) / C::NT;
     const int lo = min(Bn, tid * per), hi = min(Bn, lo + per);
     auto len_of = [&](int bb) { return streamed_len(P.seq_lens[bb], max_len, P.len_shift); };
+    // with at most one request per thread (B <= 256) its length stays in a
+    // register for the later passes
+    const int32_t my_len = lo < hi ? len_of(lo) : 0;
+    auto len_at = [&](int bb) { return (per == 1) ? my_len : len_of(bb); };
     int32_t mysum = 0;
-    for (int bb = lo; bb < hi; ++bb) mysum += len_of(bb);
+    for (int bb = lo; bb < hi; ++bb) mysum += len_at(bb);
     int32_t incl = mysum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -634,8 +647,15 @@ __global__ void __launch_bounds__(C::NT, 1)
     {
         int32_t o = base_t;
         for (int bb = lo; bb < hi; ++bb) {
-            const int32_t L = len_of(bb);
-            if (L > 0 && o <= start0 && start0 < o + L) pl[0] = bb;
+            const int32_t L = len_at(bb);
+            if (L > 0 && o <= start0 && start0 < o + L) {
+                pl[0] = bb;
+                // the page of the CTA's first tile, so the copy issuer need
+                // not read it after this barrier
+                const int pidx = (start0 - o) / P.page_size;
+                pl[10] = bb * P.max_pages + pidx;
+                pl[11] = page_row(P, bb)[pidx];
+            }
             if (L > 0 && o < end && end <= o + L) pl[1] = bb;
             o += L;
         }
@@ -647,7 +667,7 @@ __global__ void __launch_bounds__(C::NT, 1)
         int32_t o = base_t;
         for (int bb = lo; bb < hi; ++bb) {
             if (bb >= b0 && bb - b0 <= kLocalReq) pl[16 + bb - b0] = o;
-            o += len_of(bb);
+            o += len_at(bb);
         }
         if (hi == Bn && Bn - b0 <= kLocalReq) pl[16 + Bn - b0] = o;  // off[B] = total
     }
@@ -667,17 +687,12 @@ __global__ void __launch_bounds__(C::NT, 1)
             cnt[s] = 0;
         }
         fence_barrier_init();
-        prefetch_tensormap(&M.sk);
-        prefetch_tensormap(&M.sv);
-        prefetch_tensormap(&M.rk);
-        prefetch_tensormap(&M.rv);
-        if (P.norm) prefetch_tensormap(&M.nk);
         cur->b = b0;
         cur->start = start0;
         cur->done = 0;
         cur->issued = 0;
-        cur->page_key = -1;
-        cur->page_id = 0;
+        cur->page_key = pl[10];
+        cur->page_id = pl[11];
         cursor_begin_segment<C>(cur, off, end);
         for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, off, smem, full, okf, end);
     }

@@ -29,6 +29,21 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
     int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, int len_shift,
     DecodeWs ws, int32_t *status) {
     const int tid = threadIdx.x;
+    if (blockIdx.x < (unsigned)H) {
+        // warm L2 with this block's B_K[h] and query rows while the
+        // predecessor finishes: a prefetch reads nothing into the block, and
+        // the loads below, after the wait, see every earlier write
+        const char *bk = reinterpret_cast<const char *>(B_K + (size_t)blockIdx.x * d_h * r);
+        const size_t bk_bytes = (size_t)d_h * r * sizeof(T);
+        for (size_t o = (size_t)tid * 128; o < bk_bytes; o += (size_t)blockDim.x * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(bk + o));
+        const int b_first = blockIdx.y * kProRows;
+        if (tid < kProRows && b_first + tid < B) {
+            const char *qr = reinterpret_cast<const char *>(q + ((size_t)(b_first + tid) * H + blockIdx.x) * d_h);
+            for (size_t o = 0; o < (size_t)d_h * sizeof(T); o += 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + o));
+        }
+    }
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == (unsigned)H) {
@@ -121,21 +136,42 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
         for (int e = 0; e < V; ++e) qs[i * V + e] = v[e];
     }
     __syncthreads();
-    for (int o = tid; o < nb * r; o += blockDim.x) {
-        const int bb = o / r, k = o % r;
-        const float *qq = qs + bb * d_h;
-        float a0 = 0.f, a1 = 0.f;
-        if (staged) {
+    if (staged) {
+        // four consecutive private columns per thread: per d one broadcast
+        // query value, one 16-byte row slice of B_K[h] and four FMAs
+        // (r % 4 == 0 for every supported dtype)
+        const int r4 = r / 4;
+        for (int o = tid; o < nb * r4; o += blockDim.x) {
+            const int bb = o / r4, k = 4 * (o % r4);
+            const float *qq = qs + bb * d_h;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), c = a;
             int d = 0;
             for (; d + 1 < d_h; d += 2) {
-                a0 = fmaf(qq[d], bk[d * r + k], a0);
-                a1 = fmaf(qq[d + 1], bk[(d + 1) * r + k], a1);
+                const float q0 = qq[d], q1 = qq[d + 1];
+                const float4 b0 = *reinterpret_cast<const float4 *>(bk + d * r + k);
+                const float4 b1 = *reinterpret_cast<const float4 *>(bk + (d + 1) * r + k);
+                a.x = fmaf(q0, b0.x, a.x); a.y = fmaf(q0, b0.y, a.y);
+                a.z = fmaf(q0, b0.z, a.z); a.w = fmaf(q0, b0.w, a.w);
+                c.x = fmaf(q1, b1.x, c.x); c.y = fmaf(q1, b1.y, c.y);
+                c.z = fmaf(q1, b1.z, c.z); c.w = fmaf(q1, b1.w, c.w);
             }
-            if (d < d_h) a0 = fmaf(qq[d], bk[d * r + k], a0);
-        } else {
-            for (int d = 0; d < d_h; ++d) a0 = fmaf(qq[d], Elem<T>::load(src + (size_t)d * r + k), a0);
+            if (d < d_h) {
+                const float q0 = qq[d];
+                const float4 b0 = *reinterpret_cast<const float4 *>(bk + d * r + k);
+                a.x = fmaf(q0, b0.x, a.x); a.y = fmaf(q0, b0.y, a.y);
+                a.z = fmaf(q0, b0.z, a.z); a.w = fmaf(q0, b0.w, a.w);
+            }
+            *reinterpret_cast<float4 *>(ws.p + ((size_t)(b0 + bb) * H + h) * r + k) =
+                make_float4(a.x + c.x, a.y + c.y, a.z + c.z, a.w + c.w);
         }
-        ws.p[((size_t)(b0 + bb) * H + h) * r + k] = a0 + a1;
+    } else {
+        for (int o = tid; o < nb * r; o += blockDim.x) {
+            const int bb = o / r, k = o % r;
+            const float *qq = qs + bb * d_h;
+            float a0 = 0.f;
+            for (int d = 0; d < d_h; ++d) a0 = fmaf(qq[d], Elem<T>::load(src + (size_t)d * r + k), a0);
+            ws.p[((size_t)(b0 + bb) * H + h) * r + k] = a0;
+        }
     }
 }
 
