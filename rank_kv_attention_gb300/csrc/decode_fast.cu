@@ -367,13 +367,6 @@ __device__ __forceinline__ uint32_t box_chunk(int j, int cc) {
 //     (at most 2^8 under the lazy maximum) enter as f16 directly.
 // ---------------------------------------------------------------------------
 
-// Shift e with 2^e * m in [2^14, 2^15) (0 for m = 0 or non-finite m).
-__device__ __forceinline__ int f16_range_shift(float m) {
-    if (!(m > 0.f) || !isfinite(m)) return 0;
-    const int ex = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
-    return max(-125, min(125, 14 - ex));
-}
-
 template <class C>
 __device__ __forceinline__ void q8_segment_setup(const FastParams &P, int b, int warp, int gq,
                                                  int tq, uint32_t (&qb)[8][2],

@@ -8,6 +8,7 @@
 // together when the max moves) reduces S_V and R_V[h] with the same weights;
 // the private reduction is expanded once by B_V[h]^T at the end.
 #include <algorithm>
+#include <type_traits>
 
 #include "decode_kernels.cuh"
 
@@ -209,6 +210,81 @@ struct RopeArgs {
     int max_pos;
 };
 
+// Private rotary scores of one 128-key tile on the tensor cores.  Warp w takes
+// keys 32w .. 32w+31 of the tile as two 16-row m-tiles of
+//     P[key][k] = sum over the interleaved (cos, sin) channels of the key's
+//                 distance row times W[channel][k]   (f16 mma.sync, fp32 sum)
+// then dots each row of P with that key's private coordinates and adds the
+// result (scaled back by winv) to sh[key].  Keys whose row[] is -1 are not
+// read (their MMA rows use distance 0 and are discarded).
+template <typename TC, int RP>
+__device__ __forceinline__ void rope_private_scores(const RopeArgs &rope, const __half *wt, int wstride,
+                                                    const int32_t *row, float *sh, const TC *R_K, int H,
+                                                    int h, int r, int d_h, int32_t q_pos, int t0,
+                                                    float winv, int warp, int lane) {
+    constexpr int NT = RP / 8;
+    const int gq = lane >> 2, tq = lane & 3, hc = d_h / 2;
+    float pacc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pacc[mt][nt][e] = 0.f;
+    const int mtx = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = 32 * warp + 16 * mt + gq, r1 = r0 + 8;
+        const float2 *cs0 = rope.table + (size_t)(row[r0] >= 0 ? q_pos - (t0 + r0) : 0) * hc;
+        const float2 *cs1 = rope.table + (size_t)(row[r1] >= 0 ? q_pos - (t0 + r1) : 0) * hc;
+        for (int ks = 0; ks < d_h / 16; ++ks) {
+            const int c0 = 8 * ks + tq, c1 = c0 + 4;
+            const float2 e00 = cs0[c0], e10 = cs1[c0], e01 = cs0[c1], e11 = cs1[c1];
+            const uint32_t a[4] = {pack_f16(e00.x, e00.y), pack_f16(e10.x, e10.y),
+                                   pack_f16(e01.x, e01.y), pack_f16(e11.x, e11.y)};
+#pragma unroll
+            for (int nt = 0; nt < NT; nt += 2) {
+                uint32_t b0, b1, b2, b3;
+                const __half *src = wt + (8 * (nt + (mtx >> 1)) + rr) * wstride + 16 * ks + 8 * (mtx & 1);
+                ldmatrix_x4(smem_u32(src), b0, b1, b2, b3);
+                mma_f16_16816(pacc[mt][nt], a, b0, b1);
+                mma_f16_16816(pacc[mt][nt + 1], a, b2, b3);
+            }
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const int r0 = 32 * warp + 16 * mt + gq, r1 = r0 + 8;
+        const int32_t p0 = row[r0], p1 = row[r1];
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int col = 8 * nt + 2 * tq;  // r is even: col < r implies col + 1 < r
+            if (col < r) {
+                if (p0 >= 0) {
+                    const TC *z = R_K + ((size_t)p0 * H + h) * r + col;
+                    s0 = fmaf(pacc[mt][nt][0], CacheLoad<TC>::load(z), s0);
+                    s0 = fmaf(pacc[mt][nt][1], CacheLoad<TC>::load(z + 1), s0);
+                }
+                if (p1 >= 0) {
+                    const TC *z = R_K + ((size_t)p1 * H + h) * r + col;
+                    s1 = fmaf(pacc[mt][nt][2], CacheLoad<TC>::load(z), s1);
+                    s1 = fmaf(pacc[mt][nt][3], CacheLoad<TC>::load(z + 1), s1);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+            s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        }
+        if (tq == 0) {
+            if (p0 >= 0) sh[r0] += s0 * winv;
+            if (p1 >= 0) sh[r1] += s1 * winv;
+        }
+    }
+}
+
 // T: query element type; TC: cache element type (T, or 8-bit codes whose pool
 // scales sc = (S_K, S_V, R_K, R_V) fold into the queries and accumulators).
 // RP > 0: scores with the exact rotary embedding, private width padded to RP.
@@ -224,6 +300,15 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
     float *ps = qs + d_h;           // r (plain) or A, Bq [d_h / 2][RP] each (rotary)
     float *w = ps + (RP ? d_h * RP : r);  // kGenTile weights
     int32_t *row = reinterpret_cast<int32_t *>(w + kGenTile);  // kGenTile pool rows
+    // rotary on tensor cores (d_h % 16 == 0): per-key scores and the f16
+    // coefficient matrix W^T [RP][d_h + 8] (rows padded for ldmatrix)
+    float *sh = reinterpret_cast<float *>(row + kGenTile);
+    __half *wt = reinterpret_cast<__half *>(sh + kGenTile);
+    const int wstride = d_h + 8;
+    // (bf16 activations only: f16 operands carry ~11 bits, the precision of
+    // a bf16 result but not of the fp32 path)
+    const bool use_mma = RP > 0 && d_h % 16 == 0 && !std::is_same<T, float>::value;
+    float winv = 1.f;               // 2^-e of W's f16 scaling
     __shared__ float red[kGenTile / 32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -270,6 +355,26 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                 ps[c * RP + k] = a;
                 ps[hc * RP + c * RP + k] = bq;
             }
+            if (use_mma) {
+                // W[2c][k] = A[c][k], W[2c+1][k] = Bq[c][k], scaled by a power
+                // of two into f16 range and stored transposed
+                __syncthreads();
+                float mx = 0.f;
+                for (int i = tid; i < d_h * RP; i += kGenTile) mx = fmaxf(mx, fabsf(ps[i]));
+#pragma unroll
+                for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) red[warp] = mx;
+                __syncthreads();
+                mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+                const int e = f16_range_shift(mx);
+                const float up = exp2i(e);
+                winv = exp2i(-e);
+                for (int i = tid; i < RP * d_h; i += kGenTile) {
+                    const int k = i / d_h, dd = i % d_h, c = dd >> 1;
+                    const float v = (dd & 1) ? ps[hc * RP + c * RP + k] : ps[c * RP + k];
+                    wt[k * wstride + dd] = __float2half_rn(v * up);
+                }
+            }
         }
         __syncthreads();
 
@@ -293,6 +398,18 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     if constexpr (RP == 0) {
                         for (int d = 0; d < d_h; ++d) acc = fmaf(qs[d], CacheLoad<TC>::load(sk + d), acc);
                         for (int k = 0; k < r; ++k) acc = fmaf(ps[k], CacheLoad<TC>::load(rk + k), acc);
+                    } else if (use_mma) {
+                        // the rotated shared term here; the private term on
+                        // the tensor cores below
+                        const float2 *cs = rope.table + (size_t)(q_pos - j) * (d_h / 2);
+                        for (int c = 0; c < d_h / 2; ++c) {
+                            const float2 e = cs[c];
+                            const float s0 = CacheLoad<TC>::load(sk + 2 * c);
+                            const float s1 = CacheLoad<TC>::load(sk + 2 * c + 1);
+                            const float q0 = qs[2 * c], q1 = qs[2 * c + 1];
+                            acc = fmaf(e.x, fmaf(q0, s0, q1 * s1), acc);
+                            acc = fmaf(e.y, fmaf(q0, s1, -q1 * s0), acc);
+                        }
                     } else {
                         // distance from the query (the request's last row,
                         // which may lie beyond this segment) to key j
@@ -316,8 +433,26 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                         for (int k = 0; k < RP; ++k)
                             if (k < r) acc = fmaf(pk[k], CacheLoad<TC>::load(rk + k), acc);
                     }
-                    if (N_K) acc *= Elem<T>::load(N_K + (size_t)prow * H + h);  // joint key norm
-                    s = acc * scale_log2;
+                    if (use_mma) {
+                        sh[tid] = acc;
+                    } else {
+                        if (N_K) acc *= Elem<T>::load(N_K + (size_t)prow * H + h);  // joint key norm
+                        s = acc * scale_log2;
+                    }
+                }
+            }
+            if constexpr (RP > 0) {
+                if (use_mma) {
+                    row[tid] = valid ? prow : -1;
+                    __syncthreads();
+                    rope_private_scores<TC, RP>(rope, wt, wstride, row, sh, R_K, H, h, r, d_h, q_pos,
+                                                t0, winv, warp, lane);
+                    __syncthreads();
+                    if (valid) {
+                        float acc = sh[tid];
+                        if (N_K) acc *= Elem<T>::load(N_K + (size_t)prow * H + h);  // joint key norm
+                        s = acc * scale_log2;
+                    }
                 }
             }
             // tile max
@@ -595,7 +730,8 @@ template <typename T, typename TC, int RP>
 static cudaError_t launch_split_generic_t(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const auto &c = a.cache;
     const size_t sm = sizeof(float) * (c.d_h + (RP ? (size_t)c.d_h * RP : c.r) + kGenTile) +
-                      sizeof(int32_t) * kGenTile;
+                      sizeof(int32_t) * kGenTile +
+                      (RP ? sizeof(float) * kGenTile + sizeof(__half) * (size_t)RP * (c.d_h + 8) : 0);
     auto kern = decode_split_generic_kernel<T, TC, RP>;
     if (sm > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

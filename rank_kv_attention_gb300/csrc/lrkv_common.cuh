@@ -166,6 +166,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b) {
 }
 // 2^e as a float, for -126 <= e <= 127 (exact).
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+// Shift e with 2^e * m in [2^14, 2^15) (0 for m = 0 or non-finite m): the
+// exact power-of-two scaling that puts values of magnitude <= m in f16 range.
+__device__ __forceinline__ int f16_range_shift(float m) {
+    if (!(m > 0.f) || !isfinite(m)) return 0;
+    const int ex = (int)((__float_as_uint(m) >> 23) & 0xff) - 127;
+    return max(-125, min(125, 14 - ex));
+}
 
 // Value of one stored cache element, before its pool's scale.
 template <typename TC> struct CacheLoad;
