@@ -22,9 +22,10 @@ namespace lrkv {
 // ---------------------------------------------------------------------------
 constexpr int kProRows = 8;  // requests per prologue block
 constexpr size_t kStageFloats = 40 * 1024;  // largest B_K / B_V head staged in shared memory
+constexpr int kProThreads = 256;  // threads of a prologue block
 
 template <typename T>
-__global__ void __launch_bounds__(256) decode_prologue_kernel(
+__global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
     const T *__restrict__ q, const T *__restrict__ B_K, const int32_t *__restrict__ seq_lens,
     T *__restrict__ out,
     int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, int len_shift,
@@ -72,17 +73,18 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
                     Elem<T>::store(out + (size_t)(blockIdx.y * kProRows + bb) * H * d_h + i, 0.f);
         if (blockIdx.y != 0) return;
         // --- plan: exclusive scan of validated lengths ---
-        __shared__ int32_t part[256];
+        __shared__ int32_t part[kProThreads];
         const int per = (B + blockDim.x - 1) / blockDim.x;
         const int lo = tid * per, hi = min(B, lo + per);
         int32_t s = 0;
         for (int b = lo; b < hi; ++b) s += streamed_len(seq_lens[b], max_len, len_shift);
         part[tid] = s;
         __syncthreads();
-        if (tid < 32) {  // warp scan of the 256 partial sums (8 per lane)
-            int32_t v[8], run = 0;
+        constexpr int NPL = kProThreads / 32;  // partial sums per lane
+        if (tid < 32) {  // warp scan of the kProThreads partial sums
+            int32_t v[NPL], run = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { v[i] = part[tid * 8 + i]; run += v[i]; }
+            for (int i = 0; i < NPL; ++i) { v[i] = part[tid * NPL + i]; run += v[i]; }
             int32_t incl = run;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(256) decode_prologue_kernel(
             }
             int32_t ex = incl - run;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { part[tid * 8 + i] = ex; ex += v[i]; }
+            for (int i = 0; i < NPL; ++i) { part[tid * NPL + i] = ex; ex += v[i]; }
             if (tid == 31) {
                 ws.plan->total = incl;
                 int32_t chunk = (incl + G - 1) / G;
@@ -719,7 +721,7 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(decode_prologue_kernel<T>, grid, dim3(256), sm, a.stream,
+    return launch_pdl(decode_prologue_kernel<T>, grid, dim3(kProThreads), sm, a.stream,
                       static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
                       static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
                       a.max_pages * a.cache.page_size, G, tile_align, staged, a.X ? 1 : 0, ws,
