@@ -63,6 +63,7 @@ cudaError_t launch_append_rows_mma(const AppendArgsT<__nv_bfloat16> &a);
 // Tensor-core append (bf16): covered shapes and launcher.
 bool tc_append_supported(int n, int d, int d_h, int H, int r);
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);
+int device_sm_count();  // SMs of the current device (lrkv_api.cu)
 
 cudaError_t launch_step_rows(const int32_t *seq_lens, int B, int max_len, int32_t *pos,
                              int32_t *sid, cudaStream_t s);

@@ -4,17 +4,24 @@
 // X are projected through [W_S_K | W_S_V | U_K(all heads) | U_V(all heads)] and
 // each row's four blocks are stored at its token position (page table,
 // same page id in all four pools).  The projection is a dense
-// [n x d] . [d x (2 d_h + 2 H r)] GEMM, run here with tcgen05:
-//   * one CTA per 128-row x 128-column output tile, 4 warps;
-//   * warp 0 (one thread) streams 128 x 64 K-major tiles of X and of the
-//     weight segment by TMA (128-byte swizzle) through a 4-stage ring;
-//   * warp 1 (one thread) issues tcgen05.mma (kind::f16, bf16 in, fp32
-//     accumulate) into a 128 x 128 fp32 accumulator in tensor memory and
-//     releases each stage with tcgen05.commit;
-//   * all 4 warps then read the accumulator back (tcgen05.ld, one row per
-//     thread), round to bf16 and store each row's 128 columns straight into
-//     its page slot.
+// [n x d] . [d x (2 d_h + 2 H r)] GEMM, run here with tcgen05 by a persistent
+// grid (one CTA per SM walking the output tiles):
+//   * output tiles are 128 rows x 256 columns: two 128-column blocks of the
+//     concatenated output, each block inside one of the four segments (its
+//     own weight tensor map and column offset);
+//   * warp 0 (one thread) streams 128 x 64 K-major tiles of X and the two
+//     128 x 64 weight boxes by TMA (128-byte swizzle) through a 4-stage ring
+//     that runs on across tiles;
+//   * warp 1 (one thread) issues tcgen05.mma (kind::f16, M = 128, N = 256,
+//     bf16 in, fp32 accumulate) into one of two 256-column accumulators in
+//     tensor memory, so a tile's epilogue overlaps the next tile's products;
+//   * warps 2-5 read an accumulator back (tcgen05.ld, one row per thread),
+//     round to bf16 (or 8-bit codes) and store each row's columns straight
+//     into its page slot; the destination rows of a tile are looked up while
+//     its products run.
 // Weights are stored output-major ([columns][d]), so both operands are K-major.
+#include <algorithm>
+
 #include "append_kernels.cuh"
 #include "tc_common.cuh"
 
@@ -22,43 +29,51 @@ namespace lrkv {
 
 constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 4;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
-constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 16 KB
-constexpr int TC_STAGE = TC_A_BYTES + TC_B_BYTES;
-constexpr int TC_OFF_BAR = TC_STAGES * TC_STAGE;          // full[S], empty[S], accum
-constexpr int TC_OFF_TMEM = TC_OFF_BAR + 8 * (2 * TC_STAGES + 1);
-constexpr int TC_OFF_ROWS = TC_OFF_TMEM + 8;               // int64 destination rows [128]
-constexpr int TC_SMEM = TC_OFF_ROWS + 8 * TC_BM + 1024;    // + alignment slack
-constexpr int TC_TMEM_COLS = 128;
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 16 KB per 128-column block
+constexpr int TC_STAGE = TC_A_BYTES + 2 * TC_B_BYTES;
+constexpr int TC_OFF_BAR = TC_STAGES * TC_STAGE;  // full[S], empty[S], acc_full[2], acc_empty[2]
+constexpr int TC_OFF_TMEM = TC_OFF_BAR + 8 * (2 * TC_STAGES + 4);
+constexpr int TC_SMEM = TC_OFF_TMEM + 16 + 1024;  // + alignment slack
+constexpr int TC_TMEM_COLS = 512;                 // two 256-column accumulators
+constexpr int TC_THREADS = 192;                   // producer, MMA, 4 epilogue warps
 
 struct TcMaps {
     CUtensorMap x;     // X [n, d]
     CUtensorMap w[4];  // W_S_K [d_h, d], W_S_V [d_h, d], U_K [H r, d], U_V [H r, d]
 };
 
-struct TcTiles {
-    int first[5];  // first output-column tile of each segment; first[4] = total tiles
-    int width[4];  // columns of each segment
+// The output's 128-column blocks: block k lies in segment seg[k] from its
+// column col[k]; tile j pairs blocks 2j and 2j + 1 (the last may be alone).
+constexpr int TC_MAX_BLOCKS = 32;
+struct TcBlocks {
+    int nblocks, ncoltiles, nrowtiles, ntiles;
+    int seg[TC_MAX_BLOCKS];
+    int col[TC_MAX_BLOCKS];
+    int width[4];
 };
 
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ void tc_tile_of(const TcBlocks &t, int tile, int &m0, int &b0, int &nb) {
+    const int rt = tile / t.ncoltiles, ct = tile % t.ncoltiles;
+    m0 = rt * TC_BM;
+    b0 = 2 * ct;
+    nb = min(2, t.nblocks - b0);
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
     append_tc_kernel(const __grid_constant__ TcMaps maps, const AppendArgsT<__nv_bfloat16> a,
-                     const TcTiles tiles) {
+                     const __grid_constant__ TcBlocks tb) {
     extern __shared__ uint8_t tc_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_OFF_BAR);
     uint64_t *empty = full + TC_STAGES;
-    uint64_t *accum = empty + TC_STAGES;
+    uint64_t *acc_full = empty + TC_STAGES;
+    uint64_t *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TC_OFF_TMEM);
-    int64_t *dst_rows = reinterpret_cast<int64_t *>(smem + TC_OFF_ROWS);
 
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nt = blockIdx.x, m0 = blockIdx.y * TC_BM;
-    int seg = 0;
-    while (seg < 3 && nt >= tiles.first[seg + 1]) ++seg;
-    const int col0 = (nt - tiles.first[seg]) * TC_BN;  // first column inside the segment
     const int nk = a.d / TC_BK;
 
     if (tid == 0) {
@@ -66,129 +81,173 @@ __global__ void __launch_bounds__(128, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(accum, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&acc_full[k], 1);
+            mbar_init(&acc_empty[k], 4);  // one arrival per epilogue warp
+        }
         fence_barrier_init();
         prefetch_tensormap(&maps.x);
-        prefetch_tensormap(&maps.w[seg]);
+        for (int k = 0; k < 4; ++k) prefetch_tensormap(&maps.w[k]);
     }
-    if (warp == 2) tmem_alloc(tmem_slot, TC_TMEM_COLS);
-    {  // destination pool row of every tile row (or -1)
-        const int i = m0 + tid;
-        int64_t dr = -1;
-        if (i < a.n) {
-            const int32_t b = a.seq_ids[i], pos = a.positions[i];
-            if (b < 0 || b >= a.B || pos < 0 || pos >= a.max_pages * a.page_size) {
-                status_or(a.status, LRKV_STATUS_BAD_ROW);
-            } else {
-                const int32_t page = a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
-                if (page < 0 || page >= a.num_pages) status_or(a.status, LRKV_STATUS_BAD_PAGE);
-                else dr = (int64_t)page * a.page_size + pos % a.page_size;
-            }
-        }
-        dst_rows[tid] = dr;
-    }
+    if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
+    int issued = 0;  // producer: k-steps whose copies were requested
 
     if (warp == 0 && lane == 0) {
-        // ---- producer: TMA tiles of X and of the weight segment
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % TC_STAGES;
-            if (kt >= TC_STAGES && !mbar_wait(&empty[s], ((kt / TC_STAGES) - 1) & 1)) {
-                ok = false;
-                break;
+        // ---- producer
+        int it = 0;
+        for (int tile = blockIdx.x; tile < tb.ntiles && ok; tile += gridDim.x) {
+            int m0, b0, nb;
+            tc_tile_of(tb, tile, m0, b0, nb);
+            for (int kt = 0; kt < nk; ++kt, ++it) {
+                const int s = it % TC_STAGES;
+                if (it >= TC_STAGES && !mbar_wait(&empty[s], ((it / TC_STAGES) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * TC_STAGE;
+                mbar_arrive_expect_tx(&full[s], TC_A_BYTES + nb * TC_B_BYTES);
+                tma_load_2d(st, &maps.x, kt * TC_BK, m0, &full[s]);
+                for (int k = 0; k < nb; ++k)
+                    tma_load_2d(st + TC_A_BYTES + k * TC_B_BYTES, &maps.w[tb.seg[b0 + k]], kt * TC_BK,
+                                tb.col[b0 + k], &full[s]);
+                issued = it + 1;
             }
-            uint8_t *st = smem + s * TC_STAGE;
-            mbar_arrive_expect_tx(&full[s], TC_STAGE);
-            tma_load_2d(st, &maps.x, kt * TC_BK, m0, &full[s]);
-            tma_load_2d(st + TC_A_BYTES, &maps.w[seg], kt * TC_BK, col0, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        const uint32_t idesc = tc_idesc_bf16(TC_BM, TC_BN);
-        for (int kt = 0; kt < nk; ++kt) {
-            const int s = kt % TC_STAGES;
-            if (!mbar_wait(&full[s], (kt / TC_STAGES) & 1)) {
+        const uint32_t idesc2 = tc_idesc_bf16(TC_BM, 2 * TC_BN), idesc1 = tc_idesc_bf16(TC_BM, TC_BN);
+        int it = 0, i = 0;
+        for (int tile = blockIdx.x; tile < tb.ntiles && ok; tile += gridDim.x, ++i) {
+            int m0, b0, nb;
+            tc_tile_of(tb, tile, m0, b0, nb);
+            const int acc = i & 1;
+            // the epilogue has drained this accumulator's previous tile
+            if (i >= 2 && !mbar_wait(&acc_empty[acc], ((i >> 1) - 1) & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * TC_STAGE);
-            const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + TC_A_BYTES);
+            const uint32_t d = tmem + acc * 2 * TC_BN;
+            for (int kt = 0; kt < nk; ++kt, ++it) {
+                const int s = it % TC_STAGES;
+                if (!mbar_wait(&full[s], (it / TC_STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + s * TC_STAGE);
+                const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + TC_A_BYTES);
 #pragma unroll
-            for (int kk = 0; kk < TC_BK / 16; ++kk)  // K = 16 per instruction: +32 bytes
-                tc_mma_f16(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc,
-                           (kt | kk) != 0);
-            tc_commit(&empty[s]);  // stage free once these MMAs have read it
+                for (int kk = 0; kk < TC_BK / 16; ++kk)  // K = 16 per instruction: +32 bytes
+                    tc_mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                               nb == 2 ? idesc2 : idesc1, (kt | kk) != 0);
+                tc_commit(&empty[s]);  // stage free once these products have read it
+            }
+            if (!ok) break;
+            tc_commit(&acc_full[acc]);  // accumulator complete
         }
-        tc_commit(accum);  // accumulator complete
+    } else if (warp >= 2) {
+        // ---- epilogue: thread = tile row = tensor-memory lane of its quadrant
+        const int q = warp & 3, row = 32 * q + lane;
+        int i = 0;
+        for (int tile = blockIdx.x; tile < tb.ntiles; tile += gridDim.x, ++i) {
+            int m0, b0, nb;
+            tc_tile_of(tb, tile, m0, b0, nb);
+            // destination pool row while the products run
+            int64_t dr = -1;
+            {
+                const int r = m0 + row;
+                if (r < a.n) {
+                    const int32_t b = a.seq_ids[r], pos = a.positions[r];
+                    if (b < 0 || b >= a.B || pos < 0 || pos >= a.max_pages * a.page_size) {
+                        if (b0 == 0) status_or(a.status, LRKV_STATUS_BAD_ROW);
+                    } else {
+                        const int32_t page = a.page_table[(size_t)b * a.max_pages + pos / a.page_size];
+                        if (page < 0 || page >= a.num_pages) {
+                            if (b0 == 0) status_or(a.status, LRKV_STATUS_BAD_PAGE);
+                        } else {
+                            dr = (int64_t)page * a.page_size + pos % a.page_size;
+                        }
+                    }
+                }
+            }
+            const int acc = i & 1;
+            // tcgen05.ld is warp-collective: take the decision per warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], (i >> 1) & 1))) {
+                if (lane == 0) status_or(a.status, LRKV_STATUS_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            for (int k = 0; k < nb; ++k) {
+                const int seg = tb.seg[b0 + k], col0 = tb.col[b0 + k], width = tb.width[seg];
+                __nv_bfloat16 *base = seg == 0 ? a.S_K : seg == 1 ? a.S_V : seg == 2 ? a.R_K : a.R_V;
+                const size_t rowlen = seg < 2 ? (size_t)a.d_h : (size_t)a.H * a.r;
+#pragma unroll 1
+                for (int c = 0; c < TC_BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + acc * 2 * TC_BN + k * TC_BN + c * 32, v);
+                    const int cc = col0 + c * 32;
+                    if (dr < 0 || cc >= width) continue;
+                    if (a.fp8) {  // 8-bit codes of v / scale
+                        uint8_t *qd = a.q8[seg] + dr * rowlen + cc;
+                        const float is = a.inv_scale[seg];
+                        if (cc + 32 <= width) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                pk[e] = (uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e]) * is,
+                                                                  __uint_as_float(v[4 * e + 1]) * is) |
+                                        ((uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e + 2]) * is,
+                                                                   __uint_as_float(v[4 * e + 3]) * is)
+                                         << 16);
+                            uint4 *q4 = reinterpret_cast<uint4 *>(qd);
+                            q4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            q4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        } else {
+                            for (int e = 0; e < width - cc; ++e)
+                                qd[e] = (uint8_t)(e4m3x2_from_f32(__uint_as_float(v[e]) * is, 0.f) & 0xffu);
+                        }
+                        continue;
+                    }
+                    __nv_bfloat16 *dst = base + dr * rowlen + cc;
+                    if (cc + 32 <= width) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            d4[qq] = make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+                    } else {
+                        for (int e = 0; e < width - cc; ++e)
+                            dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                    }
+                }
+            }
+            // this warp has read its lanes of the accumulator
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
     }
     if (!ok) status_or(a.status, LRKV_STATUS_TIMEOUT);
-
-    // ---- epilogue: thread = tile row = TMEM lane
-    __syncwarp();
-    // tcgen05.ld is warp-collective: take the decision per warp
-    const bool got = __all_sync(0xffffffffu, mbar_wait(accum, 0));
-    tc_fence_after();
-    if (got) {
-        const int64_t dr = dst_rows[tid];
-        const int width = tiles.width[seg];
-        __nv_bfloat16 *base = nullptr;
-        size_t rowlen = 0;
-        if (seg == 0) { base = a.S_K; rowlen = a.d_h; }
-        else if (seg == 1) { base = a.S_V; rowlen = a.d_h; }
-        else if (seg == 2) { base = a.R_K; rowlen = (size_t)a.H * a.r; }
-        else { base = a.R_V; rowlen = (size_t)a.H * a.r; }
-#pragma unroll 1
-        for (int c = 0; c < TC_BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c * 32, v);
-            const int cc = col0 + c * 32;
-            if (dr < 0 || cc >= width) continue;
-            if (a.fp8) {  // 8-bit codes of v / scale
-                uint8_t *q = a.q8[seg] + dr * rowlen + cc;
-                const float is = a.inv_scale[seg];
-                if (cc + 32 <= width) {
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        pk[e] = (uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e]) * is,
-                                                          __uint_as_float(v[4 * e + 1]) * is) |
-                                ((uint32_t)e4m3x2_from_f32(__uint_as_float(v[4 * e + 2]) * is,
-                                                           __uint_as_float(v[4 * e + 3]) * is)
-                                 << 16);
-                    uint4 *q4 = reinterpret_cast<uint4 *>(q);
-                    q4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    q4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                } else {
-                    for (int e = 0; e < width - cc; ++e)
-                        q[e] = (uint8_t)(e4m3x2_from_f32(__uint_as_float(v[e]) * is, 0.f) & 0xffu);
-                }
-                continue;
-            }
-            __nv_bfloat16 *dst = base + dr * rowlen + cc;
-            if (cc + 32 <= width) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            } else {
-                for (int e = 0; e < width - cc; ++e) dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
-            }
-        }
-    } else {
-        status_or(a.status, LRKV_STATUS_TIMEOUT);
-    }
+    // Never leave with copies in flight into this CTA's shared memory (only
+    // possible after a timeout: normally the MMA issuer consumed every stage).
+    if (warp == 0 && lane == 0 && !ok)
+        for (int k = max(0, issued - TC_STAGES); k < issued; ++k)
+            mbar_wait(&full[k % TC_STAGES], (k / TC_STAGES) & 1);
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) tmem_dealloc(tmem, TC_TMEM_COLS);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TC_TMEM_COLS);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -208,9 +267,31 @@ static bool tc_map(CUtensorMap *m, const void *base, int64_t rows, int d) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The 128-column blocks of the output: per segment ceil(width / 128).
+static bool tc_blocks(const AppendArgsT<__nv_bfloat16> &a, TcBlocks &t) {
+    const int Hr = a.H * a.r;
+    const int widths[4] = {a.d_h, a.d_h, Hr, Hr};
+    t.nblocks = 0;
+    for (int k = 0; k < 4; ++k) {
+        t.width[k] = widths[k];
+        for (int c = 0; c < widths[k]; c += TC_BN) {
+            if (t.nblocks == TC_MAX_BLOCKS) return false;
+            t.seg[t.nblocks] = k;
+            t.col[t.nblocks] = c;
+            ++t.nblocks;
+        }
+    }
+    t.ncoltiles = (t.nblocks + 1) / 2;
+    t.nrowtiles = (a.n + TC_BM - 1) / TC_BM;
+    t.ntiles = t.ncoltiles * t.nrowtiles;
+    return true;
+}
+
 bool tc_append_supported(int n, int d, int d_h, int H, int r) {
-    (void)d_h; (void)H; (void)r;
-    return n > 64 && d % TC_BK == 0 && d >= TC_BK && tc_encode() != nullptr;
+    // at most TC_MAX_BLOCKS 128-column blocks in the output
+    const int blocks = 2 * ((d_h + TC_BN - 1) / TC_BN) + 2 * ((H * r + TC_BN - 1) / TC_BN);
+    return n > 64 && d % TC_BK == 0 && d >= TC_BK && blocks <= TC_MAX_BLOCKS &&
+           tc_encode() != nullptr;
 }
 
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a) {
@@ -220,13 +301,8 @@ cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a) {
         !tc_map(&maps.w[1], a.W_S_V, a.d_h, a.d) || !tc_map(&maps.w[2], a.U_K, Hr, a.d) ||
         !tc_map(&maps.w[3], a.U_V, Hr, a.d))
         return cudaErrorInvalidValue;
-    TcTiles t;
-    const int widths[4] = {a.d_h, a.d_h, Hr, Hr};
-    t.first[0] = 0;
-    for (int k = 0; k < 4; ++k) {
-        t.width[k] = widths[k];
-        t.first[k + 1] = t.first[k] + (widths[k] + TC_BN - 1) / TC_BN;
-    }
+    TcBlocks t;
+    if (!tc_blocks(a, t)) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(append_tc_kernel,
@@ -234,8 +310,8 @@ cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a) {
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(t.first[4], (a.n + TC_BM - 1) / TC_BM);
-    return launch_pdl(append_tc_kernel, grid, dim3(128), TC_SMEM, a.stream, maps, a, t);
+    const int grid = std::min(t.ntiles, device_sm_count());
+    return launch_pdl(append_tc_kernel, dim3(grid), dim3(TC_THREADS), TC_SMEM, a.stream, maps, a, t);
 }
 
 }  // namespace lrkv
