@@ -130,9 +130,12 @@ __device__ __forceinline__ void cursor_begin_segment(IssueCursor *cur, const int
 
 // Issue the copies of the cursor's next tile into its stage.
 template <class C>
+// `refill`: the stage was read by generic loads before (every issue except
+// the first STAGES of a launch, whose stages are fresh), so those reads are
+// ordered before the copy's writes.
 __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
                            const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
-                           int32_t end) {
+                           int32_t end, bool refill = true) {
     if (cur->done) return;
     const int it = cur->issued;
     const int s = it % C::STAGES;
@@ -158,7 +161,7 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
     okf[s] = ok;  // published to the consumers by the mbarrier phase
     const int row = page * P.page_size + cur->t % P.page_size;
     uint8_t *st = smem + s * C::STAGE;
-    fence_proxy_async_smem();
+    if (refill) fence_proxy_async_smem();
     mbar_arrive_expect_tx(&full[s], C::STAGE_TX + (P.norm ? C::NK_TX : 0));
     // each map is 3-D (64 columns, rows, 64-column block) with a box of
     // 64 x 16 x all blocks, so one copy lands the whole 16-row tile as
@@ -687,7 +690,9 @@ __global__ void __launch_bounds__(C::NT, 1)
         cur->page_key = pl[10];
         cur->page_id = pl[11];
         cursor_begin_segment<C>(cur, off, end);
-        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, off, smem, full, okf, end);
+        // the ring is untouched, except by the fused step's staging, which
+        // fenced its reads already
+        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, off, smem, full, okf, end, false);
     }
     __syncthreads();
     if (local) pdl_wait();  // the private queries come from the prologue kernel
