@@ -30,7 +30,6 @@ NORTH_STAR_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # FP32 FMA peak from unit counts and the maximum SM clock: 152 SMs x 128 FP32
 # lanes x 2 flops x 2.07 GHz
-FP32_FMA_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 WORKLOADS = {
     "decode_T4096": "B=16 requests, d=2048, H=16, d_h=128, r=48, history T=4096 (current row "
@@ -42,9 +41,10 @@ WORKLOADS = {
                         "scale per pool), q, bases and output bf16, f16 tensor-core inputs, fp32 "
                         "accumulation",
     "decode_T4096_rope": "decode_T4096 with the exact rotary embedding (section 8): the cache keeps "
-                         "unrotated projections, every key is scored at its distance from the query "
-                         "(q D_(i-j)).S_K + ((q D_(i-j)) B_K[h]).R_K, d_h*r multiply-adds per key and "
-                         "head on CUDA cores; cos/sin table built once",
+                         "unrotated projections, every key is scored at its distance from the query, "
+                         "q~.(S_K D_j) + (C_j W_h).R_K with q~ = q D_i and (q D_(i-j)) B_K[h] = C_j W_h "
+                         "(d_h*r multiply-adds per key and head, on tensor cores), then attention "
+                         "with those scores; cos/sin table built once",
     "decode_T4096_norm": "decode_T4096 with joint key RMSNorm (section 8): a bf16 reciprocal per "
                          "head and token multiplies each score; the step appends the rows, stores "
                          "their reciprocals (lrkv_key_norms) and decodes",
@@ -150,7 +150,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
-ROPE_SPLIT_SOURCES = ("decode_generic.cu", "decode_kernels.cuh", "lrkv_common.cuh")
+ROPE_SCORE_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 
 
 def kernel_source_hash(files=DECODE_SPLIT_SOURCES):
@@ -239,7 +239,9 @@ def run_ours(args, rank, world, local_rank):
     pt = to_dev(case.page_table, "i32")
     max_seq = int(case.seq_lens.max())
     out = torch.empty_like(q)
-    ws = L.workspace(L.decode_step_workspace_bytes(Bn, H, d_h, r, max_seq), dev)
+    rope = bool(c.get("rope"))
+    ws = L.workspace(max(L.decode_step_workspace_bytes(Bn, H, d_h, r, max_seq),
+                         L.decode_rope_workspace_bytes(Bn, H, d_h, r, max_seq) if rope else 0), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -259,10 +261,9 @@ def run_ours(args, rank, world, local_rank):
             calls.append((a, dd, fs, kn))
         return calls
 
-    rope = bool(c.get("rope"))
     if rope:   # the cos/sin table is built once, outside every timed region
         table = L.rope_table(d_h, max_seq, device=dev)
-        rope_args = (P(table), table.shape[0])
+        rope_args = (P(table.buf), table.max_pos)
 
         def dec_rope(q_, dsc, BK_, BV_, sl_, pt_, B_, mp_, msl_, out_, ws_, wsn_, st_, s_):
             return lib.lrkv_decode_rope(q_, dsc, BK_, BV_, sl_, pt_, B_, mp_, msl_, *rope_args,
@@ -339,8 +340,12 @@ def run_ours(args, rank, world, local_rank):
     tot = ctypes.c_double()
     nl = ctypes.c_int32()
     assert lib.lrkv_profile_read(0, ctypes.byref(tot), ctypes.byref(nl)) == 0
-    lib.lrkv_profile_enable(0)
     split_ms = tot.value / max(1, nl.value)
+    # the rotary score kernel (exact-RoPE tensor-core path), bracketed alone
+    tot_s, nl_s = ctypes.c_double(), ctypes.c_int32()
+    assert lib.lrkv_profile_read(2, ctypes.byref(tot_s), ctypes.byref(nl_s)) == 0
+    scores_ms = tot_s.value / nl_s.value if nl_s.value else None
+    lib.lrkv_profile_enable(0)
     st = int(status.item())
     if st:
         raise RuntimeError(f"device status {st}")
@@ -387,10 +392,15 @@ def run_ours(args, rank, world, local_rank):
                   + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
     peak, peak_kind = measured_peaks()
     achieved = split_bytes / (split_ms / 1e3) / 1e9
-    # rotary path: bound by the d_h*r multiply-adds per key and head that form
-    # (q D_(i-j)) B_K[h] (2 d_h r flops; the d_h-wide shared term and the
-    # value reductions are not counted)
-    rope_flops = seq_total * H * 2 * d_h * r
+    # rotary path: the score kernel's contractions per key and head, the
+    # private query (q D_(i-j)) B_K[h] (d_h r multiply-adds), its dot with
+    # R_K (r) and the rotated shared term (d_h): 2 (d_h r + r + d_h) flops
+    rope_flops = seq_total * H * 2 * (d_h * r + r + d_h)
+    # bytes the score kernel reads (S_K, R_K once) and writes (one fp32 score
+    # per row and head); the given-score split kernel reads S_V, R_V, scores
+    score_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)
+    gsplit_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)
+    bf16_peak, bf16_kind = measured_peaks("bf16_tflops", 1900.0)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -403,15 +413,20 @@ def run_ours(args, rank, world, local_rank):
                          f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
                    "step": "lrkv_append (B new rows) + " + ("lrkv_key_norms (their reciprocal key norms) + "
                                                             if norm else "") + "lrkv_decode (B queries)"},
-        "roofline": ({"kernel": "decode split with the exact rotary embedding (generic, FMA)",
-                      "bound": "alu", "achieved": round(rope_flops / (split_ms / 1e3) / 1e12, 3),
-                      "peak": round(FP32_FMA_TFLOPS, 2), "unit": "TFLOP/s",
-                      "frac": round(rope_flops / (split_ms / 1e3) / 1e12 / FP32_FMA_TFLOPS, 4),
-                      "peak_source": "FP32 FMA peak from unit counts: 152 SMs x 128 lanes x 2 x 2.07 GHz",
+        "roofline": ({"kernel": "rotary score kernel (f16 mma.sync; C_j W_h private products, rotated shared term)",
+                      "bound": "tensor", "achieved": round(rope_flops / (scores_ms / 1e3) / 1e12, 2),
+                      "peak": bf16_peak, "unit": "TFLOP/s",
+                      "frac": round(rope_flops / (scores_ms / 1e3) / 1e12 / bf16_peak, 4),
+                      "peak_source": f"{bf16_kind} dense bf16 tensor throughput (f16 runs at the same rate)",
                       "algorithmic_flops_per_launch": rope_flops,
-                      "hbm_gbs": round(achieved, 1),
-                      "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
-                      "traffic": profiled_traffic(name, files=ROPE_SPLIT_SOURCES)} if rope else
+                      "algorithmic_bytes_per_launch": score_bytes,
+                      "hbm_gbs": round(score_bytes / (scores_ms / 1e3) / 1e9, 1),
+                      "avg_launch_ms": round(scores_ms, 5), "launches_timed": nl_s.value,
+                      "given_score_split": {"avg_launch_ms": round(split_ms, 5),
+                                            "algorithmic_bytes_per_launch": gsplit_bytes,
+                                            "hbm_gbs": round(gsplit_bytes / (split_ms / 1e3) / 1e9, 1),
+                                            "frac_of_hbm": round(gsplit_bytes / (split_ms / 1e3) / 1e9 / peak, 4)},
+                      "traffic": profiled_traffic(name, "rope_scores", files=ROPE_SCORE_SOURCES)} if rope else
                      {"kernel": "decode split (factored scores + online softmax + value reductions)",
                      "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -422,13 +437,15 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": profiled_traffic(name)}),
         "step_effective_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
         "breakdown_ms": {"split_kernel": round(split_ms, 5),
+                         "rotary_score_kernel": None if scores_ms is None else round(scores_ms, 5),
                          "lrkv_append_alone": round(append_ms, 5),
                          "lrkv_decode_alone": round(decode_ms, 5),
                          "lrkv_decode_step": None if fused_ms is None else round(fused_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host inputs copied in, result copied out and synchronised every step"},
-        "gpu_launches": (5 if norm else 4) * K,   # per step: append, [key norms,] prologue, split, combine
+        # per step: append, [key norms,] prologue, [rotary scores,] split, combine
+        "gpu_launches": (4 + int(norm) + int(rope)) * K,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

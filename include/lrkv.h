@@ -317,22 +317,39 @@ LRKV_API int lrkv_key_norms(const int32_t *positions, const int32_t *seq_ids, in
  * Key j of a request sits at position j; the decode query at seq_lens[b]-1,
  * a prefill row at its own position.
  *
- * lrkv_rope_table fills table[dist][c] = (cos, sin)(dist * theta_c) for
- * dist < max_pos and c < d_h/2 (float pairs, computed in double precision,
- * rounded once): device memory of max_pos * d_h * 4 bytes, 8-byte aligned,
- * caller-owned.  base > 1 and finite, d_h even in [2, 256], max_pos >= 1.
+ * lrkv_rope_table fills a table of lrkv_rope_table_bytes(d_h, max_pos) bytes
+ * of device memory (16-byte aligned, caller-owned) with, for position p <
+ * max_pos and channel pair c < d_h/2, (cos, sin)(p * theta_c) computed in
+ * double precision: first as float pairs [max_pos][d_h/2][2] (rounded once),
+ * then, from byte offset max_pos * d_h * 4 rounded up to a multiple of 256,
+ * as f16 pairs in the same order (rounded once from the double, to nearest
+ * even).  base > 1 and finite, d_h even in [2, 256], 1 <= max_pos <= 2^24.
+ * lrkv_rope_table_bytes returns 0 for other sizes.
  *
  * lrkv_decode_rope / lrkv_prefill_rope take the arguments of lrkv_decode /
  * lrkv_prefill plus that table and its max_pos, which must be >= max_seq_len
- * (decode) or max_ctx (prefill).  d_h must be even and r <= 64.  The
- * workspaces are those of lrkv_decode / lrkv_prefill.  Any cache dtype.
+ * (decode) or max_ctx (prefill).  d_h must be even and r <= 64.  Any cache
+ * dtype.  lrkv_prefill_rope's workspace is lrkv_prefill's; lrkv_decode_rope
+ * needs lrkv_decode_rope_workspace_bytes (lrkv_decode's plus room for the
+ * rotated operands and one fp32 score per visible row and head).  On bf16
+ * caches with d_h = 128, the tensor-core decode shapes and no key norms, lrkv_decode_rope
+ * takes the angle-addition route D_{i-j} = D_i D_j^T: per step it forms
+ * q~ = q D_i and the d_h x r matrix W_h with (q D_{i-j}) B_K[h] = C_j W_h,
+ * C_j the key's (cos, sin) row; a score kernel evaluates q~.(S_K[j] D_j) +
+ * (C_j W_h).R_K[h,j] on the tensor cores (f16 C_j and W_h, the rotated
+ * S_K[j] and q~ in bf16, fp32 sums) and the split kernel attends with those
+ * scores.  There, a request longer than max_seq_len or than the table is
+ * not attended (zero output, LRKV_STATUS_BAD_SEQLEN).
  */
-LRKV_API int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, float *table,
+LRKV_API size_t lrkv_rope_table_bytes(int32_t d_h, int32_t max_pos);
+LRKV_API int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, void *table,
                              lrkv_stream_t stream);
+LRKV_API size_t lrkv_decode_rope_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                                 int32_t max_seq_len, int32_t dtype);
 LRKV_API int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K,
                               const void *B_V, const int32_t *seq_lens, const int32_t *page_table,
                               int32_t B, int32_t max_pages, int32_t max_seq_len,
-                              const float *rope_table, int32_t rope_max_pos, void *out,
+                              const void *rope_table, int32_t rope_max_pos, void *out,
                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
                               lrkv_stream_t stream);
 LRKV_API int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_rows,
@@ -340,7 +357,7 @@ LRKV_API int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_r
                                int32_t d, const void *W_S_K, const void *W_S_V, const void *U_K,
                                const void *U_V, const void *B_K, const void *B_V,
                                const lrkv_cache_t *cache, const int32_t *page_table,
-                               int32_t max_pages, const float *rope_table, int32_t rope_max_pos,
+                               int32_t max_pages, const void *rope_table, int32_t rope_max_pos,
                                void *out, void *workspace, size_t workspace_bytes,
                                int32_t *dev_status, lrkv_stream_t stream);
 
@@ -361,9 +378,10 @@ LRKV_API int lrkv_last_cuda_error(void);
  * Instrumentation for benchmarks.  lrkv_profile_enable(1) creates pools of
  * CUDA events (once) and starts recording: every later call brackets its
  * dominant kernel with an event pair on the call's stream -- the
- * split-attention kernel of lrkv_decode / lrkv_prefill (LRKV_PROFILE_ATTENTION)
- * and the projection kernel of lrkv_append / lrkv_prefill
- * (LRKV_PROFILE_PROJECTION); at most 8192 pairs are kept of each.
+ * split-attention kernel of lrkv_decode / lrkv_prefill (LRKV_PROFILE_ATTENTION),
+ * the projection kernel of lrkv_append / lrkv_prefill
+ * (LRKV_PROFILE_PROJECTION) and the rotary score kernel of lrkv_decode_rope's
+ * tensor-core path (LRKV_PROFILE_SCORES); at most 8192 pairs are kept of each.
  * lrkv_profile_read(which, ...) waits for that kind's last event, returns its
  * summed kernel time in milliseconds and the number of bracketed launches,
  * and clears that record.  Not for use inside CUDA-graph capture.
@@ -371,6 +389,7 @@ LRKV_API int lrkv_last_cuda_error(void);
  */
 #define LRKV_PROFILE_ATTENTION 0
 #define LRKV_PROFILE_PROJECTION 1
+#define LRKV_PROFILE_SCORES 2
 LRKV_API int lrkv_profile_enable(int on);
 LRKV_API int lrkv_profile_read(int32_t which, double *total_ms, int32_t *launches);
 

@@ -16,7 +16,8 @@ __all__ = [
     "lib", "CacheDesc", "LrkvError", "PagedCache", "append", "decode", "prefill",
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
     "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes", "rope_table",
-    "decode_rope", "prefill_rope", "key_norms",
+    "decode_rope", "prefill_rope", "key_norms", "RopeTable", "rope_table_bytes",
+    "decode_rope_workspace_bytes",
 ]
 
 
@@ -26,7 +27,8 @@ def __getattr__(name):
     if name in ("PagedCache", "append", "decode", "prefill", "decode_workspace_bytes",
                 "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind",
                 "decode_step", "decode_step_workspace_bytes", "rope_table", "decode_rope",
-                "prefill_rope", "key_norms"):
+                "prefill_rope", "key_norms", "RopeTable", "rope_table_bytes",
+                "decode_rope_workspace_bytes"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -30,6 +30,7 @@ LRKV_PREFILL_TILED = 1
 
 LRKV_PROFILE_ATTENTION = 0
 LRKV_PROFILE_PROJECTION = 1
+LRKV_PROFILE_SCORES = 2
 
 LRKV_STATUS_BAD_PAGE = 1
 LRKV_STATUS_BAD_SEQLEN = 2
@@ -79,7 +80,9 @@ SIGNATURES = {
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),
     "lrkv_prefill_kernel_kind": (ctypes.c_int, [CACHE_P]),
+    "lrkv_rope_table_bytes": (SZ, [I32, I32]),
     "lrkv_rope_table": (ctypes.c_int, [ctypes.c_double, I32, I32, P, P]),
+    "lrkv_decode_rope_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "lrkv_key_norms": (ctypes.c_int, [P, P, I32, P, CACHE_P, P, I32, I32, P, P]),
     "lrkv_decode_rope": (ctypes.c_int, [P, CACHE_P, P, P, P, P, I32, I32, I32, P, I32, P, P, SZ, P,
                                         P]),

@@ -224,12 +224,54 @@ def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
 # ----------------------------------------------------------------------------
 # Exact rotary position embedding (see include/lrkv.h)
 # ----------------------------------------------------------------------------
-def rope_table(d_h, max_pos, base=10000.0, device="cuda", stream=None) -> torch.Tensor:
-    """lrkv_rope_table: (cos, sin) of dist * base^(-2c/d_h), [max_pos, d_h/2, 2] fp32."""
-    t = torch.empty((max_pos, d_h // 2, 2), dtype=torch.float32, device=device)
-    _abi.check("lrkv_rope_table", _abi.lib().lrkv_rope_table(float(base), d_h, max_pos, _ptr(t),
+class RopeTable:
+    """The rotary table of lrkv_rope_table: one device buffer holding the
+    (cos, sin) of position * base^(-2c/d_h) as float pairs [max_pos, d_h/2, 2]
+    and, after them, the same pairs as f16."""
+
+    def __init__(self, buf: torch.Tensor, d_h: int, max_pos: int):
+        self.buf, self.d_h, self.max_pos = buf, d_h, max_pos
+
+    @property
+    def cos_sin(self) -> torch.Tensor:
+        """The float pairs, [max_pos, d_h/2, 2] fp32 (a view of the buffer)."""
+        n = self.max_pos * self.d_h
+        return self.buf[: 4 * n].view(torch.float32).view(self.max_pos, self.d_h // 2, 2)
+
+    @property
+    def cos_sin_f16(self) -> torch.Tensor:
+        """The f16 pairs, [max_pos, d_h/2, 2] (a view of the buffer)."""
+        n = self.max_pos * self.d_h
+        o = (4 * n + 255) // 256 * 256
+        return self.buf[o: o + 2 * n].view(torch.float16).view(self.max_pos, self.d_h // 2, 2)
+
+
+def rope_table_bytes(d_h, max_pos) -> int:
+    return int(_abi.lib().lrkv_rope_table_bytes(d_h, max_pos))
+
+
+def rope_table(d_h, max_pos, base=10000.0, device="cuda", stream=None) -> RopeTable:
+    """lrkv_rope_table: (cos, sin) of position * base^(-2c/d_h) for positions
+    below max_pos, in fp32 and f16."""
+    nbytes = rope_table_bytes(d_h, max_pos)
+    if nbytes == 0:
+        raise ValueError(f"invalid rotary table size d_h={d_h} max_pos={max_pos}")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _abi.check("lrkv_rope_table", _abi.lib().lrkv_rope_table(float(base), d_h, max_pos, _ptr(buf),
                                                              _stream(stream)))
-    return t
+    return RopeTable(buf, d_h, max_pos)
+
+
+def decode_rope_workspace_bytes(B, H, d_h, r, max_seq_len, dtype=torch.bfloat16) -> int:
+    return int(_abi.lib().lrkv_decode_rope_workspace_bytes(B, H, d_h, r, max_seq_len, _DT[dtype]))
+
+
+def _need_table(table, d_h):
+    if not isinstance(table, RopeTable):
+        raise TypeError("table must be a RopeTable (rope_table())")
+    if table.d_h != d_h:
+        raise ValueError(f"table is for d_h={table.d_h}, not {d_h}")
+    _need(table.buf, "table", torch.uint8)
 
 
 def decode_rope(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_len, table,
@@ -241,19 +283,19 @@ def decode_rope(q, cache: PagedCache, B_K, B_V, seq_lens, page_table, max_seq_le
         _need(t, n, dt)
     _need(seq_lens, "seq_lens", torch.int32)
     _need(page_table, "page_table", torch.int32)
-    _need(table, "table", torch.float32)
     B, H, d_h = q.shape
+    _need_table(table, d_h)
     r = cache.R_K.shape[3]
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", dt)
     if ws is None:
-        ws = workspace(decode_workspace_bytes(B, H, d_h, r, max_seq_len, dt), q.device)
+        ws = workspace(decode_rope_workspace_bytes(B, H, d_h, r, max_seq_len, dt), q.device)
     _need(ws, "ws", torch.uint8)
     desc = cache.desc()
     code = _abi.lib().lrkv_decode_rope(_ptr(q), ctypes.byref(desc), _ptr(B_K), _ptr(B_V),
                                        _ptr(seq_lens), _ptr(page_table), B, page_table.shape[1],
-                                       max_seq_len, _ptr(table), table.shape[0], _ptr(out),
+                                       max_seq_len, _ptr(table.buf), table.max_pos, _ptr(out),
                                        _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
     _abi.check("lrkv_decode_rope", code)
     return out
@@ -270,9 +312,9 @@ def prefill_rope(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K,
         _need(t, n, dt)
     for n, t in (("cu_rows", cu_rows), ("start_pos", start_pos), ("page_table", page_table)):
         _need(t, n, torch.int32)
-    _need(table, "table", torch.float32)
     n, d = X.shape
     _, H, d_h = Q.shape
+    _need_table(table, d_h)
     r = cache.R_K.shape[3]
     B = start_pos.shape[0]
     if out is None:
@@ -283,8 +325,8 @@ def prefill_rope(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K,
     code = _abi.lib().lrkv_prefill_rope(_ptr(X), _ptr(Q), _ptr(cu_rows), _ptr(start_pos), B, n,
                                         max_ctx, d, _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K),
                                         _ptr(U_V), _ptr(B_K), _ptr(B_V), ctypes.byref(desc),
-                                        _ptr(page_table), page_table.shape[1], _ptr(table),
-                                        table.shape[0], _ptr(out), _ptr(ws), ws.numel(),
+                                        _ptr(page_table), page_table.shape[1], _ptr(table.buf),
+                                        table.max_pos, _ptr(out), _ptr(ws), ws.numel(),
                                         _ptr(status), _stream(stream))
     _abi.check("lrkv_prefill_rope", code)
     return out

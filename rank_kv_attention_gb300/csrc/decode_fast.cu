@@ -33,15 +33,21 @@
 // Kernels of one decode are launched with programmatic dependent launch:
 // each waits (griddepcontrol.wait) for its predecessor before reading its
 // results, so only launch latency overlaps.
+#include <algorithm>
+
 #include "decode_kernels.cuh"
 
 namespace lrkv {
 
+constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kLocalReq]
+
 // Q8_: the cache holds 8-bit E4M3 codes (one byte per element) instead of bf16.
-template <int H_, int R_, int STAGES_, bool Q8_ = false>
+// GS_: the scores are given (written by the rotary score kernel): a stage
+// holds S_V, R_V and the tile's 16 x H fp32 scores, no S_K or R_K.
+template <int H_, int R_, int STAGES_, bool Q8_ = false, bool GS_ = false>
 struct FastCfg {
     static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_;
-    static constexpr bool Q8 = Q8_;
+    static constexpr bool Q8 = Q8_, GS = GS_;
     static constexpr int EB = Q8 ? 1 : 2;    // bytes per cache element
     static constexpr int DH = 128;
     static constexpr int NCW = 8, NT = NCW * 32;
@@ -52,20 +58,24 @@ struct FastCfg {
     static constexpr int NBOX_S = DH * EB / 128;
     static constexpr int NBOX_R = H * R * EB / 128;
     static constexpr int S_BYTES = NBOX_S * BOX, R_BYTES = NBOX_R * BOX;
-    static constexpr int OFF_SK = 0, OFF_SV = S_BYTES, OFF_RK = 2 * S_BYTES;
-    static constexpr int OFF_RV = 2 * S_BYTES + R_BYTES;
+    static constexpr int OFF_SK = 0, OFF_SV = GS ? 0 : S_BYTES, OFF_RK = 2 * S_BYTES;
+    static constexpr int OFF_RV = GS ? S_BYTES : 2 * S_BYTES + R_BYTES;
     // joint key norms (optional): the tile's 16 x H bf16 reciprocals
     static constexpr int OFF_NK = 2 * S_BYTES + 2 * R_BYTES;
     static constexpr int NK_TX = TS * H * 2;   // bytes one copy lands
-    static constexpr int STAGE_TX = 2 * S_BYTES + 2 * R_BYTES;
-    static constexpr int STAGE = STAGE_TX + 1024;
+    // given scores: the tile's 16 x H fp32 scores after S_V and R_V
+    static constexpr int OFF_SC = S_BYTES + R_BYTES;
+    static constexpr int SC_TX = TS * H * 4;
+    static constexpr int STAGE_TX = GS ? S_BYTES + R_BYTES : 2 * S_BYTES + 2 * R_BYTES;
+    static constexpr int STAGE = STAGE_TX + (GS ? (SC_TX + 1023) / 1024 * 1024 : 1024);
     static constexpr int KSP = HPW * R / 16;  // k-steps (and m-tiles) of a warp's private columns
     static constexpr int OFF_BAR = STAGES * STAGE;   // full[STAGES]
     static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
     static constexpr int OFF_OK = OFF_CNT + 64;      // per-stage "page id valid" flags
     static constexpr int OFF_CUR = OFF_OK + 64;      // issue cursor
     static constexpr int OFF_PLAN = OFF_CUR + 64;    // local plan: scan scratch + request offsets
-    static constexpr int OFF_RED = OFF_PLAN + 512;   // fused step: per-warp append partials
+    static constexpr int OFF_PEND = OFF_PLAN + 512;  // given scores: rows of the first copies
+    static constexpr int OFF_RED = OFF_PEND + 64;    // fused step: per-warp append partials
     static constexpr int OFF_DST = OFF_RED + NCW * 32 * 16;  // fused step: new rows' pool rows [16]
     static constexpr int OFF_ABAR = OFF_DST + 16 * 8;          // fused step: staging barrier
     static constexpr int SMEM = OFF_ABAR + 64 + 1024;  // + alignment slack
@@ -76,6 +86,7 @@ struct FastCfg {
     static_assert(NK_TX <= 1024 && (H * 2) % 16 == 0, "norm rows fit their slot; 16-byte TMA rows");
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
+    static_assert(!(GS && Q8), "given scores come with bf16 caches");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -96,10 +107,17 @@ struct FastParams {
     int d, len_shift;
     float4 sc;  // 8-bit cache: pool scales of S_K, S_V, R_K, R_V
     int norm;   // the cache holds joint key norms (a fifth copy per tile)
+    int max_len;  // longest valid sequence length (longer requests are not attended)
+    // rotary score kernel: operands from the prologue, scores out
+    const uint32_t *wf;
+    const float *qt;
+    const float *wsc;
+    float *sc_out;
 };
 
 struct FastMaps {
-    CUtensorMap sk, sv, rk, rv, nk;
+    CUtensorMap sk, sv, rk, rv;
+    CUtensorMap nk;  // joint key norms, or (given scores) the score array
 };
 
 // Copy-issue cursor over the CTA's tile sequence (segments in order, 16-row
@@ -112,6 +130,7 @@ struct IssueCursor {
     int done, issued;
     int page_key, page_id;  // page of the last issued tile: (request, page index) -> id
 };
+
 
 __device__ __forceinline__ const int32_t *page_row(const FastParams &P, int b) {
     return P.page_table + (size_t)(P.req_row ? P.req_row[b] : b) * P.max_pages;
@@ -128,17 +147,9 @@ __device__ __forceinline__ void cursor_begin_segment(IssueCursor *cur, const int
     cur->t_b = min(end, off[b + 1]) - base;
 }
 
-// Issue the copies of the cursor's next tile into its stage.
-template <class C>
-// `refill`: the stage was read by generic loads before (every issue except
-// the first STAGES of a launch, whose stages are fresh), so those reads are
-// ordered before the copy's writes.
-__device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
-                           const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
-                           int32_t end, bool refill = true) {
-    if (cur->done) return;
-    const int it = cur->issued;
-    const int s = it % C::STAGES;
+// Pool row of the cursor's next tile (page looked up once per page), with the
+// stage's "page id valid" flag set for the consumers.
+__device__ __forceinline__ int cursor_row(IssueCursor *cur, const FastParams &P, int *okf, int s) {
     // one page-table read per page (a page holds several 16-row tiles)
     const int pidx = cur->t / P.page_size;
     const int key = cur->b * P.max_pages + pidx;
@@ -159,27 +170,65 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
         page = 0;  // consumers mask the tile
     }
     okf[s] = ok;  // published to the consumers by the mbarrier phase
-    const int row = page * P.page_size + cur->t % P.page_size;
-    uint8_t *st = smem + s * C::STAGE;
-    if (refill) fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&full[s], C::STAGE_TX + (P.norm ? C::NK_TX : 0));
-    // each map is 3-D (64 columns, rows, 64-column block) with a box of
-    // 64 x 16 x all blocks, so one copy lands the whole 16-row tile as
-    // consecutive 16-row x 128-byte swizzled boxes
-    // the cache streams through once per step: evict it from L2 first
-    const uint64_t pol = l2_evict_first_policy();
-    tma_load_3d_hint(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s], pol);
-    tma_load_3d_hint(st + C::OFF_SV, &M.sv, 0, row, 0, &full[s], pol);
-    tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, 0, &full[s], pol);
-    tma_load_3d_hint(st + C::OFF_RV, &M.rv, 0, row, 0, &full[s], pol);
-    if (P.norm) tma_load_3d_hint(st + C::OFF_NK, &M.nk, 0, row, 0, &full[s], pol);
-    cur->issued = it + 1;
+    return page * P.page_size + cur->t % P.page_size;
+}
+
+// Move the cursor past the tile just issued.
+template <class C>
+__device__ __forceinline__ void cursor_advance(IssueCursor *cur, const int32_t *off, int32_t end) {
+    cur->issued += 1;
     cur->t += C::TS;
     if (cur->t >= cur->t_b) {
         cur->start = off[cur->b] + cur->t_b;
         if (cur->start >= end) cur->done = 1;
         else cursor_begin_segment<C>(cur, off, end);
     }
+}
+
+// Given scores: the copy of a tile's 16 x H scores (plan row srow onward).
+template <class C>
+__device__ __forceinline__ void issue_scores(uint8_t *st, const FastMaps &M, int32_t srow,
+                                             uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, C::SC_TX);
+    tma_load_3d(st + C::OFF_SC, &M.nk, 0, srow, 0, bar);
+}
+
+// Issue the copies of the cursor's next tile into its stage.
+// `refill`: the stage was read by generic loads before (every issue except
+// the first STAGES of a launch, whose stages are fresh), so those reads are
+// ordered before the copy's writes.
+// `pend` (given scores only): the scores do not exist yet; their plan row is
+// kept in pend[stage] and the copy issued after the dependency wait.
+template <class C>
+__device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
+                           const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
+                           int32_t end, bool refill = true, int32_t *pend = nullptr) {
+    if (cur->done) return;
+    const int s = cur->issued % C::STAGES;
+    const int row = cursor_row(cur, P, okf, s);
+    uint8_t *st = smem + s * C::STAGE;
+    if (refill) fence_proxy_async_smem();
+    // each map is 3-D (64 columns, rows, 64-column block) with a box of
+    // 64 x 16 x all blocks, so one copy lands the whole 16-row tile as
+    // consecutive 16-row x 128-byte swizzled boxes
+    // the cache streams through once per step: evict it from L2 first
+    const uint64_t pol = l2_evict_first_policy();
+    if constexpr (C::GS) {
+        mbar_arrive_expect_tx(&full[s], C::STAGE_TX);
+        tma_load_3d_hint(st + C::OFF_SV, &M.sv, 0, row, 0, &full[s], pol);
+        tma_load_3d_hint(st + C::OFF_RV, &M.rv, 0, row, 0, &full[s], pol);
+        const int32_t srow = off[cur->b] + cur->t;
+        if (pend) pend[s] = srow;
+        else issue_scores<C>(st, M, srow, &full[s]);
+    } else {
+        mbar_arrive_expect_tx(&full[s], C::STAGE_TX + (P.norm ? C::NK_TX : 0));
+        tma_load_3d_hint(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s], pol);
+        tma_load_3d_hint(st + C::OFF_SV, &M.sv, 0, row, 0, &full[s], pol);
+        tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, 0, &full[s], pol);
+        tma_load_3d_hint(st + C::OFF_RV, &M.rv, 0, row, 0, &full[s], pol);
+        if (P.norm) tma_load_3d_hint(st + C::OFF_NK, &M.nk, 0, row, 0, &full[s], pol);
+    }
+    cursor_advance<C>(cur, off, end);
 }
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
@@ -550,6 +599,99 @@ __device__ __forceinline__ void q8_write_partial(const FastParams &P, size_t slo
         }
 }
 
+// ---------------------------------------------------------------------------
+// Local launch plan of CTA g out of G: the rows of all requests laid end to
+// end, cut into G chunks of whole 16-row tiles, with the same validated
+// lengths and chunk formula as the prologue's plan.  It reads only caller
+// inputs (sequence lengths, page table), which were complete before the
+// prologue kernel got past its own wait and let the next grid launch, so the
+// first tiles can be requested while the prologue is still computing.  Every
+// thread calls it; a CTA without rows gets start >= end (before any barrier
+// that a CTA with rows would pass).  When the CTA's requests do not fit the
+// local offset table, it waits for the prologue and uses its offsets.
+// pl (shared, >= 96 ints): [0] first request [1] last request [2] first page
+// key [3] first page id [4 .. 4 + warps) scan sums [16 ..] request offsets.
+// ---------------------------------------------------------------------------
+struct CtaRange {
+    int b0;
+    int32_t start, end;
+    const int32_t *off;  // off[b] for the CTA's requests
+    bool local;
+};
+
+
+template <int NT>
+__device__ __forceinline__ CtaRange cta_range(const FastParams &P, int g, int G, int32_t *pl) {
+    static_assert(NT / 32 <= 12, "scan sums fit pl[4 .. 15]");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int Bn = P.B;
+    const int per = (Bn + NT - 1) / NT;
+    const int lo = min(Bn, tid * per), hi = min(Bn, lo + per);
+    auto len_of = [&](int bb) { return streamed_len(P.seq_lens[bb], P.max_len, P.len_shift); };
+    // with at most one request per thread its length stays in a register
+    const int32_t my_len = lo < hi ? len_of(lo) : 0;
+    auto len_at = [&](int bb) { return (per == 1) ? my_len : len_of(bb); };
+    int32_t mysum = 0;
+    for (int bb = lo; bb < hi; ++bb) mysum += len_at(bb);
+    int32_t incl = mysum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) pl[4 + warp] = incl;
+    __syncthreads();
+    int32_t wbase = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) {
+        const int32_t v = pl[4 + w];
+        if (w < warp) wbase += v;
+        total += v;
+    }
+    const int32_t base_t = wbase + incl - mysum;  // offset of request lo
+    int32_t chunk = (total + G - 1) / G;
+    chunk = max(chunk, kPlanTileAlign);
+    chunk = (chunk + kPlanTileAlign - 1) / kPlanTileAlign * kPlanTileAlign;
+    CtaRange rg;
+    rg.start = g * chunk;
+    rg.end = min(total, rg.start + chunk);
+    rg.b0 = 0;
+    rg.off = nullptr;
+    rg.local = true;
+    if (rg.start >= rg.end) return rg;
+    {
+        int32_t o = base_t;
+        for (int bb = lo; bb < hi; ++bb) {
+            const int32_t L = len_at(bb);
+            if (L > 0 && o <= rg.start && rg.start < o + L) {
+                pl[0] = bb;
+                // the page of the CTA's first tile, so the copy issuer need
+                // not read it after the barrier
+                const int pidx = (rg.start - o) / P.page_size;
+                pl[2] = bb * P.max_pages + pidx;
+                pl[3] = page_row(P, bb)[pidx];
+            }
+            if (L > 0 && o < rg.end && rg.end <= o + L) pl[1] = bb;
+            o += L;
+        }
+    }
+    __syncthreads();
+    rg.b0 = pl[0];
+    rg.local = pl[1] + 1 - rg.b0 <= kLocalReq;
+    if (rg.local) {
+        int32_t o = base_t;
+        for (int bb = lo; bb < hi; ++bb) {
+            if (bb >= rg.b0 && bb - rg.b0 <= kLocalReq) pl[16 + bb - rg.b0] = o;
+            o += len_at(bb);
+        }
+        if (hi == Bn && Bn - rg.b0 <= kLocalReq) pl[16 + Bn - rg.b0] = o;  // off[B] = total
+    }
+    __syncthreads();
+    rg.off = rg.local ? pl + 16 - rg.b0 : P.ws.off;
+    if (!rg.local) pdl_wait();  // fall back to the prologue's offsets
+    return rg;
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NT, 1)
     decode_split_fast_kernel(const __grid_constant__ FastMaps M, const FastParams P) {
@@ -560,6 +702,7 @@ __global__ void __launch_bounds__(C::NT, 1)
     int *cnt = reinterpret_cast<int *>(smem + C::OFF_CNT);
     int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
     IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
+    int32_t *pend = reinterpret_cast<int32_t *>(smem + C::OFF_PEND);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x;
@@ -568,11 +711,11 @@ __global__ void __launch_bounds__(C::NT, 1)
     // fetch the tensor-map descriptors now: the first copies use them right
     // after the plan below
     if (tid == 32) {
-        prefetch_tensormap(&M.sk);
+        if (!C::GS) prefetch_tensormap(&M.sk);
         prefetch_tensormap(&M.sv);
-        prefetch_tensormap(&M.rk);
+        if (!C::GS) prefetch_tensormap(&M.rk);
         prefetch_tensormap(&M.rv);
-        if (P.norm) prefetch_tensormap(&M.nk);
+        if (C::GS || P.norm) prefetch_tensormap(&M.nk);
     }
     // warm L2 with the page-table rows: the copy issuer reads them right
     // after the plan below (caller inputs, complete before this grid launched)
@@ -592,45 +735,9 @@ __global__ void __launch_bounds__(C::NT, 1)
         append_issue<C>(P, smem, abar, 0);
     }
 
-    // ---- Local launch plan.  It reads only caller inputs (sequence lengths,
-    // page table, cache), which were complete before the prologue kernel got
-    // past its own wait and let this grid launch, so the first tiles can be
-    // requested while the prologue is still computing the private queries.
-    // The same validated lengths and chunk formula as the prologue's plan.
-    int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);  // [0] b0 [1] b_last [2..9] warp sums [16..] offsets
-    constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kLocalReq]
-    const int Bn = P.B;
-    const int max_len = P.max_pages * P.page_size;
-    const int per = (Bn + C::NT - 1) / C::NT;
-    const int lo = min(Bn, tid * per), hi = min(Bn, lo + per);
-    auto len_of = [&](int bb) { return streamed_len(P.seq_lens[bb], max_len, P.len_shift); };
-    // with at most one request per thread (B <= 256) its length stays in a
-    // register for the later passes
-    const int32_t my_len = lo < hi ? len_of(lo) : 0;
-    auto len_at = [&](int bb) { return (per == 1) ? my_len : len_of(bb); };
-    int32_t mysum = 0;
-    for (int bb = lo; bb < hi; ++bb) mysum += len_at(bb);
-    int32_t incl = mysum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) pl[2 + warp] = incl;
-    __syncthreads();
-    int32_t wbase = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < C::NCW; ++w) {
-        const int32_t v = pl[2 + w];
-        if (w < warp) wbase += v;
-        total += v;
-    }
-    const int32_t base_t = wbase + incl - mysum;  // offset of request lo
-    int32_t chunk = (total + (int)gridDim.x - 1) / (int)gridDim.x;
-    chunk = max(chunk, kPlanTileAlign);
-    chunk = (chunk + kPlanTileAlign - 1) / kPlanTileAlign * kPlanTileAlign;
-    const int32_t start0 = g * chunk;
-    const int32_t end = min(total, start0 + chunk);
+    int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
+    const CtaRange rg = cta_range<C::NT>(P, g, (int)gridDim.x, pl);
+    const int32_t start0 = rg.start, end = rg.end;
     if (start0 >= end) {
         if (fused &&
             !append_new_rows<C>(P, smem, reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR),
@@ -640,36 +747,9 @@ __global__ void __launch_bounds__(C::NT, 1)
         pdl_wait();
         return;
     }
-    {
-        int32_t o = base_t;
-        for (int bb = lo; bb < hi; ++bb) {
-            const int32_t L = len_at(bb);
-            if (L > 0 && o <= start0 && start0 < o + L) {
-                pl[0] = bb;
-                // the page of the CTA's first tile, so the copy issuer need
-                // not read it after this barrier
-                const int pidx = (start0 - o) / P.page_size;
-                pl[10] = bb * P.max_pages + pidx;
-                pl[11] = page_row(P, bb)[pidx];
-            }
-            if (L > 0 && o < end && end <= o + L) pl[1] = bb;
-            o += L;
-        }
-    }
-    __syncthreads();
-    const int b0 = pl[0];
-    const bool local = pl[1] + 1 - b0 <= kLocalReq;
-    if (local) {
-        int32_t o = base_t;
-        for (int bb = lo; bb < hi; ++bb) {
-            if (bb >= b0 && bb - b0 <= kLocalReq) pl[16 + bb - b0] = o;
-            o += len_at(bb);
-        }
-        if (hi == Bn && Bn - b0 <= kLocalReq) pl[16 + Bn - b0] = o;  // off[B] = total
-    }
-    __syncthreads();
-    const int32_t *off = local ? pl + 16 - b0 : ws.off;  // off[b] for this CTA's requests
-    if (!local) pdl_wait();  // fall back to the prologue's offsets
+    const int b0 = rg.b0;
+    const bool local = rg.local;
+    const int32_t *off = rg.off;  // off[b] for this CTA's requests
 
     // fused step: project and write the new rows before the ring's first copies
     if (fused &&
@@ -678,8 +758,9 @@ __global__ void __launch_bounds__(C::NT, 1)
                             reinterpret_cast<int64_t *>(smem + C::OFF_DST)))
         if (tid == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
     if (tid == 0) {
+        // given scores: two arrivals per phase, the cache rows' and the scores'
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], C::GS ? 2 : 1);
             cnt[s] = 0;
         }
         fence_barrier_init();
@@ -687,15 +768,20 @@ __global__ void __launch_bounds__(C::NT, 1)
         cur->start = start0;
         cur->done = 0;
         cur->issued = 0;
-        cur->page_key = pl[10];
-        cur->page_id = pl[11];
+        cur->page_key = pl[2];
+        cur->page_id = pl[3];
         cursor_begin_segment<C>(cur, off, end);
         // the ring is untouched, except by the fused step's staging, which
         // fenced its reads already
-        for (int s = 0; s < C::STAGES; ++s) issue_next<C>(cur, P, M, off, smem, full, okf, end, false);
+        for (int s = 0; s < C::STAGES; ++s)
+            issue_next<C>(cur, P, M, off, smem, full, okf, end, false, C::GS ? pend : nullptr);
     }
     __syncthreads();
-    if (local) pdl_wait();  // the private queries come from the prologue kernel
+    if (local) pdl_wait();  // the private queries (or the scores) come from the previous kernel
+    if (C::GS && tid == 0)  // the first tiles' score copies
+        for (int k = 0; k < cur->issued; ++k)
+            issue_scores<C>(smem + (k % C::STAGES) * C::STAGE, M, pend[k % C::STAGES],
+                            &full[k % C::STAGES]);
     pdl_launch_dependents();
 
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
@@ -735,7 +821,9 @@ __global__ void __launch_bounds__(C::NT, 1)
         for (int mt = 0; mt < C::KSP; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accR[mt][e] = 0.f;
-        if constexpr (C::Q8) {
+        if constexpr (C::GS) {
+            // the scores arrive with the tiles
+        } else if constexpr (C::Q8) {
             q8_segment_setup<C>(P, b, warp, gq, tq, qb, pbh, fS, fR);
         } else {
             // B fragments of Q^T: column n = head warp*HPW + n (n < HPW), else 0
@@ -789,7 +877,9 @@ __global__ void __launch_bounds__(C::NT, 1)
             // accumulated in four independent chains (shared even/odd k-steps,
             // private hi/lo halves) so the tensor-core latency overlaps
             float c[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (C::Q8) {
+            if constexpr (C::GS) {
+                // given scores: read per lane in the softmax below
+            } else if constexpr (C::Q8) {
                 q8_scores<C>(st, warp, gq, tq, qb, pbh, fS, fR, c);
             } else {
                 float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -821,14 +911,21 @@ __global__ void __launch_bounds__(C::NT, 1)
             bool rescale = false;
 #pragma unroll
             for (int i = 0; i < C::NH; ++i) {
-                // D[row j][head n = hl + 2i] sits in lane (j % 8) * 4 + i, register hl + 2 (j / 8)
-                const int src = (j & 7) * 4 + i;
-                const float v0 = __shfl_sync(0xffffffffu, c[0], src);
-                const float v1 = __shfl_sync(0xffffffffu, c[1], src);
-                const float v2 = __shfl_sync(0xffffffffu, c[2], src);
-                const float v3 = __shfl_sync(0xffffffffu, c[3], src);
-                const float lo = hl ? v1 : v0, hi = hl ? v3 : v2;
-                float sc = valid ? ((j < 8) ? lo : hi) * P.scale_log2 : -INFINITY;
+                float sc;
+                if constexpr (C::GS) {
+                    sc = valid ? reinterpret_cast<const float *>(st + C::OFF_SC)[j * C::H + hd[i]] *
+                                     P.scale_log2
+                               : -INFINITY;
+                } else {
+                    // D[row j][head n = hl + 2i] sits in lane (j % 8) * 4 + i, register hl + 2 (j / 8)
+                    const int src = (j & 7) * 4 + i;
+                    const float v0 = __shfl_sync(0xffffffffu, c[0], src);
+                    const float v1 = __shfl_sync(0xffffffffu, c[1], src);
+                    const float v2 = __shfl_sync(0xffffffffu, c[2], src);
+                    const float v3 = __shfl_sync(0xffffffffu, c[3], src);
+                    const float lo = hl ? v1 : v0, hi = hl ? v3 : v2;
+                    sc = valid ? ((j < 8) ? lo : hi) * P.scale_log2 : -INFINITY;
+                }
                 if (P.norm && valid)  // joint key norm of (row j, head hd[i])
                     sc *= __bfloat162float(
                         reinterpret_cast<const __nv_bfloat16 *>(st + C::OFF_NK)[j * C::H + hd[i]]);
@@ -991,6 +1088,316 @@ __global__ void __launch_bounds__(C::NT, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Rotary scores (reading note, section 8: exact RoPE over the factored
+// cache) for bf16 caches with d_h = 128, on the tensor cores.
+//
+// With i the query's position, q~ = q D_i and j a key's position, the score
+// of head h is
+//     q~ . (S_K[j] D_j)  +  (C_j W_h) . R_K[h, j]
+// where C_j is the key's (cos, sin)(j theta_c) table row, interleaved by
+// channel pair, and W_h = [A; Bq] (d_h x r) comes from the prologue (see
+// rope_fast_operands): D_{i-j} = D_i D_j^T turns the note's per-distance
+// private query (q D_{i-j}) B_K[h] into a product of a row that depends only
+// on j and a matrix that depends only on the step.  The kernel writes the raw
+// score of every visible (row, head) to the plan-ordered score array; the
+// split kernel's given-score mode then streams S_V, R_V and those scores.
+//
+// One CTA streams a range of rows (the split kernel's plan with its own
+// CTA count) for a group of 8 heads, 8 warps; per 16-row tile, warp w
+//   * takes k-step w (channels 16w .. 16w+15) of the shared term for all 8
+//     heads: it turns the tile's S_K channel pairs by their table entries in
+//     registers (fp32, rounded to bf16), multiplies by q~ of the 8 heads (bf16
+//     hi + lo halves) and writes the partial sums to the stage, announced by a
+//     per-stage mbarrier that counts the 8 warps;
+//   * keeps W_h of head 8 grp + w as f16 mma B-fragments in registers
+//     (d_h r / 64 per thread; the W of 8 heads is 96 KB at r = 48, more than
+//     fits next to a copy ring), forms P = C_tile . W_h (mma.m16n8k16, f16 in,
+//     fp32 accumulate), dots each row of P with the row's R_K[h] (a quad
+//     shuffle reduction), and adds the 8 partial shared sums of its head.
+// Two warps per scheduler leave each thread up to 255 registers.  A tile
+// lands by TMA (128-byte swizzle) as the table rows (f16), the S_K rows and
+// the group's R_K columns; the last warp to release a stage refills it, as in
+// the split kernel.
+// ---------------------------------------------------------------------------
+template <int H_, int R_, int STAGES_>
+struct RopeCfg {
+    static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_, DH = 128;
+    static constexpr int HG = 8;                    // heads per CTA, one per warp
+    static constexpr int NG = H / HG;               // head groups
+    static constexpr int NCW = HG, NT = NCW * 32;   // warp w: head 8 grp + w, shared k-step w
+    static constexpr int NTN = R / 8;               // n-tiles of a head's private columns
+    static constexpr int BOX = TS * 128;            // one 16-row x 128-byte swizzled box
+    static constexpr int C_BYTES = 2 * BOX;         // table rows: 128 f16
+    static constexpr int S_BYTES = 2 * BOX;         // S_K rows: 128 bf16
+    static constexpr int RG_BOXES = HG * R * 2 / 128;  // the group's R_K columns
+    static constexpr int R_BYTES = RG_BOXES * BOX;
+    static constexpr int OFF_C = 0, OFF_SK = C_BYTES, OFF_RK = C_BYTES + S_BYTES;
+    static constexpr int STAGE_TX = C_BYTES + S_BYTES + R_BYTES;
+    static constexpr int OFF_SH = STAGE_TX;         // partial shared scores [8 k-steps][16][HG] fp32
+    static constexpr int STAGE = (STAGE_TX + 8 * TS * HG * 4 + 1023) / 1024 * 1024;
+    static constexpr int OFF_BAR = STAGES * STAGE;  // full[8], shd[8]
+    static constexpr int OFF_CNT = OFF_BAR + 128;   // release counters[STAGES]
+    static constexpr int OFF_OK = OFF_CNT + 64;     // per-stage "page id valid" flags
+    static constexpr int OFF_CUR = OFF_OK + 64;     // issue cursor
+    static constexpr int OFF_PLAN = OFF_CUR + 64;   // local plan
+    static constexpr int SMEM = OFF_PLAN + 512 + 1024;  // + alignment slack
+
+    static_assert(H % HG == 0 && R % 8 == 0 && R <= 64, "head groups of 8, whole n-tiles");
+    static_assert(STAGES >= 2 && STAGES <= 8, "barrier arrays hold 8 stages");
+    static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+struct RopeMaps {
+    CUtensorMap tab, sk, rk;
+};
+
+template <class C>
+__device__ void rope_issue_next(IssueCursor *cur, const FastParams &P, const RopeMaps &M,
+                                const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
+                                int32_t end, int grp, bool refill = true) {
+    if (cur->done) return;
+    const int s = cur->issued % C::STAGES;
+    const int row = cursor_row(cur, P, okf, s);
+    uint8_t *st = smem + s * C::STAGE;
+    if (refill) fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&full[s], C::STAGE_TX);
+    // table rows of positions t .. t + 15 (read by every request: default
+    // policy); S_K rows are read by every head group, R_K columns once
+    tma_load_3d(st + C::OFF_C, &M.tab, 0, cur->t, 0, &full[s]);
+    tma_load_3d(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s]);
+    tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, grp * C::RG_BOXES, &full[s],
+                     l2_evict_first_policy());
+    cursor_advance<C>(cur, off, end);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NT, 1)
+    rope_scores_kernel(const __grid_constant__ RopeMaps M, const FastParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *shd = full + 8;
+    int *cnt = reinterpret_cast<int *>(smem + C::OFF_CNT);
+    int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
+    IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
+    int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = blockIdx.x % C::NG;
+    if (tid == 32) {
+        prefetch_tensormap(&M.tab);
+        prefetch_tensormap(&M.sk);
+        prefetch_tensormap(&M.rk);
+    }
+    if (!P.req_row) {
+        const size_t pt_bytes = (size_t)P.B * P.max_pages * sizeof(int32_t);
+        if (pt_bytes <= 64 * 1024)
+            for (size_t o = (size_t)tid * 128; o < pt_bytes; o += (size_t)C::NT * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.page_table) + o));
+    }
+    const CtaRange rg = cta_range<C::NT>(P, blockIdx.x / C::NG, gridDim.x / C::NG, pl);
+    if (rg.start >= rg.end) {
+        pdl_wait();
+        return;
+    }
+    const int32_t *off = rg.off;
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&shd[s], C::NCW);
+            cnt[s] = 0;
+        }
+        fence_barrier_init();
+        cur->b = rg.b0;
+        cur->start = rg.start;
+        cur->done = 0;
+        cur->issued = 0;
+        cur->page_key = pl[2];
+        cur->page_id = pl[3];
+        cursor_begin_segment<C>(cur, off, rg.end);
+        for (int s = 0; s < C::STAGES; ++s)
+            rope_issue_next<C>(cur, P, M, off, smem, full, okf, rg.end, grp, false);
+    }
+    __syncthreads();
+    if (rg.local) pdl_wait();  // W and q~ come from the prologue kernel
+    pdl_launch_dependents();
+
+    const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3;
+    const int rr = (mi & 1) * 8 + (lane & 7);  // ldmatrix row of this lane
+    const int h = grp * C::HG + warp;
+    const uint32_t chunk = 2 * warp + (mi >> 1);  // this lane's ldmatrix chunk of k-step `warp`
+
+    uint32_t wr[8][C::NTN][2];   // W_h fragments
+    uint32_t qh[2], ql[2];       // q~ fragments of k-step `warp` for the 8 heads (bf16 hi, lo)
+    float winv = 0.f;
+    bool timed_out = false;
+    uint32_t it = 0;
+    int b = rg.b0, wb = -1;
+    int32_t start = rg.start;
+    // A tile is finished one tile later: by then every warp has long written
+    // its shared partial sums, so no warp waits for the slowest one, and the
+    // stage is released before the scores go to global memory (the release
+    // orders this thread's earlier memory operations, stores included).
+    struct Pending {
+        bool on;
+        int s;
+        uint32_t par;
+        float v0, v8;      // private scores (scaled back) of rows gq, gq + 8
+        int64_t g0, g8;    // their score-array rows (-1: not in the segment)
+    } pd = {false, 0, 0u, 0.f, 0.f, -1, -1};
+    auto finish = [&](const Pending &q) -> bool {
+        if (!mbar_wait(&shd[q.s], q.par)) {
+            if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
+            return false;
+        }
+        float f0 = q.v0, f8 = q.v8;
+        if (tq == 0) {
+            const float *sh = reinterpret_cast<const float *>(smem + q.s * C::STAGE + C::OFF_SH);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                f0 += sh[(k * C::TS + gq) * C::HG + warp];
+                f8 += sh[(k * C::TS + gq + 8) * C::HG + warp];
+            }
+        }
+        // release the stage; the last warp out refills it
+        __syncwarp();
+        if (lane == 0) {
+            int prev;
+            asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;"
+                         : "=r"(prev)
+                         : "r"(smem_u32(&cnt[q.s]))
+                         : "memory");
+            if (prev == C::NCW - 1) {
+                cnt[q.s] = 0;
+                rope_issue_next<C>(cur, P, M, off, smem, full, okf, rg.end, grp);
+            }
+        }
+        __syncwarp();
+        if (tq == 0) {
+            if (q.g0 >= 0) P.sc_out[q.g0 * C::H + h] = f0;
+            if (q.g8 >= 0) P.sc_out[q.g8 * C::H + h] = f8;
+        }
+        return true;
+    };
+    while (start < rg.end && !timed_out) {
+        while (off[b + 1] <= start) ++b;
+        const int32_t base = off[b];
+        const int32_t seg_end = min(rg.end, off[b + 1]);
+        const int t_a = start - base, t_b = seg_end - base;
+        if (b != wb) {  // this request's operands
+            wb = b;
+            const uint32_t *src = P.wf + ((size_t)b * C::H + h) * (C::DH * C::R / 2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < C::NTN; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        wr[ks][nt][e] = __ldg(src + ((ks * C::NTN + nt) * 2 + e) * 32 + lane);
+            winv = __ldg(P.wsc + (size_t)b * C::H + h);
+            // B fragment (k, n): q~ of head 8 grp + n at channel 16 warp + k
+            const float *qrow = P.qt + ((size_t)b * C::H + grp * C::HG + gq) * C::DH + 16 * warp + 2 * tq;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float2 v = __ldg(reinterpret_cast<const float2 *>(qrow + 8 * e));
+                const float hx = __bfloat162float(__float2bfloat16_rn(v.x));
+                const float hy = __bfloat162float(__float2bfloat16_rn(v.y));
+                qh[e] = pack_bf16(hx, hy);
+                ql[e] = pack_bf16(v.x - hx, v.y - hy);
+            }
+        }
+
+        for (int t = t_a / C::TS * C::TS; t < t_b; t += C::TS, ++it) {
+            const int s = it % C::STAGES;
+            const uint32_t par = (it / C::STAGES) & 1;
+            if (!mbar_wait(&full[s], par)) {
+                if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
+                timed_out = true;
+                break;
+            }
+            uint8_t *st = smem + s * C::STAGE;
+            const uint32_t cb = smem_u32(st + C::OFF_C);
+            {
+                // shared term, k-step `warp`: channel pairs (2c, 2c+1) of each
+                // row turned by the row's angles (D_j), times q~ of 8 heads
+                uint32_t a[4], cs[4], y[4];
+                ldmatrix_x4(smem_u32(st + C::OFF_SK) + box_chunk(rr, chunk), a[0], a[1], a[2], a[3]);
+                ldmatrix_x4(cb + box_chunk(rr, chunk), cs[0], cs[1], cs[2], cs[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = bf16lo(a[e]), x1 = bf16hi(a[e]);
+                    const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&cs[e]));
+                    y[e] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+                }
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16_16816(c0, y, qh[0], qh[1]);
+                mma_bf16_16816(c1, y, ql[0], ql[1]);
+                // partial [k-step][row][head]
+                float *sh = reinterpret_cast<float *>(st + C::OFF_SH) + warp * C::TS * C::HG;
+                *reinterpret_cast<float2 *>(sh + gq * C::HG + 2 * tq) = make_float2(c0[0] + c1[0], c0[1] + c1[1]);
+                *reinterpret_cast<float2 *>(sh + (gq + 8) * C::HG + 2 * tq) = make_float2(c0[2] + c1[2], c0[3] + c1[3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&shd[s]);
+            }
+            float acc[C::NTN][4];
+#pragma unroll
+            for (int nt = 0; nt < C::NTN; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a[4];
+                ldmatrix_x4(cb + box_chunk(rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int nt = 0; nt < C::NTN; ++nt) mma_f16_16816(acc[nt], a, wr[ks][nt][0], wr[ks][nt][1]);
+            }
+            // rows gq and gq + 8 of P meet R_K[h] at columns nt*8 + 2tq, +1
+            // (two chains per row)
+            const uint8_t *rk = st + C::OFF_RK;
+            float s0a = 0.f, s0b = 0.f, s8a = 0.f, s8b = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < C::NTN; ++nt) {
+                const int cc = warp * C::NTN + nt;
+                const uint32_t u0 = lds_u32(rk + box_chunk(gq, cc) + 4 * tq);
+                const uint32_t u8 = lds_u32(rk + box_chunk(gq + 8, cc) + 4 * tq);
+                s0a = fmaf(acc[nt][0], bf16lo(u0), s0a);
+                s0b = fmaf(acc[nt][1], bf16hi(u0), s0b);
+                s8a = fmaf(acc[nt][2], bf16lo(u8), s8a);
+                s8b = fmaf(acc[nt][3], bf16hi(u8), s8b);
+            }
+            float s0 = s0a + s0b, s8 = s8a + s8b;
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+            s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
+            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+            s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
+            // finish the previous tile, then leave this one pending
+            if (pd.on && !finish(pd)) {
+                timed_out = true;
+                break;
+            }
+            pd.on = true;
+            pd.s = s;
+            pd.par = par;
+            pd.v0 = s0 * winv;
+            pd.v8 = s8 * winv;
+            pd.g0 = (t + gq >= t_a && t + gq < t_b) ? (int64_t)base + t + gq : -1;
+            pd.g8 = (t + gq + 8 >= t_a && t + gq + 8 < t_b) ? (int64_t)base + t + gq + 8 : -1;
+        }
+        start = seg_end;
+    }
+    if (pd.on && !timed_out) finish(pd);
+
+    // never leave with copies in flight into this CTA's shared memory
+    __syncthreads();
+    if (tid == 0) {
+        const int issued = cur->issued;
+        for (int k = (int)it; k < issued; ++k) mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side: tensor maps and dispatch
 // ---------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1013,71 +1420,103 @@ static EncodeTiledFn get_encode_tiled() {
     return fn;
 }
 
-// Map over a pool viewed as [rows, cols] elements of eb bytes (bf16 or 8-bit
-// codes), as three dimensions (128 / eb columns, rows, cols * eb / 128 blocks
-// of 128 bytes) with strides (eb, cols * eb, 128 bytes).  A box of
-// (128 / eb) x 16 x (cols * eb / 128) with 128-byte swizzle lands a 16-row
-// tile as consecutive 16-row x 128-byte boxes (matches box_chunk).
-static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols, int eb) {
+// Encoded tensor maps depend only on (address, shape, type, box): a small
+// per-thread cache of recent encodings saves the host the encode calls of
+// every decode.
+struct MapKey {
+    const void *p;
+    int64_t rows;
+    int cols, eb, box, kind;
+    bool operator==(const MapKey &o) const {
+        return p == o.p && rows == o.rows && cols == o.cols && eb == o.eb && box == o.box &&
+               kind == o.kind;
+    }
+};
+
+template <class Encode>
+static bool encode_cached(CUtensorMap *map, const MapKey &key, Encode &&encode) {
+    constexpr int N = 16;
+    struct Entry {
+        MapKey key;
+        CUtensorMap map;
+        bool ok;
+    };
+    thread_local Entry cache[N] = {};
+    thread_local int next = 0;
+    for (const Entry &e : cache)
+        if (e.ok && e.key == key) {
+            *map = e.map;
+            return true;
+        }
+    if (!encode(map)) return false;
+    cache[next].key = key;
+    cache[next].map = *map;
+    cache[next].ok = true;
+    next = (next + 1) % N;
+    return true;
+}
+
+// Map over a pool viewed as [rows, cols] elements of eb bytes (bf16, f16 or
+// 8-bit codes), as three dimensions (128 / eb columns, rows, cols * eb / 128
+// blocks of 128 bytes) with strides (eb, cols * eb, 128 bytes).  A box of
+// (128 / eb) x 16 x box_blocks (default: all blocks) with 128-byte swizzle
+// lands a 16-row tile as consecutive 16-row x 128-byte boxes (matches
+// box_chunk).
+static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols, int eb,
+                     int box_blocks = 0, bool f16 = false) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
     const int per = 128 / eb, blocks = cols * eb / 128;
-    cuuint64_t dims[3] = {(cuuint64_t)per, (cuuint64_t)rows, (cuuint64_t)blocks};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * eb, 128};
-    cuuint32_t box[3] = {(cuuint32_t)per, 16, (cuuint32_t)blocks};
-    cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    return enc(map, dt, 3, const_cast<void *>(pool), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const int bb = box_blocks ? box_blocks : blocks;
+    return encode_cached(map, MapKey{pool, rows, cols, eb, bb, f16 ? 1 : 0}, [&](CUtensorMap *m) {
+        cuuint64_t dims[3] = {(cuuint64_t)per, (cuuint64_t)rows, (cuuint64_t)blocks};
+        cuuint64_t strides[2] = {(cuuint64_t)cols * eb, 128};
+        cuuint32_t box[3] = {(cuuint32_t)per, 16, (cuuint32_t)bb};
+        cuuint32_t estr[3] = {1, 1, 1};
+        const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : f16   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        return enc(m, dt, 3, const_cast<void *>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
 }
 
-// Map over the joint key norms [rows, H] bf16 as (H, rows, 1): a box of
-// H x 16 x 1 lands a tile's 16 rows of reciprocals, unswizzled.
-static bool make_norm_map(CUtensorMap *map, const void *nk, int64_t rows, int H) {
+// Map over a row-major [rows, H] array of elements of eb bytes (bf16 joint
+// key norms, fp32 given scores) as (H, rows, 1): a box of H x 16 x 1 lands a
+// tile's 16 rows, unswizzled.
+static bool make_row_map(CUtensorMap *map, const void *base, int64_t rows, int H, int eb) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)rows, 1};
-    cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)H * 2 * rows};
-    cuuint32_t box[3] = {(cuuint32_t)H, 16, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(nk), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(map, MapKey{base, rows, H, eb, 1, 2}, [&](CUtensorMap *m) {
+        cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)rows, 1};
+        cuuint64_t strides[2] = {(cuuint64_t)H * eb, (cuuint64_t)H * eb * rows};
+        cuuint32_t box[3] = {(cuuint32_t)H, 16, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        const CUtensorMapDataType dt = eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
 }
 
-template <int H, int R, bool Q8 = false>
+template <int H, int R, bool Q8 = false, bool GS = false>
 struct Pick {
-    static constexpr int stage = FastCfg<H, R, 1, Q8>::STAGE;
-    static constexpr int misc = FastCfg<H, R, 1, Q8>::SMEM - FastCfg<H, R, 1, Q8>::OFF_BAR;
+    static constexpr int stage = FastCfg<H, R, 1, Q8, GS>::STAGE;
+    static constexpr int misc = FastCfg<H, R, 1, Q8, GS>::SMEM - FastCfg<H, R, 1, Q8, GS>::OFF_BAR;
     static constexpr int fit = (227 * 1024 - misc) / stage;
     // deeper rings of large stages measured slower (more DRAM queueing for
     // the same consumption rate): 3 stages of >= 48 KB, else up to 4; the
-    // half-size stages of an 8-bit cache keep about as many bytes in flight
-    static constexpr int cap = Q8 ? (stage >= 24 * 1024 ? 6 : 8) : (stage >= 48 * 1024 ? 3 : 4);
+    // smaller stages of an 8-bit cache or of given scores keep about as many
+    // bytes in flight
+    static constexpr int cap = (Q8 || GS) ? (stage >= 24 * 1024 ? 6 : 8) : (stage >= 48 * 1024 ? 3 : 4);
     static constexpr int STAGES = fit > cap ? cap : fit;
-    using Cfg = FastCfg<H, R, STAGES, Q8>;
+    using Cfg = FastCfg<H, R, STAGES, Q8, GS>;
 };
 
-template <int H, int R, bool Q8>
-static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int G) {
-    using C = typename Pick<H, R, Q8>::Cfg;
-    static_assert(Pick<H, R, Q8>::STAGES >= 2, "at least double buffering");
+// Parameters every kernel of the tensor-core decode reads.
+static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
     const auto &c = a.cache;
-    FastMaps maps;
-    const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) || !make_map(&maps.sv, c.S_V, rows, 128, C::EB) ||
-        !make_map(&maps.rk, c.R_K, rows, H * R, C::EB) || !make_map(&maps.rv, c.R_V, rows, H * R, C::EB))
-        return cudaErrorInvalidValue;
-    if (c.N_K && !make_norm_map(&maps.nk, c.N_K, rows, H)) return cudaErrorInvalidValue;
-    auto kern = decode_split_fast_kernel<C>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     FastParams P;
     P.q = static_cast<const __nv_bfloat16 *>(a.q);
     P.seq_lens = a.seq_lens;
@@ -1098,9 +1537,42 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     P.pool[3] = static_cast<__nv_bfloat16 *>(c.R_V);
     P.d = a.d;
     P.len_shift = a.X ? 1 : 0;
-    P.sc = Q8 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
-              : make_float4(1.f, 1.f, 1.f, 1.f);
+    P.sc = c.dtype == LRKV_FP8_E4M3 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
+                                    : make_float4(1.f, 1.f, 1.f, 1.f);
     P.norm = c.N_K != nullptr;
+    P.max_len = decode_max_len(a);
+    P.wf = a.rope_ws.wf;
+    P.qt = a.rope_ws.qt;
+    P.wsc = a.rope_ws.wsc;
+    P.sc_out = a.rope_ws.sc;
+    return P;
+}
+
+template <int H, int R, bool Q8, bool GS = false>
+static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int G) {
+    using C = typename Pick<H, R, Q8, GS>::Cfg;
+    static_assert(Pick<H, R, Q8, GS>::STAGES >= 2, "at least double buffering");
+    const auto &c = a.cache;
+    FastMaps maps;
+    const int64_t rows = (int64_t)c.num_pages * c.page_size;
+    if (!make_map(&maps.sv, c.S_V, rows, 128, C::EB) || !make_map(&maps.rv, c.R_V, rows, H * R, C::EB))
+        return cudaErrorInvalidValue;
+    if (GS) {
+        if (!make_row_map(&maps.nk, a.rope_ws.sc, a.rope_ws.sc_rows, H, 4)) return cudaErrorInvalidValue;
+    } else if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) ||
+               !make_map(&maps.rk, c.R_K, rows, H * R, C::EB)) {
+        return cudaErrorInvalidValue;
+    }
+    if (!GS && c.N_K && !make_row_map(&maps.nk, c.N_K, rows, H, 2)) return cudaErrorInvalidValue;
+    auto kern = decode_split_fast_kernel<C>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    FastParams P = fast_params(a, ws);
+    if (GS) P.norm = 0;
     return launch_pdl(kern, dim3(G), dim3(C::NT), C::SMEM, a.stream, maps, P);
 }
 
@@ -1130,10 +1602,58 @@ bool fast_decode_step_fits(int H, int r, int d) {
 
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const int H = a.cache.H, r = a.cache.r;
-    const bool q8 = a.cache.dtype == LRKV_FP8_E4M3;
+    const bool q8 = a.cache.dtype == LRKV_FP8_E4M3, gs = a.rope_ws.wf != nullptr;
 #define X(h, rr)                                                                  \
     if (H == h && r == rr)                                                        \
-        return q8 ? launch_fast_cfg<h, rr, true>(a, ws, G) : launch_fast_cfg<h, rr, false>(a, ws, G);
+        return gs ? launch_fast_cfg<h, rr, false, true>(a, ws, G)                 \
+             : q8 ? launch_fast_cfg<h, rr, true>(a, ws, G)                        \
+                  : launch_fast_cfg<h, rr, false>(a, ws, G);
+    LRKV_FAST_SHAPES(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+// ---- exact RoPE: rotary score kernel, then the given-score split kernel
+
+template <int H, int R>
+struct RopePick {
+    static constexpr int stage = RopeCfg<H, R, 2>::STAGE;
+    static constexpr int misc = RopeCfg<H, R, 2>::SMEM - RopeCfg<H, R, 2>::OFF_BAR;
+    static constexpr int fit = (227 * 1024 - misc) / stage;
+    static constexpr int STAGES = fit > 6 ? 6 : fit;
+    using Cfg = RopeCfg<H, R, STAGES>;
+};
+
+bool rope_fast_supported(int H, int d_h, int r, int page_size, int dtype) {
+    return dtype == LRKV_BF16 && H % 8 == 0 && fast_decode_supported(H, d_h, r, page_size, dtype);
+}
+
+template <int H, int R>
+static cudaError_t launch_rope_cfg(const DecodeArgs &a, const DecodeWs &ws) {
+    using A = typename RopePick<H, R>::Cfg;
+    const auto &c = a.cache;
+    const int64_t rows = (int64_t)c.num_pages * c.page_size;
+    RopeMaps rm;
+    if (!make_map(&rm.tab, a.rope16, a.rope_max_pos, 128, 2, 0, true) ||
+        !make_map(&rm.sk, c.S_K, rows, 128, 2) ||
+        !make_map(&rm.rk, c.R_K, rows, H * R, 2, A::RG_BOXES))
+        return cudaErrorInvalidValue;
+    auto kern = rope_scores_kernel<A>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const FastParams P = fast_params(a, ws);
+    const int ranges = std::max(1, device_sm_count() / A::NG);
+    return launch_pdl(kern, dim3(ranges * A::NG), dim3(A::NT), A::SMEM, a.stream, rm, P);
+}
+
+cudaError_t launch_rope_scores(const DecodeArgs &a, const DecodeWs &ws) {
+    const int H = a.cache.H, r = a.cache.r;
+#define X(h, rr) \
+    if (H == h && r == rr) return launch_rope_cfg<h, rr>(a, ws);
     LRKV_FAST_SHAPES(X)
 #undef X
     return cudaErrorInvalidValue;

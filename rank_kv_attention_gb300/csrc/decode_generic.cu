@@ -20,16 +20,85 @@ namespace lrkv {
 // (x = H, y = 0) validates sequence lengths and writes the balanced plan (row
 // offsets and rows per CTA).
 // ---------------------------------------------------------------------------
-constexpr int kProRows = 8;  // requests per prologue block
+constexpr int kProRows = 8;  // most requests per prologue block
 constexpr size_t kStageFloats = 40 * 1024;  // largest B_K / B_V head staged in shared memory
 constexpr int kProThreads = 256;  // threads of a prologue block
 
-template <typename T>
+// Operands of the tensor-core rotary decode for head h of requests b0 ..
+// b0 + nb - 1 (reading note, section 8).  With i = seq_len - 1 the query's
+// position and q~ = q D_i its rotation, D_{i-j} = D_i D_j^T gives
+//     (q D_{i-j}) B_K[h] = sum_c cos(j theta_c) A[c] + sin(j theta_c) Bq[c],
+//     A[c][k]  = q~_2c B[2c][k] + q~_2c+1 B[2c+1][k],
+//     Bq[c][k] = q~_2c+1 B[2c][k] - q~_2c B[2c+1][k],
+// so the private query of key j is its (cos, sin) table row, interleaved by
+// channel pair, times W = [A; Bq] interleaved the same way (row 2c = A[c],
+// row 2c+1 = Bq[c]), and the shared term is q~ . (S_K[j] D_j).  Written per
+// (b, h): q~ in fp32, and W as f16 mma B-fragments (k-step ks, n-tile nt,
+// register e, lane) after the exact power-of-two scaling that puts its
+// largest |value| in [2^14, 2^15), with the inverse scale.  bk: B_K[h] as
+// fp32 [d_h][r]; qs: the query rows; scratch: d_h + d_h r floats.
+__device__ void rope_fast_operands(const float *bk, const float *qs, int nb, int b0, int h, int H,
+                                   int d_h, int r, const int32_t *seq_lens, int max_len,
+                                   const float2 *tab, const RopeFastWs &rf, float *scratch) {
+    const int tid = threadIdx.x, hc = d_h / 2;
+    float *qt = scratch, *w = scratch + d_h;
+    __shared__ float wmax[kProThreads / 32];
+    for (int bb = 0; bb < nb; ++bb) {
+        const int b = b0 + bb;
+        const int32_t L = seq_lens[b];
+        if (L < 1 || L > max_len) continue;  // zeroed and flagged by the plan block
+        const float2 *row = tab + (size_t)(L - 1) * hc;
+        for (int c = tid; c < hc; c += blockDim.x) {
+            const float2 cs = row[c];
+            const float x0 = qs[bb * d_h + 2 * c], x1 = qs[bb * d_h + 2 * c + 1];
+            const float y0 = x0 * cs.x - x1 * cs.y, y1 = x0 * cs.y + x1 * cs.x;
+            qt[2 * c] = y0;
+            qt[2 * c + 1] = y1;
+            *reinterpret_cast<float2 *>(rf.qt + ((size_t)b * H + h) * d_h + 2 * c) = make_float2(y0, y1);
+        }
+        __syncthreads();
+        float mx = 0.f;
+        for (int o = tid; o < hc * r; o += blockDim.x) {
+            const int c = o / r, k = o % r;
+            const float u0 = bk[2 * c * r + k], u1 = bk[(2 * c + 1) * r + k];
+            const float a = qt[2 * c] * u0 + qt[2 * c + 1] * u1;
+            const float bq = qt[2 * c + 1] * u0 - qt[2 * c] * u1;
+            w[2 * c * r + k] = a;
+            w[(2 * c + 1) * r + k] = bq;
+            mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(bq)));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+        __syncthreads();
+        mx = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) mx = fmaxf(mx, wmax[i]);
+        const int e = f16_range_shift(mx);
+        const float sc = exp2i(e);
+        if (tid == 0) rf.wsc[(size_t)b * H + h] = exp2i(-e);
+        // fragment f = ((ks * NTN + nt) * 2 + e) * 32 + lane holds W rows
+        // ks*16 + 2tq + 8e and the next, column nt*8 + gq
+        const int ntn = r / 8, nf = d_h * r / 2;
+        uint32_t *dst = rf.wf + ((size_t)b * H + h) * nf;
+        for (int f = tid; f < nf; f += blockDim.x) {
+            const int lane = f & 31, ee = (f >> 5) & 1, q = f >> 6;
+            const int nt = q % ntn, ks = q / ntn;
+            const int k0 = ks * 16 + 2 * (lane & 3) + 8 * ee, n = nt * 8 + (lane >> 2);
+            dst[f] = pack_f16(w[k0 * r + n] * sc, w[(k0 + 1) * r + n] * sc);
+        }
+        __syncthreads();  // qt, w and wmax are reused by the next request
+    }
+}
+
+// ROPE: the exact-RoPE tensor-core operands instead of p (one request per
+// block row).
+template <typename T, bool ROPE>
 __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
     const T *__restrict__ q, const T *__restrict__ B_K, const int32_t *__restrict__ seq_lens,
     T *__restrict__ out,
     int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, int len_shift,
-    DecodeWs ws, int32_t *status) {
+    DecodeWs ws, int32_t *status, const float2 *__restrict__ rope_tab, RopeFastWs rf) {
+    constexpr int nrows = ROPE ? 1 : kProRows;
     const int tid = threadIdx.x;
     if (blockIdx.x < (unsigned)H) {
         // warm L2 with this block's B_K[h] and query rows while the
@@ -39,8 +108,8 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
         const size_t bk_bytes = (size_t)d_h * r * sizeof(T);
         for (size_t o = (size_t)tid * 128; o < bk_bytes; o += (size_t)blockDim.x * 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(bk + o));
-        const int b_first = blockIdx.y * kProRows;
-        if (tid < kProRows && b_first + tid < B) {
+        const int b_first = blockIdx.y * nrows;
+        if (tid < nrows && b_first + tid < B) {
             const char *qr = reinterpret_cast<const char *>(q + ((size_t)(b_first + tid) * H + blockIdx.x) * d_h);
             for (size_t o = 0; o < (size_t)d_h * sizeof(T); o += 128)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + o));
@@ -52,13 +121,13 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
         // completion counters of this row group's requests start at zero, and
         // requests with an invalid length get a zero output (no segment
         // will ever write it)
-        for (int i = tid; i < kProRows * kHeadGroups; i += blockDim.x) {
-            const int b = blockIdx.y * kProRows + i / kHeadGroups;
+        for (int i = tid; i < nrows * kHeadGroups; i += blockDim.x) {
+            const int b = blockIdx.y * nrows + i / kHeadGroups;
             if (b < B) ws.done[(size_t)b * kHeadGroups + i % kHeadGroups] = 0;
         }
         __shared__ int bad_len[kProRows];
-        if (tid < kProRows) {
-            const int b = blockIdx.y * kProRows + tid;
+        if (tid < nrows) {
+            const int b = blockIdx.y * nrows + tid;
             int bad = 0;
             if (b < B) {
                 const int32_t L = seq_lens[b];
@@ -67,10 +136,10 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
             bad_len[tid] = bad;
         }
         __syncthreads();
-        for (int bb = 0; bb < kProRows; ++bb)
+        for (int bb = 0; bb < nrows; ++bb)
             if (bad_len[bb])
                 for (int i = tid; i < H * d_h; i += blockDim.x)
-                    Elem<T>::store(out + (size_t)(blockIdx.y * kProRows + bb) * H * d_h + i, 0.f);
+                    Elem<T>::store(out + (size_t)(blockIdx.y * nrows + bb) * H * d_h + i, 0.f);
         if (blockIdx.y != 0) return;
         // --- plan: exclusive scan of validated lengths ---
         __shared__ int32_t part[kProThreads];
@@ -115,9 +184,9 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
         if (bad) status_or(status, LRKV_STATUS_BAD_SEQLEN);
         return;
     }
-    // --- private queries of up to kProRows requests for head h ---
-    const int h = blockIdx.x, b0 = blockIdx.y * kProRows;
-    const int nb = min(kProRows, B - b0);
+    // --- private queries of up to nrows requests for head h ---
+    const int h = blockIdx.x, b0 = blockIdx.y * nrows;
+    const int nb = min(nrows, B - b0);
     extern __shared__ float sm[];
     float *bk = sm;                               // [d_h][r] when staged
     float *qs = bk + (staged ? d_h * r : 0);      // [kProRows][d_h]
@@ -139,6 +208,11 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
         for (int e = 0; e < V; ++e) qs[i * V + e] = v[e];
     }
     __syncthreads();
+    if constexpr (ROPE) {  // exact RoPE on the tensor cores: rotated queries and W
+        rope_fast_operands(bk, qs, nb, b0, h, H, d_h, r, seq_lens, max_len, rope_tab, rf,
+                           qs + kProRows * d_h);
+        return;
+    }
     if (staged) {
         // four consecutive private columns per thread: per d one broadcast
         // query value, one 16-byte row slice of B_K[h] and four FMAs
@@ -711,21 +785,29 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
 template <typename T>
 cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align) {
     const auto &c = a.cache;
-    dim3 grid(c.H + 1, (a.B + kProRows - 1) / kProRows);
+    // the rotary operands (W is d_h x r per request and head) take one block
+    // per (head, request); p = q B_K amortises B_K's staging over 8 requests
+    const bool rope_fast = a.rope_ws.wf != nullptr;
+    const int nrows = rope_fast ? 1 : kProRows;
+    dim3 grid(c.H + 1, (a.B + nrows - 1) / nrows);
     const bool staged = (size_t)c.d_h * c.r <= kStageFloats;
-    const size_t sm = sizeof(float) * ((staged ? (size_t)c.d_h * c.r : 0) + (size_t)kProRows * c.d_h);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_prologue_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    const size_t sm = sizeof(float) * ((staged ? (size_t)c.d_h * c.r : 0) + (size_t)kProRows * c.d_h +
+                                       (rope_fast ? (size_t)c.d_h * (c.r + 1) : 0));
+    // the tensor-core rotary path treats a request past the table's end as an
+    // invalid length (zero output, flagged), like every kernel after it
+    const int max_len = decode_max_len(a);
+    auto kern = rope_fast ? decode_prologue_kernel<T, true> : decode_prologue_kernel<T, false>;
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[rope_fast]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[rope_fast] = true;
     }
-    return launch_pdl(decode_prologue_kernel<T>, grid, dim3(kProThreads), sm, a.stream,
+    return launch_pdl(kern, grid, dim3(kProThreads), sm, a.stream,
                       static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
                       static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
-                      a.max_pages * a.cache.page_size, G, tile_align, staged, a.X ? 1 : 0, ws,
-                      a.status);
+                      max_len, G, tile_align, staged, a.X ? 1 : 0, ws, a.status,
+                      reinterpret_cast<const float2 *>(a.rope), a.rope_ws);
 }
 
 template <typename T, typename TC, int RP>
@@ -769,8 +851,8 @@ cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G)
 }
 
 // cos and sin of distance x theta_c, theta_c = base^(-2c/d_h), in double
-// precision, rounded once to float.
-__global__ void rope_table_kernel(double base, int d_h, int max_pos, float2 *table) {
+// precision, rounded once to float and once (from the double) to f16.
+__global__ void rope_table_kernel(double base, int d_h, int max_pos, float2 *table, __half2 *t16) {
     const int hc = d_h / 2;
     const size_t n = (size_t)max_pos * hc;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -781,13 +863,16 @@ __global__ void rope_table_kernel(double base, int d_h, int max_pos, float2 *tab
         double sv, cv;
         sincos(pos * th, &sv, &cv);
         table[i] = make_float2((float)cv, (float)sv);
+        t16[i] = __halves2half2(__double2half(cv), __double2half(sv));
     }
 }
 
-cudaError_t launch_rope_table(double base, int d_h, int max_pos, float *table, cudaStream_t s) {
+cudaError_t launch_rope_table(double base, int d_h, int max_pos, void *table, cudaStream_t s) {
     const size_t n = (size_t)max_pos * (d_h / 2);
     const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
-    rope_table_kernel<<<blocks, 256, 0, s>>>(base, d_h, max_pos, reinterpret_cast<float2 *>(table));
+    char *t = static_cast<char *>(table);
+    rope_table_kernel<<<blocks, 256, 0, s>>>(base, d_h, max_pos, reinterpret_cast<float2 *>(t),
+                                             reinterpret_cast<__half2 *>(t + rope_table_f16_offset(d_h, max_pos)));
     return cudaGetLastError();
 }
 

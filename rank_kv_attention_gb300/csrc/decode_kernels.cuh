@@ -28,14 +28,32 @@ struct DecodeArgs {
     const void *W[4] = {nullptr, nullptr, nullptr, nullptr};
     int d = 0;
     // Exact rotary position embedding when rope != nullptr: the cos/sin table
-    // [rope_max_pos][d_h / 2] of lrkv_rope_table (generic split kernel only).
+    // [rope_max_pos][d_h / 2] of lrkv_rope_table, and its f16 copy.  With
+    // rope_ws.wf set (lrkv_decode_rope on a tensor-core shape) the rotary
+    // score kernel and the split kernel's given-score mode run; otherwise the
+    // generic split kernel.
     const float *rope = nullptr;
+    const __half *rope16 = nullptr;
     int rope_max_pos = 0;
+    RopeFastWs rope_ws = {};
 };
+
+// Longest sequence length a decode attends: what the page table can hold;
+// on the tensor-core rotary path also no longer than the table and than
+// max_seq_len (which sizes its score array).  Longer requests get a zero
+// output and LRKV_STATUS_BAD_SEQLEN.
+inline int decode_max_len(const DecodeArgs &a) {
+    int m = a.max_pages * a.cache.page_size;
+    if (a.rope_ws.wf) {
+        m = m < a.rope_max_pos ? m : a.rope_max_pos;
+        m = m < a.max_seq_len ? m : a.max_seq_len;
+    }
+    return m;
+}
 
 // Largest private width the rotary split kernel keeps in registers.
 constexpr int kRopeMaxRank = 64;
-cudaError_t launch_rope_table(double base, int d_h, int max_pos, float *table, cudaStream_t s);
+cudaError_t launch_rope_table(double base, int d_h, int max_pos, void *table, cudaStream_t s);
 
 // Rows the split kernels stream for a request of length L: none for an
 // invalid length, else L, minus the new row that a fused step folds in later.
@@ -60,6 +78,13 @@ constexpr int kFusedStepMaxRows = 16;
 bool fast_decode_step_fits(int H, int r, int d);
 int fast_decode_grid(int H, int r);
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G);
+
+// Exact RoPE on the tensor cores (bf16 cache, a tensor-core decode shape with
+// H % 8 == 0): launch_rope_scores writes every visible row's score into
+// a.rope_ws.sc; launch_split_fast (with a.rope_ws set) then streams only S_V,
+// R_V and those scores.
+bool rope_fast_supported(int H, int d_h, int r, int page_size, int dtype);
+cudaError_t launch_rope_scores(const DecodeArgs &a, const DecodeWs &ws);
 
 int device_sm_count();
 

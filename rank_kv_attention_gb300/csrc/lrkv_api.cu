@@ -26,7 +26,7 @@ struct Profiler {
     cudaEvent_t ev[2 * kCap];
 };
 static bool g_prof_on = false;
-static Profiler g_prof[2];
+static Profiler g_prof[3];
 
 static void prof_before(int kind, cudaStream_t s) {
     Profiler &p = g_prof[kind];
@@ -113,11 +113,17 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     DecodeGeom geo = decode_geom(a.B, a.max_seq_len);
     DecodeWs ws = decode_ws_layout(workspace, a.B, c.H, c.d_h, c.r, geo.G_ws);
     if (ws_bytes < ws.bytes) return LRKV_E_WORKSPACE;
-    const bool fast = !a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype);
+    const bool rope_fast = a.rope_ws.wf != nullptr;
+    const bool fast = rope_fast || (!a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype));
     const int G = fast ? geo.G_fast : geo.G_gen;
     cudaError_t e;
     if (c.dtype != LRKV_F32) {  // bf16 activations (bf16 or 8-bit cache)
         e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign);
+        if (e == cudaSuccess && rope_fast) {
+            prof_before(LRKV_PROFILE_SCORES, a.stream);
+            e = launch_rope_scores(a, ws);
+            prof_after(LRKV_PROFILE_SCORES, a.stream);
+        }
         if (e == cudaSuccess) {
             prof_before(LRKV_PROFILE_ATTENTION, a.stream);
             e = fast ? launch_split_fast(a, ws, G) : launch_split_generic<__nv_bfloat16>(a, ws, G);
@@ -252,7 +258,7 @@ extern "C" {
 int lrkv_version(void) { return 100; }
 
 int lrkv_profile_enable(int on) {
-    for (int k = 0; k < 2 && on; ++k) {
+    for (int k = 0; k < 3 && on; ++k) {
         Profiler &p = g_prof[k];
         if (p.created) continue;
         for (int i = 0; i < 2 * Profiler::kCap; ++i) {
@@ -265,12 +271,12 @@ int lrkv_profile_enable(int on) {
         p.created = true;
     }
     g_prof_on = on != 0;
-    g_prof[0].n = g_prof[1].n = 0;
+    g_prof[0].n = g_prof[1].n = g_prof[2].n = 0;
     return LRKV_OK;
 }
 
 int lrkv_profile_read(int32_t which, double *total_ms, int32_t *launches) {
-    if (!total_ms || !launches || which < 0 || which > 1) return LRKV_E_INVALID_ARG;
+    if (!total_ms || !launches || which < 0 || which > 2) return LRKV_E_INVALID_ARG;
     Profiler &p = g_prof[which];
     *total_ms = 0.0;
     *launches = p.n;
@@ -573,13 +579,23 @@ int lrkv_prefill(const void *X, const void *Q, const int32_t *cu_rows, const int
 // ---------------------------------------------------------------------------
 // Exact rotary position embedding
 // ---------------------------------------------------------------------------
-static bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
-
-static int check_rope(const lrkv_cache_t *cache, const float *table, int32_t max_pos, int32_t need) {
+static int check_rope(const lrkv_cache_t *cache, const void *table, int32_t max_pos, int32_t need) {
     if (cache->d_h % 2 || cache->r > kRopeMaxRank) return LRKV_E_SHAPE;
-    if (!table || !aligned8(table)) return LRKV_E_INVALID_ARG;
+    if (!table || !aligned16(table)) return LRKV_E_INVALID_ARG;
     if (max_pos < need) return LRKV_E_BOUNDS;
     return LRKV_OK;
+}
+
+static size_t rope_table_bytes(int d_h, int max_pos) {
+    return rope_table_f16_offset(d_h, max_pos) + sizeof(__half) * (size_t)max_pos * d_h;
+}
+
+// Decode workspace of lrkv_decode_rope: the decode workspace, then the
+// tensor-core rotary path's operands and scores.
+static size_t rope_ws_bytes(int B, int H, int d_h, int r, int max_seq_len, size_t *dec_bytes) {
+    const size_t dec = align256(decode_ws_bytes(B, H, d_h, r, max_seq_len));
+    if (dec_bytes) *dec_bytes = dec;
+    return dec + rope_fast_ws_layout(nullptr, B, H, d_h, r, max_seq_len).bytes;
 }
 
 int lrkv_key_norms(const int32_t *positions, const int32_t *seq_ids, int32_t n, const void *B_K,
@@ -597,17 +613,28 @@ int lrkv_key_norms(const int32_t *positions, const int32_t *seq_ids, int32_t n, 
     return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }
 
-int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, float *table, lrkv_stream_t stream) {
+size_t lrkv_rope_table_bytes(int32_t d_h, int32_t max_pos) {
+    if (d_h < 2 || d_h > 256 || d_h % 2 || max_pos < 1 || max_pos > (1 << 24)) return 0;
+    return rope_table_bytes(d_h, max_pos);
+}
+
+size_t lrkv_decode_rope_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                        int32_t max_seq_len, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || B < 1 || max_seq_len < 1) return 0;
+    return rope_ws_bytes(B, H, d_h, r, max_seq_len, nullptr);
+}
+
+int lrkv_rope_table(double base, int32_t d_h, int32_t max_pos, void *table, lrkv_stream_t stream) {
     if (!(base > 1.0) || !std::isfinite(base)) return LRKV_E_INVALID_ARG;
-    if (d_h < 2 || d_h > 256 || d_h % 2 || max_pos < 1) return LRKV_E_SHAPE;
-    if (!table || !aligned8(table)) return LRKV_E_INVALID_ARG;
+    if (d_h < 2 || d_h > 256 || d_h % 2 || max_pos < 1 || max_pos > (1 << 24)) return LRKV_E_SHAPE;
+    if (!table || !aligned16(table)) return LRKV_E_INVALID_ARG;
     cudaError_t e = launch_rope_table(base, d_h, max_pos, table, (cudaStream_t)stream);
     return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
 }
 
 int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K, const void *B_V,
                      const int32_t *seq_lens, const int32_t *page_table, int32_t B,
-                     int32_t max_pages, int32_t max_seq_len, const float *rope_table,
+                     int32_t max_pages, int32_t max_seq_len, const void *rope_table,
                      int32_t rope_max_pos, void *out, void *workspace, size_t workspace_bytes,
                      int32_t *dev_status, lrkv_stream_t stream) {
     int st = check_cache(cache);
@@ -621,6 +648,9 @@ int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K, 
         return LRKV_E_INVALID_ARG;
     if ((st = check_rope(cache, rope_table, rope_max_pos, max_seq_len))) return st;
     if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    size_t dec_bytes = 0;
+    if (workspace_bytes < rope_ws_bytes(B, cache->H, cache->d_h, cache->r, max_seq_len, &dec_bytes))
+        return LRKV_E_WORKSPACE;
     DecodeArgs a;
     a.q = q;
     a.cache = *cache;
@@ -635,24 +665,30 @@ int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K, 
     a.out = out;
     a.status = dev_status;
     a.stream = (cudaStream_t)stream;
-    a.rope = rope_table;
+    a.rope = static_cast<const float *>(rope_table);
+    a.rope16 = reinterpret_cast<const __half *>(static_cast<const char *>(rope_table) +
+                                                rope_table_f16_offset(cache->d_h, rope_max_pos));
     a.rope_max_pos = rope_max_pos;
-    return run_decode(a, workspace, workspace_bytes);
+    if (rope_fast_supported(cache->H, cache->d_h, cache->r, cache->page_size, cache->dtype) &&
+        !cache->N_K)
+        a.rope_ws = rope_fast_ws_layout(static_cast<char *>(workspace) + dec_bytes, B, cache->H,
+                                        cache->d_h, cache->r, max_seq_len);
+    return run_decode(a, workspace, dec_bytes);
 }
 
 int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_rows,
                       const int32_t *start_pos, int32_t B, int32_t n, int32_t max_ctx, int32_t d,
                       const void *W_S_K, const void *W_S_V, const void *U_K, const void *U_V,
                       const void *B_K, const void *B_V, const lrkv_cache_t *cache,
-                      const int32_t *page_table, int32_t max_pages, const float *rope_table,
+                      const int32_t *page_table, int32_t max_pages, const void *rope_table,
                       int32_t rope_max_pos, void *out, void *workspace, size_t workspace_bytes,
                       int32_t *dev_status, lrkv_stream_t stream) {
     int st = check_cache(cache);
     if (st) return st;
     if ((st = check_rope(cache, rope_table, rope_max_pos, max_ctx))) return st;
     return prefill_impl(X, Q, cu_rows, start_pos, B, n, max_ctx, d, W_S_K, W_S_V, U_K, U_V, B_K,
-                        B_V, cache, page_table, max_pages, rope_table, rope_max_pos, out,
-                        workspace, workspace_bytes, dev_status, stream);
+                        B_V, cache, page_table, max_pages, static_cast<const float *>(rope_table),
+                        rope_max_pos, out, workspace, workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

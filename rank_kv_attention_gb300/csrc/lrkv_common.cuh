@@ -68,6 +68,47 @@ __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, i
     return w;
 }
 
+// Extra workspace of the tensor-core rotary decode (lrkv_decode_rope), after
+// the decode workspace (all offsets 256-byte aligned):
+//   [wf: B*H*d_h*r/2 u32]  per (request, head) the rotated private operand
+//                          W as f16 mma B-fragments, scaled by a power of two
+//   [qt: B*H*d_h f32]      rotated queries q D_i
+//   [wsc: B*H f32]         inverse scale of each W
+//   [sc: B*max_seq_len*H f32]  raw scores of every visible row, row-major by
+//                          the plan's row index (request b's rows start at off[b])
+struct RopeFastWs {
+    uint32_t *wf;
+    float *qt;
+    float *wsc;
+    float *sc;
+    int64_t sc_rows;
+    size_t bytes;
+};
+
+__host__ __device__ inline RopeFastWs rope_fast_ws_layout(void *base, int B, int H, int d_h, int r,
+                                                          int max_seq_len) {
+    RopeFastWs w;
+    char *p = static_cast<char *>(base);
+    size_t o = 0;
+    w.wf = reinterpret_cast<uint32_t *>(p + o);
+    o += align256(sizeof(uint32_t) * (size_t)B * H * d_h * r / 2);
+    w.qt = reinterpret_cast<float *>(p + o);
+    o += align256(sizeof(float) * (size_t)B * H * d_h);
+    w.wsc = reinterpret_cast<float *>(p + o);
+    o += align256(sizeof(float) * (size_t)B * H);
+    w.sc = reinterpret_cast<float *>(p + o);
+    w.sc_rows = (int64_t)B * max_seq_len;
+    o += align256(sizeof(float) * (size_t)w.sc_rows * H);
+    w.bytes = o;
+    return w;
+}
+
+// Byte offset of the f16 copy inside a rotary table of max_pos rows: the
+// float (cos, sin) pairs come first, [max_pos][d_h/2][2].
+__host__ __device__ inline size_t rope_table_f16_offset(int d_h, int max_pos) {
+    return align256(sizeof(float) * (size_t)max_pos * d_h);
+}
+
 // ---------------------------------------------------------------------------
 // Element conversion
 // ---------------------------------------------------------------------------

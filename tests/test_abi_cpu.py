@@ -180,13 +180,22 @@ def test_rope_host_checks(lib):
     assert lib.lrkv_rope_table(1e4, 128, 0, 256, None) == E.LRKV_E_SHAPE
     assert lib.lrkv_rope_table(1e4, 128, 10, None, None) == E.LRKV_E_INVALID_ARG
     assert lib.lrkv_rope_table(1e4, 128, 10, 4, None) == E.LRKV_E_INVALID_ARG       # misaligned
+    assert lib.lrkv_rope_table(1e4, 128, 10, 8, None) == E.LRKV_E_INVALID_ARG       # not 16-aligned
+    # float pairs, then f16 pairs from the next 256-byte boundary
+    assert lib.lrkv_rope_table_bytes(128, 10) == 5120 + 2560
+    assert lib.lrkv_rope_table_bytes(2, 3) == 256 + 12
+    assert lib.lrkv_rope_table_bytes(127, 10) == 0 and lib.lrkv_rope_table_bytes(128, 0) == 0
+    # the rotary decode workspace holds the decode one plus operands and scores
+    rb = lib.lrkv_decode_rope_workspace_bytes(16, 16, 128, 48, 4096, 1)
+    assert rb >= lib.lrkv_decode_workspace_bytes(16, 16, 128, 48, 4096, 1) + 16 * 4096 * 16 * 4
+    assert lib.lrkv_decode_rope_workspace_bytes(0, 16, 128, 48, 4096, 1) == 0
     ws = ctypes.c_void_p(256)
 
     def dec(cache, table=16, max_pos=100, msl=100):
         return lib.lrkv_decode_rope(16, ctypes.byref(cache), 16, 16, 16, 16, 2, 4, msl, table,
                                     max_pos, 16, ws, 1 << 30, None, None)
     assert dec(_cache(), table=None) == E.LRKV_E_INVALID_ARG
-    assert dec(_cache(), table=12) == E.LRKV_E_INVALID_ARG                        # not 8-aligned
+    assert dec(_cache(), table=24) == E.LRKV_E_INVALID_ARG                        # not 16-aligned
     assert dec(_cache(), max_pos=99) == E.LRKV_E_BOUNDS                           # table too short
     assert dec(_cache(r=72)) == E.LRKV_E_SHAPE                                    # r > 64
     assert dec(_cache(d_h=130)) == E.LRKV_E_SHAPE

@@ -18,10 +18,15 @@ pytestmark = pytest.mark.gpu
 def test_rope_table_values():
     import rank_kv_attention_gb300 as L
     for d_h, n in ((128, 5000), (16, 70), (2, 3)):
-        t = L.rope_table(d_h, n).cpu().numpy().astype(np.float64)
+        tab = L.rope_table(d_h, n)
+        t = tab.cos_sin.cpu().numpy().astype(np.float64)
         ref = R.table(d_h, n)
         # one rounding of a value in [-1, 1] to float: <= 2^-25 (2^-24 at 1)
         assert np.abs(t - ref).max() <= 6e-8, (d_h, np.abs(t - ref).max())
+        # the f16 copy: one round-to-nearest-even of the double value, the
+        # same rounding numpy applies from float64
+        t16 = tab.cos_sin_f16.cpu().numpy()
+        assert np.array_equal(t16.view(np.uint16), ref.astype(np.float16).view(np.uint16)), d_h
 
 
 def _oracle_rope(case, pairs=None):
@@ -131,3 +136,46 @@ def test_rope_T4096_sampled():
     ref = _oracle_rope(case, pairs)
     idx = tuple(np.array(pairs).T)
     assert_close(got[idx], ref[idx], "bf16", "decode_T4096 rope")
+
+
+def test_rope_many_requests_in_one_range():
+    """More requests inside one CTA's rows than its local offset table holds
+    (zero-length requests in between): the score and split kernels take the
+    prologue's offsets; the invalid lengths get zero and a flag."""
+    import rank_kv_attention_gb300 as L
+    lens = [0] * 100 + [40] + [0] * 100 + [23]
+    case = I.make_decode_case(len(lens), 16, 128, 48, lens, dtype="bf16", seed=11, shuffle=True)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    table = L.rope_table(128, 64)
+    got = host(_run_rope(case, table, status=st), "bf16")
+    assert int(st.item()) & L.LRKV_STATUS_BAD_SEQLEN
+    valid = [100, 201]
+    assert np.all(np.delete(got, valid, axis=0) == 0)
+    ref = _oracle_rope(case, [(b, h) for b in valid for h in range(16)])
+    assert_close(got[valid], ref[valid], "bf16", "requests among empty ones")
+
+
+def test_rope_stale_workspace_and_length_bound():
+    """The tensor-core rotary path writes every score it reads (a workspace
+    full of stale bytes gives the same bits), and on it a request longer than
+    max_seq_len is not attended (zero output, LRKV_STATUS_BAD_SEQLEN)."""
+    import rank_kv_attention_gb300 as L
+    lens = [300, 129, 77, 16]
+    case = I.make_decode_case(4, 16, 128, 48, lens, dtype="bf16", seed=12, shuffle=True)
+    dc = DevDecode(case)
+    table = L.rope_table(128, 300)
+    ws = L.workspace(L.decode_rope_workspace_bytes(4, 16, 128, 48, 300))
+    runs = []
+    for fill in (0xFF, 0x7F):
+        ws.fill_(fill)
+        runs.append(L.decode_rope(dc.q, dc.cache, dc.B_K, dc.B_V, dc.seq_lens, dc.page_table, 300,
+                                  table, ws=ws).clone())
+    assert torch.equal(runs[0].view(torch.int16), runs[1].view(torch.int16))
+    assert_close(host(runs[0], "bf16"), _oracle_rope(case), "bf16", "stale workspace")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = host(L.decode_rope(dc.q, dc.cache, dc.B_K, dc.B_V, dc.seq_lens, dc.page_table, 200,
+                             table, status=st), "bf16")
+    assert int(st.item()) & L.LRKV_STATUS_BAD_SEQLEN
+    assert np.all(out[0] == 0)
+    ref = _oracle_rope(case, [(b, h) for b in (1, 2, 3) for h in range(16)])
+    assert_close(out[1:], ref[1:], "bf16", "requests within max_seq_len")
