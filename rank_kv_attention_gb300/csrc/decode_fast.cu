@@ -1103,7 +1103,8 @@ __global__ void __launch_bounds__(C::NT, 1)
 // split kernel's given-score mode then streams S_V, R_V and those scores.
 //
 // One CTA streams a range of rows (the split kernel's plan with its own
-// CTA count) for a group of 8 heads, 8 warps; per 16-row tile, warp w
+// CTA count) for a group of 8 heads, 8 warps; per 32-row tile (two 16-row
+// m-tiles), warp w
 //   * takes k-step w (channels 16w .. 16w+15) of the shared term for all 8
 //     heads: it turns the tile's S_K channel pairs by their table entries in
 //     registers (fp32, rounded to bf16), multiplies by q~ of the 8 heads (bf16
@@ -1113,28 +1114,33 @@ __global__ void __launch_bounds__(C::NT, 1)
 //     (d_h r / 64 per thread; the W of 8 heads is 96 KB at r = 48, more than
 //     fits next to a copy ring), forms P = C_tile . W_h (mma.m16n8k16, f16 in,
 //     fp32 accumulate), dots each row of P with the row's R_K[h] (a quad
-//     shuffle reduction), and adds the 8 partial shared sums of its head.
+//     shuffle reduction), and one tile later adds the 8 partial shared sums of
+//     its head (each lane of a quad finishes one of the quad's four rows).
 // Two warps per scheduler leave each thread up to 255 registers.  A tile
 // lands by TMA (128-byte swizzle) as the table rows (f16), the S_K rows and
 // the group's R_K columns; the last warp to release a stage refills it, as in
-// the split kernel.
+// the split kernel.  32-row tiles halve the per-row cost of the waits and the
+// release, and give the private products 12 independent accumulators.
 // ---------------------------------------------------------------------------
 template <int H_, int R_, int STAGES_>
 struct RopeCfg {
-    static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_, DH = 128;
+    static constexpr int H = H_, R = R_, TS = 32, STAGES = STAGES_, DH = 128;
     static constexpr int HG = 8;                    // heads per CTA, one per warp
     static constexpr int NG = H / HG;               // head groups
     static constexpr int NCW = HG, NT = NCW * 32;   // warp w: head 8 grp + w, shared k-step w
     static constexpr int NTN = R / 8;               // n-tiles of a head's private columns
-    static constexpr int BOX = TS * 128;            // one 16-row x 128-byte swizzled box
+    static constexpr int BOX = TS * 128;            // one TS-row x 128-byte swizzled box
     static constexpr int C_BYTES = 2 * BOX;         // table rows: 128 f16
     static constexpr int S_BYTES = 2 * BOX;         // S_K rows: 128 bf16
     static constexpr int RG_BOXES = HG * R * 2 / 128;  // the group's R_K columns
     static constexpr int R_BYTES = RG_BOXES * BOX;
     static constexpr int OFF_C = 0, OFF_SK = C_BYTES, OFF_RK = C_BYTES + S_BYTES;
     static constexpr int STAGE_TX = C_BYTES + S_BYTES + R_BYTES;
-    static constexpr int OFF_SH = STAGE_TX;         // partial shared scores [8 k-steps][16][HG] fp32
-    static constexpr int STAGE = (STAGE_TX + 8 * TS * HG * 4 + 1023) / 1024 * 1024;
+    // partial shared scores [k-step][head][SH_ROW] fp32: a head's TS rows, padded
+    // so that the writes (8 rows x 4 heads per instruction) hit distinct banks
+    static constexpr int SH_ROW = TS + 4;
+    static constexpr int OFF_SH = STAGE_TX;
+    static constexpr int STAGE = (STAGE_TX + 8 * HG * SH_ROW * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_BAR = STAGES * STAGE;  // full[8], shd[8]
     static constexpr int OFF_CNT = OFF_BAR + 128;   // release counters[STAGES]
     static constexpr int OFF_OK = OFF_CNT + 64;     // per-stage "page id valid" flags
@@ -1147,6 +1153,13 @@ struct RopeCfg {
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
+
+// Byte offset, inside a region of 64-column swizzled boxes of TS rows, of the
+// 16-byte chunk `cc` (counted along the row) of row `j`.
+template <int TS>
+__device__ __forceinline__ uint32_t box_chunk_rows(int j, int cc) {
+    return (uint32_t)((cc >> 3) * (TS * 128)) + swz128(j, cc & 7);
+}
 
 struct RopeMaps {
     CUtensorMap tab, sk, rk;
@@ -1162,7 +1175,7 @@ __device__ void rope_issue_next(IssueCursor *cur, const FastParams &P, const Rop
     uint8_t *st = smem + s * C::STAGE;
     if (refill) fence_proxy_async_smem();
     mbar_arrive_expect_tx(&full[s], C::STAGE_TX);
-    // table rows of positions t .. t + 15 (read by every request: default
+    // table rows of positions t .. t + TS - 1 (read by every request: default
     // policy); S_K rows are read by every head group, R_K columns once
     tma_load_3d(st + C::OFF_C, &M.tab, 0, cur->t, 0, &full[s]);
     tma_load_3d(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s]);
@@ -1183,6 +1196,7 @@ __global__ void __launch_bounds__(C::NT, 1)
     int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
     IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
     int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
+    constexpr int TS = C::TS;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = blockIdx.x % C::NG;
@@ -1225,9 +1239,11 @@ __global__ void __launch_bounds__(C::NT, 1)
     pdl_launch_dependents();
 
     const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3;
-    const int rr = (mi & 1) * 8 + (lane & 7);  // ldmatrix row of this lane
+    const int rr = (mi & 1) * 8 + (lane & 7);  // ldmatrix row of this lane inside an m-tile
     const int h = grp * C::HG + warp;
     const uint32_t chunk = 2 * warp + (mi >> 1);  // this lane's ldmatrix chunk of k-step `warp`
+    // the tile row this lane finishes: quad gq's four rows, one per lane
+    const int my_row = gq + 8 * (tq & 1) + 16 * (tq >> 1);
 
     uint32_t wr[8][C::NTN][2];   // W_h fragments
     uint32_t qh[2], ql[2];       // q~ fragments of k-step `warp` for the 8 heads (bf16 hi, lo)
@@ -1244,23 +1260,19 @@ __global__ void __launch_bounds__(C::NT, 1)
         bool on;
         int s;
         uint32_t par;
-        float v0, v8;      // private scores (scaled back) of rows gq, gq + 8
-        int64_t g0, g8;    // their score-array rows (-1: not in the segment)
-    } pd = {false, 0, 0u, 0.f, 0.f, -1, -1};
+        float v;      // private score (scaled back) of this lane's row
+        int64_t g;    // its score-array row (-1: not in the segment)
+    } pd = {false, 0, 0u, 0.f, -1};
     auto finish = [&](const Pending &q) -> bool {
         if (!mbar_wait(&shd[q.s], q.par)) {
             if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
             return false;
         }
-        float f0 = q.v0, f8 = q.v8;
-        if (tq == 0) {
-            const float *sh = reinterpret_cast<const float *>(smem + q.s * C::STAGE + C::OFF_SH);
+        const float *sh = reinterpret_cast<const float *>(smem + q.s * C::STAGE + C::OFF_SH) +
+                          warp * C::SH_ROW + my_row;
+        float f = q.v;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                f0 += sh[(k * C::TS + gq) * C::HG + warp];
-                f8 += sh[(k * C::TS + gq + 8) * C::HG + warp];
-            }
-        }
+        for (int k = 0; k < 8; ++k) f += sh[k * C::HG * C::SH_ROW];
         // release the stage; the last warp out refills it
         __syncwarp();
         if (lane == 0) {
@@ -1275,10 +1287,7 @@ __global__ void __launch_bounds__(C::NT, 1)
             }
         }
         __syncwarp();
-        if (tq == 0) {
-            if (q.g0 >= 0) P.sc_out[q.g0 * C::H + h] = f0;
-            if (q.g8 >= 0) P.sc_out[q.g8 * C::H + h] = f8;
-        }
+        if (q.g >= 0) P.sc_out[q.g * C::H + h] = f;
         return true;
     };
     while (start < rg.end && !timed_out) {
@@ -1309,7 +1318,7 @@ __global__ void __launch_bounds__(C::NT, 1)
             }
         }
 
-        for (int t = t_a / C::TS * C::TS; t < t_b; t += C::TS, ++it) {
+        for (int t = t_a / TS * TS; t < t_b; t += TS, ++it) {
             const int s = it % C::STAGES;
             const uint32_t par = (it / C::STAGES) & 1;
             if (!mbar_wait(&full[s], par)) {
@@ -1322,68 +1331,88 @@ __global__ void __launch_bounds__(C::NT, 1)
             {
                 // shared term, k-step `warp`: channel pairs (2c, 2c+1) of each
                 // row turned by the row's angles (D_j), times q~ of 8 heads
-                uint32_t a[4], cs[4], y[4];
-                ldmatrix_x4(smem_u32(st + C::OFF_SK) + box_chunk(rr, chunk), a[0], a[1], a[2], a[3]);
-                ldmatrix_x4(cb + box_chunk(rr, chunk), cs[0], cs[1], cs[2], cs[3]);
+                const uint32_t skb = smem_u32(st + C::OFF_SK);
+                float *sh = reinterpret_cast<float *>(st + C::OFF_SH) + warp * C::HG * C::SH_ROW;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = bf16lo(a[e]), x1 = bf16hi(a[e]);
-                    const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&cs[e]));
-                    y[e] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+                for (int mt = 0; mt < TS / 16; ++mt) {
+                    uint32_t a[4], cs[4], y[4];
+                    ldmatrix_x4(skb + box_chunk_rows<TS>(16 * mt + rr, chunk), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4(cb + box_chunk_rows<TS>(16 * mt + rr, chunk), cs[0], cs[1], cs[2], cs[3]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x0 = bf16lo(a[e]), x1 = bf16hi(a[e]);
+                        const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&cs[e]));
+                        y[e] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+                    }
+                    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_bf16_16816(c0, y, qh[0], qh[1]);
+                    mma_bf16_16816(c1, y, ql[0], ql[1]);
+                    // partial [k-step][head][row]: heads 2tq, 2tq+1, rows gq, gq+8
+                    const int r0 = 16 * mt + gq;
+                    sh[(2 * tq) * C::SH_ROW + r0] = c0[0] + c1[0];
+                    sh[(2 * tq + 1) * C::SH_ROW + r0] = c0[1] + c1[1];
+                    sh[(2 * tq) * C::SH_ROW + r0 + 8] = c0[2] + c1[2];
+                    sh[(2 * tq + 1) * C::SH_ROW + r0 + 8] = c0[3] + c1[3];
                 }
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_bf16_16816(c0, y, qh[0], qh[1]);
-                mma_bf16_16816(c1, y, ql[0], ql[1]);
-                // partial [k-step][row][head]
-                float *sh = reinterpret_cast<float *>(st + C::OFF_SH) + warp * C::TS * C::HG;
-                *reinterpret_cast<float2 *>(sh + gq * C::HG + 2 * tq) = make_float2(c0[0] + c1[0], c0[1] + c1[1]);
-                *reinterpret_cast<float2 *>(sh + (gq + 8) * C::HG + 2 * tq) = make_float2(c0[2] + c1[2], c0[3] + c1[3]);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&shd[s]);
             }
-            float acc[C::NTN][4];
+            float acc[TS / 16][C::NTN][4];
 #pragma unroll
-            for (int nt = 0; nt < C::NTN; ++nt)
+            for (int mt = 0; mt < TS / 16; ++mt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+                for (int nt = 0; nt < C::NTN; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a[4];
-                ldmatrix_x4(cb + box_chunk(rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                uint32_t a[TS / 16][4];
 #pragma unroll
-                for (int nt = 0; nt < C::NTN; ++nt) mma_f16_16816(acc[nt], a, wr[ks][nt][0], wr[ks][nt][1]);
+                for (int mt = 0; mt < TS / 16; ++mt)
+                    ldmatrix_x4(cb + box_chunk_rows<TS>(16 * mt + rr, 2 * ks + (mi >> 1)), a[mt][0],
+                                a[mt][1], a[mt][2], a[mt][3]);
+#pragma unroll
+                for (int nt = 0; nt < C::NTN; ++nt)
+#pragma unroll
+                    for (int mt = 0; mt < TS / 16; ++mt)
+                        mma_f16_16816(acc[mt][nt], a[mt], wr[ks][nt][0], wr[ks][nt][1]);
             }
-            // rows gq and gq + 8 of P meet R_K[h] at columns nt*8 + 2tq, +1
-            // (two chains per row)
+            // row 16 mt + gq + 8 u of P meets R_K[h] at columns nt*8 + 2tq, +1
             const uint8_t *rk = st + C::OFF_RK;
-            float s0a = 0.f, s0b = 0.f, s8a = 0.f, s8b = 0.f;
+            float pv[TS / 16][2];
 #pragma unroll
-            for (int nt = 0; nt < C::NTN; ++nt) {
-                const int cc = warp * C::NTN + nt;
-                const uint32_t u0 = lds_u32(rk + box_chunk(gq, cc) + 4 * tq);
-                const uint32_t u8 = lds_u32(rk + box_chunk(gq + 8, cc) + 4 * tq);
-                s0a = fmaf(acc[nt][0], bf16lo(u0), s0a);
-                s0b = fmaf(acc[nt][1], bf16hi(u0), s0b);
-                s8a = fmaf(acc[nt][2], bf16lo(u8), s8a);
-                s8b = fmaf(acc[nt][3], bf16hi(u8), s8b);
-            }
-            float s0 = s0a + s0b, s8 = s8a + s8b;
-            s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-            s8 += __shfl_xor_sync(0xffffffffu, s8, 1);
-            s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-            s8 += __shfl_xor_sync(0xffffffffu, s8, 2);
-            // finish the previous tile, then leave this one pending
+            for (int mt = 0; mt < TS / 16; ++mt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float sa = 0.f, sb = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < C::NTN; ++nt) {
+                        const uint32_t w = lds_u32(rk + box_chunk_rows<TS>(16 * mt + gq + 8 * u, warp * C::NTN + nt) + 4 * tq);
+                        sa = fmaf(acc[mt][nt][2 * u], bf16lo(w), sa);
+                        sb = fmaf(acc[mt][nt][2 * u + 1], bf16hi(w), sb);
+                    }
+                    pv[mt][u] = sa + sb;
+                }
+#pragma unroll
+            for (int mt = 0; mt < TS / 16; ++mt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    pv[mt][u] += __shfl_xor_sync(0xffffffffu, pv[mt][u], 1);
+                    pv[mt][u] += __shfl_xor_sync(0xffffffffu, pv[mt][u], 2);
+                }
+            // finish the previous tile, then leave this one pending (this
+            // lane's row: my_row = gq + 8 (tq & 1) + 16 (tq >> 1))
             if (pd.on && !finish(pd)) {
                 timed_out = true;
                 break;
             }
+            const float mine = (tq == 0) ? pv[0][0] : (tq == 1) ? pv[0][1] : (tq == 2) ? pv[1][0] : pv[1][1];
+            const int j = t + my_row;
             pd.on = true;
             pd.s = s;
             pd.par = par;
-            pd.v0 = s0 * winv;
-            pd.v8 = s8 * winv;
-            pd.g0 = (t + gq >= t_a && t + gq < t_b) ? (int64_t)base + t + gq : -1;
-            pd.g8 = (t + gq + 8 >= t_a && t + gq + 8 < t_b) ? (int64_t)base + t + gq + 8 : -1;
+            pd.v = mine * winv;
+            pd.g = (j >= t_a && j < t_b) ? (int64_t)base + j : -1;
         }
         start = seg_end;
     }
@@ -1463,15 +1492,15 @@ static bool encode_cached(CUtensorMap *map, const MapKey &key, Encode &&encode) 
 // lands a 16-row tile as consecutive 16-row x 128-byte boxes (matches
 // box_chunk).
 static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols, int eb,
-                     int box_blocks = 0, bool f16 = false) {
+                     int box_blocks = 0, bool f16 = false, int box_rows = 16) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
     const int per = 128 / eb, blocks = cols * eb / 128;
     const int bb = box_blocks ? box_blocks : blocks;
-    return encode_cached(map, MapKey{pool, rows, cols, eb, bb, f16 ? 1 : 0}, [&](CUtensorMap *m) {
+    return encode_cached(map, MapKey{pool, rows, cols, eb, bb * 1024 + box_rows, f16 ? 1 : 0}, [&](CUtensorMap *m) {
         cuuint64_t dims[3] = {(cuuint64_t)per, (cuuint64_t)rows, (cuuint64_t)blocks};
         cuuint64_t strides[2] = {(cuuint64_t)cols * eb, 128};
-        cuuint32_t box[3] = {(cuuint32_t)per, 16, (cuuint32_t)bb};
+        cuuint32_t box[3] = {(cuuint32_t)per, (cuuint32_t)box_rows, (cuuint32_t)bb};
         cuuint32_t estr[3] = {1, 1, 1};
         const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                        : f16   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -1620,12 +1649,14 @@ struct RopePick {
     static constexpr int stage = RopeCfg<H, R, 2>::STAGE;
     static constexpr int misc = RopeCfg<H, R, 2>::SMEM - RopeCfg<H, R, 2>::OFF_BAR;
     static constexpr int fit = (227 * 1024 - misc) / stage;
-    static constexpr int STAGES = fit > 6 ? 6 : fit;
+    static constexpr int STAGES = fit > 8 ? 8 : fit;
     using Cfg = RopeCfg<H, R, STAGES>;
 };
 
 bool rope_fast_supported(int H, int d_h, int r, int page_size, int dtype) {
-    return dtype == LRKV_BF16 && H % 8 == 0 && fast_decode_supported(H, d_h, r, page_size, dtype);
+    // the score kernel's 32-row tiles stay inside a page
+    return dtype == LRKV_BF16 && H % 8 == 0 && page_size % 32 == 0 &&
+           fast_decode_supported(H, d_h, r, page_size, dtype);
 }
 
 template <int H, int R>
@@ -1634,9 +1665,9 @@ static cudaError_t launch_rope_cfg(const DecodeArgs &a, const DecodeWs &ws) {
     const auto &c = a.cache;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
     RopeMaps rm;
-    if (!make_map(&rm.tab, a.rope16, a.rope_max_pos, 128, 2, 0, true) ||
-        !make_map(&rm.sk, c.S_K, rows, 128, 2) ||
-        !make_map(&rm.rk, c.R_K, rows, H * R, 2, A::RG_BOXES))
+    if (!make_map(&rm.tab, a.rope16, a.rope_max_pos, 128, 2, 0, true, A::TS) ||
+        !make_map(&rm.sk, c.S_K, rows, 128, 2, 0, false, A::TS) ||
+        !make_map(&rm.rk, c.R_K, rows, H * R, 2, A::RG_BOXES, false, A::TS))
         return cudaErrorInvalidValue;
     auto kern = rope_scores_kernel<A>;
     static bool attr_set = false;
