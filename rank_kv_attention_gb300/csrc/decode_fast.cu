@@ -46,7 +46,9 @@ constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kL
 // holds S_V, R_V and the tile's 16 x H fp32 scores, no S_K or R_K.
 template <int H_, int R_, int STAGES_, bool Q8_ = false, bool GS_ = false>
 struct FastCfg {
-    static constexpr int H = H_, R = R_, TS = 16, STAGES = STAGES_;
+    // rows per stage: given scores carry half the bytes per row, so a stage
+    // holds 32 rows (two 16-row halves) to keep the per-stage cost per byte
+    static constexpr int H = H_, R = R_, TS = GS_ ? 32 : 16, STAGES = STAGES_;
     static constexpr bool Q8 = Q8_, GS = GS_;
     static constexpr int EB = Q8 ? 1 : 2;    // bytes per cache element
     static constexpr int DH = 128;
@@ -83,7 +85,7 @@ struct FastCfg {
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
     static_assert(STAGES <= 8, "barrier, counter and flag arrays hold 8 stages");
-    static_assert(NK_TX <= 1024 && (H * 2) % 16 == 0, "norm rows fit their slot; 16-byte TMA rows");
+    static_assert(GS || (NK_TX <= 1024 && (H * 2) % 16 == 0), "norm rows fit their slot; 16-byte TMA rows");
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(!(GS && Q8), "given scores come with bf16 caches");
@@ -395,6 +397,13 @@ constexpr float kLazyMax = 8.f;
 // 16-byte chunk `cc` (counted along the row) of tile row `j`.
 __device__ __forceinline__ uint32_t box_chunk(int j, int cc) {
     return (uint32_t)((cc >> 3) * (16 * 128)) + swz128(j, cc & 7);
+}
+
+// Byte offset, inside a region of 64-column swizzled boxes of TS rows, of the
+// 16-byte chunk `cc` (counted along the row) of row `j`.
+template <int TS>
+__device__ __forceinline__ uint32_t box_chunk_rows(int j, int cc) {
+    return (uint32_t)((cc >> 3) * (TS * 128)) + swz128(j, cc & 7);
 }
 
 // ---------------------------------------------------------------------------
@@ -868,10 +877,13 @@ __global__ void __launch_bounds__(C::NT, 1)
                 break;
             }
             const bool page_ok = okf[s] != 0;
-            const bool partial = !page_ok || t < t_a || t + C::TS > t_b;
-            const bool valid = page_ok && t + j >= t_a && t + j < t_b;
             const uint8_t *st = smem + s * C::STAGE;
             const int mi = lane >> 3;
+#pragma unroll
+            for (int h2 = 0; h2 < C::TS / 16; ++h2) {  // 16-row halves of the stage
+            const int t16 = t + 16 * h2;                 // first row of this half
+            const bool partial = !page_ok || t16 < t_a || t16 + 16 > t_b;
+            const bool valid = page_ok && t16 + j >= t_a && t16 + j < t_b;
 
             // scores: D[row x head] = S_K . Q^T + R_K(warp columns) . blockdiag(p)^T,
             // accumulated in four independent chains (shared even/odd k-steps,
@@ -890,7 +902,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a[4];
-                    ldmatrix_x4(skb + box_chunk(rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4(skb + box_chunk_rows<C::TS>(16 * h2 + rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
                     if (ks & 1) mma_bf16_16816(c1, a, qb[ks][0], qb[ks][1]);
                     else mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
                 }
@@ -898,7 +910,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int ks = 0; ks < C::KSP; ++ks) {
                     uint32_t a[4];
-                    ldmatrix_x4(rkb + box_chunk(rr, cw + 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4(rkb + box_chunk_rows<C::TS>(16 * h2 + rr, cw + 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
                     mma_bf16_16816(c2, a, pbh[ks][0], pbh[ks][1]);
                     mma_bf16_16816(c3, a, pbl[ks][0], pbl[ks][1]);
                 }
@@ -913,7 +925,7 @@ __global__ void __launch_bounds__(C::NT, 1)
             for (int i = 0; i < C::NH; ++i) {
                 float sc;
                 if constexpr (C::GS) {
-                    sc = valid ? reinterpret_cast<const float *>(st + C::OFF_SC)[j * C::H + hd[i]] *
+                    sc = valid ? reinterpret_cast<const float *>(st + C::OFF_SC)[(16 * h2 + j) * C::H + hd[i]] *
                                      P.scale_log2
                                : -INFINITY;
                 } else {
@@ -928,7 +940,7 @@ __global__ void __launch_bounds__(C::NT, 1)
                 }
                 if (P.norm && valid)  // joint key norm of (row j, head hd[i])
                     sc *= __bfloat162float(
-                        reinterpret_cast<const __nv_bfloat16 *>(st + C::OFF_NK)[j * C::H + hd[i]]);
+                        reinterpret_cast<const __nv_bfloat16 *>(st + C::OFF_NK)[(16 * h2 + j) * C::H + hd[i]]);
                 float mx = sc;
 #pragma unroll
                 for (int o = 8; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -991,7 +1003,7 @@ __global__ void __launch_bounds__(C::NT, 1)
                 }
                 uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
                 if (partial) {
-                    auto ok = [&](int r) { return page_ok && t + r >= t_a && t + r < t_b; };
+                    auto ok = [&](int r) { return page_ok && t16 + r >= t_a && t16 + r < t_b; };
                     m01 = (ok(2 * tq) ? 0x0000ffffu : 0u) | (ok(2 * tq + 1) ? 0xffff0000u : 0u);
                     m89 = (ok(2 * tq + 8) ? 0x0000ffffu : 0u) | (ok(2 * tq + 9) ? 0xffff0000u : 0u);
                 }
@@ -1004,7 +1016,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a[4];
-                    ldmatrix_x4_trans(svb + box_chunk(rr, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4_trans(svb + box_chunk_rows<C::TS>(16 * h2 + rr, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
                     a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
                     mma_bf16_16816(accS[mt], a, bh0, bh1);
                     mma_bf16_16816(accS[mt], a, bl0, bl1);
@@ -1014,13 +1026,15 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int mt = 0; mt < C::KSP; ++mt) {
                     uint32_t a[4];
-                    ldmatrix_x4_trans(rvb + box_chunk(rr, cw + 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4_trans(rvb + box_chunk_rows<C::TS>(16 * h2 + rr, cw + 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
                     a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
                     mma_bf16_16816(accR[mt], a, bh0, bh1);
                     mma_bf16_16816(accR[mt], a, bl0, bl1);
                 }
                 }
             }
+
+            }  // halves
 
             // release the stage; the last warp out refills it
             __syncwarp();
@@ -1153,13 +1167,6 @@ struct RopeCfg {
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
-
-// Byte offset, inside a region of 64-column swizzled boxes of TS rows, of the
-// 16-byte chunk `cc` (counted along the row) of row `j`.
-template <int TS>
-__device__ __forceinline__ uint32_t box_chunk_rows(int j, int cc) {
-    return (uint32_t)((cc >> 3) * (TS * 128)) + swz128(j, cc & 7);
-}
 
 struct RopeMaps {
     CUtensorMap tab, sk, rk;
@@ -1514,13 +1521,14 @@ static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols,
 // Map over a row-major [rows, H] array of elements of eb bytes (bf16 joint
 // key norms, fp32 given scores) as (H, rows, 1): a box of H x 16 x 1 lands a
 // tile's 16 rows, unswizzled.
-static bool make_row_map(CUtensorMap *map, const void *base, int64_t rows, int H, int eb) {
+static bool make_row_map(CUtensorMap *map, const void *base, int64_t rows, int H, int eb,
+                         int box_rows = 16) {
     EncodeTiledFn enc = get_encode_tiled();
     if (!enc) return false;
-    return encode_cached(map, MapKey{base, rows, H, eb, 1, 2}, [&](CUtensorMap *m) {
+    return encode_cached(map, MapKey{base, rows, H, eb, box_rows, 2}, [&](CUtensorMap *m) {
         cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)rows, 1};
         cuuint64_t strides[2] = {(cuuint64_t)H * eb, (cuuint64_t)H * eb * rows};
-        cuuint32_t box[3] = {(cuuint32_t)H, 16, 1};
+        cuuint32_t box[3] = {(cuuint32_t)H, (cuuint32_t)box_rows, 1};
         cuuint32_t estr[3] = {1, 1, 1};
         const CUtensorMapDataType dt = eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         return enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -1584,10 +1592,11 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     const auto &c = a.cache;
     FastMaps maps;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    if (!make_map(&maps.sv, c.S_V, rows, 128, C::EB) || !make_map(&maps.rv, c.R_V, rows, H * R, C::EB))
+    if (!make_map(&maps.sv, c.S_V, rows, 128, C::EB, 0, false, C::TS) ||
+        !make_map(&maps.rv, c.R_V, rows, H * R, C::EB, 0, false, C::TS))
         return cudaErrorInvalidValue;
     if (GS) {
-        if (!make_row_map(&maps.nk, a.rope_ws.sc, a.rope_ws.sc_rows, H, 4)) return cudaErrorInvalidValue;
+        if (!make_row_map(&maps.nk, a.rope_ws.sc, a.rope_ws.sc_rows, H, 4, C::TS)) return cudaErrorInvalidValue;
     } else if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) ||
                !make_map(&maps.rk, c.R_K, rows, H * R, C::EB)) {
         return cudaErrorInvalidValue;
