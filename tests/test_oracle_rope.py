@@ -118,6 +118,27 @@ def test_factored_formula_equals_materialised():
         np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
 
 
+def test_angle_addition_form_matches_materialised_scores():
+    """The tensor-core decode's form of the score (q~ = q D_i; the private
+    query of key j as its interleaved (cos, sin)(j theta) row C_j times the
+    d_h x r matrix W with rows 2c -> q~_2c B[2c] + q~_2c+1 B[2c+1] and
+    2c+1 -> q~_2c+1 B[2c] - q~_2c B[2c+1]; the shared term q~ . (S_K[j] D_j))
+    equals the materialised score (q D_i) . ((S_K[j] + R_K[j] B^T) D_j)."""
+    g = np.random.default_rng(21)
+    for d_h, r, i in ((8, 3, 9), (16, 5, 200), (128, 48, 4095)):
+        q, s, z = g.standard_normal(d_h), g.standard_normal(d_h), g.standard_normal(r)
+        B = g.standard_normal((d_h, r)) / math.sqrt(r)
+        qt = rope.rotate(q, i)
+        W = np.empty((d_h, r))
+        W[0::2] = qt[0::2, None] * B[0::2] + qt[1::2, None] * B[1::2]
+        W[1::2] = qt[1::2, None] * B[0::2] - qt[0::2, None] * B[1::2]
+        for j in (0, 1, i // 2, i):
+            C = rope.table(d_h, j + 1)[j].reshape(-1)   # (cos, sin) interleaved by pair
+            got = qt @ rope.rotate(s, j) + (C @ W) @ z
+            ref = rope.rotate(q, i) @ rope.rotate(s + B @ z, j)
+            assert abs(got - ref) <= 1e-12 * max(1.0, abs(ref)), (d_h, r, i, j, got, ref)
+
+
 def test_paged_decode_matches_per_request():
     g = np.random.default_rng(5)
     H, d_h, r, ps = 2, 8, 2, 4
