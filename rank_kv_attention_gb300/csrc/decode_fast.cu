@@ -46,9 +46,10 @@ constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kL
 // holds S_V, R_V and the tile's 16 x H fp32 scores, no S_K or R_K.
 template <int H_, int R_, int STAGES_, bool Q8_ = false, bool GS_ = false>
 struct FastCfg {
-    // rows per stage: given scores carry half the bytes per row, so a stage
-    // holds 32 rows (two 16-row halves) to keep the per-stage cost per byte
-    static constexpr int H = H_, R = R_, TS = GS_ ? 32 : 16, STAGES = STAGES_;
+    // rows per stage: given scores and 8-bit codes carry half the bytes per
+    // row, so a stage holds 32 rows (two 16-row halves) to keep the cost of
+    // a stage's wait and release per byte
+    static constexpr int H = H_, R = R_, TS = (GS_ || Q8_) ? 32 : 16, STAGES = STAGES_;
     static constexpr bool Q8 = Q8_, GS = GS_;
     static constexpr int EB = Q8 ? 1 : 2;    // bytes per cache element
     static constexpr int DH = 128;
@@ -69,7 +70,7 @@ struct FastCfg {
     static constexpr int OFF_SC = S_BYTES + R_BYTES;
     static constexpr int SC_TX = TS * H * 4;
     static constexpr int STAGE_TX = GS ? S_BYTES + R_BYTES : 2 * S_BYTES + 2 * R_BYTES;
-    static constexpr int STAGE = STAGE_TX + (GS ? (SC_TX + 1023) / 1024 * 1024 : 1024);
+    static constexpr int STAGE = STAGE_TX + (GS ? (SC_TX + 1023) / 1024 * 1024 : (NK_TX + 1023) / 1024 * 1024);
     static constexpr int KSP = HPW * R / 16;  // k-steps (and m-tiles) of a warp's private columns
     static constexpr int OFF_BAR = STAGES * STAGE;   // full[STAGES]
     static constexpr int OFF_CNT = OFF_BAR + 64;     // release counters[STAGES]
@@ -85,7 +86,7 @@ struct FastCfg {
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
     static_assert(STAGES <= 8, "barrier, counter and flag arrays hold 8 stages");
-    static_assert(GS || (NK_TX <= 1024 && (H * 2) % 16 == 0), "norm rows fit their slot; 16-byte TMA rows");
+    static_assert((H * 2) % 16 == 0, "16-byte TMA rows of norms");
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(!(GS && Q8), "given scores come with bf16 caches");
@@ -498,8 +499,9 @@ __device__ __forceinline__ uint32_t f16x2_hi(uint32_t w) {
 }
 
 // Scores of a tile: c[row x head] = fS . (S_K . Q^T) + fR . (R_K . blockdiag(p)^T).
+// rb: first stage row of the 16-row half being scored.
 template <class C>
-__device__ __forceinline__ void q8_scores(const uint8_t *st, int warp, int gq, int tq,
+__device__ __forceinline__ void q8_scores(const uint8_t *st, int rb, int warp, int gq, int tq,
                                           const uint32_t (&qb)[8][2],
                                           const uint32_t (&pb)[C::KSP][2], const float (&fS)[2],
                                           const float (&fR)[2], float (&c)[4]) {
@@ -507,8 +509,8 @@ __device__ __forceinline__ void q8_scores(const uint8_t *st, int warp, int gq, i
     const uint8_t *sk = st + C::OFF_SK, *rk = st + C::OFF_RK;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t w0 = lds_u32(sk + box_chunk(gq, ks) + 4 * tq);
-        const uint32_t w1 = lds_u32(sk + box_chunk(gq + 8, ks) + 4 * tq);
+        const uint32_t w0 = lds_u32(sk + box_chunk_rows<C::TS>(rb + gq, ks) + 4 * tq);
+        const uint32_t w1 = lds_u32(sk + box_chunk_rows<C::TS>(rb + gq + 8, ks) + 4 * tq);
         const uint32_t a[4] = {f16x2_lo(w0), f16x2_lo(w1), f16x2_hi(w0), f16x2_hi(w1)};
         if (ks & 1) mma_f16_16816(c1, a, qb[ks][0], qb[ks][1]);
         else mma_f16_16816(c, a, qb[ks][0], qb[ks][1]);
@@ -516,8 +518,8 @@ __device__ __forceinline__ void q8_scores(const uint8_t *st, int warp, int gq, i
     const int cw = warp * (C::HPW * C::R / 16);  // first 16-byte chunk of the warp's columns
 #pragma unroll
     for (int ks = 0; ks < C::KSP; ++ks) {
-        const uint32_t w0 = lds_u32(rk + box_chunk(gq, cw + ks) + 4 * tq);
-        const uint32_t w1 = lds_u32(rk + box_chunk(gq + 8, cw + ks) + 4 * tq);
+        const uint32_t w0 = lds_u32(rk + box_chunk_rows<C::TS>(rb + gq, cw + ks) + 4 * tq);
+        const uint32_t w1 = lds_u32(rk + box_chunk_rows<C::TS>(rb + gq + 8, cw + ks) + 4 * tq);
         const uint32_t a[4] = {f16x2_lo(w0), f16x2_lo(w1), f16x2_hi(w0), f16x2_hi(w1)};
         if (ks & 1) mma_f16_16816(c3, a, pb[ks][0], pb[ks][1]);
         else mma_f16_16816(c2, a, pb[ks][0], pb[ks][1]);
@@ -543,17 +545,19 @@ __device__ __forceinline__ void q8_pair_frags(uint32_t w0, uint32_t w1, uint32_t
 }
 
 // Values of a tile: accS += S_V^T . P^T, accR += R_V^T(warp columns) . P^T.
+// rb: first stage row of the 16-row half being reduced.
 template <class C, bool MASK>
-__device__ __forceinline__ void q8_values(const uint8_t *st, int warp, int gq, int tq, uint32_t m01,
-                                          uint32_t m89, uint32_t b0, uint32_t b1,
+__device__ __forceinline__ void q8_values(const uint8_t *st, int rb, int warp, int gq, int tq,
+                                          uint32_t m01, uint32_t m89, uint32_t b0, uint32_t b1,
                                           float (&accS)[8][4], float (&accR)[C::KSP][4]) {
     const uint8_t *sv = st + C::OFF_SV, *rv = st + C::OFF_RV;
-    const int r0 = 2 * tq, r1 = r0 + 1, r8 = r0 + 8, r9 = r0 + 9;
+    const int r0 = rb + 2 * tq, r1 = r0 + 1, r8 = r0 + 8, r9 = r0 + 9;
+    auto bc = [](int j, int ch) { return box_chunk_rows<C::TS>(j, ch); };
     auto pair = [&](const uint8_t *t, int cb, float (&d0)[4], float (&d1)[4]) {
         const int ch = cb >> 4, o = cb & 15;
         uint32_t a[4], a2[4];
-        q8_pair_frags<MASK>(lds_u32(t + box_chunk(r0, ch) + o), lds_u32(t + box_chunk(r1, ch) + o),
-                            lds_u32(t + box_chunk(r8, ch) + o), lds_u32(t + box_chunk(r9, ch) + o),
+        q8_pair_frags<MASK>(lds_u32(t + bc(r0, ch) + o), lds_u32(t + bc(r1, ch) + o),
+                            lds_u32(t + bc(r8, ch) + o), lds_u32(t + bc(r9, ch) + o),
                             m01, m89, a, a2);
         mma_f16_16816(d0, a, b0, b1);
         mma_f16_16816(d1, a2, b0, b1);
@@ -566,8 +570,8 @@ __device__ __forceinline__ void q8_values(const uint8_t *st, int warp, int gq, i
     if constexpr (C::KSP & 1) {
         constexpr int mt = C::KSP - 1;
         const int cb = cwb + 16 * mt + 2 * gq, ch = cb >> 4, o = cb & 15;
-        const uint32_t h0 = lds_u16(rv + box_chunk(r0, ch) + o), h1 = lds_u16(rv + box_chunk(r1, ch) + o);
-        const uint32_t h8 = lds_u16(rv + box_chunk(r8, ch) + o), h9 = lds_u16(rv + box_chunk(r9, ch) + o);
+        const uint32_t h0 = lds_u16(rv + bc(r0, ch) + o), h1 = lds_u16(rv + bc(r1, ch) + o);
+        const uint32_t h8 = lds_u16(rv + bc(r8, ch) + o), h9 = lds_u16(rv + bc(r9, ch) + o);
         const uint32_t x01 = prmt<0x5140>(h0, h1), x89 = prmt<0x5140>(h8, h9);
         uint32_t a[4] = {f16x2_lo(x01), f16x2_hi(x01), f16x2_lo(x89), f16x2_hi(x89)};
         if (MASK) { a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89; }
@@ -892,7 +896,7 @@ __global__ void __launch_bounds__(C::NT, 1)
             if constexpr (C::GS) {
                 // given scores: read per lane in the softmax below
             } else if constexpr (C::Q8) {
-                q8_scores<C>(st, warp, gq, tq, qb, pbh, fS, fR, c);
+                q8_scores<C>(st, 16 * h2, warp, gq, tq, qb, pbh, fS, fR, c);
             } else {
                 float c1[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
                 float c3[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1008,8 +1012,8 @@ __global__ void __launch_bounds__(C::NT, 1)
                     m89 = (ok(2 * tq + 8) ? 0x0000ffffu : 0u) | (ok(2 * tq + 9) ? 0xffff0000u : 0u);
                 }
                 if constexpr (C::Q8) {
-                    if (partial) q8_values<C, true>(st, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
-                    else q8_values<C, false>(st, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
+                    if (partial) q8_values<C, true>(st, 16 * h2, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
+                    else q8_values<C, false>(st, 16 * h2, warp, gq, tq, m01, m89, fh0, fh1, accS, accR);
                 } else {
                 const int rr = (mi >> 1) * 8 + (lane & 7);
                 const uint32_t svb = smem_u32(st + C::OFF_SV);
@@ -1597,11 +1601,11 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
         return cudaErrorInvalidValue;
     if (GS) {
         if (!make_row_map(&maps.nk, a.rope_ws.sc, a.rope_ws.sc_rows, H, 4, C::TS)) return cudaErrorInvalidValue;
-    } else if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB) ||
-               !make_map(&maps.rk, c.R_K, rows, H * R, C::EB)) {
+    } else if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB, 0, false, C::TS) ||
+               !make_map(&maps.rk, c.R_K, rows, H * R, C::EB, 0, false, C::TS)) {
         return cudaErrorInvalidValue;
     }
-    if (!GS && c.N_K && !make_row_map(&maps.nk, c.N_K, rows, H, 2)) return cudaErrorInvalidValue;
+    if (!GS && c.N_K && !make_row_map(&maps.nk, c.N_K, rows, H, 2, C::TS)) return cudaErrorInvalidValue;
     auto kern = decode_split_fast_kernel<C>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -1617,7 +1621,9 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
 #define LRKV_FAST_SHAPES(X) X(16, 16) X(16, 32) X(16, 48) X(16, 56) X(16, 64) X(32, 16) X(32, 32)
 
 bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype) {
-    if ((dtype != LRKV_BF16 && dtype != LRKV_FP8_E4M3) || d_h != 128 || page_size % 16 != 0)
+    // a tile (16 rows, 32 for 8-bit codes) stays inside a page
+    if ((dtype != LRKV_BF16 && dtype != LRKV_FP8_E4M3) || d_h != 128 ||
+        page_size % (dtype == LRKV_FP8_E4M3 ? 32 : 16) != 0)
         return false;
     if (!get_encode_tiled()) return false;
 #define X(h, rr) if (H == h && r == rr) return true;
