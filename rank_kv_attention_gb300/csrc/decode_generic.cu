@@ -118,13 +118,8 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == (unsigned)H) {
-        // completion counters of this row group's requests start at zero, and
-        // requests with an invalid length get a zero output (no segment
-        // will ever write it)
-        for (int i = tid; i < nrows * kHeadGroups; i += blockDim.x) {
-            const int b = blockIdx.y * nrows + i / kHeadGroups;
-            if (b < B) ws.done[(size_t)b * kHeadGroups + i % kHeadGroups] = 0;
-        }
+        // requests with an invalid length get a zero output (no segment will
+        // ever write it)
         __shared__ int bad_len[kProRows];
         if (tid < nrows) {
             const int b = blockIdx.y * nrows + tid;

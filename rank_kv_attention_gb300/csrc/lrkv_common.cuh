@@ -32,8 +32,7 @@ constexpr int kPlanTileAlign = 16;
 
 // Workspace layout of lrkv_decode (all offsets 256-byte aligned):
 //   [plan header + off[B+1]] [p: B*H*r f32] [ml: slots*H*2 f32]
-//   [acc: slots*H*(d_h+r) f32] [done: B*kHeadGroups int32]
-constexpr int kHeadGroups = 16;  // completion counters per request (one per head group)
+//   [acc: slots*H*(d_h+r) f32]
 
 struct DecodeWs {
     DecodePlan *plan;
@@ -41,7 +40,6 @@ struct DecodeWs {
     float *p;
     float *ml;
     float *acc;
-    int32_t *done;
     size_t bytes;
 };
 
@@ -62,8 +60,6 @@ __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, i
     o += align256(sizeof(float) * slots * H * 2);
     w.acc = reinterpret_cast<float *>(p + o);
     o += align256(sizeof(float) * slots * H * (size_t)(d_h + r));
-    w.done = reinterpret_cast<int32_t *>(p + o);
-    o += align256(sizeof(int32_t) * (size_t)B * kHeadGroups);
     w.bytes = o;
     return w;
 }
