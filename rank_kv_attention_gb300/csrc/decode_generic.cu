@@ -91,14 +91,15 @@ __device__ void rope_fast_operands(const float *bk, const float *qs, int nb, int
 }
 
 // ROPE: the exact-RoPE tensor-core operands instead of p (one request per
-// block row).
-template <typename T, bool ROPE>
-__global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
+// block row).  NTHR: threads per block; 128-thread blocks (one request each,
+// at most 51 registers a thread) fit on an SM beside a tensor-core split CTA.
+template <typename T, bool ROPE, int NTHR>
+__global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_kernel(
     const T *__restrict__ q, const T *__restrict__ B_K, const int32_t *__restrict__ seq_lens,
     T *__restrict__ out,
     int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, int len_shift,
     DecodeWs ws, int32_t *status, const float2 *__restrict__ rope_tab, RopeFastWs rf) {
-    constexpr int nrows = ROPE ? 1 : kProRows;
+    constexpr int nrows = (ROPE || NTHR == 128) ? 1 : kProRows;
     const int tid = threadIdx.x;
     if (blockIdx.x < (unsigned)H) {
         // warm L2 with this block's B_K[h] and query rows while the
@@ -137,15 +138,15 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
                     Elem<T>::store(out + (size_t)(blockIdx.y * nrows + bb) * H * d_h + i, 0.f);
         if (blockIdx.y != 0) return;
         // --- plan: exclusive scan of validated lengths ---
-        __shared__ int32_t part[kProThreads];
+        __shared__ int32_t part[NTHR];
         const int per = (B + blockDim.x - 1) / blockDim.x;
         const int lo = tid * per, hi = min(B, lo + per);
         int32_t s = 0;
         for (int b = lo; b < hi; ++b) s += streamed_len(seq_lens[b], max_len, len_shift);
         part[tid] = s;
         __syncthreads();
-        constexpr int NPL = kProThreads / 32;  // partial sums per lane
-        if (tid < 32) {  // warp scan of the kProThreads partial sums
+        constexpr int NPL = NTHR / 32;  // partial sums per lane
+        if (tid < 32) {  // warp scan of the NTHR partial sums
             int32_t v[NPL], run = 0;
 #pragma unroll
             for (int i = 0; i < NPL; ++i) { v[i] = part[tid * NPL + i]; run += v[i]; }
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
     const int nb = min(nrows, B - b0);
     extern __shared__ float sm[];
     float *bk = sm;                               // [d_h][r] when staged
-    float *qs = bk + (staged ? d_h * r : 0);      // [kProRows][d_h]
+    float *qs = bk + (staged ? d_h * r : 0);      // [nrows][d_h]
     const T *src = B_K + (size_t)h * d_h * r;
     // query rows (one 16-byte vector per thread in flight) overlap the B_K staging
     constexpr int V = Vec16<T>::N;
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(kProThreads) decode_prologue_kernel(
     __syncthreads();
     if constexpr (ROPE) {  // exact RoPE on the tensor cores: rotated queries and W
         rope_fast_operands(bk, qs, nb, b0, h, H, d_h, r, seq_lens, max_len, rope_tab, rf,
-                           qs + kProRows * d_h);
+                           qs + nrows * d_h);
         return;
     }
     if (staged) {
@@ -778,27 +779,35 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
 // Host launchers
 // ---------------------------------------------------------------------------
 template <typename T>
-cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align) {
+cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align,
+                            bool beside_split) {
     const auto &c = a.cache;
-    // the rotary operands (W is d_h x r per request and head) take one block
-    // per (head, request); p = q B_K amortises B_K's staging over 8 requests
+    // the rotary operands (W is d_h x r per request and head) take one 256-
+    // thread block per (head, request); before the tensor-core split kernel,
+    // p = q B_K runs in 128-thread blocks of one request each, which fit on
+    // an SM beside a split CTA (so no split CTA waits for a prologue block to
+    // leave); otherwise a block amortises B_K's staging over 8 requests
     const bool rope_fast = a.rope_ws.wf != nullptr;
-    const int nrows = rope_fast ? 1 : kProRows;
+    const bool small = !rope_fast && beside_split;
+    const int nrows = (rope_fast || small) ? 1 : kProRows;
     dim3 grid(c.H + 1, (a.B + nrows - 1) / nrows);
     const bool staged = (size_t)c.d_h * c.r <= kStageFloats;
-    const size_t sm = sizeof(float) * ((staged ? (size_t)c.d_h * c.r : 0) + (size_t)kProRows * c.d_h +
+    const size_t sm = sizeof(float) * ((staged ? (size_t)c.d_h * c.r : 0) + (size_t)nrows * c.d_h +
                                        (rope_fast ? (size_t)c.d_h * (c.r + 1) : 0));
     // the tensor-core rotary path treats a request past the table's end as an
     // invalid length (zero output, flagged), like every kernel after it
     const int max_len = decode_max_len(a);
-    auto kern = rope_fast ? decode_prologue_kernel<T, true> : decode_prologue_kernel<T, false>;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[rope_fast]) {
+    const int kind = rope_fast ? 1 : small ? 2 : 0;
+    auto kern = rope_fast ? decode_prologue_kernel<T, true, kProThreads>
+              : small     ? decode_prologue_kernel<T, false, 128>
+                          : decode_prologue_kernel<T, false, kProThreads>;
+    static bool attr_set[3] = {false, false, false};
+    if (!attr_set[kind]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
-        attr_set[rope_fast] = true;
+        attr_set[kind] = true;
     }
-    return launch_pdl(kern, grid, dim3(kProThreads), sm, a.stream,
+    return launch_pdl(kern, grid, dim3(small ? 128 : kProThreads), sm, a.stream,
                       static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
                       static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
                       max_len, G, tile_align, staged, a.X ? 1 : 0, ws, a.status,
@@ -905,8 +914,8 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G) {
                       staged, ws, static_cast<T *>(a.out), st);
 }
 
-template cudaError_t launch_prologue<float>(const DecodeArgs &, const DecodeWs &, int, int);
-template cudaError_t launch_prologue<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int, int);
+template cudaError_t launch_prologue<float>(const DecodeArgs &, const DecodeWs &, int, int, bool);
+template cudaError_t launch_prologue<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int, int, bool);
 template cudaError_t launch_split_generic<float>(const DecodeArgs &, const DecodeWs &, int);
 template cudaError_t launch_split_generic<__nv_bfloat16>(const DecodeArgs &, const DecodeWs &, int);
 template cudaError_t launch_combine<float>(const DecodeArgs &, const DecodeWs &, int);

@@ -61,8 +61,10 @@ __host__ __device__ __forceinline__ int32_t streamed_len(int32_t L, int max_len,
     return (L < 1 || L > max_len) ? 0 : L - shift;
 }
 
+// beside_split: the tensor-core split kernel follows (smaller prologue blocks).
 template <typename T>
-cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align);
+cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int tile_align,
+                            bool beside_split);
 template <typename T>
 cudaError_t launch_split_generic(const DecodeArgs &a, const DecodeWs &ws, int G);
 template <typename T>

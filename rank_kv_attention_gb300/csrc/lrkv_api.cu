@@ -118,7 +118,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     const int G = fast ? geo.G_fast : geo.G_gen;
     cudaError_t e;
     if (c.dtype != LRKV_F32) {  // bf16 activations (bf16 or 8-bit cache)
-        e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign);
+        e = launch_prologue<__nv_bfloat16>(a, ws, G, kPlanTileAlign, fast);
         if (e == cudaSuccess && rope_fast) {
             prof_before(LRKV_PROFILE_SCORES, a.stream);
             e = launch_rope_scores(a, ws);
@@ -131,7 +131,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
         }
         if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws, G);
     } else {
-        e = launch_prologue<float>(a, ws, G, kPlanTileAlign);
+        e = launch_prologue<float>(a, ws, G, kPlanTileAlign, false);
         if (e == cudaSuccess) {
             prof_before(LRKV_PROFILE_ATTENTION, a.stream);
             e = launch_split_generic<float>(a, ws, G);
