@@ -9,3 +9,4 @@ from .lrkv_oracle import *  # noqa: F401,F403
 from . import fp8  # noqa: F401  (8-bit cache storage)
 from . import rope  # noqa: F401  (exact rotary position embedding)
 from . import norm  # noqa: F401  (joint RMSNorm of the keys)
+from . import grouped  # noqa: F401  (a shared basis per group of heads)
