@@ -48,6 +48,10 @@ WORKLOADS = {
     "decode_T4096_norm": "decode_T4096 with joint key RMSNorm (section 8): a bf16 reciprocal per "
                          "head and token multiplies each score; the step appends the rows, stores "
                          "their reciprocals (lrkv_key_norms) and decodes",
+    "decode_T4096_g2": "decode_T4096 with one shared basis per group of heads (section 3): G=2 "
+                       "groups of 8 consecutive heads, each token caches 2 shared rows of d_h=128 "
+                       "and r=32 private ranks per head (payload ratio 3/8 of multi-head "
+                       "attention, against 7/16 for one basis with r=48), bf16",
     "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
                     "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
@@ -201,7 +205,8 @@ def run_ours(args, rank, world, local_rank):
     c = workload_shape(name)
     case = I.config_decode_case(name)
     Bn, H, d_h, r, d = case.B, case.H, case.d_h, case.r, c["d"]
-    w = I.make_weights(d, H, d_h, r, "bf16", seed=1)
+    G = case.groups
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=1, groups=G)
     x_new = I.make_append_case([1] * Bn, case.seq_lens - 1, d, seed=2).X
 
     def to_dev(a, kind="bf16"):
@@ -399,9 +404,9 @@ def run_ours(args, rank, world, local_rank):
     tokens = world * Bn * K
     value = tokens / (total_ms / 1e3)
     seq_total = int(case.seq_lens.astype(np.int64).sum())
-    split_bytes = seq_total * (2 * (d_h + H * r) * eb + (2 * H if norm else 0))  # cache rows read once
+    split_bytes = seq_total * (2 * (G * d_h + H * r) * eb + (2 * H if norm else 0))  # cache rows read once
     step_bytes = (split_bytes + 2 * H * d_h * r * 2 + 2 * Bn * H * d_h * 2   # + bases, q, out
-                  + (2 * d_h + 2 * H * r) * d * 2 + Bn * d * 2)             # + append W, X
+                  + (2 * G * d_h + 2 * H * r) * d * 2 + Bn * d * 2)         # + append W, X
     peak, peak_kind = measured_peaks()
     achieved = split_bytes / (split_ms / 1e3) / 1e9
     # rotary path: the score kernel's contractions per key and head, the
@@ -419,7 +424,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 cache, f16 mma inputs" if eb == 1 else "bf16", "data": "synthetic",
         "config": {"workload": f"{name}: {WORKLOADS[name]}", "B": Bn, "d": d, "H": H, "d_h": d_h,
-                   "r": r, "seq_len": max_seq, "cached_rows": seq_total,
+                   "r": r, "groups": G, "seq_len": max_seq, "cached_rows": seq_total,
                    "parallelism": f"replicas x{world} (requests are independent)",
                    "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
                          f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",

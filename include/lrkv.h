@@ -103,6 +103,18 @@ enum {
  * lrkv_prefill and lrkv_decode_step for the rows they append).  A
  * per-channel gain and the query's own normalisation belong to q.  Costs one
  * scalar per head and token, 1/(2 d_h) of a dense K/V cache.
+ *
+ * Grouped shared basis (reading note, section 3 after equations 2-5: a basis
+ * per group of heads whose needs differ): with G > 1 the heads form G groups
+ * of H/G consecutive heads, each with its own shared projection, and a token
+ * caches G shared rows:
+ *     S_K, S_V : [num_pages, page_size, G, d_h]   (group-major)
+ * head h reads group h / (H/G):  K_h = S_K[.., h/(H/G), :] + R_K[h] B_K[h]^T.
+ * The shared weights of lrkv_append / lrkv_prefill / lrkv_decode_step are
+ * then W_S_K, W_S_V [G*d_h, d] (group-major rows).  G must divide H; 0 and 1
+ * both mean one shared basis.  The tiled prefill, the fused decode step and
+ * the tensor-core rotary decode serve G = 1 (other G take the per-row and
+ * generic kernels); the tensor-core decode covers G = 1 and G = 2.
  */
 typedef struct {
     void *S_K;
@@ -118,6 +130,7 @@ typedef struct {
     float scale[4]; /* LRKV_FP8_E4M3: scale of S_K, S_V, R_K, R_V (positive, finite) */
     void *N_K;      /* NULL, or the reciprocal key norms [num_pages, page_size, H] */
     float norm_eps; /* N_K: eps of the root mean square (finite, >= 0) */
+    int32_t G;      /* shared key/value groups (0 or 1: one shared basis) */
 } lrkv_cache_t;
 
 /*
@@ -367,6 +380,9 @@ LRKV_API int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_r
  * Returns 0 for invalid arguments.
  */
 LRKV_API size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype);
+/* The same with G shared groups: tokens * 2 * (G*d_h + H*r) * sizeof(dtype). */
+LRKV_API size_t lrkv_cache_bytes_grouped(int32_t H, int32_t d_h, int32_t r, int32_t G,
+                                         int64_t tokens, int32_t dtype);
 
 /* Human-readable name of an LRKV_E_* code. */
 LRKV_API const char *lrkv_status_string(int status);

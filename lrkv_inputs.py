@@ -165,7 +165,7 @@ class DecodeCase:
     page_table: np.ndarray     # [B, max_pages] int32
     num_pages: int
     q: np.ndarray              # [B, H, d_h]
-    S_K: np.ndarray            # [num_pages, page_size, d_h]
+    S_K: np.ndarray            # [num_pages, page_size, d_h] (or [.., G, d_h]: G groups)
     S_V: np.ndarray
     R_K: np.ndarray            # [num_pages, page_size, H, r]
     R_V: np.ndarray
@@ -181,6 +181,11 @@ class DecodeCase:
     def max_pages(self):
         return int(self.page_table.shape[1])
 
+    @property
+    def groups(self):
+        """Shared key/value groups (1: one shared basis)."""
+        return int(self.S_K.shape[2]) if self.S_K.ndim == 4 else 1
+
     def rows(self, b):
         """(page ids, valid tokens) of request b, in token order."""
         L = int(self.seq_lens[b])
@@ -191,7 +196,7 @@ class DecodeCase:
 def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
                      shuffle=False, spare_pages=0, page_size=PAGE_SIZE,
                      q_std=1.0, cache_std=1.0, base_std=None,
-                     max_pages=None, fp8_scale=None) -> DecodeCase:
+                     max_pages=None, fp8_scale=None, groups=1) -> DecodeCase:
     """Decode inputs: a filled paged cache plus one query row per request.
 
     Queries and cache rows ~ N(0, q_std^2 / cache_std^2); bases ~ N(0, 1/r)
@@ -214,8 +219,10 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
     q = _draw(rng, (B, H, d_h), q_std, adt)
     B_K = _draw(rng, (H, d_h, r), base_std, adt)
     B_V = _draw(rng, (H, d_h, r), base_std, adt)
-    S_K = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc[0])
-    S_V = _draw_chunked(rng, (num_pages, page_size, d_h), cache_std, dtype, scale=sc[1])
+    # groups > 1: one shared row per group of heads, [pages, page_size, G, d_h]
+    s_shape = (num_pages, page_size, d_h) if groups == 1 else (num_pages, page_size, groups, d_h)
+    S_K = _draw_chunked(rng, s_shape, cache_std, dtype, scale=sc[0])
+    S_V = _draw_chunked(rng, s_shape, cache_std, dtype, scale=sc[1])
     R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc[2])
     R_V = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc[3])
     for pool in (S_K, S_V, R_K, R_V):
@@ -249,13 +256,14 @@ class ProjWeights:
     W_Q: np.ndarray     # [H, d_h, d]  (query projection, used by harnesses only)
 
 
-def make_weights(d, H, d_h, r, dtype="bf16", seed=0) -> ProjWeights:
-    """Projection weights ~ N(0, 1/d), bases ~ N(0, 1/r); W_Q drawn last."""
+def make_weights(d, H, d_h, r, dtype="bf16", seed=0, groups=1) -> ProjWeights:
+    """Projection weights ~ N(0, 1/d), bases ~ N(0, 1/r); W_Q drawn last.
+    groups > 1: the shared weights are [groups * d_h, d] (group-major rows)."""
     rng = np.random.default_rng(seed)
     sw = 1.0 / np.sqrt(d)
     sb = 1.0 / np.sqrt(r)
-    W_S_K = _draw(rng, (d_h, d), sw, dtype)
-    W_S_V = _draw(rng, (d_h, d), sw, dtype)
+    W_S_K = _draw(rng, (groups * d_h, d), sw, dtype)
+    W_S_V = _draw(rng, (groups * d_h, d), sw, dtype)
     U_K = _draw(rng, (H, r, d), sw, dtype)
     U_V = _draw(rng, (H, r, d), sw, dtype)
     B_K = _draw(rng, (H, d_h, r), sb, dtype)
@@ -300,7 +308,7 @@ def make_append_case(n_per_seq, start_pos, d, dtype="bf16", seed=0,
                       max(num_pages, 1), page_size)
 
 
-def empty_pools(num_pages, page_size, H, d_h, r, dtype, canary=True):
+def empty_pools(num_pages, page_size, H, d_h, r, dtype, canary=True, groups=1):
     """Cache pools filled with the canary (bit pattern) so untouched slots show."""
     if dtype == "bf16":
         fill = BF16_NAN_BITS if canary else np.uint16(0)
@@ -311,7 +319,8 @@ def empty_pools(num_pages, page_size, H, d_h, r, dtype, canary=True):
     else:
         fill = F32_NAN_CANARY if canary else np.float32(0)
         mk = lambda shape: np.full(shape, fill, dtype=np.float32)
-    return (mk((num_pages, page_size, d_h)), mk((num_pages, page_size, d_h)),
+    s_shape = (num_pages, page_size, d_h) if groups == 1 else (num_pages, page_size, groups, d_h)
+    return (mk(s_shape), mk(s_shape),
             mk((num_pages, page_size, H, r)), mk((num_pages, page_size, H, r)))
 
 
@@ -337,6 +346,10 @@ CONFIGS = {
     # the 16 x 4096 decode with joint key RMSNorm (a reciprocal per head and token)
     "decode_T4096_norm": dict(B=16, d=2048, H=16, d_h=128, r=48, T=4096, dtype="bf16", seed=0,
                               norm=True),
+    # the 16 x 4096 decode with a shared basis per group of 8 heads (2 groups)
+    # and private rank 32: 3072 B per token against 3584 for one basis, r = 48
+    "decode_T4096_g2": dict(B=16, d=2048, H=16, d_h=128, r=32, T=4096, dtype="bf16", seed=0,
+                            groups=2),
 }
 
 
@@ -353,4 +366,4 @@ def config_decode_case(name, seed=None, scale_T=None) -> DecodeCase:
                                 s, shuffle=True, spare_pages=3)
     T = c["T"] if scale_T is None else scale_T
     return make_decode_case(c["B"], c["H"], c["d_h"], c["r"], [T] * c["B"],
-                            c["dtype"], s, shuffle=False)
+                            c["dtype"], s, shuffle=False, groups=c.get("groups", 1))

@@ -32,7 +32,7 @@ def _run_pairs(pairs):
     import numpy as np
     import lrkv_inputs as I
     from . import lrkv_oracle as O
-    from . import fp8, norm, rope
+    from . import fp8, grouped, norm, rope
     c = _CASE
     f = lambda a: I.to_f64(a, c.act_dtype)
     if c.dtype == "fp8":  # 8-bit pools: codes times the pool's scale
@@ -44,6 +44,9 @@ def _run_pairs(pairs):
         pages, L = c.rows(b)
         sk = fp(O.gather_rows(c.S_K, pages, L, c.page_size), 0)
         sv = fp(O.gather_rows(c.S_V, pages, L, c.page_size), 1)
+        if c.groups > 1:  # pools [pages, page_size, G, d_h]: this head's group
+            g = grouped.group_of(h, c.H, c.groups)
+            sk, sv = sk[:, g, :], sv[:, g, :]
         rk = fp(O.gather_rows(c.R_K, pages, L, c.page_size)[:, h, :], 2)
         rv = fp(O.gather_rows(c.R_V, pages, L, c.page_size)[:, h, :], 3)
         K_h = O.expand_head(sk, rk, f(c.B_K[h]))

@@ -47,6 +47,7 @@ class CacheDesc(ctypes.Structure):
         ("H", ctypes.c_int32), ("d_h", ctypes.c_int32), ("r", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("scale", ctypes.c_float * 4),
         ("N_K", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+        ("G", ctypes.c_int32),
     ]
 
 
@@ -89,6 +90,7 @@ SIGNATURES = {
     "lrkv_prefill_rope": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P,
                                          P, I32, P, I32, P, P, SZ, P, P]),
     "lrkv_cache_bytes": (SZ, [I32, I32, I32, ctypes.c_int64, I32]),
+    "lrkv_cache_bytes_grouped": (SZ, [I32, I32, I32, I32, ctypes.c_int64, I32]),
     "lrkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "lrkv_last_cuda_error": (ctypes.c_int, []),
     "lrkv_version": (ctypes.c_int, []),

@@ -42,7 +42,9 @@ def _need(t, name, dtype=None, device=True):
 class PagedCache:
     """Caller-owned paged factored cache (four pools sharing page ids).
 
-    S_K, S_V: [num_pages, page_size, d_h]; R_K, R_V: [num_pages, page_size, H, r].
+    S_K, S_V: [num_pages, page_size, d_h], or [num_pages, page_size, G, d_h]
+    for G shared groups (head h reads group h // (H // G)); R_K, R_V:
+    [num_pages, page_size, H, r].
     Pools of torch.float8_e4m3fn hold 8-bit codes whose values are the codes
     times ``scale`` (one scale per pool: S_K, S_V, R_K, R_V); the activations
     used with such a cache are bf16.  ``N_K`` ([num_pages, page_size, H] in
@@ -58,10 +60,15 @@ class PagedCache:
     norm_eps: float = 0.0
 
     @classmethod
-    def empty(cls, num_pages, page_size, H, d_h, r, dtype=torch.bfloat16, device="cuda"):
+    def empty(cls, num_pages, page_size, H, d_h, r, dtype=torch.bfloat16, device="cuda", groups=1):
         mk = lambda *s: torch.empty(s, dtype=dtype, device=device)
-        return cls(mk(num_pages, page_size, d_h), mk(num_pages, page_size, d_h),
-                   mk(num_pages, page_size, H, r), mk(num_pages, page_size, H, r))
+        sh = (num_pages, page_size, d_h) if groups == 1 else (num_pages, page_size, groups, d_h)
+        return cls(mk(*sh), mk(*sh), mk(num_pages, page_size, H, r), mk(num_pages, page_size, H, r))
+
+    @property
+    def groups(self):
+        """Shared key/value groups (1: one shared basis)."""
+        return self.S_K.shape[2] if self.S_K.dim() == 4 else 1
 
     @property
     def dtype(self):
@@ -75,8 +82,10 @@ class PagedCache:
     def desc(self) -> _abi.CacheDesc:
         for n in ("S_K", "S_V", "R_K", "R_V"):
             _need(getattr(self, n), n, self.dtype)
-        npg, ps, d_h = self.S_K.shape
+        npg, ps, d_h = self.S_K.shape[0], self.S_K.shape[1], self.S_K.shape[-1]
         _, _, H, r = self.R_K.shape
+        if tuple(self.S_V.shape) != tuple(self.S_K.shape):
+            raise ValueError("S_K and S_V must have the same shape")
         if self.N_K is not None:
             _need(self.N_K, "N_K", self.act_dtype)
             if tuple(self.N_K.shape) != (npg, ps, H):
@@ -85,7 +94,7 @@ class PagedCache:
                               self.R_V.data_ptr(), npg, ps, H, d_h, r, _DT[self.dtype],
                               (ctypes.c_float * 4)(*[float(x) for x in self.scale]),
                               self.N_K.data_ptr() if self.N_K is not None else None,
-                              float(self.norm_eps))
+                              float(self.norm_eps), self.groups)
 
 
 def prefill_kernel_kind(cache: PagedCache) -> int:
@@ -98,8 +107,8 @@ def prefill_kernel_kind(cache: PagedCache) -> int:
     return st
 
 
-def cache_bytes(H, d_h, r, tokens, dtype=torch.bfloat16) -> int:
-    return int(_abi.lib().lrkv_cache_bytes(H, d_h, r, tokens, _DT[dtype]))
+def cache_bytes(H, d_h, r, tokens, dtype=torch.bfloat16, groups=1) -> int:
+    return int(_abi.lib().lrkv_cache_bytes_grouped(H, d_h, r, groups, tokens, _DT[dtype]))
 
 
 def decode_workspace_bytes(B, H, d_h, r, max_seq_len, dtype=torch.bfloat16) -> int:

@@ -428,7 +428,9 @@ __global__ void __launch_bounds__(256) key_norms_kernel(
     const int32_t *__restrict__ positions, const int32_t *__restrict__ seq_ids, int n,
     const T *__restrict__ B_K, const TC *__restrict__ S_K, const TC *__restrict__ R_K,
     T *__restrict__ N_K, const int32_t *__restrict__ page_table, int B, int max_pages, int num_pages,
-    int page_size, int H, int d_h, int r, float sk_scale, float rk_scale, float eps, int32_t *status) {
+    int page_size, int H, int d_h, int r, float sk_scale, float rk_scale, float eps, int32_t *status,
+    int groups) {
+    // groups: shared key/value groups; head h reads group h / (H / groups)
     pdl_wait();
     pdl_launch_dependents();
     __shared__ float zs[8][256];
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(256) key_norms_kernel(
     // for every supported dtype and B_K is 16-byte aligned), all in flight
     constexpr int V = Vec16<T>::N;
     for (int d = lane; d < d_h; d += 32) {
-        float kd = CacheLoad<TC>::load(S_K + prow * d_h + d) * sk_scale;
+        float kd = CacheLoad<TC>::load(S_K + (prow * groups + h / (H / groups)) * d_h + d) * sk_scale;
         const T *row = bk + (size_t)d * r;
         for (int k = 0; k < r; k += V) {
             float bv[V];
@@ -481,18 +483,19 @@ cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, i
                           seq_ids, n, static_cast<const float *>(B_K), static_cast<const float *>(c.S_K),
                           static_cast<const float *>(c.R_K), static_cast<float *>(c.N_K), page_table, B,
                           max_pages, c.num_pages, c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps,
-                          status);
+                          status, cache_groups(c));
     if (c.dtype == LRKV_FP8_E4M3)
         return launch_pdl(key_norms_kernel<__nv_bfloat16, uint8_t>, dim3(blocks), dim3(256), 0, s,
                           positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
                           static_cast<const uint8_t *>(c.S_K), static_cast<const uint8_t *>(c.R_K),
                           static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
-                          c.page_size, c.H, c.d_h, c.r, c.scale[0], c.scale[2], c.norm_eps, status);
+                          c.page_size, c.H, c.d_h, c.r, c.scale[0], c.scale[2], c.norm_eps, status,
+                          cache_groups(c));
     return launch_pdl(key_norms_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
                       positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
                       static_cast<const __nv_bfloat16 *>(c.S_K), static_cast<const __nv_bfloat16 *>(c.R_K),
                       static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
-                      c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps, status);
+                      c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps, status, cache_groups(c));
 }
 
 }  // namespace lrkv

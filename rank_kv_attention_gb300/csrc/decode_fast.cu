@@ -44,13 +44,15 @@ constexpr int kLocalReq = 64;  // requests whose offsets fit in pl[16 .. 16 + kL
 // Q8_: the cache holds 8-bit E4M3 codes (one byte per element) instead of bf16.
 // GS_: the scores are given (written by the rotary score kernel): a stage
 // holds S_V, R_V and the tile's 16 x H fp32 scores, no S_K or R_K.
-template <int H_, int R_, int STAGES_, bool Q8_ = false, bool GS_ = false>
+// NGRP_: shared key/value groups (a token's shared rows hold NGRP x d_h).
+template <int H_, int R_, int STAGES_, bool Q8_ = false, bool GS_ = false, int NGRP_ = 1>
 struct FastCfg {
     // rows per stage: given scores and 8-bit codes carry half the bytes per
     // row, so a stage holds 32 rows (two 16-row halves) to keep the cost of
     // a stage's wait and release per byte
     static constexpr int H = H_, R = R_, TS = (GS_ || Q8_) ? 32 : 16, STAGES = STAGES_;
     static constexpr bool Q8 = Q8_, GS = GS_;
+    static constexpr int NGRP = NGRP_;
     static constexpr int EB = Q8 ? 1 : 2;    // bytes per cache element
     static constexpr int DH = 128;
     static constexpr int NCW = 8, NT = NCW * 32;
@@ -58,7 +60,8 @@ struct FastCfg {
     static constexpr int NH = HPW / 2;       // head slots per thread
     static constexpr int RC = R / 8;         // 16-byte chunks per private row
     static constexpr int BOX = TS * 128;     // one 16-row x 128-byte swizzled box
-    static constexpr int NBOX_S = DH * EB / 128;
+    static constexpr int NBOX_S = NGRP * DH * EB / 128;  // all groups' shared columns
+    static constexpr int GCH = DH * EB / 16;                // 16-byte chunks of one group's row
     static constexpr int NBOX_R = H * R * EB / 128;
     static constexpr int S_BYTES = NBOX_S * BOX, R_BYTES = NBOX_R * BOX;
     static constexpr int OFF_SK = 0, OFF_SV = GS ? 0 : S_BYTES, OFF_RK = 2 * S_BYTES;
@@ -90,6 +93,8 @@ struct FastCfg {
     static_assert((HPW * R) % 16 == 0, "a warp's private columns form whole mma k-steps");
     static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
     static_assert(!(GS && Q8), "given scores come with bf16 caches");
+    static_assert(NGRP == 1 || (!Q8 && !GS && H % NGRP == 0 && (H / NGRP) % HPW == 0),
+                  "a warp's heads share one group (bf16 caches)");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(C::NT, 1)
     }
     // fused step (bf16 caches): the new rows' staging copies go out first and
     // land while the plan below is computed
-    const bool fused = !C::Q8 && P.X != nullptr;
+    const bool fused = !C::Q8 && C::NGRP == 1 && P.X != nullptr;
     if (fused && tid == 0) {
         uint64_t *abar = reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR);
         mbar_init(abar, 1);
@@ -799,6 +804,8 @@ __global__ void __launch_bounds__(C::NT, 1)
 
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
     const int hl = lane >> 4, j = lane & 15;  // this lane's (head slot, tile row)
+    // first 16-byte chunk of the shared group of this warp's heads
+    const int sgc = (warp * C::HPW) / (C::H / C::NGRP) * C::GCH;
     int hd[C::NH];                            // heads of this lane's slots
 #pragma unroll
     for (int i = 0; i < C::NH; ++i) hd[i] = warp * C::HPW + hl + 2 * i;
@@ -906,7 +913,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a[4];
-                    ldmatrix_x4(skb + box_chunk_rows<C::TS>(16 * h2 + rr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4(skb + box_chunk_rows<C::TS>(16 * h2 + rr, sgc + 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
                     if (ks & 1) mma_bf16_16816(c1, a, qb[ks][0], qb[ks][1]);
                     else mma_bf16_16816(c, a, qb[ks][0], qb[ks][1]);
                 }
@@ -1020,7 +1027,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a[4];
-                    ldmatrix_x4_trans(svb + box_chunk_rows<C::TS>(16 * h2 + rr, 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
+                    ldmatrix_x4_trans(svb + box_chunk_rows<C::TS>(16 * h2 + rr, sgc + 2 * mt + (mi & 1)), a[0], a[1], a[2], a[3]);
                     a[0] &= m01; a[1] &= m01; a[2] &= m89; a[3] &= m89;
                     mma_bf16_16816(accS[mt], a, bh0, bh1);
                     mma_bf16_16816(accS[mt], a, bl0, bl1);
@@ -1541,10 +1548,10 @@ static bool make_row_map(CUtensorMap *map, const void *base, int64_t rows, int H
     });
 }
 
-template <int H, int R, bool Q8 = false, bool GS = false>
+template <int H, int R, bool Q8 = false, bool GS = false, int NGRP = 1>
 struct Pick {
-    static constexpr int stage = FastCfg<H, R, 1, Q8, GS>::STAGE;
-    static constexpr int misc = FastCfg<H, R, 1, Q8, GS>::SMEM - FastCfg<H, R, 1, Q8, GS>::OFF_BAR;
+    static constexpr int stage = FastCfg<H, R, 1, Q8, GS, NGRP>::STAGE;
+    static constexpr int misc = FastCfg<H, R, 1, Q8, GS, NGRP>::SMEM - FastCfg<H, R, 1, Q8, GS, NGRP>::OFF_BAR;
     static constexpr int fit = (227 * 1024 - misc) / stage;
     // deeper rings of large stages measured slower (more DRAM queueing for
     // the same consumption rate): 3 stages of >= 48 KB, else up to 4; the
@@ -1552,7 +1559,7 @@ struct Pick {
     // bytes in flight
     static constexpr int cap = (Q8 || GS) ? (stage >= 24 * 1024 ? 6 : 8) : (stage >= 48 * 1024 ? 3 : 4);
     static constexpr int STAGES = fit > cap ? cap : fit;
-    using Cfg = FastCfg<H, R, STAGES, Q8, GS>;
+    using Cfg = FastCfg<H, R, STAGES, Q8, GS, NGRP>;
 };
 
 // Parameters every kernel of the tensor-core decode reads.
@@ -1589,19 +1596,19 @@ static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
     return P;
 }
 
-template <int H, int R, bool Q8, bool GS = false>
+template <int H, int R, bool Q8, bool GS = false, int NGRP = 1>
 static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int G) {
-    using C = typename Pick<H, R, Q8, GS>::Cfg;
-    static_assert(Pick<H, R, Q8, GS>::STAGES >= 2, "at least double buffering");
+    using C = typename Pick<H, R, Q8, GS, NGRP>::Cfg;
+    static_assert(Pick<H, R, Q8, GS, NGRP>::STAGES >= 2, "at least double buffering");
     const auto &c = a.cache;
     FastMaps maps;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    if (!make_map(&maps.sv, c.S_V, rows, 128, C::EB, 0, false, C::TS) ||
+    if (!make_map(&maps.sv, c.S_V, rows, 128 * NGRP, C::EB, 0, false, C::TS) ||
         !make_map(&maps.rv, c.R_V, rows, H * R, C::EB, 0, false, C::TS))
         return cudaErrorInvalidValue;
     if (GS) {
         if (!make_row_map(&maps.nk, a.rope_ws.sc, a.rope_ws.sc_rows, H, 4, C::TS)) return cudaErrorInvalidValue;
-    } else if (!make_map(&maps.sk, c.S_K, rows, 128, C::EB, 0, false, C::TS) ||
+    } else if (!make_map(&maps.sk, c.S_K, rows, 128 * NGRP, C::EB, 0, false, C::TS) ||
                !make_map(&maps.rk, c.R_K, rows, H * R, C::EB, 0, false, C::TS)) {
         return cudaErrorInvalidValue;
     }
@@ -1620,7 +1627,18 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
 
 #define LRKV_FAST_SHAPES(X) X(16, 16) X(16, 32) X(16, 48) X(16, 56) X(16, 64) X(32, 16) X(32, 32)
 
-bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype) {
+// Shapes the tensor-core decode serves with two shared groups (bf16).
+#define LRKV_FAST_SHAPES_G2(X) X(16, 32) X(16, 48)
+
+bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype, int groups) {
+    if (groups == 2) {
+        if (dtype != LRKV_BF16 || d_h != 128 || page_size % 16 != 0 || !get_encode_tiled()) return false;
+#define X(h, rr) if (H == h && r == rr) return true;
+        LRKV_FAST_SHAPES_G2(X)
+#undef X
+        return false;
+    }
+    if (groups != 1) return false;
     // a tile (16 rows, 32 for 8-bit codes) stays inside a page
     if ((dtype != LRKV_BF16 && dtype != LRKV_FP8_E4M3) || d_h != 128 ||
         page_size % (dtype == LRKV_FP8_E4M3 ? 32 : 16) != 0)
@@ -1647,6 +1665,13 @@ bool fast_decode_step_fits(int H, int r, int d) {
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const int H = a.cache.H, r = a.cache.r;
     const bool q8 = a.cache.dtype == LRKV_FP8_E4M3, gs = a.rope_ws.wf != nullptr;
+    if (cache_groups(a.cache) == 2) {
+#define X(h, rr) \
+        if (H == h && r == rr) return launch_fast_cfg<h, rr, false, false, 2>(a, ws, G);
+        LRKV_FAST_SHAPES_G2(X)
+#undef X
+        return cudaErrorInvalidValue;
+    }
 #define X(h, rr)                                                                  \
     if (H == h && r == rr)                                                        \
         return gs ? launch_fast_cfg<h, rr, false, true>(a, ws, G)                 \

@@ -366,7 +366,8 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
     const TC *__restrict__ R_K, const TC *__restrict__ R_V, const int32_t *__restrict__ page_table,
     const int32_t *__restrict__ req_row, int max_pages, int num_pages, int page_size, int B, int H, int d_h, int r,
     float scale_log2, float4 sc, DecodeWs ws, int32_t *status, const T *__restrict__ B_K, RopeArgs rope,
-    const T *__restrict__ N_K) {
+    const T *__restrict__ N_K, int s_stride, int hpg) {
+    // s_stride: elements of a token's shared row (G d_h); hpg: heads per shared group
     extern __shared__ float sm[];
     float *qs = sm;                 // d_h
     float *ps = qs + d_h;           // r (plain) or A, Bq [d_h / 2][RP] each (rotary)
@@ -385,6 +386,8 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.x, h = blockIdx.y;
+    S_K += (size_t)(h / hpg) * d_h;  // this head's group of the shared rows
+    S_V += (size_t)(h / hpg) * d_h;
     pdl_wait();
     pdl_launch_dependents();
     const int32_t total = ws.plan->total, chunk = ws.plan->chunk;
@@ -464,7 +467,7 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     valid = false;
                 } else {
                     prow = page * page_size + j % page_size;
-                    const TC *sk = S_K + (size_t)prow * d_h;
+                    const TC *sk = S_K + (size_t)prow * s_stride;
                     const TC *rk = R_K + ((size_t)prow * H + h) * r;
                     float acc = 0.f;
                     if constexpr (RP == 0) {
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
                     float a = accS[i];
                     for (int jj = 0; jj < n; ++jj) {
                         if (row[jj] < 0) continue;
-                        a = fmaf(w[jj], CacheLoad<TC>::load(S_V + (size_t)row[jj] * d_h + d), a);
+                        a = fmaf(w[jj], CacheLoad<TC>::load(S_V + (size_t)row[jj] * s_stride + d), a);
                     }
                     accS[i] = a;
                 }
@@ -835,7 +838,7 @@ static cudaError_t launch_split_generic_t(const DecodeArgs &a, const DecodeWs &w
                       static_cast<const TC *>(c.R_K), static_cast<const TC *>(c.R_V), a.page_table,
                       a.req_row, a.max_pages, c.num_pages, c.page_size, a.B, c.H, c.d_h, c.r,
                       scale_log2, sc, ws, a.status, static_cast<const T *>(a.B_K), rope,
-                      static_cast<const T *>(c.N_K));
+                      static_cast<const T *>(c.N_K), cache_groups(c) * c.d_h, c.H / cache_groups(c));
 }
 
 template <typename T, typename TC>

@@ -73,7 +73,7 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G);
 // Tensor-core split kernel (bf16, d_h = 128, page_size % 16 == 0, selected
 // (H, r) pairs).  `fast_decode_supported` says whether a shape is covered;
 // `fast_decode_grid` is its CTA count on this device.
-bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype);
+bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype, int groups = 1);
 // Rows a fused decode step may append inside the split kernel, and whether
 // its staging (16 rows of X and 16 weight rows of d) fits a shape's ring.
 constexpr int kFusedStepMaxRows = 16;

@@ -78,6 +78,7 @@ static int check_cache(const lrkv_cache_t *c) {
     if (c->num_pages < 1 || c->page_size < 16 || c->page_size > 1024 || c->page_size % 16)
         return LRKV_E_SHAPE;
     if ((int64_t)c->num_pages * c->page_size > INT32_MAX / 2) return LRKV_E_SHAPE;
+    if (c->G < 0 || c->G > c->H || c->H % cache_groups(*c)) return LRKV_E_SHAPE;
     if (c->N_K && (!aligned16(c->N_K) || !(c->norm_eps >= 0.f) || !std::isfinite(c->norm_eps)))
         return LRKV_E_INVALID_ARG;
     if (c->dtype == LRKV_FP8_E4M3)
@@ -114,7 +115,8 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     DecodeWs ws = decode_ws_layout(workspace, a.B, c.H, c.d_h, c.r, geo.G_ws);
     if (ws_bytes < ws.bytes) return LRKV_E_WORKSPACE;
     const bool rope_fast = a.rope_ws.wf != nullptr;
-    const bool fast = rope_fast || (!a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype));
+    const bool fast = rope_fast || (!a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype,
+                                                                      cache_groups(c)));
     const int G = fast ? geo.G_fast : geo.G_gen;
     cudaError_t e;
     if (c.dtype != LRKV_F32) {  // bf16 activations (bf16 or 8-bit cache)
@@ -168,7 +170,7 @@ static AppendArgsT<T> make_append_args(const void *X, const int32_t *positions,
     a.num_pages = c->num_pages;
     a.page_size = c->page_size;
     a.H = c->H;
-    a.d_h = c->d_h;
+    a.d_h = c->d_h * cache_groups(*c);  // width of a token's shared row (all groups)
     a.r = c->r;
     a.status = status;
     a.stream = s;
@@ -317,8 +319,13 @@ int lrkv_prefill_kernel_kind(const lrkv_cache_t *cache) {
 }
 
 size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype) {
-    if (check_dims(H, d_h, r, dtype) || tokens < 0) return 0;
-    return (size_t)tokens * 2 * ((size_t)d_h + (size_t)H * r) * elem_bytes(dtype);
+    return lrkv_cache_bytes_grouped(H, d_h, r, 1, tokens, dtype);
+}
+
+size_t lrkv_cache_bytes_grouped(int32_t H, int32_t d_h, int32_t r, int32_t G, int64_t tokens,
+                                int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || tokens < 0 || G < 1 || G > H || H % G) return 0;
+    return (size_t)tokens * 2 * ((size_t)G * d_h + (size_t)H * r) * elem_bytes(dtype);
 }
 
 size_t lrkv_decode_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
@@ -457,9 +464,10 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     a.out = out;
     a.status = dev_status;
     a.stream = s;
-    const bool fused = cache->dtype == LRKV_BF16 && !cache->N_K && d % 128 == 0 && B <= kFusedStepMaxRows &&
+    const bool fused = cache->dtype == LRKV_BF16 && !cache->N_K && cache_groups(*cache) == 1 &&
+                       d % 128 == 0 && B <= kFusedStepMaxRows &&
                        fast_decode_supported(cache->H, cache->d_h, cache->r, cache->page_size,
-                                             cache->dtype) &&
+                                             cache->dtype, 1) &&
                        fast_decode_step_fits(cache->H, cache->r, d);
     if (fused) {
         a.X = X;
@@ -670,7 +678,7 @@ int lrkv_decode_rope(const void *q, const lrkv_cache_t *cache, const void *B_K, 
                                                 rope_table_f16_offset(cache->d_h, rope_max_pos));
     a.rope_max_pos = rope_max_pos;
     if (rope_fast_supported(cache->H, cache->d_h, cache->r, cache->page_size, cache->dtype) &&
-        !cache->N_K)
+        !cache->N_K && cache_groups(*cache) == 1)
         a.rope_ws = rope_fast_ws_layout(static_cast<char *>(workspace) + dec_bytes, B, cache->H,
                                         cache->d_h, cache->r, max_seq_len);
     return run_decode(a, workspace, dec_bytes);

@@ -45,6 +45,10 @@ struct DecodeWs {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Shared key/value groups of a cache (0 and 1 both mean one shared basis);
+// head h reads group h / (H / groups).
+__host__ __device__ inline int cache_groups(const lrkv_cache_t &c) { return c.G > 1 ? c.G : 1; }
+
 __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, int d_h, int r,
                                                      int G) {
     DecodeWs w;

@@ -619,7 +619,7 @@ cudaError_t launch_r16(const PfMaps &maps, const PfArgs &a, dim3 grid, cudaStrea
 // Shape checks and tensor maps of one call; false when the shape is not covered.
 static bool prefill_tc_plan(const PrefillTcArgs &p, PfMaps &maps, int &n_qtiles) {
     const lrkv_cache_t &c = p.cache;
-    if (c.dtype != LRKV_BF16 || c.N_K || c.d_h != 128 || c.r < 8 || c.r > 64 || c.r % 8 != 0 ||
+    if (c.dtype != LRKV_BF16 || c.N_K || cache_groups(c) != 1 || c.d_h != 128 || c.r < 8 || c.r > 64 || c.r % 8 != 0 ||
         c.page_size % PF_HALF != 0 || c.H > 65535 || p.B > 65535 || p.n < 1 || p.max_ctx < 1)
         return false;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;

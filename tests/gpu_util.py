@@ -98,5 +98,6 @@ def pools_f64(case, pools=None):
 def oracle_decode(case, pairs=None):
     import oracle
     f = lambda a: I.to_f64(a, case.act_dtype)
-    return oracle.decode(f(case.q), *pools_f64(case), f(case.B_K), f(case.B_V), case.page_table,
-                         case.seq_lens, case.page_size, pairs=pairs)
+    fn = oracle.grouped.decode_grouped if case.groups > 1 else oracle.decode
+    return fn(f(case.q), *pools_f64(case), f(case.B_K), f(case.B_V), case.page_table,
+              case.seq_lens, case.page_size, pairs=pairs)

@@ -3,12 +3,14 @@ function include/lrkv.h declares, and its host-only entry points (sizes,
 status strings, argument validation that rejects before any CUDA work)
 behave as documented.  No call here touches a GPU."""
 import ctypes
+from fractions import Fraction
 import os
 import re
 
 import pytest
 
 import oracle
+from oracle import grouped
 from rank_kv_attention_gb300 import _abi
 from rank_kv_attention_gb300 import build as B
 
@@ -55,6 +57,32 @@ def test_cache_bytes_rejects_bad_shapes(lib):
     assert lib.lrkv_cache_bytes(16, 128, 48, 10, 7) == 0   # bad dtype
     assert lib.lrkv_cache_bytes(16, 120, 48, 10, 2) == 0   # 8-bit codes need d_h % 16 == 0
     assert lib.lrkv_cache_bytes(3, 128, 8, 10, 2) == 0     # ... and H * r % 16 == 0
+
+
+@pytest.mark.parametrize("H,d_h,r,G,T,dt,eb", [(16, 128, 32, 2, 4096, 1, 2), (32, 128, 32, 8, 100, 1, 2),
+                                               (4, 16, 4, 4, 65, 0, 4), (16, 128, 48, 1, 7, 2, 1)])
+def test_cache_bytes_grouped(lib, H, d_h, r, G, T, dt, eb):
+    """Equation 9 with G shared rows per token: 2 T (G d_h + H r) elements;
+    the oracle's grouped payload ratio times the multi-head bytes."""
+    got = lib.lrkv_cache_bytes_grouped(H, d_h, r, G, T, dt)
+    assert got == 2 * T * (G * d_h + H * r) * eb
+    assert Fraction(got, 2 * T * H * d_h * eb) == grouped.payload_ratio_grouped(H, d_h, r, G)
+    if G == 1:
+        assert got == lib.lrkv_cache_bytes(H, d_h, r, T, dt)
+
+
+def test_cache_groups_checked_on_host(lib):
+    assert lib.lrkv_cache_bytes_grouped(16, 128, 48, 3, 10, 1) == 0    # G must divide H
+    assert lib.lrkv_cache_bytes_grouped(16, 128, 48, 0, 10, 1) == 0
+    assert lib.lrkv_cache_bytes_grouped(16, 128, 48, 32, 10, 1) == 0   # G <= H
+    ws = ctypes.c_void_p(256)
+
+    def call(cache):
+        return lib.lrkv_decode(16, ctypes.byref(cache), 16, 16, 16, 16, 2, 4, 100, 16, ws, 1 << 30, None,
+                               None)
+    assert call(_cache(G=3)) == _abi.LRKV_E_SHAPE
+    assert call(_cache(G=-1)) == _abi.LRKV_E_SHAPE
+    assert call(_cache(G=32)) == _abi.LRKV_E_SHAPE
 
 
 def test_fp8_cache_scales_checked_on_host(lib):
