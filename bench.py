@@ -277,8 +277,20 @@ def run_ours(args, rank, world, local_rank):
     f_app, f_dec, f_step = lib.lrkv_append, (dec_rope if rope else lib.lrkv_decode), lib.lrkv_decode_step
 
     def step(i):
-        # one decode step: append the B new rows (and store their key norms),
-        # then decode the B queries
+        # one decode step: append the B new rows (with their key norms when
+        # the cache keeps them) and decode the B queries -- one
+        # lrkv_decode_step call; the rotary path calls lrkv_append, then
+        # lrkv_decode_rope
+        a, dd, fs, _ = calls[i % n_copies]
+        if rope:
+            rc, rc2 = f_app(*a), f_dec(*dd)
+        else:
+            rc, rc2 = f_step(*fs), 0
+        if rc or rc2:
+            raise RuntimeError(f"lrkv call failed: {rc} {rc2}")
+
+    def separate(i):
+        # the same step as separate calls: lrkv_append, [lrkv_key_norms,] lrkv_decode
         a, dd, _, kn = calls[i % n_copies]
         rc = f_app(*a)
         rc3 = lib.lrkv_key_norms(*kn) if norm else 0
@@ -332,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
         return a0.elapsed_time(a1) / K
     append_ms = timed(lambda i: f_app(*calls[i % n_copies][0]))
     decode_ms = timed(lambda i: f_dec(*calls[i % n_copies][1]))
-    fused_ms = None if rope else timed(lambda i: f_step(*calls[i % n_copies][2]))
+    separate_ms = None if rope else timed(separate)
 
     # ---- the split kernel's own duration: the library brackets each launch
     # with CUDA events on its stream (a second pass over K steps, so those
@@ -357,10 +369,11 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the C ABI with host buffers
     Ke = args.e2e_steps or max(50, min(K, 2000))
-    # the step's inputs (new rows X, queries, positions, ids, lengths) live in
-    # one pinned host staging buffer and move with one copy; the C-ABI calls
-    # take device views of its device twin (256-byte aligned)
-    parts = (X, q, pos, sid, seq_lens)
+    # the step's inputs (new rows X, queries, lengths; positions and ids for
+    # the rotary path's lrkv_append) live in one pinned host staging buffer and
+    # move with one copy; the C-ABI calls take device views of its device twin
+    # (256-byte aligned)
+    parts = (X, q, seq_lens) + ((pos, sid) if rope else ())
     offs, o = [], 0
     for t in parts:
         offs.append(o)
@@ -372,7 +385,8 @@ def run_ours(args, rank, world, local_rank):
         nb = t.numel() * t.element_size()
         hbuf[a:a + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
         views.append(dbuf[a:a + nb].view(t.dtype).view(t.shape))
-    dX, dq, dpos, dsid, dsl = views
+    dX, dq, dsl = views[:3]
+    dpos, dsid = views[3:] if rope else (pos, sid)
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dout = torch.empty_like(out)
     calls = make_calls(dX, dq, dpos, dsid, dsl, dout)
@@ -428,8 +442,9 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world} (requests are independent)",
                    "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
                          f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
-                   "step": "lrkv_append (B new rows) + " + ("lrkv_key_norms (their reciprocal key norms) + "
-                                                            if norm else "") + "lrkv_decode (B queries)"},
+                   "step": ("lrkv_append (B new rows) + lrkv_decode_rope (B queries)" if rope else
+                            "lrkv_decode_step (append of the B new rows" +
+                            (", their reciprocal key norms" if norm else "") + ", decode of the B queries)")},
         "roofline": ({"kernel": "rotary score kernel (f16 mma.sync; C_j W_h private products, rotated shared term)",
                       "bound": "tensor", "achieved": round(rope_flops / (scores_ms / 1e3) / 1e12, 2),
                       "peak": bf16_peak, "unit": "TFLOP/s",
@@ -457,7 +472,7 @@ def run_ours(args, rank, world, local_rank):
                          "rotary_score_kernel": None if scores_ms is None else round(scores_ms, 5),
                          "lrkv_append_alone": round(append_ms, 5),
                          "lrkv_decode_alone": round(decode_ms, 5),
-                         "lrkv_decode_step": None if fused_ms is None else round(fused_ms, 5)},
+                         "lrkv_append_then_lrkv_decode": None if separate_ms is None else round(separate_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "pinned host inputs (one staging buffer) copied in, result copied out and "

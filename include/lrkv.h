@@ -240,14 +240,14 @@ LRKV_API int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const
  *                dtype) bytes, 256-byte aligned, caller-owned scratch.
  *
  * Same result as lrkv_append (positions seq_lens[b] - 1, sequence ids b)
- * followed by lrkv_decode, up to floating-point rounding order.  For bf16
- * caches with d_h = 128, d % 128 == 0 and a (H, r) that the tensor-core decode
- * covers, the decode's split kernel itself projects and writes the new rows
- * while it streams the older ones, and the combine folds each new row in as
- * one more key; other shapes run the append and the decode kernels in turn.
+ * followed by lrkv_decode, up to floating-point rounding order.  The append
+ * kernel takes each row's place from seq_lens itself (and so do the key
+ * norms of a cache that keeps them), and the decode's first kernel, whose
+ * inputs are none of the append's, runs beside it instead of after it.
  * A request with an invalid length gets no new row, out = 0 and
- * LRKV_STATUS_BAD_SEQLEN; a new row on an invalid page is skipped (not
- * attended) and flagged LRKV_STATUS_BAD_PAGE.
+ * LRKV_STATUS_BAD_SEQLEN (with LRKV_STATUS_BAD_ROW from the append); a new
+ * row on an invalid page is neither written nor attended and is flagged
+ * LRKV_STATUS_BAD_PAGE.
  */
 LRKV_API size_t lrkv_decode_step_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
                                                  int32_t max_seq_len, int32_t dtype);

@@ -28,6 +28,20 @@ __device__ __forceinline__ int64_t append_dest_row(const int32_t *positions, con
     return (int64_t)page * page_size + pos % page_size;
 }
 
+// The same for row i of an append: its (request, position) from the step's
+// lengths or from the caller's arrays.
+template <typename T>
+__device__ __forceinline__ int64_t append_dest_row(const AppendArgsT<T> &a, int i) {
+    if (a.step_lens) {
+        const int32_t L = a.step_lens[i];
+        const int32_t b = i, pos = (L < 1 || L > a.step_max_len) ? -1 : L - 1;
+        return append_dest_row(&pos, &b, 0, a.page_table, a.B, a.max_pages, a.num_pages,
+                               a.page_size, a.status);
+    }
+    return append_dest_row(a.positions, a.seq_ids, i, a.page_table, a.B, a.max_pages, a.num_pages,
+                           a.page_size, a.status);
+}
+
 constexpr int kAM = 32, kAN = 64, kAK = 32;
 
 template <typename T>
@@ -44,9 +58,7 @@ __global__ void __launch_bounds__(256) append_generic_kernel(AppendArgsT<T> a) {
 
     if (tid < kAM) {
         const int i = i0 + tid;
-        dst_row[tid] = (i < a.n) ? append_dest_row(a.positions, a.seq_ids, i, a.page_table, a.B,
-                                                   a.max_pages, a.num_pages, a.page_size, a.status)
-                                 : -1;
+        dst_row[tid] = (i < a.n) ? append_dest_row(a, i) : -1;
     }
     const int ty = tid / 16, tx = tid % 16;
     float acc[2][4] = {};
@@ -157,10 +169,7 @@ __global__ void __launch_bounds__(kSkWarps * 32) append_rows_kernel(AppendArgsT<
     for (int cc = 0; cc < kSkCols; ++cc)
         if (lane < nchunk) wn[cc] = *reinterpret_cast<const uint4 *>(wrow[cc] + (size_t)lane * V);
     if (tid < kSkRows)
-        dst_row[tid] = (tid < nr) ? append_dest_row(a.positions, a.seq_ids, i0 + tid, a.page_table,
-                                                    a.B, a.max_pages, a.num_pages, a.page_size,
-                                                    a.status)
-                                  : -1;
+        dst_row[tid] = (tid < nr) ? append_dest_row(a, i0 + tid) : -1;
     __syncthreads();
     if (!mbar_wait(&xbar, 0)) {
         status_or(a.status, LRKV_STATUS_TIMEOUT);
@@ -214,23 +223,28 @@ __global__ void __launch_bounds__(kSkWarps * 32) append_rows_kernel(AppendArgsT<
 }
 
 // ---------------------------------------------------------------------------
-// Few-row append on tensor cores (bf16).  A block holds 16 rows of X in
-// shared memory (rows padded by 16 bytes so ldmatrix is conflict-free) and
-// produces 16 output columns; its 4 warps split the contraction d, each
-// running mma.m16n8k16 (rows of X = M, output columns = N) with the weight
-// fragments read straight from global memory, then the partial sums meet in
-// shared memory and are scattered to the cache.
+// Few-row append on tensor cores (bf16).  A block makes 16 output columns
+// (two 8-column n-tiles) for 16 rows of X; its 16 warps split the
+// contraction d into 32-wide chunks (chunk c goes to warp c mod 16).  In a
+// chunk a lane needs four 16-byte runs, straight from global memory: X rows
+// gq and gq + 8 and weight rows gq and 8 + gq, each at k = 8 tq .. 8 tq + 7.
+// The chunk's two k-steps give both operands the same map from physical k
+// to fragment slot (k-step s takes 8 tq + 4 s + {0, 1} for slots 2 tq, 2 tq + 1
+// and 8 tq + 4 s + {2, 3} for slots 2 tq + 8, 2 tq + 9), so each dot product
+// still pairs matching k and every operand load is one 16-byte access; a
+// warp's whole share (four chunks at d = 2048) is in flight at once.
+// Partial sums meet in shared memory in a fixed order and are scattered to
+// the cache.
 // ---------------------------------------------------------------------------
-constexpr int kTcRows = 16, kTcCols = 16, kTcWarps = 4, kTcBatch = 8;
+constexpr int kTcRows = 16, kTcCols = 16, kTcWarps = 16, kTcBatch = 4;
 
-__global__ void __launch_bounds__(kTcWarps * 32) append_rows_mma_kernel(AppendArgsT<__nv_bfloat16> a) {
-    extern __shared__ __align__(16) unsigned char tc_raw[];
-    const int d = a.d;
-    const int xstride = d * 2 + 16;                    // bytes per padded row of X
-    unsigned char *xs = tc_raw;                         // [16][xstride]
-    float *part = reinterpret_cast<float *>(tc_raw + kTcRows * xstride);  // [warps][16][16]
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+__global__ void __launch_bounds__(kTcWarps * 32, 1) append_rows_mma_kernel(AppendArgsT<__nv_bfloat16> a) {
+    __shared__ float part[kTcWarps][kTcRows][kTcCols + 1];
     __shared__ int64_t dst_row[kTcRows];
-    __shared__ __align__(8) uint64_t xbar;
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,97 +253,74 @@ __global__ void __launch_bounds__(kTcWarps * 32) append_rows_mma_kernel(AppendAr
     const int nr = min(kTcRows, a.n - i0);
     const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
     const int c0 = blockIdx.x * kTcCols;
-
-    if (tid == 0) {
-        mbar_init(&xbar, 1);
-        fence_barrier_init();
-        mbar_arrive_expect_tx(&xbar, (uint32_t)(nr * d * 2));
-        for (int r = 0; r < nr; ++r)
-            bulk_load(xs + r * xstride, a.X + (size_t)(i0 + r) * d, (uint32_t)(d * 2), &xbar);
-    }
-    for (int r = nr; r < kTcRows; ++r)
-        for (int e = tid; e < d / 8; e += blockDim.x)
-            reinterpret_cast<uint4 *>(xs + r * xstride)[e] = make_uint4(0, 0, 0, 0);
+    const int d = a.d, nch = d / 32;
     if (tid < kTcRows)
-        dst_row[tid] = (tid < nr) ? append_dest_row(a.positions, a.seq_ids, i0 + tid, a.page_table,
-                                                    a.B, a.max_pages, a.num_pages, a.page_size,
-                                                    a.status)
-                                  : -1;
-    const __nv_bfloat16 *w0 = weight_row(a, min(c0 + gq, Ntot - 1));
-    const __nv_bfloat16 *w1 = weight_row(a, min(c0 + 8 + gq, Ntot - 1));
-    const int nks = d / 16, per = nks / kTcWarps;      // k-steps per warp (d % 64 == 0)
-    const int ks0 = warp * per;
-    __syncthreads();
-    if (!mbar_wait(&xbar, 0)) {
-        status_or(a.status, LRKV_STATUS_TIMEOUT);
-        return;
-    }
-
+        dst_row[tid] = (tid < nr) ? append_dest_row(a, i0 + tid) : -1;
+    const bool ok0 = gq < nr, ok1 = gq + 8 < nr;
+    const __nv_bfloat16 *x0 = a.X + (size_t)(i0 + (ok0 ? gq : 0)) * d + 8 * tq;
+    const __nv_bfloat16 *x1 = a.X + (size_t)(i0 + (ok1 ? gq + 8 : 0)) * d + 8 * tq;
+    const __nv_bfloat16 *w0 = weight_row(a, min(c0 + gq, Ntot - 1)) + 8 * tq;
+    const __nv_bfloat16 *w1 = weight_row(a, min(c0 + 8 + gq, Ntot - 1)) + 8 * tq;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
     float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const uint32_t xb = smem_u32(xs);
-    const int arow = (lane & 7) + 8 * ((lane >> 3) & 1);
-    for (int ks = ks0; ks < ks0 + per; ks += kTcBatch) {
-        uint32_t b[kTcBatch][4];
+    for (int base = warp; base < nch; base += kTcBatch * kTcWarps) {
+        uint4 xa[kTcBatch], xb[kTcBatch], wa[kTcBatch], wb[kTcBatch];
 #pragma unroll
         for (int u = 0; u < kTcBatch; ++u) {
-            if (ks + u < ks0 + per) {
-                const int k = (ks + u) * 16 + 2 * tq;
-                b[u][0] = *reinterpret_cast<const uint32_t *>(w0 + k);
-                b[u][1] = *reinterpret_cast<const uint32_t *>(w0 + k + 8);
-                b[u][2] = *reinterpret_cast<const uint32_t *>(w1 + k);
-                b[u][3] = *reinterpret_cast<const uint32_t *>(w1 + k + 8);
+            const int ch = base + u * kTcWarps;
+            xa[u] = xb[u] = wa[u] = wb[u] = zero;
+            if (ch < nch) {
+                const size_t k = (size_t)ch * 32;
+                if (ok0) xa[u] = __ldg(reinterpret_cast<const uint4 *>(x0 + k));
+                if (ok1) xb[u] = __ldg(reinterpret_cast<const uint4 *>(x1 + k));
+                wa[u] = __ldg(reinterpret_cast<const uint4 *>(w0 + k));
+                wb[u] = __ldg(reinterpret_cast<const uint4 *>(w1 + k));
             }
         }
 #pragma unroll
         for (int u = 0; u < kTcBatch; ++u) {
-            if (ks + u < ks0 + per) {
-                uint32_t av[4];
-                ldmatrix_x4(xb + arow * xstride + (2 * (ks + u) + (lane >> 4)) * 16, av[0], av[1], av[2], av[3]);
-                mma_bf16_16816(c[0], av, b[u][0], b[u][1]);
-                mma_bf16_16816(c[1], av, b[u][2], b[u][3]);
+            if (base + u * kTcWarps < nch) {
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    const uint32_t av[4] = {word_of(xa[u], 2 * s), word_of(xb[u], 2 * s),
+                                            word_of(xa[u], 2 * s + 1), word_of(xb[u], 2 * s + 1)};
+                    mma_bf16_16816(c[0], av, word_of(wa[u], 2 * s), word_of(wa[u], 2 * s + 1));
+                    mma_bf16_16816(c[1], av, word_of(wb[u], 2 * s), word_of(wb[u], 2 * s + 1));
+                }
             }
         }
     }
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb) {
-        float *pw = part + warp * kTcRows * kTcCols;
         const int col = nb * 8 + 2 * tq;
-        pw[gq * kTcCols + col] = c[nb][0];
-        pw[gq * kTcCols + col + 1] = c[nb][1];
-        pw[(gq + 8) * kTcCols + col] = c[nb][2];
-        pw[(gq + 8) * kTcCols + col + 1] = c[nb][3];
+        part[warp][gq][col] = c[nb][0];
+        part[warp][gq][col + 1] = c[nb][1];
+        part[warp][gq + 8][col] = c[nb][2];
+        part[warp][gq + 8][col + 1] = c[nb][3];
     }
     __syncthreads();
-    const int d_h = a.d_h, Hr = a.H * a.r;
-    for (int o = tid; o < kTcRows * kTcCols; o += blockDim.x) {
-        const int row = o / kTcCols, cidx = c0 + o % kTcCols;
-        if (row >= nr || cidx >= Ntot) continue;
-        const int64_t dr = dst_row[row];
-        if (dr < 0) continue;
-        float v = 0.f;
+    if (tid < kTcRows * kTcCols) {
+        const int row = tid / kTcCols, cc = tid % kTcCols, cidx = c0 + cc;
+        if (row < nr && cidx < Ntot) {
+            const int64_t dr = dst_row[row];
+            if (dr >= 0) {
+                float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kTcWarps; ++w) v += part[(w * kTcRows + row) * kTcCols + o % kTcCols];
-        store_projected(a, (size_t)dr, cidx, v);
+                for (int w = 0; w < kTcWarps; ++w) v += part[w][row][cc];
+                store_projected(a, (size_t)dr, cidx, v);
+            }
+        }
     }
 }
 
 bool rows_mma_append_fits(const AppendArgsT<__nv_bfloat16> &a) {
-    return a.n <= 4 * kTcRows && a.d % 64 == 0 &&
-           (size_t)kTcRows * (a.d * 2 + 16) + kTcWarps * kTcRows * kTcCols * 4 <= 200 * 1024;
+    return a.n <= 4 * kTcRows && a.d % 32 == 0;
 }
 
 cudaError_t launch_append_rows_mma(const AppendArgsT<__nv_bfloat16> &a) {
     const int Ntot = 2 * a.d_h + 2 * a.H * a.r;
     dim3 grid((Ntot + kTcCols - 1) / kTcCols, (a.n + kTcRows - 1) / kTcRows);
-    const size_t sm = (size_t)kTcRows * (a.d * 2 + 16) + kTcWarps * kTcRows * kTcCols * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(append_rows_mma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    return launch_pdl(append_rows_mma_kernel, grid, dim3(kTcWarps * 32), sm, a.stream, a);
+    return launch_pdl(append_rows_mma_kernel, grid, dim3(kTcWarps * 32), 0, a.stream, a);
 }
 
 template <typename T>
@@ -389,25 +380,7 @@ __global__ void prefill_rows_kernel(const int32_t *__restrict__ cu_rows,
     req_row[i] = ok ? b : 0;
 }
 
-// Decode step through the separate append: request b's new row sits at
-// position seq_lens[b] - 1 (an invalid length gives position -1, which the
-// append skips and flags).
-__global__ void step_rows_kernel(const int32_t *__restrict__ seq_lens, int B, int max_len,
-                                 int32_t *pos, int32_t *sid) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
-    const int32_t L = seq_lens[b];
-    pos[b] = (L < 1 || L > max_len) ? -1 : L - 1;
-    sid[b] = b;
-}
 
-cudaError_t launch_step_rows(const int32_t *seq_lens, int B, int max_len, int32_t *pos,
-                             int32_t *sid, cudaStream_t s) {
-    return launch_pdl(step_rows_kernel, dim3((B + 255) / 256), dim3(256), 0, s, seq_lens, B,
-                      max_len, pos, sid);
-}
 
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
@@ -429,8 +402,9 @@ __global__ void __launch_bounds__(256) key_norms_kernel(
     const T *__restrict__ B_K, const TC *__restrict__ S_K, const TC *__restrict__ R_K,
     T *__restrict__ N_K, const int32_t *__restrict__ page_table, int B, int max_pages, int num_pages,
     int page_size, int H, int d_h, int r, float sk_scale, float rk_scale, float eps, int32_t *status,
-    int groups) {
-    // groups: shared key/value groups; head h reads group h / (H / groups)
+    int groups, const int32_t *__restrict__ step_lens) {
+    // groups: shared key/value groups; head h reads group h / (H / groups).
+    // step_lens (decode step): row i is request i's row at step_lens[i] - 1.
     pdl_wait();
     pdl_launch_dependents();
     __shared__ float zs[8][256];
@@ -438,7 +412,15 @@ __global__ void __launch_bounds__(256) key_norms_kernel(
     const int64_t gw = (int64_t)blockIdx.x * 8 + warp;  // (row, head) pair; warp-uniform
     if (gw >= (int64_t)n * H) return;
     const int i = (int)(gw / H), h = (int)(gw % H);
-    const int32_t b = seq_ids[i], pos = positions[i];
+    int32_t b, pos;
+    if (step_lens) {
+        const int32_t L = step_lens[i];
+        b = i;
+        pos = (L < 1 || (int64_t)L > (int64_t)max_pages * page_size) ? -1 : L - 1;
+    } else {
+        b = seq_ids[i];
+        pos = positions[i];
+    }
     if (b < 0 || b >= B || pos < 0 || (int64_t)pos >= (int64_t)max_pages * page_size) {
         if (lane == 0 && h == 0) status_or(status, LRKV_STATUS_BAD_ROW);
         return;
@@ -474,7 +456,7 @@ __global__ void __launch_bounds__(256) key_norms_kernel(
 
 cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, int n, const void *B_K,
                              const lrkv_cache_t &c, const int32_t *page_table, int B, int max_pages,
-                             int32_t *status, cudaStream_t s) {
+                             int32_t *status, cudaStream_t s, const int32_t *step_lens) {
     if (n <= 0) return cudaSuccess;
     const int64_t warps = (int64_t)n * c.H;
     const unsigned blocks = (unsigned)((warps + 7) / 8);
@@ -483,19 +465,20 @@ cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, i
                           seq_ids, n, static_cast<const float *>(B_K), static_cast<const float *>(c.S_K),
                           static_cast<const float *>(c.R_K), static_cast<float *>(c.N_K), page_table, B,
                           max_pages, c.num_pages, c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps,
-                          status, cache_groups(c));
+                          status, cache_groups(c), step_lens);
     if (c.dtype == LRKV_FP8_E4M3)
         return launch_pdl(key_norms_kernel<__nv_bfloat16, uint8_t>, dim3(blocks), dim3(256), 0, s,
                           positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
                           static_cast<const uint8_t *>(c.S_K), static_cast<const uint8_t *>(c.R_K),
                           static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
                           c.page_size, c.H, c.d_h, c.r, c.scale[0], c.scale[2], c.norm_eps, status,
-                          cache_groups(c));
+                          cache_groups(c), step_lens);
     return launch_pdl(key_norms_kernel<__nv_bfloat16, __nv_bfloat16>, dim3(blocks), dim3(256), 0, s,
                       positions, seq_ids, n, static_cast<const __nv_bfloat16 *>(B_K),
                       static_cast<const __nv_bfloat16 *>(c.S_K), static_cast<const __nv_bfloat16 *>(c.R_K),
                       static_cast<__nv_bfloat16 *>(c.N_K), page_table, B, max_pages, c.num_pages,
-                      c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps, status, cache_groups(c));
+                      c.page_size, c.H, c.d_h, c.r, 1.f, 1.f, c.norm_eps, status, cache_groups(c),
+                      step_lens);
 }
 
 }  // namespace lrkv

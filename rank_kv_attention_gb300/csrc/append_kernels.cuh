@@ -10,6 +10,11 @@ struct AppendArgsT {
     const T *X;
     const int32_t *positions;
     const int32_t *seq_ids;
+    // decode step: when set, row i is request i's row at position
+    // step_lens[i] - 1 (positions and seq_ids unused; a length outside
+    // [1, step_max_len] skips the row and flags it)
+    const int32_t *step_lens = nullptr;
+    int step_max_len = 0;
     int n, d;
     const T *W_S_K, *W_S_V, *U_K, *U_V;
     T *S_K, *S_V, *R_K, *R_V;
@@ -48,7 +53,7 @@ cudaError_t launch_append_generic(const AppendArgsT<T> &a);
 // Reciprocal joint key norms of n cached rows into c.N_K (see lrkv_key_norms).
 cudaError_t launch_key_norms(const int32_t *positions, const int32_t *seq_ids, int n, const void *B_K,
                              const lrkv_cache_t &c, const int32_t *page_table, int B, int max_pages,
-                             int32_t *status, cudaStream_t s);
+                             int32_t *status, cudaStream_t s, const int32_t *step_lens = nullptr);
 
 // Few-row append (decode step): whether the shape fits, and the launcher.
 template <typename T>
@@ -65,8 +70,6 @@ bool tc_append_supported(int n, int d, int d_h, int H, int r);
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);
 int device_sm_count();  // SMs of the current device (lrkv_api.cu)
 
-cudaError_t launch_step_rows(const int32_t *seq_lens, int B, int max_len, int32_t *pos,
-                             int32_t *sid, cudaStream_t s);
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s);

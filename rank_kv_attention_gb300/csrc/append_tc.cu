@@ -163,7 +163,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             {
                 const int r = m0 + row;
                 if (r < a.n) {
-                    const int32_t b = a.seq_ids[r], pos = a.positions[r];
+                    int32_t b, pos;
+                    if (a.step_lens) {  // decode step: request r at its length - 1
+                        const int32_t L = a.step_lens[r];
+                        b = r;
+                        pos = (L < 1 || L > a.step_max_len) ? -1 : L - 1;
+                    } else {
+                        b = a.seq_ids[r];
+                        pos = a.positions[r];
+                    }
                     if (b < 0 || b >= a.B || pos < 0 || pos >= a.max_pages * a.page_size) {
                         if (b0 == 0) status_or(a.status, LRKV_STATUS_BAD_ROW);
                     } else {

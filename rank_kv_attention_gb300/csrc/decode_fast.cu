@@ -81,10 +81,7 @@ struct FastCfg {
     static constexpr int OFF_CUR = OFF_OK + 64;      // issue cursor
     static constexpr int OFF_PLAN = OFF_CUR + 64;    // local plan: scan scratch + request offsets
     static constexpr int OFF_PEND = OFF_PLAN + 512;  // given scores: rows of the first copies
-    static constexpr int OFF_RED = OFF_PEND + 64;    // fused step: per-warp append partials
-    static constexpr int OFF_DST = OFF_RED + NCW * 32 * 16;  // fused step: new rows' pool rows [16]
-    static constexpr int OFF_ABAR = OFF_DST + 16 * 8;          // fused step: staging barrier
-    static constexpr int SMEM = OFF_ABAR + 64 + 1024;  // + alignment slack
+    static constexpr int SMEM = OFF_PEND + 64 + 1024;  // + alignment slack
 
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
@@ -107,12 +104,6 @@ struct FastParams {
     float scale_log2;
     DecodeWs ws;
     int32_t *status;
-    // fused decode step (X != nullptr): new rows X [B, d], weights W_S_K,
-    // W_S_V, U_K, U_V (output-major), destination pools S_K, S_V, R_K, R_V
-    const __nv_bfloat16 *X;
-    const __nv_bfloat16 *W[4];
-    __nv_bfloat16 *pool[4];
-    int d, len_shift;
     float4 sc;  // 8-bit cache: pool scales of S_K, S_V, R_K, R_V
     int norm;   // the cache holds joint key norms (a fifth copy per tile)
     int max_len;  // longest valid sequence length (longer requests are not attended)
@@ -241,158 +232,6 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
     return *reinterpret_cast<const uint32_t *>(p);
-}
-
-// Fused decode step: this CTA's share of the new rows' projection
-// X [B, d] . [W_S_K | W_S_V | U_K | U_V]^T (section 3, Algorithm 1), written
-// at position seq_lens[b] - 1 of request b through the page table.  Output
-// columns go in groups of 8 (one mma n-tile), two groups at a time per CTA
-// (four warps each, splitting the contraction and meeting in shared memory).
-// It runs before the CTA requests its first cache tiles, in the then empty
-// ring: bulk copies stage the (at most 16) rows of X and the two groups' 8
-// weight rows each into rows padded by 16 bytes, so the mma fragment loads
-// from shared memory are free of bank conflicts.  The split kernel never
-// reads these rows: it streams rows 0 .. seq_lens[b] - 2, and the combine
-// folds the new row in.
-constexpr int kFusedStepStride = 16;  // bytes of padding after each staged row
-
-// Column group `slot` (0 or 1) of round `it` for this CTA, and the pool it
-// lies in (seg) with that pool's first packed column (base).
-template <class C>
-__device__ __forceinline__ int append_group(int it, int slot, int &seg, int &base) {
-    constexpr int HR = C::H * C::R, NG = (2 * C::DH + 2 * HR) / 8;
-    const int grp = blockIdx.x + (2 * it + slot) * gridDim.x;
-    const int c0 = grp < NG ? grp * 8 : 0;
-    if (c0 < C::DH) { seg = 0; base = 0; }
-    else if (c0 < 2 * C::DH) { seg = 1; base = C::DH; }
-    else if (c0 < 2 * C::DH + HR) { seg = 2; base = 2 * C::DH; }
-    else { seg = 3; base = 2 * C::DH + HR; }
-    return grp < NG ? grp : -1;
-}
-
-// One thread: the staging copies of round `it` (X rows on round 0, then the
-// round's weight rows), L2 evict-last (the same X and weights serve every
-// CTA and every step).
-template <class C>
-__device__ void append_issue(const FastParams &P, uint8_t *stage, uint64_t *bar, int it) {
-    const int stride = 2 * P.d + kFusedStepStride;
-    const uint32_t row_bytes = 2 * P.d;
-    const uint64_t keep = l2_evict_last_policy();
-    int grp[2], seg[2], base[2];
-    uint32_t bytes = it == 0 ? P.B * row_bytes : 0;
-    for (int hs = 0; hs < 2; ++hs) {
-        grp[hs] = append_group<C>(it, hs, seg[hs], base[hs]);
-        if (grp[hs] >= 0) bytes += 8 * row_bytes;
-    }
-    mbar_arrive_expect_tx(bar, bytes);
-    if (it == 0)
-        for (int b = 0; b < P.B; ++b)
-            bulk_load_hint(stage + b * stride, P.X + (size_t)b * P.d, row_bytes, bar, keep);
-    for (int hs = 0; hs < 2; ++hs) {
-        if (grp[hs] < 0) continue;
-        const __nv_bfloat16 *w0 = P.W[seg[hs]] + (size_t)(grp[hs] * 8 - base[hs]) * P.d;
-        for (int j = 0; j < 8; ++j)
-            bulk_load_hint(stage + (16 + 8 * hs + j) * stride, w0 + (size_t)j * P.d, row_bytes, bar,
-                           keep);
-    }
-}
-
-// Whole CTA, after append_issue(..., 0) ran at kernel start: wait for each
-// round's rows, multiply, reduce across the four warps of a group and write
-// the rounded results into the new rows' slots.
-template <class C>
-__device__ bool append_new_rows(const FastParams &P, uint8_t *stage, uint64_t *bar, float4 *red,
-                                int64_t *dst) {
-    constexpr int HR = C::H * C::R, NG = (2 * C::DH + 2 * HR) / 8;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gq = lane >> 2, tq = lane & 3;
-    const int half = warp >> 2, wq = warp & 3;  // column group slot, warp inside it
-    const int kper = P.d / 4, k0 = wq * kper;   // kper % 32 == 0 (host checks d % 128)
-    const int stride = 2 * P.d + kFusedStepStride;
-    const uint8_t *xs = stage;                   // X rows 0..15
-    const uint8_t *ws = stage + 16 * stride;     // weight rows: slot h at rows 8h .. 8h+7
-    const int max_len = P.max_pages * P.page_size;
-    // destination pool row of every new row (-1: invalid length or page),
-    // while the copies are in flight
-    if (tid < P.B) {
-        const int32_t L = P.seq_lens[tid];
-        int64_t row = -1;
-        if (L >= 1 && L <= max_len) {
-            const int pos = L - 1;
-            const int32_t page = P.page_table[(size_t)tid * P.max_pages + pos / P.page_size];
-            if (page >= 0 && page < P.num_pages)
-                row = (int64_t)page * P.page_size + pos % P.page_size;
-            else
-                status_or(P.status, LRKV_STATUS_BAD_PAGE);
-        }
-        dst[tid] = row;
-    }
-    const int n_iter = (NG + 2 * (int)gridDim.x - 1) / (2 * (int)gridDim.x);
-    bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
-        if (it > 0 && tid == 0) {
-            // the previous round's generic reads of the staging area are done
-            // (__syncthreads below): order them before the async-proxy writes
-            fence_proxy_async_smem();
-            append_issue<C>(P, stage, bar, it);
-        }
-        // block-uniform: every thread leaves together if the copies never land
-        if (!__syncthreads_and(mbar_wait(bar, it & 1))) {
-            ok = false;
-            break;
-        }
-        int seg, base;
-        const int grp = append_group<C>(it, half, seg, base);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (grp >= 0) {
-            // A fragment rows gq, gq + 8 (rows past B hold stale bytes; their
-            // results are dropped), B fragment column gq = weight row gq
-            const uint8_t *x0 = xs + gq * stride + 2 * k0 + 4 * tq;
-            const uint8_t *x1 = x0 + 8 * stride;
-            const uint8_t *w = ws + (8 * half + gq) * stride + 2 * k0 + 4 * tq;
-#pragma unroll 4
-            for (int k = 0; k < kper; k += 16) {
-                uint32_t a[4];
-                a[0] = *reinterpret_cast<const uint32_t *>(x0 + 2 * k);
-                a[1] = *reinterpret_cast<const uint32_t *>(x1 + 2 * k);
-                a[2] = *reinterpret_cast<const uint32_t *>(x0 + 2 * k + 16);
-                a[3] = *reinterpret_cast<const uint32_t *>(x1 + 2 * k + 16);
-                mma_bf16_16816(acc, a, *reinterpret_cast<const uint32_t *>(w + 2 * k),
-                               *reinterpret_cast<const uint32_t *>(w + 2 * k + 16));
-            }
-        }
-        red[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        __syncthreads();
-        if (grp >= 0 && wq == 0) {
-            float4 t = red[warp * 32 + lane];
-#pragma unroll
-            for (int w = 1; w < 4; ++w) {
-                const float4 u = red[(warp + w) * 32 + lane];
-                t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
-            }
-            // accumulator fragment: row gq holds columns 2tq, 2tq+1 in (x, y),
-            // row gq + 8 in (z, w)
-            const int width = seg < 2 ? C::DH : HR;  // row length of the pool
-            const int col = grp * 8 - base + 2 * tq;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int b = gq + 8 * hh;
-                if (b >= P.B || dst[b] < 0) continue;
-                *reinterpret_cast<uint32_t *>(P.pool[seg] + dst[b] * width + col) =
-                    hh ? pack_bf16(t.z, t.w) : pack_bf16(t.x, t.y);
-            }
-        }
-        __syncthreads();
-    }
-    // the ring reuses the staging area: order these generic reads before its
-    // async-proxy writes
-    fence_proxy_async_smem();
-    return ok;
-}
-
-// Bytes of ring the fused step's staging needs (16 rows of X, 16 weight rows).
-__host__ __device__ constexpr size_t fused_step_stage_bytes(int d) {
-    return (size_t)32 * (2 * d + kFusedStepStride);
 }
 
 // The running maximum (log2 units) only moves when a tile exceeds it by this
@@ -645,7 +484,7 @@ __device__ __forceinline__ CtaRange cta_range(const FastParams &P, int g, int G,
     const int Bn = P.B;
     const int per = (Bn + NT - 1) / NT;
     const int lo = min(Bn, tid * per), hi = min(Bn, lo + per);
-    auto len_of = [&](int bb) { return streamed_len(P.seq_lens[bb], P.max_len, P.len_shift); };
+    auto len_of = [&](int bb) { return streamed_len(P.seq_lens[bb], P.max_len); };
     // with at most one request per thread its length stays in a register
     const int32_t my_len = lo < hi ? len_of(lo) : 0;
     auto len_at = [&](int bb) { return (per == 1) ? my_len : len_of(bb); };
@@ -743,25 +582,10 @@ __global__ void __launch_bounds__(C::NT, 1)
             for (size_t o = (size_t)tid * 128; o < pt_bytes; o += (size_t)C::NT * 128)
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(P.page_table) + o));
     }
-    // fused step (bf16 caches): the new rows' staging copies go out first and
-    // land while the plan below is computed
-    const bool fused = !C::Q8 && C::NGRP == 1 && P.X != nullptr;
-    if (fused && tid == 0) {
-        uint64_t *abar = reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR);
-        mbar_init(abar, 1);
-        fence_barrier_init();
-        append_issue<C>(P, smem, abar, 0);
-    }
-
     int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
     const CtaRange rg = cta_range<C::NT>(P, g, (int)gridDim.x, pl);
     const int32_t start0 = rg.start, end = rg.end;
     if (start0 >= end) {
-        if (fused &&
-            !append_new_rows<C>(P, smem, reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR),
-                                reinterpret_cast<float4 *>(smem + C::OFF_RED),
-                                reinterpret_cast<int64_t *>(smem + C::OFF_DST)))
-            if (tid == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
         pdl_wait();
         return;
     }
@@ -769,12 +593,6 @@ __global__ void __launch_bounds__(C::NT, 1)
     const bool local = rg.local;
     const int32_t *off = rg.off;  // off[b] for this CTA's requests
 
-    // fused step: project and write the new rows before the ring's first copies
-    if (fused &&
-        !append_new_rows<C>(P, smem, reinterpret_cast<uint64_t *>(smem + C::OFF_ABAR),
-                            reinterpret_cast<float4 *>(smem + C::OFF_RED),
-                            reinterpret_cast<int64_t *>(smem + C::OFF_DST)))
-        if (tid == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
     if (tid == 0) {
         // given scores: two arrivals per phase, the cache rows' and the scores'
         for (int s = 0; s < C::STAGES; ++s) {
@@ -789,8 +607,7 @@ __global__ void __launch_bounds__(C::NT, 1)
         cur->page_key = pl[2];
         cur->page_id = pl[3];
         cursor_begin_segment<C>(cur, off, end);
-        // the ring is untouched, except by the fused step's staging, which
-        // fenced its reads already
+        // the ring is untouched: no generic-proxy access precedes these copies
         for (int s = 0; s < C::STAGES; ++s)
             issue_next<C>(cur, P, M, off, smem, full, okf, end, false, C::GS ? pend : nullptr);
     }
@@ -1577,14 +1394,6 @@ static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
     P.scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     P.ws = ws;
     P.status = a.status;
-    P.X = static_cast<const __nv_bfloat16 *>(a.X);
-    for (int k = 0; k < 4; ++k) P.W[k] = static_cast<const __nv_bfloat16 *>(a.W[k]);
-    P.pool[0] = static_cast<__nv_bfloat16 *>(c.S_K);
-    P.pool[1] = static_cast<__nv_bfloat16 *>(c.S_V);
-    P.pool[2] = static_cast<__nv_bfloat16 *>(c.R_K);
-    P.pool[3] = static_cast<__nv_bfloat16 *>(c.R_V);
-    P.d = a.d;
-    P.len_shift = a.X ? 1 : 0;
     P.sc = c.dtype == LRKV_FP8_E4M3 ? make_float4(c.scale[0], c.scale[1], c.scale[2], c.scale[3])
                                     : make_float4(1.f, 1.f, 1.f, 1.f);
     P.norm = c.N_K != nullptr;
@@ -1651,16 +1460,6 @@ bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype, int 
 }
 
 int fast_decode_grid(int, int) { return device_sm_count(); }
-
-bool fast_decode_step_fits(int H, int r, int d) {
-#define X(h, rr)                                                                            \
-    if (H == h && r == rr)                                                                  \
-        return fused_step_stage_bytes(d) <=                                                 \
-               (size_t)Pick<h, rr>::STAGES * Pick<h, rr>::stage;
-    LRKV_FAST_SHAPES(X)
-#undef X
-    return false;
-}
 
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const int H = a.cache.H, r = a.cache.r;

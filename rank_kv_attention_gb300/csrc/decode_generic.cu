@@ -97,11 +97,12 @@ template <typename T, bool ROPE, int NTHR>
 __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_kernel(
     const T *__restrict__ q, const T *__restrict__ B_K, const int32_t *__restrict__ seq_lens,
     T *__restrict__ out,
-    int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged, int len_shift,
-    DecodeWs ws, int32_t *status, const float2 *__restrict__ rope_tab, RopeFastWs rf) {
+    int B, int H, int d_h, int r, int max_len, int G, int tile_align, bool staged,
+    DecodeWs ws, int32_t *status, const float2 *__restrict__ rope_tab, RopeFastWs rf, bool early) {
     constexpr int nrows = (ROPE || NTHR == 128) ? 1 : kProRows;
     const int tid = threadIdx.x;
-    if (blockIdx.x < (unsigned)H) {
+    const PdlTail tail{early};  // early mode: the dependency wait runs as the block exits
+    if (!early && blockIdx.x < (unsigned)H) {
         // warm L2 with this block's B_K[h] and query rows while the
         // predecessor finishes: a prefetch reads nothing into the block, and
         // the loads below, after the wait, see every earlier write
@@ -116,8 +117,10 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + o));
         }
     }
-    pdl_wait();
-    pdl_launch_dependents();
+    if (!early) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     if (blockIdx.x == (unsigned)H) {
         // requests with an invalid length get a zero output (no segment will
         // ever write it)
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
         const int per = (B + blockDim.x - 1) / blockDim.x;
         const int lo = tid * per, hi = min(B, lo + per);
         int32_t s = 0;
-        for (int b = lo; b < hi; ++b) s += streamed_len(seq_lens[b], max_len, len_shift);
+        for (int b = lo; b < hi; ++b) s += streamed_len(seq_lens[b], max_len);
         part[tid] = s;
         __syncthreads();
         constexpr int NPL = NTHR / 32;  // partial sums per lane
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
             const int32_t L = seq_lens[b];
             bad |= (L < 1 || L > max_len);
             ws.off[b] = run;
-            run += streamed_len(L, max_len, len_shift);
+            run += streamed_len(L, max_len);
         }
         if (bad) status_or(status, LRKV_STATUS_BAD_SEQLEN);
         return;
@@ -604,39 +607,16 @@ __global__ void __launch_bounds__(kGenTile) decode_split_generic_kernel(
 // ---------------------------------------------------------------------------
 constexpr int kCombSeg = 16;  // segments whose partials a thread keeps in flight
 
-// Fused decode step: the new row (position seq_lens[b] - 1, written by the
-// split kernel) enters the merge as one more key.
-template <typename T>
-struct CombineStep {
-    const T *q, *S_K, *S_V, *R_K, *R_V;
-    const int32_t *seq_lens, *page_table;
-    int max_pages, page_size, num_pages, max_len;
-    float scale_log2;  // log2(e) / sqrt(d_h): the partials' units
-    int on;
-};
-
 template <typename T>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict__ B_V,
                                                              int B, int H, int d_h, int r,
                                                              bool staged, DecodeWs ws,
-                                                             T *__restrict__ out,
-                                                             const CombineStep<T> st) {
+                                                             T *__restrict__ out) {
     extern __shared__ __align__(16) float cs[];
     const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-    // Until the wait below only caller inputs are read (they were complete
-    // before the prologue got past its own wait, which precedes this grid's
-    // launch): the new row's pool slot, and B_V[h] staged in shared memory
-    // while the split kernel is still running.
-    size_t nrow = 0;  // pool row of the fused step's new row
-    bool has_new = false;
-    if (st.on) {
-        const int32_t Ln = st.seq_lens[b];
-        if (Ln < 1 || Ln > st.max_len) return;  // zeroed and flagged by the prologue
-        const int pos = Ln - 1;
-        const int32_t page = st.page_table[(size_t)b * st.max_pages + pos / st.page_size];
-        has_new = page >= 0 && page < st.num_pages;  // else flagged by the split kernel
-        if (has_new) nrow = (size_t)page * st.page_size + pos % st.page_size;
-    }
+    // Until the wait below only a caller input is read (complete before the
+    // prologue got past its own wait, which precedes this grid's launch):
+    // B_V[h], staged in shared memory while the split kernel is still running.
     T *bv = reinterpret_cast<T *>(cs);                                   // [d_h][r] when staged
     const T *src = B_V + (size_t)h * d_h * r;
     const int nthr = blockDim.x, nwarp = nthr >> 5;
@@ -661,12 +641,12 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
     pdl_launch_dependents();
     const int32_t o0 = ws.off[b], o1 = ws.off[b + 1];
     T *dst = out + ((size_t)b * H + h) * d_h;
-    if (o1 <= o0 && !has_new) {
+    if (o1 <= o0) {
         for (int d = tid; d < d_h; d += blockDim.x) Elem<T>::store(dst + d, 0.f);
         return;
     }
     const int32_t chunk = ws.plan->chunk;
-    const int g_lo = o1 > o0 ? o0 / chunk : 0, nseg = o1 > o0 ? (o1 - 1) / chunk - g_lo + 1 : 0;
+    const int g_lo = o0 / chunk, nseg = (o1 - 1) / chunk - g_lo + 1;
     const int W = d_h + r;
     const size_t s0 = ((size_t)b + g_lo) * H + h;  // slot of segment g: s0 + g H
     float *cr = cs + (staged ? ((size_t)d_h * r * sizeof(T) + 15) / 16 * 4 : 0);  // [r]
@@ -687,30 +667,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
         v0[g] = (g < nseg && c0 < W) ? ws.acc[(s0 + (size_t)g * H) * W + c0] : 0.f;
         v1[g] = (g < nseg && c1 < W) ? ws.acc[(s0 + (size_t)g * H) * W + c1] : 0.f;
     }
-    // the new row: score (log2 units) and this thread's value columns
-    __shared__ float red_s[8];
-    float s_new = -INFINITY, nv0 = 0.f, nv1 = 0.f;
-    if (has_new) {
-        float part = 0.f;
-        const T *qr = st.q + ((size_t)b * H + h) * d_h;
-        for (int i = tid; i < d_h; i += nthr)
-            part = fmaf(Elem<T>::load(qr + i), Elem<T>::load(st.S_K + nrow * d_h + i), part);
-        for (int i = tid; i < r; i += nthr)
-            part = fmaf(ws.p[((size_t)b * H + h) * r + i],
-                        Elem<T>::load(st.R_K + (nrow * H + h) * r + i), part);
-        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if ((tid & 31) == 0) red_s[tid >> 5] = part;
-        auto val = [&](int c) {
-            return c < d_h ? Elem<T>::load(st.S_V + nrow * d_h + c)
-                           : Elem<T>::load(st.R_V + (nrow * H + h) * r + (c - d_h));
-        };
-        if (c0 < W) nv0 = val(c0);
-        if (c1 < W) nv1 = val(c1);
-        __syncthreads();
-        float sum = 0.f;
-        for (int i = 0; i < nwarp; ++i) sum += red_s[i];
-        s_new = sum * st.scale_log2;
-    }
     // 2. merge weights
     float mx = m_my;
     for (int k = tid + nthr; k < nseg; k += nthr) mx = fmaxf(mx, ws.ml[(s0 + (size_t)k * H) * 2]);
@@ -719,7 +675,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
     __syncthreads();
     float M = red[0][0];
     for (int i = 1; i < nwarp; ++i) M = fmaxf(M, red[0][i]);
-    M = fmaxf(M, s_new);
     for (int k = tid; k < nseg; k += blockDim.x) {
         const float mk = (k == tid) ? m_my : ws.ml[(s0 + (size_t)k * H) * 2];
         w[k] = (mk == -INFINITY) ? 0.f : exp2f(mk - M);
@@ -734,11 +689,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const T *__restrict
     __syncthreads();
     float L = 0.f;
     for (int i = 0; i < nwarp; ++i) L += red[1][i];
-    const float w_new = has_new ? exp2f(s_new - M) : 0.f;
-    L += w_new;
     const float invL = (L > 0.f) ? 1.f / L : 0.f;
-    a0 = w_new * nv0;
-    a1 = w_new * nv1;
     // 3. weighted sums over segments
 #pragma unroll
     for (int g = 0; g < kCombSeg; ++g) {
@@ -813,8 +764,8 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
     return launch_pdl(kern, grid, dim3(small ? 128 : kProThreads), sm, a.stream,
                       static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
                       static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
-                      max_len, G, tile_align, staged, a.X ? 1 : 0, ws, a.status,
-                      reinterpret_cast<const float2 *>(a.rope), a.rope_ws);
+                      max_len, G, tile_align, staged, ws, a.status,
+                      reinterpret_cast<const float2 *>(a.rope), a.rope_ws, a.early);
 }
 
 template <typename T, typename TC, int RP>
@@ -898,23 +849,9 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G) {
         attr_set = true;
     }
     const int nthr = (a.cache.d_h + a.cache.r <= 256) ? 128 : 256;
-    CombineStep<T> st;
-    st.on = a.X != nullptr;
-    st.q = static_cast<const T *>(a.q);
-    st.S_K = static_cast<const T *>(a.cache.S_K);
-    st.S_V = static_cast<const T *>(a.cache.S_V);
-    st.R_K = static_cast<const T *>(a.cache.R_K);
-    st.R_V = static_cast<const T *>(a.cache.R_V);
-    st.seq_lens = a.seq_lens;
-    st.page_table = a.page_table;
-    st.max_pages = a.max_pages;
-    st.page_size = a.cache.page_size;
-    st.num_pages = a.cache.num_pages;
-    st.max_len = a.max_pages * a.cache.page_size;
-    st.scale_log2 = 1.4426950408889634f / sqrtf((float)a.cache.d_h);
     return launch_pdl(decode_combine_kernel<T>, grid, dim3(nthr), sm, a.stream,
                       static_cast<const T *>(a.B_V), a.B, a.cache.H, a.cache.d_h, a.cache.r,
-                      staged, ws, static_cast<T *>(a.out), st);
+                      staged, ws, static_cast<T *>(a.out));
 }
 
 template cudaError_t launch_prologue<float>(const DecodeArgs &, const DecodeWs &, int, int, bool);

@@ -19,14 +19,6 @@ struct DecodeArgs {
     void *out;
     int32_t *status;
     cudaStream_t stream;
-    // Fused decode step (lrkv_decode_step) when X != nullptr: the B new rows
-    // X [B, d] are projected through W = {W_S_K, W_S_V, U_K, U_V} and written
-    // at position seq_lens[b] - 1 inside the split kernel; the split kernels
-    // stream rows 0 .. seq_lens[b] - 2 and the combine folds row
-    // seq_lens[b] - 1 in as one more key.
-    const void *X = nullptr;
-    const void *W[4] = {nullptr, nullptr, nullptr, nullptr};
-    int d = 0;
     // Exact rotary position embedding when rope != nullptr: the cos/sin table
     // [rope_max_pos][d_h / 2] of lrkv_rope_table, and its f16 copy.  With
     // rope_ws.wf set (lrkv_decode_rope on a tensor-core shape) the rotary
@@ -36,6 +28,12 @@ struct DecodeArgs {
     const __half *rope16 = nullptr;
     int rope_max_pos = 0;
     RopeFastWs rope_ws = {};
+    // The prologue's predecessor in the stream is the same call's append
+    // (lrkv_decode_step), which writes none of q, B_K, seq_lens, out or the
+    // workspace, and which let it launch only after passing its own wait: the
+    // prologue then does all its work first and waits for the append at its
+    // end, so the private queries overlap the append.
+    bool early = false;
 };
 
 // Longest sequence length a decode attends: what the page table can hold;
@@ -56,9 +54,9 @@ constexpr int kRopeMaxRank = 64;
 cudaError_t launch_rope_table(double base, int d_h, int max_pos, void *table, cudaStream_t s);
 
 // Rows the split kernels stream for a request of length L: none for an
-// invalid length, else L, minus the new row that a fused step folds in later.
-__host__ __device__ __forceinline__ int32_t streamed_len(int32_t L, int max_len, int shift) {
-    return (L < 1 || L > max_len) ? 0 : L - shift;
+// invalid length, else L.
+__host__ __device__ __forceinline__ int32_t streamed_len(int32_t L, int max_len) {
+    return (L < 1 || L > max_len) ? 0 : L;
 }
 
 // beside_split: the tensor-core split kernel follows (smaller prologue blocks).
@@ -74,10 +72,6 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G);
 // (H, r) pairs).  `fast_decode_supported` says whether a shape is covered;
 // `fast_decode_grid` is its CTA count on this device.
 bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype, int groups = 1);
-// Rows a fused decode step may append inside the split kernel, and whether
-// its staging (16 rows of X and 16 weight rows of d) fits a shape's ring.
-constexpr int kFusedStepMaxRows = 16;
-bool fast_decode_step_fits(int H, int r, int d);
 int fast_decode_grid(int H, int r);
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G);
 

@@ -207,13 +207,18 @@ static int check_append(const void *X, const int32_t *positions, const int32_t *
 static int run_append(const void *X, const int32_t *positions, const int32_t *seq_ids, int n,
                       int d, const void *W_S_K, const void *W_S_V, const void *U_K,
                       const void *U_V, const lrkv_cache_t *c, const int32_t *page_table, int B,
-                      int max_pages, int32_t *status, cudaStream_t s) {
+                      int max_pages, int32_t *status, cudaStream_t s,
+                      const int32_t *step_lens = nullptr) {
+    // step_lens: row i is request i's row at position step_lens[i] - 1
+    // (positions and seq_ids unused)
     if (n == 0) return LRKV_OK;
     cudaError_t e;
     prof_before(LRKV_PROFILE_PROJECTION, s);
     if (c->dtype != LRKV_F32) {  // bf16 rows and weights (bf16 or 8-bit cache)
         auto a = make_append_args<__nv_bfloat16>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K,
                                                  U_V, c, page_table, B, max_pages, status, s);
+        a.step_lens = step_lens;
+        a.step_max_len = max_pages * c->page_size;
         if (rows_mma_append_fits(a)) e = launch_append_rows_mma(a);
         else if (rows_append_fits(a)) e = launch_append_rows(a);
         else if (tc_append_supported(n, d, c->d_h, c->H, c->r)) e = launch_append_tc(a);
@@ -221,6 +226,8 @@ static int run_append(const void *X, const int32_t *positions, const int32_t *se
     } else {
         auto a = make_append_args<float>(X, positions, seq_ids, n, d, W_S_K, W_S_V, U_K, U_V, c,
                                          page_table, B, max_pages, status, s);
+        a.step_lens = step_lens;
+        a.step_max_len = max_pages * c->page_size;
         e = rows_append_fits(a) ? launch_append_rows(a) : launch_append_generic(a);
     }
     prof_after(LRKV_PROFILE_PROJECTION, s);
@@ -414,12 +421,12 @@ int lrkv_decode_noalloc(const void *q, const lrkv_cache_t *cache, const void *B_
     return run_decode(a, scratch, (size_t)LRKV_NOALLOC_SCRATCH_BYTES);
 }
 
-// Decode-step workspace: the decode workspace, then positions and ids of the
-// new rows for shapes that run the separate append.
+// Decode-step workspace: the decode's (the append derives its rows' places
+// from the lengths and needs none).
 static size_t step_ws_bytes(int B, int H, int d_h, int r, int max_seq_len, size_t *dec_bytes) {
     const size_t dec = align256(decode_ws_bytes(B, H, d_h, r, max_seq_len));
     if (dec_bytes) *dec_bytes = dec;
-    return dec + 2 * align256(sizeof(int32_t) * (size_t)B);
+    return dec;
 }
 
 size_t lrkv_decode_step_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
@@ -464,31 +471,18 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     a.out = out;
     a.status = dev_status;
     a.stream = s;
-    const bool fused = cache->dtype == LRKV_BF16 && !cache->N_K && cache_groups(*cache) == 1 &&
-                       d % 128 == 0 && B <= kFusedStepMaxRows &&
-                       fast_decode_supported(cache->H, cache->d_h, cache->r, cache->page_size,
-                                             cache->dtype, 1) &&
-                       fast_decode_step_fits(cache->H, cache->r, d);
-    if (fused) {
-        a.X = X;
-        a.W[0] = W_S_K;
-        a.W[1] = W_S_V;
-        a.W[2] = U_K;
-        a.W[3] = U_V;
-        a.d = d;
-        return run_decode(a, workspace, dec_bytes);
-    }
-    int32_t *pos = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + dec_bytes);
-    int32_t *sid = pos + align256(sizeof(int32_t) * (size_t)B) / sizeof(int32_t);
-    cudaError_t e = launch_step_rows(seq_lens, B, max_pages * cache->page_size, pos, sid, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    st = run_append(X, pos, sid, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B, max_pages,
-                    dev_status, s);
+    // the append (and the key norms) place request b's row at seq_lens[b] - 1
+    // themselves; the decode's prologue then overlaps them, since its inputs
+    // are none of theirs
+    st = run_append(X, nullptr, nullptr, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table, B,
+                    max_pages, dev_status, s, seq_lens);
     if (st) return st;
     if (cache->N_K) {
-        e = launch_key_norms(pos, sid, B, B_K, *cache, page_table, B, max_pages, dev_status, s);
+        cudaError_t e = launch_key_norms(nullptr, nullptr, B, B_K, *cache, page_table, B, max_pages,
+                                         dev_status, s, seq_lens);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    a.early = true;
     return run_decode(a, workspace, dec_bytes);
 }
 

@@ -412,6 +412,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Scope guard of a kernel that works before its dependency wait: when on,
+// the wait (and the launch of dependents) runs as the thread leaves the
+// scope, on every return path.
+struct PdlTail {
+    bool on;
+    __device__ ~PdlTail() {
+        if (on) {
+            pdl_wait();
+            pdl_launch_dependents();
+        }
+    }
+};
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

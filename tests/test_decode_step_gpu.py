@@ -1,10 +1,11 @@
 """GPU parity of lrkv_decode_step (through the C ABI): each request's new row
 lands where lrkv_append would put it (position seq_lens[b] - 1), nothing else
 in the cache changes, and the output matches the float64 oracle's
-append-then-decode.  Covers the fused shapes (the split kernel projects and
-writes the new rows, the combine folds them in), shapes that run the separate
-append and decode kernels, a request whose only row is the new one, invalid
-lengths and pages, and the 16 x 4096 decode workload."""
+append-then-decode.  Covers the tensor-core decode shapes, shapes that run
+the generic kernels, a request whose only row is the new one, more than 64
+requests (the many-row append kernel), invalid lengths and pages, and the
+16 x 4096 decode workload.  The append kernels take each row's place from the
+lengths and the decode's prologue runs beside the append."""
 import numpy as np
 import pytest
 import torch
@@ -83,10 +84,10 @@ def _new_slots(case, which=None):
 LENS = [1, 17, 300, 64, 65, 129]
 
 
-# (H, r, d): the shapes the tensor-core decode covers, with d % 128 == 0
+# (H, r, d): shapes the tensor-core decode covers
 @pytest.mark.parametrize("H,r,d", [(16, 48, 2048), (32, 32, 256), (16, 64, 256), (16, 16, 512),
                                    (16, 56, 384)])
-def test_decode_step_fused_parity(H, r, d):
+def test_decode_step_tensor_core_parity(H, r, d):
     case, w, X = _step_case(H, 128, r, LENS, d, "bf16", seed=H * 100 + r + d)
     out, dc, st = _run_step(case, w, X)
     assert st == 0
@@ -98,8 +99,8 @@ def test_decode_step_fused_parity(H, r, d):
     assert_close(host(out, "bf16"), ref, "bf16", f"H={H} r={r} d={d}")
 
 
-# d not a multiple of 128, d_h != 128 and an fp32 cache run lrkv_append's and
-# lrkv_decode's kernels in turn; 32-row pages run the fused path
+# d not a multiple of 32 (the FMA few-row append), d_h != 128 (the generic
+# decode), an fp32 cache and 32-row pages
 @pytest.mark.parametrize("H,d_h,r,d,dtype,ps", [(16, 128, 48, 136, "bf16", 64),
                                                 (8, 64, 24, 256, "bf16", 64),
                                                 (4, 16, 4, 64, "f32", 64),
@@ -116,9 +117,25 @@ def test_decode_step_other_shapes(H, d_h, r, d, dtype, ps):
     assert_close(host(out, dtype), ref, dtype, f"H={H} d_h={d_h} r={r} d={d} {dtype} ps={ps}")
 
 
+def test_decode_step_many_requests():
+    """70 requests: the step's rows go through the many-row (tcgen05) append
+    kernel with places taken from the lengths."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 200, size=70)]
+    case, w, X = _step_case(16, 128, 48, lens, 256, "bf16", seed=53)
+    out, dc, st = _run_step(case, w, X)
+    assert st == 0
+    pools = _oracle(case, w, X)
+    _check_cache(case, dc, pools, _new_slots(case))
+    f = lambda a: I.to_f64(a, "bf16")
+    ref = oracle.decode(f(case.q), *pools, f(case.B_K), f(case.B_V), case.page_table,
+                        case.seq_lens, case.page_size)
+    assert_close(host(out, "bf16"), ref, "bf16", "70 requests")
+
+
 def test_decode_step_equals_append_then_decode():
-    """The fused step and lrkv_append + lrkv_decode agree (same inputs, two
-    copies of the cache)."""
+    """The step and lrkv_append + lrkv_decode agree (same inputs, two copies
+    of the cache)."""
     import rank_kv_attention_gb300 as L
     lens = [5, 900, 64, 1, 333]
     case, w, X = _step_case(16, 128, 48, lens, 1024, "bf16", seed=31)
@@ -129,7 +146,7 @@ def test_decode_step_equals_append_then_decode():
     L.append(dev(X, "bf16"), pos, ids, dev(w.W_S_K, "bf16"), dev(w.W_S_V, "bf16"),
              dev(w.U_K, "bf16"), dev(w.U_V, "bf16"), dc.cache, dc.page_table)
     out_s = dc.run()
-    assert_close(host(out_f, "bf16"), host(out_s, "bf16"), "bf16", "fused vs separate")
+    assert_close(host(out_f, "bf16"), host(out_s, "bf16"), "bf16", "step vs separate")
     for a, b in zip((dc_f.cache.S_K, dc_f.cache.R_V), (dc.cache.S_K, dc.cache.R_V)):
         assert_close(host(a, "bf16")[_new_slots(case)], host(b, "bf16")[_new_slots(case)], "bf16")
 
