@@ -369,35 +369,65 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- end to end through the C ABI with host buffers
     Ke = args.e2e_steps or max(50, min(K, 2000))
-    # the step's inputs (new rows X, queries, lengths; positions and ids for
-    # the rotary path's lrkv_append) live in one pinned host staging buffer and
-    # move with one copy; the C-ABI calls take device views of its device twin
-    # (256-byte aligned)
-    parts = (X, q, seq_lens) + ((pos, sid) if rope else ())
-    offs, o = [], 0
-    for t in parts:
-        offs.append(o)
-        o += (t.numel() * t.element_size() + 255) // 256 * 256
-    hbuf = torch.empty(o, dtype=torch.uint8).pin_memory()
-    dbuf = torch.empty(o, dtype=torch.uint8, device=dev)
-    views = []
-    for t, a in zip(parts, offs):
-        nb = t.numel() * t.element_size()
-        hbuf[a:a + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
-        views.append(dbuf[a:a + nb].view(t.dtype).view(t.shape))
-    dX, dq, dsl = views[:3]
-    dpos, dsid = views[3:] if rope else (pos, sid)
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dout = torch.empty_like(out)
-    calls = make_calls(dX, dq, dpos, dsid, dsl, dout)
-    h2d = hbuf.numel()   # the staging buffer as copied (payload rounded up to 256 B per input)
     d2h = hout.numel() * hout.element_size()
+    if not rope:
+        # a step graph (lrkv_step_graph_create, one per rotated cache copy)
+        # replays lrkv_decode_step_host: X, q and the lengths in pinned host
+        # memory are copied in, the step runs and out is copied back, with one
+        # launch; the host then waits for the result
+        hX, hq, hsl = (t.cpu().contiguous().pin_memory() for t in (X, q, seq_lens))
+        ws_h = L.workspace(L.decode_step_host_workspace_bytes(Bn, H, d_h, r, d, max_seq), dev)
+        graphs = []
+        for dsc in descs:
+            hg = ctypes.c_void_p()
+            rc = lib.lrkv_step_graph_create(ctypes.byref(hg), P(hX), d, P(Wsk), P(Wsv), P(Uk), P(Uv),
+                                            P(hq), ctypes.byref(dsc), P(BK), P(BV), P(hsl), P(pt), Bn,
+                                            pt.shape[1], max_seq, P(hout), P(ws_h), ws_h.numel(),
+                                            P(status))
+            if rc:
+                raise RuntimeError(f"lrkv_step_graph_create failed: {rc}")
+            graphs.append(hg)
+        h2d = sum(t.numel() * t.element_size() for t in (hX, hq, hsl))
+        e2e_note = ("lrkv_step_graph_launch (lrkv_decode_step_host as a graph): pinned host X, q "
+                    "and lengths copied in by a copy kernel through their device-mapped "
+                    "addresses, the step, out written back to pinned host memory by the decode's "
+                    "last kernel, then the host synchronises; every step")
 
-    def e2e_step(i):
-        dbuf.copy_(hbuf, non_blocking=True)
-        step(i)
-        hout.copy_(dout, non_blocking=True)
-        stream.synchronize()   # the host reads this step's result
+        def e2e_step(i):
+            rc = lib.lrkv_step_graph_launch(graphs[i % n_copies], sp)
+            if rc:
+                raise RuntimeError(f"lrkv_step_graph_launch failed: {rc}")
+            stream.synchronize()   # the host reads this step's result
+    else:
+        # the rotary path: the step's inputs (new rows, queries, lengths,
+        # positions, ids) live in one pinned host staging buffer and move with
+        # one copy; the C-ABI calls take device views of its device twin
+        # (256-byte aligned)
+        parts = (X, q, seq_lens, pos, sid)
+        offs, o = [], 0
+        for t in parts:
+            offs.append(o)
+            o += (t.numel() * t.element_size() + 255) // 256 * 256
+        hbuf = torch.empty(o, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(o, dtype=torch.uint8, device=dev)
+        views = []
+        for t, a in zip(parts, offs):
+            nb = t.numel() * t.element_size()
+            hbuf[a:a + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            views.append(dbuf[a:a + nb].view(t.dtype).view(t.shape))
+        dX, dq, dsl, dpos, dsid = views
+        dout = torch.empty_like(out)
+        calls = make_calls(dX, dq, dpos, dsid, dsl, dout)
+        h2d = hbuf.numel()   # the staging buffer as copied (payload rounded up to 256 B per input)
+        e2e_note = ("pinned host inputs (one staging buffer) copied in, result copied out and "
+                    "synchronised every step")
+
+        def e2e_step(i):
+            dbuf.copy_(hbuf, non_blocking=True)
+            step(i)
+            hout.copy_(dout, non_blocking=True)
+            stream.synchronize()   # the host reads this step's result
 
     for i in range(5):
         e2e_step(i)
@@ -412,6 +442,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(g0.elapsed_time(g1))
+    if not rope:
+        for hg in graphs:
+            lib.lrkv_step_graph_destroy(hg)
 
     # ---- numbers
     ms_step = total_ms / K
@@ -475,8 +508,7 @@ def run_ours(args, rank, world, local_rank):
                          "lrkv_append_then_lrkv_decode": None if separate_ms is None else round(separate_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "pinned host inputs (one staging buffer) copied in, result copied out and "
-                        "synchronised every step"},
+                "note": e2e_note},
         # per step: append, [key norms,] prologue, [rotary scores,] split, combine
         "gpu_launches": (4 + int(norm) + int(rope)) * K,
         "clocks": clk,

@@ -258,6 +258,66 @@ LRKV_API int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const
                               int32_t max_pages, int32_t max_seq_len, void *out, void *workspace,
                               size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream);
 
+/*
+ * lrkv_decode_step_host - lrkv_decode_step with the step's per-token inputs
+ * and its output in HOST memory: the new rows X, the queries q and the
+ * lengths seq_lens are copied to the device, the step runs, and out is
+ * copied back, all enqueued on `stream` by this one call (it does not
+ * synchronise: read out_host after the stream has reached this point).
+ * Weights, bases, the cache and the page table stay on the device.
+ *
+ *   X_host [B, d], q_host [B, H, d_h], out_host [B, H, d_h]: host memory,
+ *     element type as lrkv_decode_step; seq_lens_host [B] int32, host.
+ *     Page-locked buffers (cudaHostAlloc / cudaHostRegister) let the copies
+ *     run asynchronously; pageable ones work but the copies then block.
+ *   workspace >= lrkv_decode_step_host_workspace_bytes(B, H, d_h, r, d,
+ *                max_seq_len, dtype) bytes of device memory, 256-byte
+ *                aligned: the step's workspace plus device copies of the
+ *                inputs and the output.
+ *
+ * Errors as lrkv_decode_step, checked before anything is enqueued; a failed
+ * copy returns LRKV_E_CUDA.
+ */
+LRKV_API size_t lrkv_decode_step_host_workspace_bytes(int32_t B, int32_t H, int32_t d_h,
+                                                      int32_t r, int32_t d, int32_t max_seq_len,
+                                                      int32_t dtype);
+LRKV_API int lrkv_decode_step_host(const void *X_host, int32_t d, const void *W_S_K,
+                                   const void *W_S_V, const void *U_K, const void *U_V,
+                                   const void *q_host, const lrkv_cache_t *cache, const void *B_K,
+                                   const void *B_V, const int32_t *seq_lens_host,
+                                   const int32_t *page_table, int32_t B, int32_t max_pages,
+                                   int32_t max_seq_len, void *out_host, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status,
+                                   lrkv_stream_t stream);
+
+/*
+ * Decode-step graphs - lrkv_decode_step_host recorded once as a CUDA graph
+ * (the three input copies, the step's kernels with their programmatic
+ * dependencies, the output copy) and replayed per step with one launch, so
+ * the host's per-step cost is one graph launch instead of eight enqueues.
+ *
+ * lrkv_step_graph_create takes the arguments of lrkv_decode_step_host and
+ * checks them the same way; nothing runs.  The graph keeps every pointer and
+ * size it was made with: each lrkv_step_graph_launch reads X_host, q_host and
+ * seq_lens_host as they are when the copies run (refill them between steps;
+ * every length stays within max_seq_len) and writes out_host, which the
+ * caller reads after synchronising the stream.  The cache, weights, page
+ * table and workspace must stay allocated while the graph exists.
+ *
+ * Returns LRKV_OK and sets *graph, or an error (then *graph = NULL).
+ * lrkv_step_graph_destroy frees a graph (NULL is a no-op).
+ */
+typedef struct lrkv_step_graph_s *lrkv_step_graph_t;
+LRKV_API int lrkv_step_graph_create(lrkv_step_graph_t *graph, const void *X_host, int32_t d,
+                                    const void *W_S_K, const void *W_S_V, const void *U_K,
+                                    const void *U_V, const void *q_host, const lrkv_cache_t *cache,
+                                    const void *B_K, const void *B_V, const int32_t *seq_lens_host,
+                                    const int32_t *page_table, int32_t B, int32_t max_pages,
+                                    int32_t max_seq_len, void *out_host, void *workspace,
+                                    size_t workspace_bytes, int32_t *dev_status);
+LRKV_API int lrkv_step_graph_launch(lrkv_step_graph_t graph, lrkv_stream_t stream);
+LRKV_API void lrkv_step_graph_destroy(lrkv_step_graph_t graph);
+
 /* Bytes of device workspace lrkv_prefill needs. */
 LRKV_API size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h,
                                     int32_t r, int32_t max_ctx, int32_t dtype);

@@ -17,7 +17,8 @@ __all__ = [
     "decode_workspace_bytes", "prefill_workspace_bytes", "cache_bytes", "workspace",
     "prefill_kernel_kind", "decode_step", "decode_step_workspace_bytes", "rope_table",
     "decode_rope", "prefill_rope", "key_norms", "RopeTable", "rope_table_bytes",
-    "decode_rope_workspace_bytes",
+    "decode_rope_workspace_bytes", "decode_step_host", "decode_step_host_workspace_bytes",
+    "StepGraph",
 ]
 
 
@@ -28,7 +29,8 @@ def __getattr__(name):
                 "prefill_workspace_bytes", "cache_bytes", "workspace", "prefill_kernel_kind",
                 "decode_step", "decode_step_workspace_bytes", "rope_table", "decode_rope",
                 "prefill_rope", "key_norms", "RopeTable", "rope_table_bytes",
-                "decode_rope_workspace_bytes"):
+                "decode_rope_workspace_bytes", "decode_step_host",
+                "decode_step_host_workspace_bytes", "StepGraph"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

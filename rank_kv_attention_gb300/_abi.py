@@ -77,6 +77,13 @@ SIGNATURES = {
     "lrkv_decode_step_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32]),
     "lrkv_decode_step": (ctypes.c_int, [P, I32, P, P, P, P, P, CACHE_P, P, P, P, P, I32, I32, I32, P,
                                         P, SZ, P, P]),
+    "lrkv_decode_step_host_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
+    "lrkv_decode_step_host": (ctypes.c_int, [P, I32, P, P, P, P, P, CACHE_P, P, P, P, P, I32, I32, I32,
+                                             P, P, SZ, P, P]),
+    "lrkv_step_graph_create": (ctypes.c_int, [ctypes.POINTER(P), P, I32, P, P, P, P, P, CACHE_P, P, P,
+                                              P, P, I32, I32, I32, P, P, SZ, P]),
+    "lrkv_step_graph_launch": (ctypes.c_int, [P, P]),
+    "lrkv_step_graph_destroy": (None, [P]),
     "lrkv_prefill_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "lrkv_prefill": (ctypes.c_int, [P, P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, CACHE_P, P,
                                     I32, P, P, SZ, P, P]),

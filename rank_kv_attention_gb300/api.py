@@ -202,6 +202,112 @@ def decode_step(X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_l
     return out
 
 
+def decode_step_host_workspace_bytes(B, H, d_h, r, d, max_seq_len, dtype=torch.bfloat16) -> int:
+    return _abi.lib().lrkv_decode_step_host_workspace_bytes(B, H, d_h, r, d, max_seq_len, _DT[dtype])
+
+
+def decode_step_host(X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_lens,
+                     page_table, max_seq_len, out=None, ws=None, status=None, stream=None):
+    """lrkv_decode_step_host: the decode step with X, q, seq_lens and out in
+    host memory (CPU tensors, best pinned); the copies and the step are
+    enqueued on the stream, which the caller synchronises before reading out."""
+    dt = cache.act_dtype
+    for n, t in (("X", X), ("q", q)):
+        _need(t, n, dt, device=False)
+        if t.is_cuda:
+            raise ValueError(f"{n} must be a host tensor")
+    _need(seq_lens, "seq_lens", torch.int32, device=False)
+    if seq_lens.is_cuda:
+        raise ValueError("seq_lens must be a host tensor")
+    for n, t in (("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V), ("B_K", B_K),
+                 ("B_V", B_V)):
+        _need(t, n, dt)
+    _need(page_table, "page_table", torch.int32)
+    B, H, d_h = q.shape
+    r = cache.R_K.shape[3]
+    d = X.shape[1]
+    if out is None:
+        out = torch.empty(q.shape, dtype=dt, pin_memory=True)
+    _need(out, "out", dt, device=False)
+    if out.is_cuda:
+        raise ValueError("out must be a host tensor")
+    need = decode_step_host_workspace_bytes(B, H, d_h, r, d, max_seq_len, dt)
+    if ws is None:
+        ws = workspace(need, page_table.device)
+    _need(ws, "ws", torch.uint8)
+    desc = cache.desc()
+    code = _abi.lib().lrkv_decode_step_host(_ptr(X), d, _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K),
+                                            _ptr(U_V), _ptr(q), ctypes.byref(desc), _ptr(B_K),
+                                            _ptr(B_V), _ptr(seq_lens), _ptr(page_table), B,
+                                            page_table.shape[1], max_seq_len, _ptr(out), _ptr(ws),
+                                            ws.numel(), _ptr(status), _stream(stream))
+    _abi.check("lrkv_decode_step_host", code)
+    return out
+
+
+class StepGraph:
+    """lrkv_step_graph_*: the host-buffer decode step recorded once as a
+    CUDA graph and replayed with one launch per step.  The graph keeps every
+    tensor it was made with (held here so they stay allocated): refill X, q
+    and seq_lens (pinned host tensors) between steps, launch, synchronise
+    the stream, then read out."""
+
+    def __init__(self, X, W_S_K, W_S_V, U_K, U_V, q, cache: PagedCache, B_K, B_V, seq_lens,
+                 page_table, max_seq_len, out=None, ws=None, status=None):
+        dt = cache.act_dtype
+        for n, t in (("X", X), ("q", q)):
+            _need(t, n, dt, device=False)
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError(f"{n} must be a pinned host tensor")
+        _need(seq_lens, "seq_lens", torch.int32, device=False)
+        if seq_lens.is_cuda or not seq_lens.is_pinned():
+            raise ValueError("seq_lens must be a pinned host tensor")
+        for n, t in (("W_S_K", W_S_K), ("W_S_V", W_S_V), ("U_K", U_K), ("U_V", U_V),
+                     ("B_K", B_K), ("B_V", B_V)):
+            _need(t, n, dt)
+        _need(page_table, "page_table", torch.int32)
+        B, H, d_h = q.shape
+        r, d = cache.R_K.shape[3], X.shape[1]
+        if out is None:
+            out = torch.empty(q.shape, dtype=dt, pin_memory=True)
+        if out.is_cuda or not out.is_pinned():
+            raise ValueError("out must be a pinned host tensor")
+        _need(out, "out", dt, device=False)
+        if ws is None:
+            ws = workspace(decode_step_host_workspace_bytes(B, H, d_h, r, d, max_seq_len, dt),
+                           page_table.device)
+        _need(ws, "ws", torch.uint8)
+        self._desc = cache.desc()
+        self._keep = (X, W_S_K, W_S_V, U_K, U_V, q, cache, B_K, B_V, seq_lens, page_table, ws,
+                      status)
+        self.X, self.q, self.seq_lens, self.out = X, q, seq_lens, out
+        h = ctypes.c_void_p()
+        code = _abi.lib().lrkv_step_graph_create(
+            ctypes.byref(h), _ptr(X), d, _ptr(W_S_K), _ptr(W_S_V), _ptr(U_K), _ptr(U_V), _ptr(q),
+            ctypes.byref(self._desc), _ptr(B_K), _ptr(B_V), _ptr(seq_lens), _ptr(page_table), B,
+            page_table.shape[1], max_seq_len, _ptr(out), _ptr(ws), ws.numel(), _ptr(status))
+        _abi.check("lrkv_step_graph_create", code)
+        self._h = h
+
+    def launch(self, stream=None):
+        """Enqueue one step (copies in, kernels, copy out) on the stream."""
+        if self._h is None:
+            raise ValueError("graph destroyed")
+        _abi.check("lrkv_step_graph_launch", _abi.lib().lrkv_step_graph_launch(self._h, _stream(stream)))
+        return self.out
+
+    def close(self):
+        if self._h is not None:
+            _abi.lib().lrkv_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def prefill(X, Q, cu_rows, start_pos, max_ctx, W_S_K, W_S_V, U_K, U_V, B_K, B_V,
             cache: PagedCache, page_table, out=None, ws=None, status=None, stream=None):
     """lrkv_prefill: append the chunk X, then causal attention for each row's Q."""

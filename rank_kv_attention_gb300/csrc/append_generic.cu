@@ -8,6 +8,8 @@
 // page id in all four pools.
 #include "append_kernels.cuh"
 
+#include <algorithm>
+
 namespace lrkv {
 
 // Destination pool row (page * page_size + slot) of append row i, or -1.
@@ -381,6 +383,41 @@ __global__ void prefill_rows_kernel(const int32_t *__restrict__ cu_rows,
 }
 
 
+
+// Decode step with host buffers: copies up to three page-locked host
+// buffers (device-mapped addresses) into device memory in one launch, 16, 4
+// or 2 bytes per access as the addresses and sizes allow.
+__global__ void __launch_bounds__(256) stage_copy_kernel(StageCopy c) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t nth = (size_t)gridDim.x * blockDim.x;
+#pragma unroll 1
+    for (int k = 0; k < StageCopy::kMax; ++k) {
+        const char *src = static_cast<const char *>(c.src[k]);
+        char *dst = static_cast<char *>(c.dst[k]);
+        const size_t n = c.bytes[k];
+        const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) | n;
+        if (al % 16 == 0) {
+            for (size_t i = t0; i < n / 16; i += nth)
+                reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(src)[i];
+        } else if (al % 4 == 0) {
+            for (size_t i = t0; i < n / 4; i += nth)
+                reinterpret_cast<uint32_t *>(dst)[i] = reinterpret_cast<const uint32_t *>(src)[i];
+        } else {
+            for (size_t i = t0; i < n / 2; i += nth)
+                reinterpret_cast<uint16_t *>(dst)[i] = reinterpret_cast<const uint16_t *>(src)[i];
+        }
+    }
+}
+
+cudaError_t launch_stage_copy(const StageCopy &c, cudaStream_t s) {
+    size_t most = 0;
+    for (int k = 0; k < StageCopy::kMax; ++k) most = c.bytes[k] > most ? c.bytes[k] : most;
+    const unsigned blocks = (unsigned)std::min<size_t>(4 * (size_t)device_sm_count(),
+                                                       std::max<size_t>(1, (most / 16 + 255) / 256));
+    return launch_pdl(stage_copy_kernel, dim3(blocks), dim3(256), 0, s, c);
+}
 
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,

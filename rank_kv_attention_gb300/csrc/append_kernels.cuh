@@ -70,6 +70,15 @@ bool tc_append_supported(int n, int d, int d_h, int H, int r);
 cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a);
 int device_sm_count();  // SMs of the current device (lrkv_api.cu)
 
+// Up to three buffer copies (even byte counts) done by one kernel; unused
+// entries have bytes = 0.
+struct StageCopy {
+    static constexpr int kMax = 3;
+    const void *src[kMax] = {nullptr, nullptr, nullptr};
+    void *dst[kMax] = {nullptr, nullptr, nullptr};
+    size_t bytes[kMax] = {0, 0, 0};
+};
+cudaError_t launch_stage_copy(const StageCopy &c, cudaStream_t s);
 cudaError_t launch_prefill_rows(const int32_t *cu_rows, const int32_t *start_pos, int B, int n,
                                 int max_len, int32_t *pos, int32_t *sid, int32_t *vlen,
                                 int32_t *req_row, int32_t *status, cudaStream_t s);

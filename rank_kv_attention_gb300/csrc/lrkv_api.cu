@@ -435,14 +435,13 @@ size_t lrkv_decode_step_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32
     return step_ws_bytes(B, H, d_h, r, max_seq_len, nullptr);
 }
 
-int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_S_V,
-                     const void *U_K, const void *U_V, const void *q, const lrkv_cache_t *cache,
-                     const void *B_K, const void *B_V, const int32_t *seq_lens,
-                     const int32_t *page_table, int32_t B, int32_t max_pages,
-                     int32_t max_seq_len, void *out, void *workspace, size_t workspace_bytes,
-                     int32_t *dev_status, lrkv_stream_t stream) {
-    // the append's checks (positions and ids are derived here, so any
-    // non-null stand-in passes) and the decode's
+// Host-side checks of a decode step (the append's, with positions and ids
+// derived from the lengths, and the decode's).
+static int check_step(const void *X, int32_t d, const void *W_S_K, const void *W_S_V,
+                      const void *U_K, const void *U_V, const void *q, const lrkv_cache_t *cache,
+                      const void *B_K, const void *B_V, const int32_t *seq_lens,
+                      const int32_t *page_table, int32_t B, int32_t max_pages,
+                      int32_t max_seq_len, const void *out) {
     int st = check_append(X, seq_lens, seq_lens, B, d, W_S_K, W_S_V, U_K, U_V, cache, page_table,
                           B, max_pages);
     if (st) return st;
@@ -452,6 +451,18 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     if (!q || !B_K || !B_V || !out) return LRKV_E_INVALID_ARG;
     if (!aligned16(q) || !aligned16(B_K) || !aligned16(B_V) || !aligned16(out))
         return LRKV_E_INVALID_ARG;
+    return LRKV_OK;
+}
+
+int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_S_V,
+                     const void *U_K, const void *U_V, const void *q, const lrkv_cache_t *cache,
+                     const void *B_K, const void *B_V, const int32_t *seq_lens,
+                     const int32_t *page_table, int32_t B, int32_t max_pages,
+                     int32_t max_seq_len, void *out, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_step(X, d, W_S_K, W_S_V, U_K, U_V, q, cache, B_K, B_V, seq_lens, page_table, B,
+                        max_pages, max_seq_len, out);
+    if (st) return st;
     if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
     size_t dec_bytes = 0;
     if (workspace_bytes < step_ws_bytes(B, cache->H, cache->d_h, cache->r, max_seq_len, &dec_bytes))
@@ -484,6 +495,174 @@ int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const void *W_
     }
     a.early = true;
     return run_decode(a, workspace, dec_bytes);
+}
+
+// Host-buffer decode step: the step's workspace, then device copies of X,
+// q, seq_lens and out (256-byte aligned each).
+struct HostStepWs {
+    size_t step, x, q, lens, out, bytes;
+};
+
+static HostStepWs host_step_layout(int B, int H, int d_h, int r, int d, int max_seq_len,
+                                   int dtype) {
+    HostStepWs w;
+    const size_t eb = dtype == LRKV_F32 ? 4 : 2;  // activations: fp32, else bf16
+    size_t o = step_ws_bytes(B, H, d_h, r, max_seq_len, nullptr);
+    w.step = o;
+    w.x = o; o += align256((size_t)B * d * eb);
+    w.q = o; o += align256((size_t)B * H * d_h * eb);
+    w.lens = o; o += align256(sizeof(int32_t) * (size_t)B);
+    w.out = o; o += align256((size_t)B * H * d_h * eb);
+    w.bytes = o;
+    return w;
+}
+
+// Device address of page-locked (or registered) host memory, if it has one;
+// a failed lookup leaves no pending error behind.
+static bool host_mapped(const void *p, void **dev) {
+    *dev = nullptr;
+    if (cudaHostGetDevicePointer(dev, const_cast<void *>(p), 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        *dev = nullptr;
+        return false;
+    }
+    return *dev != nullptr;
+}
+
+static int check_host_step(const void *X_host, int32_t d, const void *W_S_K, const void *W_S_V,
+                           const void *U_K, const void *U_V, const void *q_host,
+                           const lrkv_cache_t *cache, const void *B_K, const void *B_V,
+                           const int32_t *seq_lens_host, const int32_t *page_table, int32_t B,
+                           int32_t max_pages, int32_t max_seq_len, const void *out_host,
+                           const void *workspace, size_t workspace_bytes) {
+    if (!X_host || !q_host || !seq_lens_host || !out_host) return LRKV_E_INVALID_ARG;
+    if (!workspace || !aligned256(workspace)) return LRKV_E_WORKSPACE;
+    // the device copies (256-byte aligned, inside the workspace) stand in for
+    // the host buffers, which need no alignment
+    int st = check_step(workspace, d, W_S_K, W_S_V, U_K, U_V, workspace, cache, B_K, B_V,
+                        seq_lens_host, page_table, B, max_pages, max_seq_len, workspace);
+    if (st) return st;
+    if (workspace_bytes <
+        host_step_layout(B, cache->H, cache->d_h, cache->r, d, max_seq_len, cache->dtype).bytes)
+        return LRKV_E_WORKSPACE;
+    return LRKV_OK;
+}
+
+size_t lrkv_decode_step_host_workspace_bytes(int32_t B, int32_t H, int32_t d_h, int32_t r,
+                                             int32_t d, int32_t max_seq_len, int32_t dtype) {
+    if (check_dims(H, d_h, r, dtype) || B < 1 || max_seq_len < 1 || d < 1 || d > 65536) return 0;
+    return host_step_layout(B, H, d_h, r, d, max_seq_len, dtype).bytes;
+}
+
+int lrkv_decode_step_host(const void *X_host, int32_t d, const void *W_S_K, const void *W_S_V,
+                          const void *U_K, const void *U_V, const void *q_host,
+                          const lrkv_cache_t *cache, const void *B_K, const void *B_V,
+                          const int32_t *seq_lens_host, const int32_t *page_table, int32_t B,
+                          int32_t max_pages, int32_t max_seq_len, void *out_host, void *workspace,
+                          size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream) {
+    int st = check_host_step(X_host, d, W_S_K, W_S_V, U_K, U_V, q_host, cache, B_K, B_V,
+                             seq_lens_host, page_table, B, max_pages, max_seq_len, out_host,
+                             workspace, workspace_bytes);
+    if (st) return st;
+    const HostStepWs w = host_step_layout(B, cache->H, cache->d_h, cache->r, d, max_seq_len,
+                                          cache->dtype);
+    char *base = static_cast<char *>(workspace);
+    const size_t eb = cache->dtype == LRKV_F32 ? 4 : 2;
+    const size_t x_bytes = (size_t)B * d * eb, q_bytes = (size_t)B * cache->H * cache->d_h * eb;
+    cudaStream_t s = (cudaStream_t)stream;
+    // page-locked buffers are read and written by the kernels through their
+    // device-mapped addresses (one copy kernel stages the inputs, the decode's
+    // last kernel writes out); other host memory goes through the copy engines
+    void *mX, *mq, *ml, *mo;
+    const bool in_mapped = host_mapped(X_host, &mX) && host_mapped(q_host, &mq) &&
+                           host_mapped(seq_lens_host, &ml);
+    const bool out_mapped = host_mapped(out_host, &mo) && aligned16(mo);
+    cudaError_t e = cudaSuccess;
+    if (in_mapped) {
+        StageCopy c;
+        c.src[0] = mX; c.dst[0] = base + w.x; c.bytes[0] = x_bytes;
+        c.src[1] = mq; c.dst[1] = base + w.q; c.bytes[1] = q_bytes;
+        c.src[2] = ml; c.dst[2] = base + w.lens; c.bytes[2] = sizeof(int32_t) * (size_t)B;
+        e = launch_stage_copy(c, s);
+    } else {
+        e = cudaMemcpyAsync(base + w.x, X_host, x_bytes, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(base + w.q, q_host, q_bytes, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(base + w.lens, seq_lens_host, sizeof(int32_t) * (size_t)B,
+                                cudaMemcpyHostToDevice, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = lrkv_decode_step(base + w.x, d, W_S_K, W_S_V, U_K, U_V, base + w.q, cache, B_K, B_V,
+                          reinterpret_cast<const int32_t *>(base + w.lens), page_table, B, max_pages,
+                          max_seq_len, out_mapped ? mo : base + w.out, workspace, w.step,
+                          dev_status, stream);
+    if (st || out_mapped) return st;
+    e = cudaMemcpyAsync(out_host, base + w.out, q_bytes, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+}
+
+}  // extern "C"
+
+struct lrkv_step_graph_s {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+int lrkv_step_graph_create(lrkv_step_graph_t *graph, const void *X_host, int32_t d,
+                           const void *W_S_K, const void *W_S_V, const void *U_K, const void *U_V,
+                           const void *q_host, const lrkv_cache_t *cache, const void *B_K,
+                           const void *B_V, const int32_t *seq_lens_host, const int32_t *page_table,
+                           int32_t B, int32_t max_pages, int32_t max_seq_len, void *out_host,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status) {
+    if (!graph) return LRKV_E_INVALID_ARG;
+    *graph = nullptr;
+    const int chk = check_host_step(X_host, d, W_S_K, W_S_V, U_K, U_V, q_host, cache, B_K, B_V,
+                                    seq_lens_host, page_table, B, max_pages, max_seq_len, out_host,
+                                    workspace, workspace_bytes);
+    if (chk) return chk;
+    // record on a private stream (relaxed mode: the launchers' one-time
+    // kernel attribute calls run during the recording); a failed check ends
+    // the capture before any node exists
+    cudaStream_t cs;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e);
+    auto *g = new lrkv_step_graph_s;
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+    int st = e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+    if (st == LRKV_OK) {
+        st = lrkv_decode_step_host(X_host, d, W_S_K, W_S_V, U_K, U_V, q_host, cache, B_K, B_V,
+                                   seq_lens_host, page_table, B, max_pages, max_seq_len, out_host,
+                                   workspace, workspace_bytes, dev_status, cs);
+        e = cudaStreamEndCapture(cs, &g->graph);
+        if (st == LRKV_OK && e != cudaSuccess) st = cuda_fail(e);
+    }
+    if (st == LRKV_OK) {
+        e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+        if (e != cudaSuccess) st = cuda_fail(e);
+    }
+    cudaStreamDestroy(cs);
+    if (st != LRKV_OK) {
+        lrkv_step_graph_destroy(g);
+        return st;
+    }
+    *graph = g;
+    return LRKV_OK;
+}
+
+int lrkv_step_graph_launch(lrkv_step_graph_t graph, lrkv_stream_t stream) {
+    if (!graph || !graph->exec) return LRKV_E_INVALID_ARG;
+    const cudaError_t e = cudaGraphLaunch(graph->exec, (cudaStream_t)stream);
+    return e == cudaSuccess ? LRKV_OK : cuda_fail(e);
+}
+
+void lrkv_step_graph_destroy(lrkv_step_graph_t graph) {
+    if (!graph) return;
+    if (graph->exec) cudaGraphExecDestroy(graph->exec);
+    if (graph->graph) cudaGraphDestroy(graph->graph);
+    delete graph;
 }
 
 size_t lrkv_prefill_workspace_bytes(int32_t B, int32_t n, int32_t H, int32_t d_h, int32_t r,

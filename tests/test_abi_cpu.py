@@ -199,6 +199,62 @@ def test_decode_step_rejects_on_host(lib):
     assert lib.lrkv_decode_step_workspace_bytes(0, 16, 128, 48, 4096, 1) == 0
 
 
+def test_decode_step_host_rejects_on_host(lib):
+    """The host-buffer step checks everything before it enqueues a copy; its
+    host buffers need no alignment, its workspace holds the step's plus the
+    device copies of X, q, the lengths and out."""
+    ws = ctypes.c_void_p(256)
+
+    def call(**over):
+        a = dict(X=3, d=2048, W=16, q=5, c=_cache(), BK=16, BV=16, sl=7, pt=16, B=2, mp=4,
+                 msl=100, out=9, ws=ws, wsb=1 << 30)
+        a.update(over)
+        return lib.lrkv_decode_step_host(a["X"], a["d"], a["W"], a["W"], a["W"], a["W"], a["q"],
+                                         ctypes.byref(a["c"]), a["BK"], a["BV"], a["sl"], a["pt"],
+                                         a["B"], a["mp"], a["msl"], a["out"], a["ws"], a["wsb"],
+                                         None, None)
+    for k in ("X", "q", "sl", "out", "W", "BK", "pt"):
+        assert call(**{k: None}) == _abi.LRKV_E_INVALID_ARG, k
+    assert call(BK=8) == _abi.LRKV_E_INVALID_ARG           # device bases stay 16-byte aligned
+    assert call(d=2047) == _abi.LRKV_E_SHAPE
+    assert call(msl=4 * 64 + 1) == _abi.LRKV_E_BOUNDS
+    assert call(ws=None) == _abi.LRKV_E_WORKSPACE
+    assert call(ws=ctypes.c_void_p(272)) == _abi.LRKV_E_WORKSPACE   # 256-byte alignment
+    need = lib.lrkv_decode_step_host_workspace_bytes(2, 16, 128, 48, 2048, 100, 1)
+    assert call(wsb=need - 1) == _abi.LRKV_E_WORKSPACE
+    step = lib.lrkv_decode_step_workspace_bytes(2, 16, 128, 48, 100, 1)
+    # + X (2 x 2048), q and out (2 x 16 x 128) bf16, lengths: each rounded to 256 bytes
+    assert need == step + 8192 + 8192 + 256 + 8192
+    assert lib.lrkv_decode_step_host_workspace_bytes(2, 16, 128, 48, 0, 100, 1) == 0
+
+
+def test_step_graph_checks_before_recording(lib):
+    """lrkv_step_graph_create checks its arguments like the host step before
+    it touches a stream (so these run without a GPU); NULL handles are
+    refused or ignored."""
+    ws = ctypes.c_void_p(256)
+    h = ctypes.c_void_p(12345)
+
+    def create(**over):
+        a = dict(X=3, d=2048, W=16, q=5, c=_cache(), BK=16, BV=16, sl=7, pt=16, B=2, mp=4,
+                 msl=100, out=9, ws=ws, wsb=1 << 30)
+        a.update(over)
+        return lib.lrkv_step_graph_create(ctypes.byref(h), a["X"], a["d"], a["W"], a["W"], a["W"],
+                                          a["W"], a["q"], ctypes.byref(a["c"]), a["BK"], a["BV"],
+                                          a["sl"], a["pt"], a["B"], a["mp"], a["msl"], a["out"],
+                                          a["ws"], a["wsb"], None)
+    assert create(X=None) == _abi.LRKV_E_INVALID_ARG and h.value is None
+    h.value = 12345
+    assert create(sl=None) == _abi.LRKV_E_INVALID_ARG and h.value is None
+    assert create(msl=4 * 64 + 1) == _abi.LRKV_E_BOUNDS
+    assert create(wsb=1024) == _abi.LRKV_E_WORKSPACE
+    assert lib.lrkv_step_graph_create(None, 3, 2048, 16, 16, 16, 16, 5, ctypes.byref(_cache()), 16,
+                                      16, 7, 16, 2, 4, 100, 9, ws, 1 << 30, None) == \
+        _abi.LRKV_E_INVALID_ARG
+    assert lib.lrkv_step_graph_launch(None, None) == _abi.LRKV_E_INVALID_ARG
+    lib.lrkv_step_graph_destroy(None)
+
+
 def test_rope_host_checks(lib):
     """Rotary entry points reject bad tables and shapes before any launch."""
     E = _abi

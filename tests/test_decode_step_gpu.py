@@ -199,3 +199,98 @@ def test_decode_step_T4096_sampled():
                         case.seq_lens, case.page_size, pairs=pairs)
     idx = tuple(np.array(pairs).T)
     assert_close(host(out, "bf16")[idx], ref[idx], "bf16", "decode_T4096 step")
+
+
+@pytest.mark.parametrize("dtype,H,d_h,r,d,pinned", [("bf16", 16, 128, 48, 2048, True),
+                                                    ("f32", 4, 16, 4, 64, True),
+                                                    ("bf16", 16, 128, 48, 2048, False)])
+def test_decode_step_host_buffers(dtype, H, d_h, r, d, pinned):
+    """lrkv_decode_step_host (X, q, lengths and out in host memory) gives the
+    same bits as lrkv_decode_step on device copies of the same inputs, in the
+    output and in the cache, and matches the oracle.  Page-locked buffers go
+    through their device-mapped addresses (a copy kernel in, the combine's
+    stores out), pageable ones through the copy engines."""
+    import rank_kv_attention_gb300 as L
+    lens = [5, 900, 64, 1, 333]
+    case, w, X = _step_case(H, d_h, r, lens, d, dtype, seed=61)
+    out_d, dc_d, st_d = _run_step(case, w, X)
+    dc = DevDecode(case)
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    hX = pin(host_tensor(X, dtype))
+    hq = pin(dc.q.cpu())
+    hl = pin(torch.from_numpy(np.ascontiguousarray(case.seq_lens, dtype=np.int32)))
+    ho = pin(torch.full(tuple(dc.q.shape), float("nan"), dtype=dc.q.dtype))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_h = L.decode_step_host(hX, dev(w.W_S_K, dtype), dev(w.W_S_V, dtype), dev(w.U_K, dtype),
+                               dev(w.U_V, dtype), hq, dc.cache, dc.B_K, dc.B_V, hl, dc.page_table,
+                               dc.max_seq_len, out=ho, status=st)
+    torch.cuda.synchronize()
+    assert out_h is ho and out_h.is_pinned() == pinned
+    assert int(st.item()) == 0 and st_d == 0
+    assert torch.equal(out_h.view(torch.int16 if dtype == "bf16" else torch.int32),
+                       out_d.cpu().view(torch.int16 if dtype == "bf16" else torch.int32))
+    for a, b in zip((dc.cache.S_K, dc.cache.S_V, dc.cache.R_K, dc.cache.R_V),
+                    (dc_d.cache.S_K, dc_d.cache.S_V, dc_d.cache.R_K, dc_d.cache.R_V)):
+        assert np.array_equal(host_bits(a), host_bits(b))
+    pools = _oracle(case, w, X)
+    f = lambda a: I.to_f64(a, dtype)
+    ref = oracle.decode(f(case.q), *pools, f(case.B_K), f(case.B_V), case.page_table,
+                        case.seq_lens, case.page_size)
+    assert_close(host(out_h, dtype), ref, dtype, f"host step {dtype}")
+
+
+def host_tensor(a, kind):
+    """A pinned host tensor of an array of bf16 bits or fp32 values."""
+    if kind == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).pin_memory()
+
+
+def test_step_graph_replays_with_new_inputs():
+    """A step graph recorded once and launched for two consecutive steps,
+    with the pinned inputs refilled in between (new rows, new queries,
+    lengths + 1), gives the same bits as lrkv_decode_step_host called for the
+    same two steps on a second copy of the cache, and matches the oracle."""
+    import rank_kv_attention_gb300 as L
+    lens = [5, 900, 64, 1, 333]
+    H, d_h, r, d = 16, 128, 48, 2048
+    case, w, X = _step_case(H, d_h, r, [x + 1 for x in lens], d, "bf16", seed=71)
+    rng = np.random.default_rng(72)
+    X2 = I.f32_to_bf16_bits(rng.standard_normal(X.shape).astype(np.float32))
+    q2 = I.f32_to_bf16_bits(rng.standard_normal(case.q.shape).astype(np.float32))
+    steps = [(X, case.q, np.array(lens, np.int32)), (X2, q2, np.array(lens, np.int32) + 1)]
+    Wd = [dev(getattr(w, n), "bf16") for n in ("W_S_K", "W_S_V", "U_K", "U_V")]
+    dg, dh = DevDecode(case), DevDecode(case)
+    hX, hq = host_tensor(X, "bf16"), host_tensor(case.q, "bf16")
+    hl = torch.zeros(len(lens), dtype=torch.int32).pin_memory()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = L.StepGraph(hX, *Wd, hq, dg.cache, dg.B_K, dg.B_V, hl, dg.page_table, dg.max_seq_len,
+                    status=st)
+    outs = []
+    for Xs, qs, ls in steps:
+        hX.copy_(host_tensor(Xs, "bf16"))
+        hq.copy_(host_tensor(qs, "bf16"))
+        hl.copy_(torch.from_numpy(ls))
+        g.launch()
+        torch.cuda.synchronize()
+        ref = L.decode_step_host(host_tensor(Xs, "bf16"), *Wd, host_tensor(qs, "bf16"), dh.cache,
+                                 dh.B_K, dh.B_V, torch.from_numpy(ls).pin_memory(), dh.page_table,
+                                 dh.max_seq_len, status=st)
+        torch.cuda.synchronize()
+        assert torch.equal(g.out.view(torch.int16), ref.view(torch.int16))
+        outs.append(host(g.out, "bf16"))
+    g.close()
+    assert int(st.item()) == 0
+    for a, b in zip((dg.cache.S_K, dg.cache.R_V), (dh.cache.S_K, dh.cache.R_V)):
+        assert np.array_equal(host_bits(a), host_bits(b))
+    # the oracle: both steps' rows appended, then the second step's decode
+    f = lambda a: I.to_f64(a, "bf16")
+    pools = [f(p) for p in (case.S_K, case.S_V, case.R_K, case.R_V)]
+    for Xs, _, ls in steps:
+        rows = oracle.project(f(Xs), f(w.W_S_K), f(w.W_S_V), f(w.U_K), f(w.U_V))
+        rows = [I.bf16_bits_to_f64(I.f32_to_bf16_bits(x.astype(np.float32))) for x in rows]
+        pools = oracle.place(pools, rows, ls - 1, np.arange(len(lens)), case.page_table,
+                             case.page_size)
+    ref = oracle.decode(f(q2), *pools, f(case.B_K), f(case.B_V), case.page_table, steps[1][2],
+                        case.page_size)
+    assert_close(outs[1], ref, "bf16", "graph step 2")
