@@ -154,7 +154,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
-ROPE_SCORE_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
+ROPE_SCORE_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh", "tc_common.cuh")
 
 
 def kernel_source_hash(files=DECODE_SPLIT_SOURCES):
@@ -478,7 +478,7 @@ def run_ours(args, rank, world, local_rank):
                    "step": ("lrkv_append (B new rows) + lrkv_decode_rope (B queries)" if rope else
                             "lrkv_decode_step (append of the B new rows" +
                             (", their reciprocal key norms" if norm else "") + ", decode of the B queries)")},
-        "roofline": ({"kernel": "rotary score kernel (f16 mma.sync; C_j W_h private products, rotated shared term)",
+        "roofline": ({"kernel": "rotary score kernel (tcgen05, f16/bf16 in, fp32 in tensor memory; C_j W_h private products, rotated shared term)",
                       "bound": "tensor", "achieved": round(rope_flops / (scores_ms / 1e3) / 1e12, 2),
                       "peak": bf16_peak, "unit": "TFLOP/s",
                       "frac": round(rope_flops / (scores_ms / 1e3) / 1e12 / bf16_peak, 4),

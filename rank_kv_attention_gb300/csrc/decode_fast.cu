@@ -36,6 +36,7 @@
 #include <algorithm>
 
 #include "decode_kernels.cuh"
+#include "tc_common.cuh"
 
 namespace lrkv {
 
@@ -108,8 +109,8 @@ struct FastParams {
     int norm;   // the cache holds joint key norms (a fifth copy per tile)
     int max_len;  // longest valid sequence length (longer requests are not attended)
     // rotary score kernel: operands from the prologue, scores out
-    const uint32_t *wf;
-    const float *qt;
+    const uint16_t *wt;
+    const uint16_t *qb;
     const float *wsc;
     float *sc_out;
 };
@@ -931,7 +932,7 @@ __global__ void __launch_bounds__(C::NT, 1)
 
 // ---------------------------------------------------------------------------
 // Rotary scores (reading note, section 8: exact RoPE over the factored
-// cache) for bf16 caches with d_h = 128, on the tensor cores.
+// cache) for bf16 caches with d_h = 128, on 5th-generation tensor cores.
 //
 // With i the query's position, q~ = q D_i and j a key's position, the score
 // of head h is
@@ -944,94 +945,144 @@ __global__ void __launch_bounds__(C::NT, 1)
 // score of every visible (row, head) to the plan-ordered score array; the
 // split kernel's given-score mode then streams S_V, R_V and those scores.
 //
-// One CTA streams a range of rows (the split kernel's plan with its own
-// CTA count) for a group of 8 heads, 8 warps; per 32-row tile (two 16-row
-// m-tiles), warp w
-//   * takes k-step w (channels 16w .. 16w+15) of the shared term for all 8
-//     heads: it turns the tile's S_K channel pairs by their table entries in
-//     registers (fp32, rounded to bf16), multiplies by q~ of the 8 heads (bf16
-//     hi + lo halves) and writes the partial sums to the stage, announced by a
-//     per-stage mbarrier that counts the 8 warps;
-//   * keeps W_h of head 8 grp + w as f16 mma B-fragments in registers
-//     (d_h r / 64 per thread; the W of 8 heads is 96 KB at r = 48, more than
-//     fits next to a copy ring), forms P = C_tile . W_h (mma.m16n8k16, f16 in,
-//     fp32 accumulate), dots each row of P with the row's R_K[h] (a quad
-//     shuffle reduction), and one tile later adds the 8 partial shared sums of
-//     its head (each lane of a quad finishes one of the quad's four rows).
-// Two warps per scheduler leave each thread up to 255 registers.  A tile
-// lands by TMA (128-byte swizzle) as the table rows (f16), the S_K rows and
-// the group's R_K columns; the last warp to release a stage refills it, as in
-// the split kernel.  32-row tiles halve the per-row cost of the waits and the
-// release, and give the private products 12 independent accumulators.
+// A CTA takes a range of rows (the split kernel's plan, one range per NG
+// CTAs) for a group of g heads (g = rope_tc_heads_per_cta(r)), in 128-row
+// tiles of one request:
+//   * warp 0 (one thread) lands by TMA, per tile, the table rows (f16) and
+//     the S_K rows (bf16) as two K-halves of 64 channels through a ring of
+//     half-tile stages (128-byte swizzle), and the group's R_K columns
+//     (bf16, 128- or 64-byte swizzle) into a ring of tile buffers; the S_K and
+//     R_K rows come in pieces of 32 to 128 rows, each inside one page.  Per
+//     request it lands the group's W^T (f16, [g r][128]) and query block
+//     (bf16, [16][128]);
+//   * warps 2-9 turn each landed S_K channel pair by its table entry in
+//     place (fp32, rounded to bf16);
+//   * warp 1 (one thread) issues tcgen05.mma (kind::f16, M = 128, fp32
+//     accumulate in tensor memory): the private products C_tile . W (N = g r)
+//     and the shared term (turned S_K) . [q~ values; q~ remainders]^T
+//     (N = 16), into one of two 256-column accumulators;
+//   * one tile later, warps 2-9 read the accumulator back (tcgen05.ld, one
+//     tile row per thread; two warps share a 32-lane quarter, each for half
+//     the heads), dot each head's r private columns with the row's R_K[h]
+//     from shared memory (the swizzle makes the row-per-thread reads free of
+//     bank conflicts), scale by the inverse W scale, add the shared value and
+//     remainder, and store the row's scores.
 // ---------------------------------------------------------------------------
-template <int H_, int R_, int STAGES_>
-struct RopeCfg {
-    static constexpr int H = H_, R = R_, TS = 32, STAGES = STAGES_, DH = 128;
-    static constexpr int HG = 8;                    // heads per CTA, one per warp
-    static constexpr int NG = H / HG;               // head groups
-    static constexpr int NCW = HG, NT = NCW * 32;   // warp w: head 8 grp + w, shared k-step w
-    static constexpr int NTN = R / 8;               // n-tiles of a head's private columns
-    static constexpr int BOX = TS * 128;            // one TS-row x 128-byte swizzled box
-    static constexpr int C_BYTES = 2 * BOX;         // table rows: 128 f16
-    static constexpr int S_BYTES = 2 * BOX;         // S_K rows: 128 bf16
-    static constexpr int RG_BOXES = HG * R * 2 / 128;  // the group's R_K columns
-    static constexpr int R_BYTES = RG_BOXES * BOX;
-    static constexpr int OFF_C = 0, OFF_SK = C_BYTES, OFF_RK = C_BYTES + S_BYTES;
-    static constexpr int STAGE_TX = C_BYTES + S_BYTES + R_BYTES;
-    // partial shared scores [k-step][head][SH_ROW] fp32: a head's TS rows, padded
-    // so that the writes (8 rows x 4 heads per instruction) hit distinct banks
-    static constexpr int SH_ROW = TS + 4;
-    static constexpr int OFF_SH = STAGE_TX;
-    static constexpr int STAGE = (STAGE_TX + 8 * HG * SH_ROW * 4 + 1023) / 1024 * 1024;
-    static constexpr int OFF_BAR = STAGES * STAGE;  // full[8], shd[8]
-    static constexpr int OFF_CNT = OFF_BAR + 128;   // release counters[STAGES]
-    static constexpr int OFF_OK = OFF_CNT + 64;     // per-stage "page id valid" flags
-    static constexpr int OFF_CUR = OFF_OK + 64;     // issue cursor
-    static constexpr int OFF_PLAN = OFF_CUR + 64;   // local plan
+template <int H_, int R_>
+struct RtcCfg {
+    static constexpr int H = H_, R = R_, DH = 128, TM = 128;  // tile rows = MMA M
+    static constexpr int HPC = rope_tc_heads_per_cta(R);       // heads per CTA
+    static constexpr int NG = H / HPC;                          // CTAs per row range
+    static constexpr int NPRIV = HPC * R;                       // private MMA N
+    static constexpr int EPI = 8, NT = (2 + EPI) * 32;          // producer, MMA, 8 turn/epilogue warps
+    static constexpr int HPE = HPC / 2;                         // heads per epilogue warp
+    static constexpr int HALF = TM * 128;                       // one K-half of a tile: 16 KB
+    static constexpr int STAGE = 2 * HALF;                      // half-tile stage: table + S_K
+    // R_K columns of the group: blocks of SWZ bytes per row (128-byte swizzle
+    // when the group's columns fill 64-element blocks, else 64-byte)
+    static constexpr int SWZ = (NPRIV % 64 == 0) ? 128 : 64;
+    static constexpr int RBLK = SWZ / 2;                        // elements per block row
+    static constexpr int NRB = NPRIV / RBLK;                    // blocks
+    static constexpr int RK_TILE = NRB * TM * SWZ;              // = TM * NPRIV * 2 bytes
+    static constexpr int W_BYTES = 2 * NPRIV * 128;             // W^T of the group, two K-halves
+    static constexpr int QB_BYTES = 2 * 16 * 128;               // query block, two K-halves
+    // two R_K buffers when that leaves two tiles of stages, up to four stages
+    static constexpr int BUDGET = 227 * 1024 - 3072 - W_BYTES - QB_BYTES;
+    static constexpr int RKB = (BUDGET - 2 * RK_TILE) / STAGE >= 2 ? 2 : 1;
+    static constexpr int S_FIT = (BUDGET - RKB * RK_TILE) / STAGE;
+    static constexpr int STAGES = S_FIT > 4 ? 4 : S_FIT;
+    static constexpr int OFF_RK = STAGES * STAGE;
+    static constexpr int OFF_W = OFF_RK + RKB * RK_TILE;
+    static constexpr int OFF_QB = OFF_W + W_BYTES;
+    // full[S], turned[S], empty[S], wfull, wfree, rkfull[2], rkfree[2],
+    // acc_full[2], acc_empty[2], drain
+    static constexpr int OFF_BAR = OFF_QB + QB_BYTES;
+    static constexpr int OFF_TMEM = OFF_BAR + 8 * (3 * STAGES + 11);
+    static constexpr int OFF_PLAN = OFF_TMEM + 16;
     static constexpr int SMEM = OFF_PLAN + 512 + 1024;  // + alignment slack
+    static constexpr int ACC = 256, SH_COL = 224;       // accumulator a at 256 a; shared term at +224
+    static constexpr uint32_t TMEM_COLS = 512;
 
-    static_assert(H % HG == 0 && R % 8 == 0 && R <= 64, "head groups of 8, whole n-tiles");
-    static_assert(STAGES >= 2 && STAGES <= 8, "barrier arrays hold 8 stages");
-    static_assert(STAGE % 1024 == 0, "128B-swizzle boxes need 1 KB alignment");
+    static_assert(H % HPC == 0 && HPC % 2 == 0, "whole head groups, two epilogue halves");
+    static_assert(STAGES >= 2, "a tile's two halves in flight");
+    static_assert(NPRIV <= SH_COL && NPRIV % 32 == 0, "private N fits before the shared columns");
+    static_assert((HPE * R) % 16 == 0, "whole 16-column TMEM loads per epilogue warp");
+    static_assert(W_BYTES % 1024 == 0 && RK_TILE % 1024 == 0, "1 KB-aligned swizzled buffers");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-struct RopeMaps {
-    CUtensorMap tab, sk, rk;
+struct RtcMaps {
+    CUtensorMap tab, sk, rk, wt, qb;
 };
 
-template <class C>
-__device__ void rope_issue_next(IssueCursor *cur, const FastParams &P, const RopeMaps &M,
-                                const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
-                                int32_t end, int grp, bool refill = true) {
-    if (cur->done) return;
-    const int s = cur->issued % C::STAGES;
-    const int row = cursor_row(cur, P, okf, s);
-    uint8_t *st = smem + s * C::STAGE;
-    if (refill) fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&full[s], C::STAGE_TX);
-    // table rows of positions t .. t + TS - 1 (read by every request: default
-    // policy); S_K rows are read by every head group, R_K columns once
-    tma_load_3d(st + C::OFF_C, &M.tab, 0, cur->t, 0, &full[s]);
-    tma_load_3d(st + C::OFF_SK, &M.sk, 0, row, 0, &full[s]);
-    tma_load_3d_hint(st + C::OFF_RK, &M.rk, 0, row, grp * C::RG_BOXES, &full[s],
-                     l2_evict_first_policy());
-    cursor_advance<C>(cur, off, end);
+// The 128-row tiles of a CTA's range in order: request segments, tiles
+// aligned to the request's positions.
+struct TileWalk {
+    int b, seg;
+    int32_t base, t, t_a, t_b, start;
+    bool done;
+};
+
+__device__ __forceinline__ void walk_segment(TileWalk &w, const int32_t *off, int32_t end, int tm) {
+    while (off[w.b + 1] <= w.start) ++w.b;
+    w.base = off[w.b];
+    w.t_a = w.start - w.base;
+    w.t_b = min(end, off[w.b + 1]) - w.base;
+    w.t = w.t_a / tm * tm;
+}
+
+__device__ __forceinline__ TileWalk walk_begin(const CtaRange &rg, int tm) {
+    TileWalk w;
+    w.b = rg.b0;
+    w.seg = 0;
+    w.start = rg.start;
+    w.done = rg.start >= rg.end;
+    if (!w.done) walk_segment(w, rg.off, rg.end, tm);
+    return w;
+}
+
+__device__ __forceinline__ void walk_next(TileWalk &w, const CtaRange &rg, int tm) {
+    w.t += tm;
+    if (w.t >= w.t_b) {
+        w.start = w.base + w.t_b;
+        if (w.start >= rg.end) {
+            w.done = true;
+            return;
+        }
+        ++w.seg;
+        walk_segment(w, rg.off, rg.end, tm);
+    }
+}
+
+// A bf16 channel pair (2c, 2c+1) turned by its f16 (cos, sin) table entry.
+__device__ __forceinline__ uint32_t turn_pair(uint32_t s, uint32_t cs) {
+    const float x0 = bf16lo(s), x1 = bf16hi(s);
+    const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&cs));
+    return pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+}
+
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
 template <class C>
 __global__ void __launch_bounds__(C::NT, 1)
-    rope_scores_kernel(const __grid_constant__ RopeMaps M, const FastParams P) {
+    rope_scores_tc_kernel(const __grid_constant__ RtcMaps M, const FastParams P, int br) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *shd = full + 8;
-    int *cnt = reinterpret_cast<int *>(smem + C::OFF_CNT);
-    int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
-    IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
+    uint64_t *turned = full + C::STAGES;
+    uint64_t *empty = turned + C::STAGES;
+    uint64_t *wfull = empty + C::STAGES;
+    uint64_t *wfree = wfull + 1;
+    uint64_t *rkfull = wfree + 1;
+    uint64_t *rkfree = rkfull + 2;
+    uint64_t *acc_full = rkfree + 2;
+    uint64_t *acc_empty = acc_full + 2;
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_TMEM);
     int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
-    constexpr int TS = C::TS;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = blockIdx.x % C::NG;
@@ -1039,8 +1090,10 @@ __global__ void __launch_bounds__(C::NT, 1)
         prefetch_tensormap(&M.tab);
         prefetch_tensormap(&M.sk);
         prefetch_tensormap(&M.rk);
+        prefetch_tensormap(&M.wt);
+        prefetch_tensormap(&M.qb);
     }
-    if (!P.req_row) {
+    if (!P.req_row) {  // the producer reads the page-table rows right after the plan
         const size_t pt_bytes = (size_t)P.B * P.max_pages * sizeof(int32_t);
         if (pt_bytes <= 64 * 1024)
             for (size_t o = (size_t)tid * 128; o < pt_bytes; o += (size_t)C::NT * 128)
@@ -1051,214 +1104,303 @@ __global__ void __launch_bounds__(C::NT, 1)
         pdl_wait();
         return;
     }
-    const int32_t *off = rg.off;
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&shd[s], C::NCW);
-            cnt[s] = 0;
+            mbar_init(&turned[s], C::EPI);
+            mbar_init(&empty[s], 1);
         }
+        mbar_init(wfull, 1);
+        mbar_init(wfree, 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&rkfull[k], 1);
+            mbar_init(&rkfree[k], C::EPI);
+            mbar_init(&acc_full[k], 1);
+            mbar_init(&acc_empty[k], C::EPI);
+        }
+        mbar_init(drain, 1);
         fence_barrier_init();
-        cur->b = rg.b0;
-        cur->start = rg.start;
-        cur->done = 0;
-        cur->issued = 0;
-        cur->page_key = pl[2];
-        cur->page_id = pl[3];
-        cursor_begin_segment<C>(cur, off, rg.end);
-        for (int s = 0; s < C::STAGES; ++s)
-            rope_issue_next<C>(cur, P, M, off, smem, full, okf, rg.end, grp, false);
     }
+    if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
     __syncthreads();
-    if (rg.local) pdl_wait();  // W and q~ come from the prologue kernel
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // W, the query blocks and their scales come from the prologue
+    pdl_wait();
     pdl_launch_dependents();
+    bool ok = true;
 
-    const int gq = lane >> 2, tq = lane & 3, mi = lane >> 3;
-    const int rr = (mi & 1) * 8 + (lane & 7);  // ldmatrix row of this lane inside an m-tile
-    const int h = grp * C::HG + warp;
-    const uint32_t chunk = 2 * warp + (mi >> 1);  // this lane's ldmatrix chunk of k-step `warp`
-    // the tile row this lane finishes: quad gq's four rows, one per lane
-    const int my_row = gq + 8 * (tq & 1) + 16 * (tq >> 1);
-
-    uint32_t wr[8][C::NTN][2];   // W_h fragments
-    uint32_t qh[2], ql[2];       // q~ fragments of k-step `warp` for the 8 heads (bf16 hi, lo)
-    float winv = 0.f;
-    bool timed_out = false;
-    uint32_t it = 0;
-    int b = rg.b0, wb = -1;
-    int32_t start = rg.start;
-    // A tile is finished one tile later: by then every warp has long written
-    // its shared partial sums, so no warp waits for the slowest one, and the
-    // stage is released before the scores go to global memory (the release
-    // orders this thread's earlier memory operations, stores included).
-    struct Pending {
-        bool on;
-        int s;
-        uint32_t par;
-        float v;      // private score (scaled back) of this lane's row
-        int64_t g;    // its score-array row (-1: not in the segment)
-    } pd = {false, 0, 0u, 0.f, -1};
-    auto finish = [&](const Pending &q) -> bool {
-        if (!mbar_wait(&shd[q.s], q.par)) {
-            if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
-            return false;
-        }
-        const float *sh = reinterpret_cast<const float *>(smem + q.s * C::STAGE + C::OFF_SH) +
-                          warp * C::SH_ROW + my_row;
-        float f = q.v;
+    if (warp == 0 && lane == 0) {
+        // ---- producer
+        TileWalk w = walk_begin(rg, C::TM);
+        int it = 0, i = 0, seg_loaded = -1;
+        // page ids of a tile's pieces (br rows, inside one page), read one
+        // tile ahead so that their latency passes while the producer waits
+        int32_t pid[C::TM / 32];
+        int np = 0;
+        auto read_pages = [&](const TileWalk &tw) {
+            const int32_t *pt = page_row(P, tw.b);
+            np = 0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) f += sh[k * C::HG * C::SH_ROW];
-        // release the stage; the last warp out refills it
-        __syncwarp();
-        if (lane == 0) {
-            int prev;
-            asm volatile("atom.acq_rel.cta.shared::cta.add.s32 %0, [%1], 1;"
-                         : "=r"(prev)
-                         : "r"(smem_u32(&cnt[q.s]))
-                         : "memory");
-            if (prev == C::NCW - 1) {
-                cnt[q.s] = 0;
-                rope_issue_next<C>(cur, P, M, off, smem, full, okf, rg.end, grp);
+            for (int p = 0; p < C::TM / 32; ++p) {
+                const int pos = tw.t + p * br;
+                if (p < C::TM / br && pos < tw.t_b) {
+                    pid[p] = pt[pos / P.page_size];
+                    np = p + 1;
+                }
             }
-        }
-        __syncwarp();
-        if (q.g >= 0) P.sc_out[q.g * C::H + h] = f;
-        return true;
-    };
-    while (start < rg.end && !timed_out) {
-        while (off[b + 1] <= start) ++b;
-        const int32_t base = off[b];
-        const int32_t seg_end = min(rg.end, off[b + 1]);
-        const int t_a = start - base, t_b = seg_end - base;
-        if (b != wb) {  // this request's operands
-            wb = b;
-            const uint32_t *src = P.wf + ((size_t)b * C::H + h) * (C::DH * C::R / 2);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-                for (int nt = 0; nt < C::NTN; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        wr[ks][nt][e] = __ldg(src + ((ks * C::NTN + nt) * 2 + e) * 32 + lane);
-            winv = __ldg(P.wsc + (size_t)b * C::H + h);
-            // B fragment (k, n): q~ of head 8 grp + n at channel 16 warp + k
-            const float *qrow = P.qt + ((size_t)b * C::H + grp * C::HG + gq) * C::DH + 16 * warp + 2 * tq;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float2 v = __ldg(reinterpret_cast<const float2 *>(qrow + 8 * e));
-                const float hx = __bfloat162float(__float2bfloat16_rn(v.x));
-                const float hy = __bfloat162float(__float2bfloat16_rn(v.y));
-                qh[e] = pack_bf16(hx, hy);
-                ql[e] = pack_bf16(v.x - hx, v.y - hy);
+        };
+        if (!w.done) read_pages(w);
+        while (!w.done) {
+            if (w.seg != seg_loaded) {
+                // the previous request's products are done with W
+                if (seg_loaded >= 0 && !mbar_wait(wfree, seg_loaded & 1)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(wfull, C::W_BYTES + C::QB_BYTES);
+                tma_load_3d(smem + C::OFF_W, &M.wt, 0, (w.b * C::H + grp * C::HPC) * C::R, 0, wfull);
+                tma_load_3d(smem + C::OFF_QB, &M.qb, 0, (w.b * C::NG + grp) * 16, 0, wfull);
+                seg_loaded = w.seg;
             }
+            int prow[C::TM / 32];
+            for (int kh = 0; kh < 2; ++kh, ++it) {
+                const int s = it % C::STAGES;
+                if (it >= C::STAGES && !mbar_wait(&empty[s], ((it / C::STAGES) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (kh == 0) {
+                    // pool rows of the pieces; pieces past the segment's end are
+                    // not loaded (their rows are not stored)
+#pragma unroll
+                    for (int p = 0; p < C::TM / 32; ++p) {
+                        if (p >= np) continue;
+                        int32_t page = pid[p];
+                        if (page < 0 || page >= P.num_pages) {
+                            status_or(P.status, LRKV_STATUS_BAD_PAGE);
+                            page = 0;
+                        }
+                        prow[p] = page * P.page_size + (w.t + p * br) % P.page_size;
+                    }
+                }
+                uint8_t *st = smem + s * C::STAGE;
+                mbar_arrive_expect_tx(&full[s], C::HALF + np * br * 128);
+                tma_load_3d(st, &M.tab, 0, w.t, kh, &full[s]);
+#pragma unroll
+                for (int p = 0; p < C::TM / 32; ++p)
+                    if (p < np) tma_load_3d(st + C::HALF + p * br * 128, &M.sk, 0, prow[p], kh, &full[s]);
+            }
+            if (!ok) break;
+            // the tile's R_K columns of the group (read once: evict first)
+            const int rb = i % C::RKB;
+            if (i >= C::RKB && !mbar_wait(&rkfree[rb], ((i / C::RKB) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            uint8_t *rk = smem + C::OFF_RK + rb * C::RK_TILE;
+            mbar_arrive_expect_tx(&rkfull[rb], np * br * C::NPRIV * 2);
+            const uint64_t ef = l2_evict_first_policy();
+#pragma unroll
+            for (int p = 0; p < C::TM / 32; ++p)
+                if (p < np)
+#pragma unroll
+                    for (int k = 0; k < C::NRB; ++k)
+                        tma_load_3d_hint(rk + k * (C::TM * C::SWZ) + p * br * C::SWZ, &M.rk, 0, prow[p],
+                                         grp * C::NRB + k, &rkfull[rb], ef);
+            ++i;
+            walk_next(w, rg, C::TM);
+            if (!w.done) read_pages(w);
         }
-
-        for (int t = t_a / TS * TS; t < t_b; t += TS, ++it) {
-            const int s = it % C::STAGES;
-            const uint32_t par = (it / C::STAGES) & 1;
-            if (!mbar_wait(&full[s], par)) {
+        // never leave with copies in flight into this CTA's shared memory
+        for (int k = max(0, it - C::STAGES); k < it; ++k)
+            mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
+        for (int k = max(0, i - C::RKB); k < i; ++k) mbar_wait(&rkfull[k % C::RKB], (k / C::RKB) & 1);
+        if (seg_loaded >= 0) mbar_wait(wfull, seg_loaded & 1);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t id_p = tc_idesc_f16(C::TM, C::NPRIV), id_s = tc_idesc_bf16(C::TM, 16);
+        const uint32_t wbase = smem_u32(smem + C::OFF_W), qbase = smem_u32(smem + C::OFF_QB);
+        TileWalk w = walk_begin(rg, C::TM);
+        int it = 0, i = 0, seg_cur = -1;
+        while (!w.done && ok) {
+            if (w.seg != seg_cur) {
+                if (seg_cur >= 0) tc_commit(wfree);  // W is free once these products read it
+                seg_cur = w.seg;
+                if (!mbar_wait(wfull, seg_cur & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            const int a = i & 1;
+            if (i >= 2 && !mbar_wait(&acc_empty[a], ((i >> 1) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dp = tmem + a * C::ACC, ds = dp + C::SH_COL;
+            // private products: C_tile (f16) . W (f16), K = 128 in two halves
+            for (int kh = 0; kh < 2 && ok; ++kh) {
+                const int k = it + kh, s = k % C::STAGES;
+                if (!mbar_wait(&full[s], (k / C::STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(smem + s * C::STAGE));
+                const uint64_t bd = sw128_kmajor_desc(wbase + kh * C::NPRIV * 128);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(dp, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), id_p, (kh | kk) != 0);
+            }
+            // shared term: turned S_K (bf16) . query block (bf16); a half's
+            // stage is free once these products have read it
+            for (int kh = 0; kh < 2 && ok; ++kh) {
+                const int k = it + kh, s = k % C::STAGES;
+                if (!mbar_wait(&turned[s], (k / C::STAGES) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(smem + s * C::STAGE + C::HALF));
+                const uint64_t bd = sw128_kmajor_desc(qbase + kh * 2048);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc_mma_f16(ds, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), id_s, (kh | kk) != 0);
+                tc_commit(&empty[s]);
+            }
+            if (!ok) break;
+            tc_commit(&acc_full[a]);
+            it += 2;
+            ++i;
+            walk_next(w, rg, C::TM);
+        }
+        // every issued product has completed before tensor memory is freed
+        tc_commit(drain);
+        mbar_wait(drain, 0);
+    } else if (warp >= 2) {
+        // ---- turn S_K, then the epilogue one tile later
+        const int ew = warp - 2, q4 = warp & 3, row = 32 * q4 + lane;
+        const int hh = ew >> 2;                          // half of the group's heads
+        const int h0 = grp * C::HPC + hh * C::HPE;       // this thread's first head
+        const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
+        TileWalk w = walk_begin(rg, C::TM);
+        int it = 0, i = 0, seg_cur = -1;
+        float winv[C::HPE];
+        struct Pending {
+            bool on;
+            int i;
+            int64_t g;  // score-array row (-1: not stored)
+            float winv[C::HPE];
+        } pd;
+        pd.on = false;
+        auto finish = [&](const Pending &q) -> bool {
+            const int a = q.i & 1, rb = q.i % C::RKB;
+            if (!mbar_wait(&acc_full[a], (q.i >> 1) & 1) || !mbar_wait(&rkfull[rb], (q.i / C::RKB) & 1)) {
                 if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
-                timed_out = true;
-                break;
+                return false;
             }
-            uint8_t *st = smem + s * C::STAGE;
-            const uint32_t cb = smem_u32(st + C::OFF_C);
-            {
-                // shared term, k-step `warp`: channel pairs (2c, 2c+1) of each
-                // row turned by the row's angles (D_j), times q~ of 8 heads
-                const uint32_t skb = smem_u32(st + C::OFF_SK);
-                float *sh = reinterpret_cast<float *>(st + C::OFF_SH) + warp * C::HG * C::SH_ROW;
+            tc_fence_after();
+            // this row's R_K columns from the swizzled tile: logical 16-byte
+            // chunk x of block k sits at chunk x ^ (row bits) of the row
+            const uint8_t *rk = smem + C::OFF_RK + rb * C::RK_TILE + row * C::SWZ;
+            const int sw = C::SWZ == 128 ? (row & 7) : ((row >> 1) & 3);
+            float pr[C::HPE];
 #pragma unroll
-                for (int mt = 0; mt < TS / 16; ++mt) {
-                    uint32_t a[4], cs[4], y[4];
-                    ldmatrix_x4(skb + box_chunk_rows<TS>(16 * mt + rr, chunk), a[0], a[1], a[2], a[3]);
-                    ldmatrix_x4(cb + box_chunk_rows<TS>(16 * mt + rr, chunk), cs[0], cs[1], cs[2], cs[3]);
+            for (int e = 0; e < C::HPE; ++e) pr[e] = 0.f;
+            const int e_base = hh * C::HPE * C::R;  // first private column of this thread
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float x0 = bf16lo(a[e]), x1 = bf16hi(a[e]);
-                        const float2 r = __half22float2(*reinterpret_cast<const __half2 *>(&cs[e]));
-                        y[e] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+            for (int c = 0; c < C::HPE * C::R / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(tl + a * C::ACC + e_base + 16 * c, v);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int e0 = e_base + 16 * c + 8 * half;  // 8 columns, one 16-byte chunk
+                    const int kb = e0 / C::RBLK, x = (e0 % C::RBLK) / 8;
+                    const uint4 r4 = *reinterpret_cast<const uint4 *>(
+                        rk + kb * (C::TM * C::SWZ) + ((x ^ sw) << 4));
+                    const int hx = (16 * c + 8 * half) / C::R;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t rw = u4_word(r4, q);
+                        pr[hx] = fmaf(__uint_as_float(v[8 * half + 2 * q]), bf16lo(rw), pr[hx]);
+                        pr[hx] = fmaf(__uint_as_float(v[8 * half + 2 * q + 1]), bf16hi(rw), pr[hx]);
                     }
-                    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_bf16_16816(c0, y, qh[0], qh[1]);
-                    mma_bf16_16816(c1, y, ql[0], ql[1]);
-                    // partial [k-step][head][row]: heads 2tq, 2tq+1, rows gq, gq+8
-                    const int r0 = 16 * mt + gq;
-                    sh[(2 * tq) * C::SH_ROW + r0] = c0[0] + c1[0];
-                    sh[(2 * tq + 1) * C::SH_ROW + r0] = c0[1] + c1[1];
-                    sh[(2 * tq) * C::SH_ROW + r0 + 8] = c0[2] + c1[2];
-                    sh[(2 * tq + 1) * C::SH_ROW + r0 + 8] = c0[3] + c1[3];
                 }
+            }
+            uint32_t sv[8];
+            tmem_ld8(tl + a * C::ACC + C::SH_COL, sv);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&acc_empty[a]);
+                mbar_arrive(&rkfree[rb]);
+            }
+            if (q.g >= 0) {
+                float o[C::HPE];
+#pragma unroll
+                for (int e = 0; e < C::HPE; ++e)
+                    o[e] = __uint_as_float(sv[hh * C::HPE + e]) +
+                           __uint_as_float(sv[C::HPC + hh * C::HPE + e]) + q.winv[e] * pr[e];
+                float *dst = P.sc_out + q.g * C::H + h0;
+                if constexpr (C::HPE == 2)
+                    *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
+                else
+                    dst[0] = o[0];
+            }
+            return true;
+        };
+        while (!w.done && ok) {
+            if (w.seg != seg_cur) {
+                seg_cur = w.seg;
+#pragma unroll
+                for (int e = 0; e < C::HPE; ++e) winv[e] = __ldg(P.wsc + (size_t)w.b * C::H + h0 + e);
+            }
+            // turn the tile's two S_K halves in place
+            for (int kh = 0; kh < 2; ++kh) {
+                const int k = it + kh, s = k % C::STAGES;
+                if (!mbar_wait(&full[s], (k / C::STAGES) & 1)) {
+                    if (lane == 0) status_or(P.status, LRKV_STATUS_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * C::STAGE;
+                const uint4 *cs = reinterpret_cast<const uint4 *>(st);
+                uint4 *sk = reinterpret_cast<uint4 *>(st + C::HALF);
+#pragma unroll 4
+                for (int c = ew * 32 + lane; c < C::HALF / 16; c += C::EPI * 32) {
+                    const uint4 x = sk[c], y = cs[c];
+                    sk[c] = make_uint4(turn_pair(x.x, y.x), turn_pair(x.y, y.y), turn_pair(x.z, y.z),
+                                       turn_pair(x.w, y.w));
+                }
+                fence_proxy_async_smem();  // the products read these bytes next
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&shd[s]);
+                if (lane == 0) mbar_arrive(&turned[s]);
             }
-            float acc[TS / 16][C::NTN][4];
-#pragma unroll
-            for (int mt = 0; mt < TS / 16; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < C::NTN; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a[TS / 16][4];
-#pragma unroll
-                for (int mt = 0; mt < TS / 16; ++mt)
-                    ldmatrix_x4(cb + box_chunk_rows<TS>(16 * mt + rr, 2 * ks + (mi >> 1)), a[mt][0],
-                                a[mt][1], a[mt][2], a[mt][3]);
-#pragma unroll
-                for (int nt = 0; nt < C::NTN; ++nt)
-#pragma unroll
-                    for (int mt = 0; mt < TS / 16; ++mt)
-                        mma_f16_16816(acc[mt][nt], a[mt], wr[ks][nt][0], wr[ks][nt][1]);
-            }
-            // row 16 mt + gq + 8 u of P meets R_K[h] at columns nt*8 + 2tq, +1
-            const uint8_t *rk = st + C::OFF_RK;
-            float pv[TS / 16][2];
-#pragma unroll
-            for (int mt = 0; mt < TS / 16; ++mt)
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    float sa = 0.f, sb = 0.f;
-#pragma unroll
-                    for (int nt = 0; nt < C::NTN; ++nt) {
-                        const uint32_t w = lds_u32(rk + box_chunk_rows<TS>(16 * mt + gq + 8 * u, warp * C::NTN + nt) + 4 * tq);
-                        sa = fmaf(acc[mt][nt][2 * u], bf16lo(w), sa);
-                        sb = fmaf(acc[mt][nt][2 * u + 1], bf16hi(w), sb);
-                    }
-                    pv[mt][u] = sa + sb;
-                }
-#pragma unroll
-            for (int mt = 0; mt < TS / 16; ++mt)
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    pv[mt][u] += __shfl_xor_sync(0xffffffffu, pv[mt][u], 1);
-                    pv[mt][u] += __shfl_xor_sync(0xffffffffu, pv[mt][u], 2);
-                }
-            // finish the previous tile, then leave this one pending (this
-            // lane's row: my_row = gq + 8 (tq & 1) + 16 (tq >> 1))
+            if (!ok) break;
+            // finish the previous tile while this one's products run
             if (pd.on && !finish(pd)) {
-                timed_out = true;
+                ok = false;
                 break;
             }
-            const float mine = (tq == 0) ? pv[0][0] : (tq == 1) ? pv[0][1] : (tq == 2) ? pv[1][0] : pv[1][1];
-            const int j = t + my_row;
+            const int j = w.t + row;
             pd.on = true;
-            pd.s = s;
-            pd.par = par;
-            pd.v = mine * winv;
-            pd.g = (j >= t_a && j < t_b) ? (int64_t)base + j : -1;
+            pd.i = i;
+            pd.g = (j >= w.t_a && j < w.t_b) ? (int64_t)w.base + j : -1;
+#pragma unroll
+            for (int e = 0; e < C::HPE; ++e) pd.winv[e] = winv[e];
+            it += 2;
+            ++i;
+            walk_next(w, rg, C::TM);
         }
-        start = seg_end;
+        if (pd.on && ok) finish(pd);
     }
-    if (pd.on && !timed_out) finish(pd);
-
-    // never leave with copies in flight into this CTA's shared memory
+    tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-        const int issued = cur->issued;
-        for (int k = (int)it; k < issued; ++k) mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
-    }
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -1346,6 +1488,25 @@ static bool make_map(CUtensorMap *map, const void *pool, int64_t rows, int cols,
     });
 }
 
+// Map over a bf16 pool [rows, cols] as (blk, rows, cols / blk) with blocks
+// of blk = 64 (128-byte swizzle) or 32 (64-byte swizzle) elements; a box of
+// blk x box_rows x 1 lands one block of box_rows rows.
+static bool make_block_map(CUtensorMap *map, const void *pool, int64_t rows, int cols, int blk,
+                           int box_rows) {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return false;
+    return encode_cached(map, MapKey{pool, rows, cols, 2, blk * 1024 + box_rows, 3}, [&](CUtensorMap *m) {
+        cuuint64_t dims[3] = {(cuuint64_t)blk, (cuuint64_t)rows, (cuuint64_t)(cols / blk)};
+        cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)blk * 2};
+        cuuint32_t box[3] = {(cuuint32_t)blk, (cuuint32_t)box_rows, 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   blk == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
+}
+
 // Map over a row-major [rows, H] array of elements of eb bytes (bf16 joint
 // key norms, fp32 given scores) as (H, rows, 1): a box of H x 16 x 1 lands a
 // tile's 16 rows, unswizzled.
@@ -1398,8 +1559,8 @@ static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
                                     : make_float4(1.f, 1.f, 1.f, 1.f);
     P.norm = c.N_K != nullptr;
     P.max_len = decode_max_len(a);
-    P.wf = a.rope_ws.wf;
-    P.qt = a.rope_ws.qt;
+    P.wt = a.rope_ws.wt;
+    P.qb = a.rope_ws.qb;
     P.wsc = a.rope_ws.wsc;
     P.sc_out = a.rope_ws.sc;
     return P;
@@ -1463,7 +1624,7 @@ int fast_decode_grid(int, int) { return device_sm_count(); }
 
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const int H = a.cache.H, r = a.cache.r;
-    const bool q8 = a.cache.dtype == LRKV_FP8_E4M3, gs = a.rope_ws.wf != nullptr;
+    const bool q8 = a.cache.dtype == LRKV_FP8_E4M3, gs = a.rope_ws.wt != nullptr;
     if (cache_groups(a.cache) == 2) {
 #define X(h, rr) \
         if (H == h && r == rr) return launch_fast_cfg<h, rr, false, false, 2>(a, ws, G);
@@ -1483,41 +1644,37 @@ cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G) {
 
 // ---- exact RoPE: rotary score kernel, then the given-score split kernel
 
-template <int H, int R>
-struct RopePick {
-    static constexpr int stage = RopeCfg<H, R, 2>::STAGE;
-    static constexpr int misc = RopeCfg<H, R, 2>::SMEM - RopeCfg<H, R, 2>::OFF_BAR;
-    static constexpr int fit = (227 * 1024 - misc) / stage;
-    static constexpr int STAGES = fit > 8 ? 8 : fit;
-    using Cfg = RopeCfg<H, R, STAGES>;
-};
-
 bool rope_fast_supported(int H, int d_h, int r, int page_size, int dtype) {
-    // the score kernel's 32-row tiles stay inside a page
-    return dtype == LRKV_BF16 && H % 8 == 0 && page_size % 32 == 0 &&
-           fast_decode_supported(H, d_h, r, page_size, dtype);
+    // the score kernel lands its 128-row tiles in pieces of 32 or more rows,
+    // each inside one page
+    return dtype == LRKV_BF16 && r >= 8 && H % rope_tc_heads_per_cta(r) == 0 &&
+           page_size % 32 == 0 && fast_decode_supported(H, d_h, r, page_size, dtype);
 }
 
 template <int H, int R>
 static cudaError_t launch_rope_cfg(const DecodeArgs &a, const DecodeWs &ws) {
-    using A = typename RopePick<H, R>::Cfg;
+    using C = RtcCfg<H, R>;
     const auto &c = a.cache;
     const int64_t rows = (int64_t)c.num_pages * c.page_size;
-    RopeMaps rm;
-    if (!make_map(&rm.tab, a.rope16, a.rope_max_pos, 128, 2, 0, true, A::TS) ||
-        !make_map(&rm.sk, c.S_K, rows, 128, 2, 0, false, A::TS) ||
-        !make_map(&rm.rk, c.R_K, rows, H * R, 2, A::RG_BOXES, false, A::TS))
+    // S_K lands in pieces of br rows, each inside a page
+    const int br = c.page_size % 128 == 0 ? 128 : c.page_size % 64 == 0 ? 64 : 32;
+    RtcMaps m;
+    if (!make_map(&m.tab, a.rope16, a.rope_max_pos, 128, 2, 1, true, C::TM) ||
+        !make_map(&m.sk, c.S_K, rows, 128, 2, 1, false, br) ||
+        !make_block_map(&m.rk, c.R_K, rows, H * R, C::RBLK, br) ||
+        !make_map(&m.wt, a.rope_ws.wt, (int64_t)a.B * H * R, 128, 2, 0, true, C::NPRIV) ||
+        !make_map(&m.qb, a.rope_ws.qb, (int64_t)a.B * C::NG * 16, 128, 2, 0, false, 16))
         return cudaErrorInvalidValue;
-    auto kern = rope_scores_kernel<A>;
+    auto kern = rope_scores_tc_kernel<C>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const FastParams P = fast_params(a, ws);
-    const int ranges = std::max(1, device_sm_count() / A::NG);
-    return launch_pdl(kern, dim3(ranges * A::NG), dim3(A::NT), A::SMEM, a.stream, rm, P);
+    const int ranges = std::max(1, device_sm_count() / C::NG);
+    return launch_pdl(kern, dim3(ranges * C::NG), dim3(C::NT), C::SMEM, a.stream, m, P, br);
 }
 
 cudaError_t launch_rope_scores(const DecodeArgs &a, const DecodeWs &ws) {

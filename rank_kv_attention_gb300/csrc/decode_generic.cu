@@ -33,10 +33,11 @@ constexpr int kProThreads = 256;  // threads of a prologue block
 // so the private query of key j is its (cos, sin) table row, interleaved by
 // channel pair, times W = [A; Bq] interleaved the same way (row 2c = A[c],
 // row 2c+1 = Bq[c]), and the shared term is q~ . (S_K[j] D_j).  Written per
-// (b, h): q~ in fp32, and W as f16 mma B-fragments (k-step ks, n-tile nt,
-// register e, lane) after the exact power-of-two scaling that puts its
-// largest |value| in [2^14, 2^15), with the inverse scale.  bk: B_K[h] as
-// fp32 [d_h][r]; qs: the query rows; scratch: d_h + d_h r floats.
+// (b, h): q~ as a bf16 value row and a bf16 remainder row of the head group's
+// block, and W transposed ([r][d_h], f16) after the exact power-of-two
+// scaling that puts its largest |value| in [2^14, 2^15), with the inverse
+// scale.  bk: B_K[h] as fp32 [d_h][r]; qs: the query rows; scratch: d_h +
+// d_h r floats.
 __device__ void rope_fast_operands(const float *bk, const float *qs, int nb, int b0, int h, int H,
                                    int d_h, int r, const int32_t *seq_lens, int max_len,
                                    const float2 *tab, const RopeFastWs &rf, float *scratch) {
@@ -54,7 +55,21 @@ __device__ void rope_fast_operands(const float *bk, const float *qs, int nb, int
             const float y0 = x0 * cs.x - x1 * cs.y, y1 = x0 * cs.y + x1 * cs.x;
             qt[2 * c] = y0;
             qt[2 * c + 1] = y1;
-            *reinterpret_cast<float2 *>(rf.qt + ((size_t)b * H + h) * d_h + 2 * c) = make_float2(y0, y1);
+        }
+        {
+            // this head's rows of the group block: bf16 value, bf16 remainder;
+            // the group's first head also zeroes rows 2g .. 15
+            const int g = rope_tc_heads_per_cta(r), i = h % g;
+            uint16_t *blk = rf.qb + ((size_t)b * (H / g) + h / g) * 16 * d_h;
+            __syncthreads();
+            for (int c = tid; c < d_h; c += blockDim.x) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(qt[c]);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(qt[c] - __bfloat162float(hi));
+                blk[(size_t)i * d_h + c] = __bfloat16_as_ushort(hi);
+                blk[(size_t)(g + i) * d_h + c] = __bfloat16_as_ushort(lo);
+            }
+            if (i == 0)
+                for (int o = tid; o < (16 - 2 * g) * d_h; o += blockDim.x) blk[2 * g * d_h + o] = 0;
         }
         __syncthreads();
         float mx = 0.f;
@@ -76,14 +91,11 @@ __device__ void rope_fast_operands(const float *bk, const float *qs, int nb, int
         const int e = f16_range_shift(mx);
         const float sc = exp2i(e);
         if (tid == 0) rf.wsc[(size_t)b * H + h] = exp2i(-e);
-        // fragment f = ((ks * NTN + nt) * 2 + e) * 32 + lane holds W rows
-        // ks*16 + 2tq + 8e and the next, column nt*8 + gq
-        const int ntn = r / 8, nf = d_h * r / 2;
-        uint32_t *dst = rf.wf + ((size_t)b * H + h) * nf;
+        // W^T: row n holds W[0 .. d_h)[n], two channels per 32-bit word
+        const int nf = d_h * r / 2, hw = d_h / 2;
+        uint32_t *dst = reinterpret_cast<uint32_t *>(rf.wt) + ((size_t)b * H + h) * nf;
         for (int f = tid; f < nf; f += blockDim.x) {
-            const int lane = f & 31, ee = (f >> 5) & 1, q = f >> 6;
-            const int nt = q % ntn, ks = q / ntn;
-            const int k0 = ks * 16 + 2 * (lane & 3) + 8 * ee, n = nt * 8 + (lane >> 2);
+            const int n = f / hw, k0 = 2 * (f % hw);
             dst[f] = pack_f16(w[k0 * r + n] * sc, w[(k0 + 1) * r + n] * sc);
         }
         __syncthreads();  // qt, w and wmax are reused by the next request
@@ -741,7 +753,7 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
     // p = q B_K runs in 128-thread blocks of one request each, which fit on
     // an SM beside a split CTA (so no split CTA waits for a prologue block to
     // leave); otherwise a block amortises B_K's staging over 8 requests
-    const bool rope_fast = a.rope_ws.wf != nullptr;
+    const bool rope_fast = a.rope_ws.wt != nullptr;
     const bool small = !rope_fast && beside_split;
     const int nrows = (rope_fast || small) ? 1 : kProRows;
     dim3 grid(c.H + 1, (a.B + nrows - 1) / nrows);

@@ -21,7 +21,7 @@ struct DecodeArgs {
     cudaStream_t stream;
     // Exact rotary position embedding when rope != nullptr: the cos/sin table
     // [rope_max_pos][d_h / 2] of lrkv_rope_table, and its f16 copy.  With
-    // rope_ws.wf set (lrkv_decode_rope on a tensor-core shape) the rotary
+    // rope_ws.wt set (lrkv_decode_rope on a tensor-core shape) the rotary
     // score kernel and the split kernel's given-score mode run; otherwise the
     // generic split kernel.
     const float *rope = nullptr;
@@ -42,7 +42,7 @@ struct DecodeArgs {
 // output and LRKV_STATUS_BAD_SEQLEN.
 inline int decode_max_len(const DecodeArgs &a) {
     int m = a.max_pages * a.cache.page_size;
-    if (a.rope_ws.wf) {
+    if (a.rope_ws.wt) {
         m = m < a.rope_max_pos ? m : a.rope_max_pos;
         m = m < a.max_seq_len ? m : a.max_seq_len;
     }

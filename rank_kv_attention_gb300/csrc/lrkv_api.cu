@@ -114,7 +114,7 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
     DecodeGeom geo = decode_geom(a.B, a.max_seq_len);
     DecodeWs ws = decode_ws_layout(workspace, a.B, c.H, c.d_h, c.r, geo.G_ws);
     if (ws_bytes < ws.bytes) return LRKV_E_WORKSPACE;
-    const bool rope_fast = a.rope_ws.wf != nullptr;
+    const bool rope_fast = a.rope_ws.wt != nullptr;
     const bool fast = rope_fast || (!a.rope && fast_decode_supported(c.H, c.d_h, c.r, c.page_size, c.dtype,
                                                                       cache_groups(c)));
     const int G = fast ? geo.G_fast : geo.G_gen;

@@ -68,17 +68,26 @@ __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, i
     return w;
 }
 
+// Heads of one CTA of the tensor-core rotary score kernel: its private
+// products C_j W_h of those heads form one MMA of N = heads * r columns, at
+// most 224 (the rest of a 256-column accumulator holds the shared term).
+__host__ __device__ constexpr int rope_tc_heads_per_cta(int r) { return 4 * r <= 224 ? 4 : 2; }
+
 // Extra workspace of the tensor-core rotary decode (lrkv_decode_rope), after
 // the decode workspace (all offsets 256-byte aligned):
-//   [wf: B*H*d_h*r/2 u32]  per (request, head) the rotated private operand
-//                          W as f16 mma B-fragments, scaled by a power of two
-//   [qt: B*H*d_h f32]      rotated queries q D_i
+//   [wt: B*H*r*d_h f16]    per (request, head) the rotated private operand W,
+//                          transposed ([r][d_h], d_h contiguous), scaled by a
+//                          power of two
+//   [qb: B*(H/g)*16*d_h bf16]  per (request, group of g heads) the rotated
+//                          queries q D_i as rows: row i the bf16 value of head
+//                          i of the group, row g + i the bf16 remainder, rows
+//                          2g .. 15 zero (g = rope_tc_heads_per_cta(r))
 //   [wsc: B*H f32]         inverse scale of each W
 //   [sc: B*max_seq_len*H f32]  raw scores of every visible row, row-major by
 //                          the plan's row index (request b's rows start at off[b])
 struct RopeFastWs {
-    uint32_t *wf;
-    float *qt;
+    uint16_t *wt;
+    uint16_t *qb;
     float *wsc;
     float *sc;
     int64_t sc_rows;
@@ -90,10 +99,10 @@ __host__ __device__ inline RopeFastWs rope_fast_ws_layout(void *base, int B, int
     RopeFastWs w;
     char *p = static_cast<char *>(base);
     size_t o = 0;
-    w.wf = reinterpret_cast<uint32_t *>(p + o);
-    o += align256(sizeof(uint32_t) * (size_t)B * H * d_h * r / 2);
-    w.qt = reinterpret_cast<float *>(p + o);
-    o += align256(sizeof(float) * (size_t)B * H * d_h);
+    w.wt = reinterpret_cast<uint16_t *>(p + o);
+    o += align256(sizeof(uint16_t) * (size_t)B * H * d_h * r);
+    w.qb = reinterpret_cast<uint16_t *>(p + o);
+    o += align256(sizeof(uint16_t) * (size_t)B * (H / rope_tc_heads_per_cta(r)) * 16 * d_h);
     w.wsc = reinterpret_cast<float *>(p + o);
     o += align256(sizeof(float) * (size_t)B * H);
     w.sc = reinterpret_cast<float *>(p + o);
