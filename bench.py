@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_T4096", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-workers", type=int, default=0,
+                    help="host processes for the oracle timing (0: one per core)")
     ap.add_argument("--cpu-pairs", type=int, default=1024,
                     help="(request, head) pairs of the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -74,6 +76,26 @@ def parse():
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_barrier(world):
+    """Barrier across the ranks of a multi-process run (no-op on one)."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (a duration): the job takes as long as
+    its slowest rank.  device: where the process group's backend reduces
+    (cuda for nccl, cpu for gloo)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def measured_peaks(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
@@ -298,18 +320,8 @@ def run_ours(args, rank, world, local_rank):
         if rc or rc2 or rc3:
             raise RuntimeError(f"lrkv call failed: {rc} {rc3} {rc2}")
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier = lambda: rank_barrier(world)
+    ranks_max = lambda x: max_over_ranks(x, world, dev)
 
     # ---- device-resident timed region (step throughput)
     K, W = args.steps, args.warmup
@@ -330,7 +342,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    total_ms = max_over_ranks(e0.elapsed_time(e1))
+    total_ms = ranks_max(e0.elapsed_time(e1))
 
     # ---- live breakdown: the same K steps with only one of the two calls
     def timed(fn):
@@ -441,7 +453,7 @@ def run_ours(args, rank, world, local_rank):
     g1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(g0.elapsed_time(g1))
+    e2e_ms = ranks_max(g0.elapsed_time(g1))
     if not rope:
         for hg in graphs:
             lib.lrkv_step_graph_destroy(hg)
@@ -514,18 +526,18 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(name, args.cpu_pairs)
+        res["cpu_baseline"] = cpu_baseline(name, args.cpu_pairs, args.cpu_workers)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return res
 
 
-def cpu_baseline(name, n_pairs):
+def cpu_baseline(name, n_pairs, workers=0):
     """The oracle on all host cores (the reported value), and once more on one
     core over a proportionally smaller sample."""
     from oracle.cpu_timing import time_oracle_decode
-    t = time_oracle_decode(name, n_pairs)
+    t = time_oracle_decode(name, n_pairs, workers=workers or None)
     n1 = max(4, n_pairs // max(1, t["cores"]))
     t1 = time_oracle_decode(name, n1, workers=1, seed=1)
     return {"value": round(t["pairs"] / t["heads"] / t["wall_s"], 3), "unit": "tokens/s",
@@ -548,7 +560,7 @@ def run_reference(args, rank, world):
     import lrkv_inputs as I
     c = workload_shape(args.config)
     n = max(16, min(args.steps, 4096))   # bounded so the run ends within minutes
-    t = time_oracle_decode(args.config, n)
+    t = time_oracle_decode(args.config, n, workers=args.cpu_workers or None)
     value = t["pairs"] / t["heads"] / t["wall_s"]
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
@@ -611,17 +623,21 @@ def run_prefill(args, rank, world, local_rank):
     for _ in range(max(W, 3)):
         step()
     torch.cuda.synchronize()
+    rank_barrier(world)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.25)
+    torch.cuda.synchronize()
+    rank_barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    rank_barrier(world)
     clk = clocks.stop()
-    total_ms = e0.elapsed_time(e1)
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     assert lib.lrkv_profile_enable(1) == 0
     for _ in range(K):
         step()
@@ -643,7 +659,7 @@ def run_prefill(args, rank, world, local_rank):
     attn_tf = attn_flops / (res_k["attention"] / 1e3) / 1e12
     proj_tf = proj_flops / (res_k["projection"] / 1e3) / 1e12
     return {
-        "metric": "LRKV prefill tokens/s", "value": round(n / (ms / 1e3), 1), "unit": "tokens/s",
+        "metric": "LRKV prefill tokens/s", "value": round(world * n / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",

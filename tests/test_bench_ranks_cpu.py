@@ -1,0 +1,69 @@
+"""The multi-process path of bench.py on CPU (gloo, world size 2): the
+requests of a decode step are independent, so ranks run replicas and meet
+only to time the job; the slowest rank's time is the job's, and only rank 0
+prints.  The GPU arms use the same helpers over NCCL."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _ranks_worker(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.rank_barrier(world)
+        mine = 1.5 + rank              # this rank's duration
+        got = bench.max_over_ranks(mine, world, torch.device("cpu"))
+        with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+            json.dump({"mine": mine, "max": got}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo(tmp_path):
+    world = 2
+    mp.spawn(_ranks_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(world)]
+    assert [r["max"] for r in res] == [2.5, 2.5]          # every rank sees the slowest
+    assert sorted(r["mine"] for r in res) == [1.5, 2.5]
+
+
+def test_max_over_ranks_one_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.25, 1, torch.device("cpu")) == 3.25
+    bench.rank_barrier(1)   # no process group needed
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """bench.py --impl reference launched as the driver launches N > 1: rank 0
+    alone times the oracle and prints one JSON line; rank 1 exits 0 quietly."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "16", "--warmup", "3",
+           "--cpu-workers", "1"]
+    p = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["cores"] == 1 and d["e2e"]["h2d_bytes_per_step"] == 0
