@@ -551,6 +551,17 @@ def cpu_baseline(name, n_pairs, workers=0):
                             "sample": f"{t1['pairs']} random (request, head) pairs, one process"}}
 
 
+def cpu_baseline_prefill(name, workers=0, k_rows=8):
+    from oracle.cpu_timing import time_oracle_prefill
+    t = time_oracle_prefill(name, k_rows, workers=workers or None)
+    return {"value": round(t["tokens_per_s"], 3), "unit": "tokens/s", "cores": t["cores"],
+            "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"{t['cores']} requests of the {name} workload, one per single-threaded "
+                      f"process: the float64 projection of the request's rows, then causal "
+                      f"attention of {k_rows} sampled rows (all heads), scaled to the full "
+                      f"request; {t['wall_s']:.1f} s wall"}
+
+
 def run_reference(args, rank, world):
     """The float64 oracle timed on host cores: each step is one (request, head)
     pair of the workload; tokens/s counts H pairs as one request-step."""
@@ -559,6 +570,19 @@ def run_reference(args, rank, world):
     from oracle.cpu_timing import time_oracle_decode
     import lrkv_inputs as I
     c = workload_shape(args.config)
+    if args.config == "prefill_2048":   # the prefill line's metric, on host cores
+        cb = cpu_baseline_prefill(args.config, args.cpu_workers)
+        v = cb["value"]
+        return {
+            "impl": "reference", "metric": "LRKV prefill tokens/s", "value": v, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(c["B"] * c["T"] / v * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": c["B"],
+                       "d": c["d"], "H": c["H"], "d_h": c["d_h"], "r": c["r"], "seq_len": c["T"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     n = max(16, min(args.steps, 4096))   # bounded so the run ends within minutes
     t = time_oracle_decode(args.config, n, workers=args.cpu_workers or None)
     value = t["pairs"] / t["heads"] / t["wall_s"]
@@ -585,6 +609,7 @@ def run_prefill(args, rank, world, local_rank):
     import torch
     import lrkv_inputs as I
     import rank_kv_attention_gb300 as L
+    from rank_kv_attention_gb300 import _abi
     from rank_kv_attention_gb300.api import PagedCache
 
     torch.cuda.set_device(local_rank)
@@ -648,6 +673,36 @@ def run_prefill(args, rank, world, local_rank):
         assert lib.lrkv_profile_read(which, ctypes.byref(tot), ctypes.byref(nl)) == 0
         res_k[name] = tot.value / max(1, nl.value)
     lib.lrkv_profile_enable(0)
+
+    # ---- end to end with host buffers: the step's rows X and queries Q from
+    # pinned host memory, the output back to pinned host memory, the host
+    # synchronising every step
+    hX, hQ = X.cpu().pin_memory(), Qd.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        X.copy_(hX, non_blocking=True)
+        Qd.copy_(hQ, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    Ke = max(3, min(K, 50))
+    for _ in range(3):
+        e2e_step()
+    rank_barrier(world)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    rank_barrier(world)
+    e2e_ms = max_over_ranks(g0.elapsed_time(g1), world, dev) / Ke
+    h2d = hX.numel() * hX.element_size() + hQ.numel() * hQ.element_size()
+    d2h = hout.numel() * hout.element_size()
+    tiled = lib.lrkv_prefill_kernel_kind(ctypes.byref(cache.desc())) == _abi.LRKV_PREFILL_TILED
+
     ms = total_ms / K
     Ntot = 2 * d_h + 2 * H * r
     proj_flops = 2 * n * d * Ntot
@@ -658,7 +713,7 @@ def run_prefill(args, rank, world, local_rank):
     attn_flops = H * (4 * visible * (d_h + r) + 4 * n * d_h * r)
     attn_tf = attn_flops / (res_k["attention"] / 1e3) / 1e12
     proj_tf = proj_flops / (res_k["projection"] / 1e3) / 1e12
-    return {
+    res = {
         "metric": "LRKV prefill tokens/s", "value": round(world * n / (ms / 1e3), 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -676,8 +731,17 @@ def run_prefill(args, rank, world, local_rank):
                        "flops_per_launch": proj_flops, "avg_launch_ms": round(res_k["projection"], 4)},
         "breakdown_ms": {"projection": round(res_k["projection"], 4),
                          "attention": round(res_k["attention"], 4)},
+        "e2e": {"value": round(world * n / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "pinned host X and Q copied in, lrkv_prefill, out copied back and "
+                        "synchronised every step"},
+        # per step: row metadata, the projection, the attention (tiled path)
+        "gpu_launches": 3 * K if tiled else None,
         "clocks": clk,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_prefill(args.config, args.cpu_workers)
+    return res
 
 
 def main():

@@ -90,3 +90,76 @@ def time_oracle_decode(config: str, n_pairs: int, workers: int | None = None, se
             else:
                 os.environ[k] = v
     return dict(wall_s=wall, cpu_s=float(sum(cpu)), pairs=n_pairs, cores=workers, heads=H)
+
+
+_PF = None
+
+
+def _init_prefill(config):
+    """The prefill workload's inputs, drawn as bench.py draws them: rows of
+    request b are X[b T : (b + 1) T] at positions 0 .. T - 1."""
+    global _PF
+    import numpy as np
+    import lrkv_inputs as I
+    c = I.CONFIGS[config]
+    B, d, H, d_h, r, T = c["B"], c["d"], c["H"], c["d_h"], c["r"], c["T"]
+    ac = I.make_append_case([T] * B, [0] * B, d, dtype="bf16", seed=c["seed"], shuffle=True)
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=c["seed"])
+    rng = np.random.default_rng(99)
+    Q = I.f32_to_bf16_bits(rng.standard_normal((B * T, H, d_h)).astype(np.float32))
+    _PF = (c, ac.X, Q, w)
+
+
+def _run_prefill_request(job):
+    """Request b of the prefill workload through the oracle: the projection
+    of its T rows (timed alone), then oracle.prefill for k sampled rows and
+    all heads (which projects again); returns (t_proj, t_attn, k, T)."""
+    import numpy as np
+    import lrkv_inputs as I
+    from . import lrkv_oracle as O
+    b, k, seed = job
+    c, X, Q, w = _PF
+    T = c["T"]
+    f = lambda a: I.to_f64(a, "bf16")
+    Xb, Qb = f(X[b * T:(b + 1) * T]), f(Q[b * T:(b + 1) * T])
+    Ws = [f(w.W_S_K), f(w.W_S_V), f(w.U_K), f(w.U_V)]
+    Bk, Bv = f(w.B_K), f(w.B_V)
+    rows = np.random.default_rng(seed).choice(T, size=k, replace=False)
+    t0 = time.perf_counter()
+    O.project(Xb, *Ws)
+    t1 = time.perf_counter()
+    out = O.prefill(Qb, Xb, np.arange(T), np.full(T, b), *Ws, Bk, Bv, rows_wanted=rows)
+    t2 = time.perf_counter()
+    assert np.all(np.isfinite(out[rows]))
+    return t1 - t0, max(0.0, (t2 - t1) - (t1 - t0)), k, T
+
+
+def time_oracle_prefill(config: str, k_rows: int, workers: int | None = None):
+    """The oracle's prefill of the fresh-prompt workload on host cores: each
+    process takes one request (b = process index), times the projection of
+    its T rows and the causal attention of k_rows sampled rows (all heads),
+    and scales to a full request: T / (t_proj + t_attn T / k).  Processes run
+    concurrently, so the job's tokens/s is the sum of theirs.  Returns
+    dict(tokens_per_s, wall_s, cpu_s, cores, rows_sampled)."""
+    import lrkv_inputs as I
+    B = I.CONFIGS[config]["B"]
+    workers = max(1, min(workers or os.cpu_count() or 1, B))
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                             "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers, initializer=_init_prefill, initargs=(config,)) as pool:
+            t0 = time.perf_counter()
+            res = pool.map(_run_prefill_request, [(b, k_rows, 100 + b) for b in range(workers)])
+            wall = time.perf_counter() - t0
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    rate = sum(T / (tp + ta * T / k) for tp, ta, k, T in res)
+    return dict(tokens_per_s=rate, wall_s=wall, cpu_s=float(sum(tp * 2 + ta for tp, ta, _, _ in res)),
+                cores=workers, rows_sampled=k_rows * workers)
