@@ -112,9 +112,9 @@ enum {
  * head h reads group h / (H/G):  K_h = S_K[.., h/(H/G), :] + R_K[h] B_K[h]^T.
  * The shared weights of lrkv_append / lrkv_prefill / lrkv_decode_step are
  * then W_S_K, W_S_V [G*d_h, d] (group-major rows).  G must divide H; 0 and 1
- * both mean one shared basis.  The tiled prefill, the fused decode step and
- * the tensor-core rotary decode serve G = 1 (other G take the per-row and
- * generic kernels); the tensor-core decode covers G = 1 and G = 2.
+ * both mean one shared basis.  The tiled prefill and the tensor-core rotary
+ * decode serve G = 1 (other G take the per-row and generic kernels); the
+ * tensor-core decode covers G = 1 and G = 2.
  */
 typedef struct {
     void *S_K;
