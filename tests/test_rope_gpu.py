@@ -45,10 +45,14 @@ def _run_rope(case, table, status=None):
 LENS = [1, 2, 17, 300, 64, 65, 129, 900]
 
 
+# the tensor-core rotary kernel at every group shape: 4 heads with 128-byte
+# (r = 48, 32, 16) or 64-byte (r = 56, one R_K buffer) swizzled R_K, 2 heads
+# (r = 64), H = 32, and pages of 32, 64 and 128 rows
 @pytest.mark.parametrize("H,d_h,r,dtype,ps", [(16, 128, 48, "bf16", 64), (8, 64, 24, "bf16", 16),
                                               (4, 16, 4, "f32", 64), (32, 128, 32, "bf16", 32),
                                               (16, 128, 64, "bf16", 64), (16, 128, 56, "fp8", 64),
-                                              (2, 256, 8, "f32", 16)])
+                                              (2, 256, 8, "f32", 16), (16, 128, 56, "bf16", 64),
+                                              (16, 128, 16, "bf16", 128), (16, 128, 32, "bf16", 32)])
 def test_rope_decode_parity(H, d_h, r, dtype, ps):
     import rank_kv_attention_gb300 as L
     case = I.make_decode_case(len(LENS), H, d_h, r, LENS, dtype=dtype, seed=H + r, shuffle=True,
