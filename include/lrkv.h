@@ -259,7 +259,9 @@ LRKV_API int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const
                               size_t workspace_bytes, int32_t *dev_status, lrkv_stream_t stream);
 
 /*
- * lrkv_decode_step_host - lrkv_decode_step with the step's per-token inputs
+ * lrkv_decode_step_host - lrkv_decode_step (reading note "Low-Rank Key Value
+ * Attention", section 3: Algorithm 1 for the new rows, Algorithm 2 with
+ * equations 6 and 7 for the queries) with the step's per-token inputs
  * and its output in HOST memory: the new rows X, the queries q and the
  * lengths seq_lens are copied to the device, the step runs, and out is
  * copied back, all enqueued on `stream` by this one call (it does not
@@ -440,7 +442,9 @@ LRKV_API int lrkv_prefill_rope(const void *X, const void *Q, const int32_t *cu_r
  * Returns 0 for invalid arguments.
  */
 LRKV_API size_t lrkv_cache_bytes(int32_t H, int32_t d_h, int32_t r, int64_t tokens, int32_t dtype);
-/* The same with G shared groups: tokens * 2 * (G*d_h + H*r) * sizeof(dtype). */
+/* The same with G shared groups (section 4, equation 9 with G shared rows per
+ * token; the grouped variant of section 3): tokens * 2 * (G*d_h + H*r) *
+ * sizeof(dtype); 0 for a G that does not divide H. */
 LRKV_API size_t lrkv_cache_bytes_grouped(int32_t H, int32_t d_h, int32_t r, int32_t G,
                                          int64_t tokens, int32_t dtype);
 
