@@ -270,8 +270,10 @@ LRKV_API int lrkv_decode_step(const void *X, int32_t d, const void *W_S_K, const
  *
  *   X_host [B, d], q_host [B, H, d_h], out_host [B, H, d_h]: host memory,
  *     element type as lrkv_decode_step; seq_lens_host [B] int32, host.
- *     Page-locked buffers (cudaHostAlloc / cudaHostRegister) let the copies
- *     run asynchronously; pageable ones work but the copies then block.
+ *     Page-locked buffers (cudaHostAlloc / cudaHostRegister) are read and
+ *     written through their device-mapped addresses: one copy kernel stages
+ *     the inputs and the decode's last kernel stores out; pageable buffers go
+ *     through the copy engines (cudaMemcpyAsync, which may then block).
  *   workspace >= lrkv_decode_step_host_workspace_bytes(B, H, d_h, r, d,
  *                max_seq_len, dtype) bytes of device memory, 256-byte
  *                aligned: the step's workspace plus device copies of the
