@@ -297,7 +297,9 @@ class StepGraph:
         return self.out
 
     def close(self):
+        """Destroy the graph once every launch of it has finished."""
         if self._h is not None:
+            torch.cuda.synchronize()
             _abi.lib().lrkv_step_graph_destroy(self._h)
             self._h = None
 
