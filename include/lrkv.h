@@ -309,7 +309,8 @@ LRKV_API int lrkv_decode_step_host(const void *X_host, int32_t d, const void *W_
  * table and workspace must stay allocated while the graph exists.
  *
  * Returns LRKV_OK and sets *graph, or an error (then *graph = NULL).
- * lrkv_step_graph_destroy frees a graph (NULL is a no-op).
+ * lrkv_step_graph_destroy frees a graph (NULL is a no-op); synchronise the
+ * streams it was launched on first.
  */
 typedef struct lrkv_step_graph_s *lrkv_step_graph_t;
 LRKV_API int lrkv_step_graph_create(lrkv_step_graph_t *graph, const void *X_host, int32_t d,
