@@ -109,6 +109,23 @@ def test_projection_by_hand_and_against_single_basis():
         np.testing.assert_allclose(x.reshape(y.shape), y, rtol=1e-14)
 
 
+def test_identical_groups_are_one_basis():
+    """G copies of the same shared rows (every group's basis equal) give the
+    single-basis oracle's result for every head, paged, to rounding."""
+    g = np.random.default_rng(6)
+    H, G, d_h, r, ps = 6, 3, 8, 2, 4
+    lens = [5, 9]
+    pt = np.array([[0, 1, 0], [2, 3, 4]])
+    S_K, S_V = g.standard_normal((5, ps, d_h)), g.standard_normal((5, ps, d_h))
+    R_K, R_V = g.standard_normal((5, ps, H, r)), g.standard_normal((5, ps, H, r))
+    q = g.standard_normal((2, H, d_h))
+    BK, BV = g.standard_normal((H, d_h, r)), g.standard_normal((H, d_h, r))
+    rep = lambda S: np.repeat(S[:, :, None, :], G, axis=2)
+    a = grouped.decode_grouped(q, rep(S_K), rep(S_V), R_K, R_V, BK, BV, pt, lens, ps)
+    b = oracle.decode(q, S_K, S_V, R_K, R_V, BK, BV, pt, lens, ps)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
 def test_paged_matches_per_request():
     g = np.random.default_rng(5)
     H, G, d_h, r, ps = 4, 2, 8, 2, 4
