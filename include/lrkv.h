@@ -205,13 +205,17 @@ LRKV_API int lrkv_decode(const void *q, const lrkv_cache_t *cache, const void *B
  * workspace lrkv_decode asks for.  This entry point takes the same arguments
  * minus the workspace and keeps its scratch (launch plan, private queries,
  * per-segment softmax partials) in a device array built into the library:
- *   - the array is LRKV_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU that loads
- *     the library, held until the process exits;
+ *   - the array is LRKV_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU where the
+ *     library's device code is loaded, held until the process exits.  CUDA
+ *     loads device code lazily by default, so the array's memory is committed
+ *     by the first call on each device, not when the library is opened: make
+ *     that first call before the host reserves the rest of device memory for
+ *     its own pool, and before any stream capture;
  *   - sizes whose lrkv_decode_workspace_bytes(B, H, d_h, r, max_seq_len,
  *     dtype) exceeds that are rejected with LRKV_E_WORKSPACE before any work;
- *   - the first call on each device looks up the array's device address with
- *     that device current (set-up done once per device); make that first call
- *     before any stream capture;
+ *   - every call looks up the array's device address with its device current
+ *     (after the first call on a device this is a table read), so the entry
+ *     point stays valid after the device's primary context is reset;
  *   - every call on a device shares the one array and leaves its scratch
  *     behind; nothing in it needs clearing (each call writes every value before
  *     reading it), but two calls that can run at the same time on the GPU

@@ -16,7 +16,7 @@ G = 1 is the single shared basis of the rest of the note; G = H with no
 private part is multi-head attention, and 1 < G < H with no private part is
 grouped-query attention.
 
-Readings (each also listed in the design doc):
+Readings where the note leaves a choice open:
   * groups are runs of consecutive heads of equal size: g(h) = h // (H / G),
     G divides H;
   * a token's shared row holds the G groups one after another

@@ -23,7 +23,7 @@ A second, factored path (section 3, equations 6 and 7) exists only so the
 tests can check the oracle against itself; it never feeds a comparison with
 the CUDA path.
 
-Readings where the note is silent (each also listed in the design doc):
+Readings where the note is silent:
   * the current decode token is visible to itself (causal j <= i): decode
     runs after the new row has been appended (Algorithm 1 tracks sequence
     boundaries for the causal mask, section 2 says decode adds one new row);

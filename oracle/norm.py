@@ -13,7 +13,7 @@ RoPE) computes 1 / n_{h,j} when the token is appended, stores it per head
 and position, and multiplies it onto the sum of the two score terms; a fixed
 per-channel gain moves to the query side.
 
-Readings (each also listed in the design doc):
+Readings where the note leaves a choice open:
   * the library applies only 1 / n_{h,j}; a per-channel gain g is folded
     into the query by the caller (q g . k / n = q . (k g) / n), as is the
     query's own normalisation;

@@ -15,7 +15,7 @@ linear, so it distributes over the shared and private terms of the key
 (s_j + z_j B_h^T) D_j, the query at position i is q~_i = q_i D_i.  Values
 are not rotated.
 
-Readings (the note fixes no convention; each also listed in the design doc):
+Readings (the note fixes no convention):
   * D_j is the rotation of the original rotary embedding: channel pairs
     (2c, 2c+1) of a row vector x turn by angle j * theta_c,
         (x_2c, x_2c+1) -> (x_2c cos - x_2c+1 sin, x_2c sin + x_2c+1 cos),

@@ -337,13 +337,8 @@ cudaError_t launch_append_rows(const AppendArgsT<T> &a) {
     const int cols_per_block = kSkWarps * kSkCols;
     dim3 grid((Ntot + cols_per_block - 1) / cols_per_block, (a.n + kSkRows - 1) / kSkRows);
     const size_t sm = (size_t)kSkRows * a.d * sizeof(T);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(append_rows_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(append_rows_kernel<T>, 160 * 1024);
+    if (e != cudaSuccess) return e;
     return launch_pdl(append_rows_kernel<T>, grid, dim3(kSkWarps * 32), sm, a.stream, a);
 }
 

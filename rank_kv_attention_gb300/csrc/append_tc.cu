@@ -311,13 +311,8 @@ cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a) {
         return cudaErrorInvalidValue;
     TcBlocks t;
     if (!tc_blocks(a, t)) return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(append_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(append_tc_kernel, TC_SMEM);
+    if (e != cudaSuccess) return e;
     const int grid = std::min(t.ntiles, device_sm_count());
     return launch_pdl(append_tc_kernel, dim3(grid), dim3(TC_THREADS), TC_SMEM, a.stream, maps, a, t);
 }

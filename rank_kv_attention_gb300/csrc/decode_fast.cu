@@ -1584,12 +1584,8 @@ static cudaError_t launch_fast_cfg(const DecodeArgs &a, const DecodeWs &ws, int 
     }
     if (!GS && c.N_K && !make_row_map(&maps.nk, c.N_K, rows, H, 2, C::TS)) return cudaErrorInvalidValue;
     auto kern = decode_split_fast_kernel<C>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(kern, C::SMEM);
+    if (e != cudaSuccess) return e;
     FastParams P = fast_params(a, ws);
     if (GS) P.norm = 0;
     return launch_pdl(kern, dim3(G), dim3(C::NT), C::SMEM, a.stream, maps, P);
@@ -1666,12 +1662,8 @@ static cudaError_t launch_rope_cfg(const DecodeArgs &a, const DecodeWs &ws) {
         !make_map(&m.qb, a.rope_ws.qb, (int64_t)a.B * C::NG * 16, 128, 2, 0, false, 16))
         return cudaErrorInvalidValue;
     auto kern = rope_scores_tc_kernel<C>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(kern, C::SMEM);
+    if (e != cudaSuccess) return e;
     const FastParams P = fast_params(a, ws);
     const int ranges = std::max(1, device_sm_count() / C::NG);
     return launch_pdl(kern, dim3(ranges * C::NG), dim3(C::NT), C::SMEM, a.stream, m, P, br);

@@ -763,16 +763,11 @@ cudaError_t launch_prologue(const DecodeArgs &a, const DecodeWs &ws, int G, int 
     // the tensor-core rotary path treats a request past the table's end as an
     // invalid length (zero output, flagged), like every kernel after it
     const int max_len = decode_max_len(a);
-    const int kind = rope_fast ? 1 : small ? 2 : 0;
     auto kern = rope_fast ? decode_prologue_kernel<T, true, kProThreads>
               : small     ? decode_prologue_kernel<T, false, 128>
                           : decode_prologue_kernel<T, false, kProThreads>;
-    static bool attr_set[3] = {false, false, false};
-    if (!attr_set[kind]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set[kind] = true;
-    }
+    cudaError_t e = smem_limit_once(kern, 200 * 1024);
+    if (e != cudaSuccess) return e;
     return launch_pdl(kern, grid, dim3(small ? 128 : kProThreads), sm, a.stream,
                       static_cast<const T *>(a.q), static_cast<const T *>(a.B_K), a.seq_lens,
                       static_cast<T *>(a.out), a.B, a.cache.H, a.cache.d_h, a.cache.r,
@@ -853,13 +848,8 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G) {
     const bool staged = (size_t)a.cache.d_h * a.cache.r <= kStageFloats;
     const size_t bv_bytes = staged ? ((size_t)a.cache.d_h * a.cache.r * sizeof(T) + 15) / 16 * 16 : 0;
     const size_t sm = bv_bytes + sizeof(float) * ((size_t)a.cache.r + G);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(decode_combine_kernel<T>, 200 * 1024);
+    if (e != cudaSuccess) return e;
     const int nthr = (a.cache.d_h + a.cache.r <= 256) ? 128 : 256;
     return launch_pdl(decode_combine_kernel<T>, grid, dim3(nthr), sm, a.stream,
                       static_cast<const T *>(a.B_V), a.B, a.cache.H, a.cache.d_h, a.cache.r,

@@ -2,8 +2,6 @@
 // memory.  The decode's scratch (launch plan, private queries and per-segment
 // partial softmax states) lives in one file-scope device array that is part
 // of the library image, so the caller passes only inputs and outputs.
-#include <mutex>
-
 #include "decode_kernels.cuh"
 
 namespace lrkv {
@@ -13,31 +11,21 @@ namespace lrkv {
 // address: its device address is obtained with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LRKV_NOALLOC_SCRATCH_BYTES];
 
-namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_addr[kMaxDevices] = {};
-}  // namespace
-
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current).  Returns nullptr on failure.
+// Device address of the scratch array on the current device, looked up on
+// every call with that device current.  The first lookup on a device loads
+// the library's device code there (CUDA loads modules lazily), which is when
+// the array's memory is committed; later lookups are a table read.  Looking
+// it up each time, instead of caching it, keeps the address right after the
+// device's primary context has been reset and the module loaded again.
+// Returns nullptr (and sets *err) on failure.
 void *noalloc_scratch_address(cudaError_t *err) {
-    int dev = 0;
-    *err = cudaGetDevice(&dev);
-    if (*err != cudaSuccess) return nullptr;
-    if (dev < 0 || dev >= kMaxDevices) {
-        *err = cudaErrorInvalidDevice;
+    void *p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) {
+        cudaGetLastError();  // reset the last-error state so later CUDA calls start clean
         return nullptr;
     }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
-        void *p = nullptr;
-        *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (*err != cudaSuccess) return nullptr;
-        g_addr[dev] = p;
-    }
-    *err = cudaSuccess;
-    return g_addr[dev];
+    return p;
 }
 
 }  // namespace lrkv

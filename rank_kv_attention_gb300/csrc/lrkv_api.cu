@@ -4,6 +4,8 @@
 #include <algorithm>
 #include <cmath>
 #include <string.h>
+#include <mutex>
+#include <vector>
 
 #include "append_kernels.cuh"
 #include "decode_kernels.cuh"
@@ -48,6 +50,24 @@ int device_sm_count() {
         return 160;  // no device visible (sizing queries only): an upper bound
     }
     return n;
+}
+
+cudaError_t smem_limit_once(const void *kern, int bytes) {
+    struct Key {
+        const void *kern;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Key> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Key &k : done)
+        if (k.kern == kern && k.dev == dev && k.bytes == bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back({kern, dev, bytes});
+    return e;
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

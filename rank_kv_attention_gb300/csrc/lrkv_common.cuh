@@ -480,6 +480,16 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device that is current when it is
+// set, so it is recorded per (kernel, device, size) and set once for each:
+// a process that drives several GPUs gets it on every one of them.
+cudaError_t smem_limit_once(const void *kern, int bytes);
+template <typename... KArgs>
+inline cudaError_t smem_limit_once(void (*kern)(KArgs...), int bytes) {
+    return smem_limit_once(reinterpret_cast<const void *>(kern), bytes);
+}
+
 // Launch with programmatic dependent launch allowed: the kernel may be
 // scheduled while its predecessor in the stream drains; every kernel of this
 // library starts with pdl_wait(), so stream order is kept for its reads.

@@ -604,13 +604,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
 template <int R16>
 cudaError_t launch_r16(const PfMaps &maps, const PfArgs &a, dim3 grid, cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<R16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = smem_limit_once(prefill_tc_kernel<R16>, PF_SMEM);
+    if (e != cudaSuccess) return e;
     return launch_pdl(prefill_tc_kernel<R16>, grid, dim3(PF_THREADS), PF_SMEM, s, maps, a);
 }
 

@@ -117,3 +117,47 @@ def test_append_bad_rows_skipped_and_flagged():
     got = host_bits(cache.S_K)
     assert np.all(got[~t] == I.BF16_NAN_BITS)
     assert not np.any(got[t] == I.BF16_NAN_BITS)
+
+
+def _integer_case(n_per_seq, d, density, seed, H=16, d_h=128, r=48):
+    """Integer rows in [-2, 2] and sparse {-1, 0, 1} weights: every projection
+    is an integer of magnitude below 256, exact in fp32 accumulation and in
+    bf16 storage, so the written bytes are fixed bit for bit."""
+    ac = I.make_append_case(n_per_seq, [0] * len(n_per_seq), d, dtype="bf16", seed=seed,
+                            shuffle=True, spare_pages=3, interleave=True)
+    rng = np.random.default_rng(seed + 1)
+    ac.X = I.f32_to_bf16_bits(rng.integers(-2, 3, size=ac.X.shape).astype(np.float32))
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=seed + 2)
+    for name in ("W_S_K", "W_S_V", "U_K", "U_V"):
+        a = getattr(w, name)
+        vals = rng.integers(-1, 2, size=a.shape).astype(np.float32) * (rng.random(a.shape) < density)
+        setattr(w, name, I.f32_to_bf16_bits(vals))
+    return ac, w
+
+
+# The persistent tensor-core projection walks its 128 x 256 output tiles with
+# a stride of one grid (one CTA per SM); more than two grids' worth of tiles
+# makes every CTA run its tile loop at least twice, so the second tensor-
+# memory accumulator, the operand ring running on across tiles and the
+# epilogue overlapping the next tile's products are all compared here.
+@pytest.mark.parametrize("n_per_seq,d,density", [
+    ([4096, 3000, 1173], 256, 0.1),   # 8269 rows: 65 x 7 = 455 tiles of 4 k-blocks
+    ([3000, 2600], 2048, 0.02),       # 5600 rows at d = 2048: 44 x 7 = 308 tiles of 32 k-blocks
+])
+def test_append_many_tiles_bit_exact(n_per_seq, d, density):
+    H, d_h, r = 16, 128, 48
+    n = sum(n_per_seq)
+    tiles = -(-n // 128) * ((2 * d_h + 2 * H * r) // 256)
+    assert tiles > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    ac, w = _integer_case(n_per_seq, d, density, seed=n % 1000)
+    pools, cache = _run_append(ac, w, H, d_h, r, "bf16")
+    want = _oracle_pools(ac, w, pools, "bf16")
+    touched = _touched(ac)
+    for k, t in enumerate((cache.S_K, cache.S_V, cache.R_K, cache.R_V)):
+        wk = want[k][touched]
+        assert np.all(wk == np.round(wk)) and np.abs(wk).max() < 256, "case must be exact in bf16"
+        got_bits = host_bits(t)
+        want_bits = I.f32_to_bf16_bits(want[k].astype(np.float32))
+        assert np.array_equal(got_bits[touched], want_bits[touched]), f"pool {k}"
+        canary = np.asarray(pools[k]).view(got_bits.dtype)
+        assert np.array_equal(got_bits[~touched], canary[~touched]), f"pool {k} canary"

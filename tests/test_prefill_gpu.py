@@ -208,3 +208,39 @@ def test_tiled_prefill_bad_page_flagged():
     assert np.all(np.isfinite(got))
     keep = (sid == 0) | (pos < 64)
     assert_close(got[keep], ref[keep], "bf16", "rows unaffected by the bad page")
+
+
+def test_prefill_2048_pools_full():
+    """The four pools lrkv_prefill writes for the whole 8 x 2048 workload
+    (16384 rows, d = 2048, 128 x 7 output tiles of the persistent projection)
+    against the float64 projection placed by the oracle: every written slot
+    within the bf16 tolerance and, tighter, equal to the oracle's value
+    rounded to bf16 except for rare rounding-boundary cases one bf16 unit
+    apart (fp32 accumulation can land on the other side of a tie); spare
+    pages keep their NaN canary."""
+    c = I.CONFIGS["prefill_2048"]
+    Bq, d, H, d_h, r, T = c["B"], c["d"], c["H"], c["d_h"], c["r"], c["T"]
+    ac = I.make_append_case([T] * Bq, [0] * Bq, d, dtype="bf16", seed=c["seed"], shuffle=True,
+                            spare_pages=2)
+    w = I.make_weights(d, H, d_h, r, "bf16", seed=c["seed"])
+    rng = np.random.default_rng(99)
+    Q = I.f32_to_bf16_bits(rng.standard_normal((Bq * T, H, d_h)).astype(np.float32))
+    pools = I.empty_pools(ac.num_pages, 64, H, d_h, r, "bf16", canary=True)
+    _, cache = _run_prefill(ac.X, Q, [T] * Bq, [0] * Bq, w, ac.page_table, pools, "bf16")
+    f = lambda a: I.to_f64(a, "bf16")
+    rows = oracle.project(f(ac.X), f(w.W_S_K), f(w.W_S_V), f(w.U_K), f(w.U_V))
+    want = oracle.place([f(p) for p in pools], rows, ac.positions, ac.seq_ids, ac.page_table, 64)
+    touched = np.zeros((ac.num_pages, 64), bool)
+    for b, p in zip(ac.seq_ids, ac.positions):
+        touched[ac.page_table[b, p // 64], p % 64] = True
+    assert touched.sum() == Bq * T and (~touched).sum() == 2 * 64
+    from gpu_util import host_bits
+    for k, t in enumerate((cache.S_K, cache.S_V, cache.R_K, cache.R_V)):
+        got_bits = host_bits(t)
+        got = I.bf16_bits_to_f64(got_bits)
+        assert_close(got[touched], want[k][touched], "bf16", f"pool {k}")
+        want_bits = I.f32_to_bf16_bits(want[k][touched].astype(np.float32)).astype(np.int32)
+        diff = np.abs(got_bits[touched].astype(np.int32) - want_bits)
+        assert diff.max() <= 1, f"pool {k}: a value more than one bf16 unit from the oracle"
+        assert np.count_nonzero(diff) <= 1e-4 * diff.size, f"pool {k}: {np.count_nonzero(diff)} off"
+        assert np.all(got_bits[~touched] == I.BF16_NAN_BITS), f"pool {k} canary"
