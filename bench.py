@@ -2,14 +2,18 @@
 """LRKV decode benchmark on GB300.
 
 One step = one decode step of one layer for a batch of requests, through the
-C ABI: lrkv_append writes each request's new row (shared + private
-projections) at position T-1, then lrkv_decode attends over the T cached
-rows (factored scores, one online softmax, shared + private value
-reductions, expansion by B_V^T).  Inputs are seeded synthetic tensors of the
-workload's shape, resident in HBM when the timed region starts.
+C ABI: lrkv_decode_step appends each request's new row (shared + private
+projections) at position T-1 and attends over the T cached rows (factored
+scores, one online softmax, shared + private value reductions, expansion by
+B_V^T).  Inputs are seeded synthetic tensors of the workload's shape,
+resident in HBM when the timed region starts.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
-oracle on the same workload instead.
+Prints one JSON line (rank 0).  The headline is the decode_T4096 workload;
+the same line carries, under "configs", the long-context, ragged-paged and
+prefill workloads measured the same way (step time, the dominant kernel's
+roofline over >= 500 launches, end-to-end throughput from host buffers).
+``--impl reference`` times the float64 CPU oracle on the same workload and
+sample as the line's cpu_baseline.
 """
 import argparse
 import hashlib
@@ -25,11 +29,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "LRKV decode tokens/s and achieved HBM GB/s (% of roofline) at 1 GB300"
+PREFILL_METRIC = "LRKV prefill tokens/s"
 L2_BYTES = 129 * 10 ** 6
 NORTH_STAR_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-# FP32 FMA peak from unit counts and the maximum SM clock: 152 SMs x 128 FP32
-# lanes x 2 flops x 2.07 GHz
+FALLBACK_BF16_TFLOPS = 1900.0
 
 WORKLOADS = {
     "decode_T4096": "B=16 requests, d=2048, H=16, d_h=128, r=48, history T=4096 (current row "
@@ -55,22 +59,33 @@ WORKLOADS = {
     "prefill_2048": "B=8 fresh 2048-token prompts, d=2048, H=16, d_h=128, r=48, bf16: append "
                     "projection X.[W_S_K|W_S_V|U_K|U_V] then causal LRKV attention of every row",
 }
+# measured beside the headline in the same run (one entry each under "configs")
+EXTRA_CONFIGS = "decode_T32768,ragged_paged,prefill_2048"
+# the cache is drawn on the device for these (host drawing of 0.6-1.1 GB
+# would dominate the run); every other workload uses the host generator
+DEVICE_DRAWN = ("decode_T32768", "ragged_paged")
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_T4096", choices=sorted(WORKLOADS))
+    ap.add_argument("--extra-configs", default=EXTRA_CONFIGS,
+                    help="comma-separated workloads measured beside the headline ('' for none)")
+    ap.add_argument("--extra-steps", type=int, default=300,
+                    help="timed steps of each extra workload")
+    ap.add_argument("--roofline-launches", type=int, default=512,
+                    help="launches the dominant kernel is timed over (outside the timed steps)")
     ap.add_argument("--cpu-workers", type=int, default=0,
                     help="host processes for the oracle timing (0: one per core)")
     ap.add_argument("--cpu-pairs", type=int, default=1024,
-                    help="(request, head) pairs of the CPU-baseline sample")
+                    help="(request, head) pairs of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -112,6 +127,54 @@ def workload_shape(name):
     c = dict(I.CONFIGS[name])
     c.setdefault("d", 2048)
     return c
+
+
+def decode_lengths(name):
+    """Sequence lengths of a decode workload (host only, no pools drawn)."""
+    import numpy as np
+    import lrkv_inputs as I
+    c = I.CONFIGS[name]
+    if name == "ragged_paged":
+        return I.ragged_lengths(c["B"], c["lo"], c["hi"], c["seed"])
+    return np.full(c["B"], c["T"], np.int32)
+
+
+def cache_copies(cache_bytes):
+    """Copies of the cache the timed steps rotate over: at least two, and
+    enough that the working set is four times L2, so every step reads its
+    cache from HBM (the previous step's rows are never the next step's)."""
+    return max(2, math.ceil(4 * L2_BYTES / cache_bytes))
+
+
+def describe(name, world):
+    """The line's ``config`` object for a workload (both arms print the same)."""
+    c = workload_shape(name)
+    base = {"workload": f"{name}: {WORKLOADS[name]}", "B": c["B"], "d": c["d"], "H": c["H"],
+            "d_h": c["d_h"], "r": c["r"], "parallelism": f"replicas x{world} (requests are independent)"}
+    if name == "prefill_2048":
+        base.update({"seq_len": c["T"], "rows": c["B"] * c["T"],
+                     "l2": "no flush: one step's working set (~0.35 GB) exceeds L2",
+                     "step": "lrkv_prefill (projection and placement of every row, then causal "
+                             "attention of every row)"})
+        return base
+    lens = decode_lengths(name)
+    G = c.get("groups", 1)
+    eb = 1 if c["dtype"] == "fp8" else 2
+    norm, rope = bool(c.get("norm")), bool(c.get("rope"))
+    cached = int(lens.astype("int64").sum())
+    pages = int(sum((int(L) + 63) // 64 for L in lens)) + (3 if name == "ragged_paged" else 0)
+    cache_bytes = pages * 64 * (2 * (G * c["d_h"] + c["H"] * c["r"]) * eb + (2 * c["H"] if norm else 0))
+    n = cache_copies(cache_bytes)
+    base.update({"groups": G, "seq_len": int(lens.max()), "cached_rows": cached,
+                 "l2": f"inputs larger than L2: the cache is rotated over {n} copies "
+                       f"({n * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
+                 "step": ("lrkv_append (B new rows) + lrkv_decode_rope (B queries)" if rope else
+                          "lrkv_decode_step (append of the B new rows" +
+                          (", their reciprocal key norms" if norm else "") + ", decode of the B queries)")})
+    if name in DEVICE_DRAWN:
+        base["inputs"] = ("lengths, page table, queries and bases from the host generator; cache "
+                          "pools N(0,1) bf16 drawn on the device by torch's seeded generator")
+    return base
 
 
 # ----------------------------------------------------------------------------
@@ -172,7 +235,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# our arm
+# committed ncu summaries
 # ----------------------------------------------------------------------------
 DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
 PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
@@ -187,51 +250,88 @@ def kernel_source_hash(files=DECODE_SPLIT_SOURCES):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config, name="decode_split", files=DECODE_SPLIT_SOURCES):
-    """DRAM bytes per launch of a kernel from its committed ncu summary
-    (profiles/<name>_<config>.md), or None if absent or taken on a different
+def summary_sections(path):
+    """The '- key: value' figures of an ncu summary, per kernel: a section
+    starts at a '- kernel: `name`' line and runs to the next one.  Figures
+    before the first such line (the capture's source hash) belong to the
+    file."""
+    head, sections, cur = {}, {}, None
+    for line in open(path):
+        t = line.strip()
+        if not (t.startswith("- ") and ":" in t):
+            continue
+        k, v = t[2:].split(":", 1)
+        k, v = k.strip(), v.strip().split("  (")[0].strip().strip("`")
+        if k == "kernel":
+            cur = sections.setdefault(v, {})
+        elif cur is None:
+            head[k] = v
+        else:
+            cur[k] = v
+    return head, sections
+
+
+def profiled_traffic(summary, kernel, files):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary
+    profiles/<summary>.md (read from that kernel's own section), or None if
+    the file or section is absent or the capture was taken on a different
     kernel source."""
-    path = os.path.join(ROOT, "profiles", f"{name}_{config}.md")
+    path = os.path.join(ROOT, "profiles", f"{summary}.md")
     if not os.path.exists(path):
         return None
-    vals = {}
-    for line in open(path):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("kernel_source_sha256_16") != kernel_source_hash(files):
+    head, sections = summary_sections(path)
+    sec = sections.get(kernel)
+    if sec is None:
+        return None
+    if head.get("kernel_source_sha256_16") != kernel_source_hash(files):
         return None
     try:
-        return float(vals["dram_bytes_per_full_launch"])
+        return float(sec["dram_bytes_per_full_launch"])
     except (KeyError, ValueError):
         return None
 
 
-def run_ours(args, rank, world, local_rank):
+# ----------------------------------------------------------------------------
+# our arm: one decode workload
+# ----------------------------------------------------------------------------
+def profile_pass(lib, fn, n):
+    """Run fn(i) n times with the library's per-kernel event pairs on and
+    return {kind: (mean ms per launch, launches)}."""
+    import ctypes
+    import torch
+    assert lib.lrkv_profile_enable(1) == 0
+    for i in range(n):
+        fn(i)
+    torch.cuda.synchronize()
+    out = {}
+    for which in (0, 1, 2):
+        tot, nl = ctypes.c_double(), ctypes.c_int32()
+        assert lib.lrkv_profile_read(which, ctypes.byref(tot), ctypes.byref(nl)) == 0
+        out[which] = (tot.value / nl.value if nl.value else None, nl.value)
+    lib.lrkv_profile_enable(0)
+    return out
+
+
+def decode_leg(lib, name, dev, world, local_rank, K, W, R, Ke, headline):
+    """Step timing, the split kernel's roofline and the end-to-end rate of
+    one decode workload; returns the line's fields for it."""
     import ctypes
     import numpy as np
     import torch
     import lrkv_inputs as I
     import rank_kv_attention_gb300 as L
-    from rank_kv_attention_gb300 import _abi
     from rank_kv_attention_gb300.api import PagedCache
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    lib = L.lib()
-
-    name = args.config
     c = workload_shape(name)
-    case = I.config_decode_case(name)
+    case = I.config_decode_case(name, device=dev if name in DEVICE_DRAWN else None)
     Bn, H, d_h, r, d = case.B, case.H, case.d_h, case.r, c["d"]
     G = case.groups
     w = I.make_weights(d, H, d_h, r, "bf16", seed=1, groups=G)
     x_new = I.make_append_case([1] * Bn, case.seq_lens - 1, d, seed=2).X
 
     def to_dev(a, kind="bf16"):
+        if isinstance(a, torch.Tensor):
+            return a.to(dev)
         if kind == "bf16":
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
         if kind == "fp8":
@@ -239,7 +339,7 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
     eb = 1 if case.dtype == "fp8" else 2   # bytes per cache element
-    norm = bool(c.get("norm"))
+    norm, rope = bool(c.get("norm")), bool(c.get("rope"))
     base = PagedCache(*(to_dev(t, case.dtype) for t in (case.S_K, case.S_V, case.R_K, case.R_V)),
                       tuple(case.scale))
     if norm:   # joint key norms of every cached row, written once before timing
@@ -252,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
                     to_dev(case.page_table, "i32"))
     cache_bytes = sum(t.numel() * eb for t in (base.S_K, base.S_V, base.R_K, base.R_V)) + \
         (base.N_K.numel() * 2 if norm else 0)
-    n_copies = max(1, math.ceil(4 * L2_BYTES / cache_bytes))
+    n_copies = cache_copies(cache_bytes)
     caches = [base] + [PagedCache(*(t.clone() for t in (base.S_K, base.S_V, base.R_K, base.R_V)),
                                   base.scale, base.N_K.clone() if norm else None, base.norm_eps)
                        for _ in range(n_copies - 1)]
@@ -266,7 +366,6 @@ def run_ours(args, rank, world, local_rank):
     pt = to_dev(case.page_table, "i32")
     max_seq = int(case.seq_lens.max())
     out = torch.empty_like(q)
-    rope = bool(c.get("rope"))
     ws = L.workspace(max(L.decode_step_workspace_bytes(Bn, H, d_h, r, max_seq),
                          L.decode_rope_workspace_bytes(Bn, H, d_h, r, max_seq) if rope else 0), dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -323,8 +422,7 @@ def run_ours(args, rank, world, local_rank):
     barrier = lambda: rank_barrier(world)
     ranks_max = lambda x: max_over_ranks(x, world, dev)
 
-    # ---- device-resident timed region (step throughput)
-    K, W = args.steps, args.warmup
+    # ---- device-resident timed region (step throughput): exactly K steps
     for i in range(max(W, 3)):
         step(i)
     torch.cuda.synchronize()
@@ -344,43 +442,32 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     total_ms = ranks_max(e0.elapsed_time(e1))
 
-    # ---- live breakdown: the same K steps with only one of the two calls
-    def timed(fn):
+    # ---- live breakdown: the calls of a step on their own
+    def timed(fn, n):
         torch.cuda.synchronize()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for i in range(K):
+        for i in range(n):
             fn(i)
         a1.record(stream)
         torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / K
-    append_ms = timed(lambda i: f_app(*calls[i % n_copies][0]))
-    decode_ms = timed(lambda i: f_dec(*calls[i % n_copies][1]))
-    separate_ms = None if rope else timed(separate)
+        return a0.elapsed_time(a1) / n
+    nb = max(K, R)
+    append_ms = timed(lambda i: f_app(*calls[i % n_copies][0]), nb)
+    decode_ms = timed(lambda i: f_dec(*calls[i % n_copies][1]), nb)
+    separate_ms = None if rope else timed(separate, nb)
 
-    # ---- the split kernel's own duration: the library brackets each launch
-    # with CUDA events on its stream (a second pass over K steps, so those
-    # events do not perturb the step timing above)
-    ok = lib.lrkv_profile_enable(1)
-    assert ok == 0
-    for i in range(K):
-        step(i)
-    torch.cuda.synchronize()
-    tot = ctypes.c_double()
-    nl = ctypes.c_int32()
-    assert lib.lrkv_profile_read(0, ctypes.byref(tot), ctypes.byref(nl)) == 0
-    split_ms = tot.value / max(1, nl.value)
-    # the rotary score kernel (exact-RoPE tensor-core path), bracketed alone
-    tot_s, nl_s = ctypes.c_double(), ctypes.c_int32()
-    assert lib.lrkv_profile_read(2, ctypes.byref(tot_s), ctypes.byref(nl_s)) == 0
-    scores_ms = tot_s.value / nl_s.value if nl_s.value else None
-    lib.lrkv_profile_enable(0)
+    # ---- the dominant kernel's own duration over R launches: the library
+    # brackets each launch with CUDA events on its stream (outside the timed
+    # steps above, so those events do not perturb the step timing)
+    prof = profile_pass(lib, step, R)
+    split_ms, n_split = prof[0]
+    scores_ms, n_scores = prof[2]
     st = int(status.item())
     if st:
         raise RuntimeError(f"device status {st}")
 
     # ---- end to end through the C ABI with host buffers
-    Ke = args.e2e_steps or max(50, min(K, 2000))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     d2h = hout.numel() * hout.element_size()
     if not rope:
@@ -425,9 +512,9 @@ def run_ours(args, rank, world, local_rank):
         dbuf = torch.empty(o, dtype=torch.uint8, device=dev)
         views = []
         for t, a in zip(parts, offs):
-            nb = t.numel() * t.element_size()
-            hbuf[a:a + nb].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
-            views.append(dbuf[a:a + nb].view(t.dtype).view(t.shape))
+            nbytes = t.numel() * t.element_size()
+            hbuf[a:a + nbytes].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+            views.append(dbuf[a:a + nbytes].view(t.dtype).view(t.shape))
         dX, dq, dsl, dpos, dsid = views
         dout = torch.empty_like(out)
         calls = make_calls(dX, dq, dpos, dsid, dsl, dout)
@@ -444,7 +531,6 @@ def run_ours(args, rank, world, local_rank):
     for i in range(5):
         e2e_step(i)
     barrier()
-    t0 = time.perf_counter()
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
     g0.record(stream)
@@ -460,150 +546,79 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- numbers
     ms_step = total_ms / K
-    tokens = world * Bn * K
-    value = tokens / (total_ms / 1e3)
+    value = world * Bn * K / (total_ms / 1e3)
     seq_total = int(case.seq_lens.astype(np.int64).sum())
     split_bytes = seq_total * (2 * (G * d_h + H * r) * eb + (2 * H if norm else 0))  # cache rows read once
     step_bytes = (split_bytes + 2 * H * d_h * r * 2 + 2 * Bn * H * d_h * 2   # + bases, q, out
                   + (2 * G * d_h + 2 * H * r) * d * 2 + Bn * d * 2)         # + append W, X
     peak, peak_kind = measured_peaks()
-    achieved = split_bytes / (split_ms / 1e3) / 1e9
-    # rotary path: the score kernel's contractions per key and head, the
-    # private query (q D_(i-j)) B_K[h] (d_h r multiply-adds), its dot with
-    # R_K (r) and the rotated shared term (d_h): 2 (d_h r + r + d_h) flops
-    rope_flops = seq_total * H * 2 * (d_h * r + r + d_h)
-    # bytes the score kernel reads (S_K, R_K once) and writes (one fp32 score
-    # per row and head); the given-score split kernel reads S_V, R_V, scores
-    score_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)
-    gsplit_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)
-    bf16_peak, bf16_kind = measured_peaks("bf16_tflops", 1900.0)
+    bf16_peak, bf16_kind = measured_peaks("bf16_tflops", FALLBACK_BF16_TFLOPS)
+    if rope:
+        # the rotary score kernel reads S_K and R_K once and writes one fp32
+        # score per row and head: an HBM-bound pass (about 104 flops per byte,
+        # below the tensor/HBM ridge of ~290); its contractions per key and
+        # head, 2 (d_h r + r + d_h) flops, are reported beside it
+        score_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)
+        gsplit_bytes = seq_total * ((d_h + H * r) * eb + 4 * H)   # S_V, R_V and the scores
+        rope_flops = seq_total * H * 2 * (d_h * r + r + d_h)
+        ach = score_bytes / (scores_ms / 1e3) / 1e9
+        roof = {"kernel": "rotary score kernel (tcgen05: C_j W_h private products and the rotated "
+                          "shared term; S_K and R_K read once, one fp32 score per row and head written)",
+                "bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "frac_of_8TBs": round(ach / NORTH_STAR_HBM_GBS, 4),
+                "algorithmic_bytes_per_launch": score_bytes,
+                "avg_launch_ms": round(scores_ms, 5), "launches_timed": n_scores,
+                "flops_per_launch": rope_flops,
+                "tflops": round(rope_flops / (scores_ms / 1e3) / 1e12, 1),
+                "tensor_frac_of_bf16_peak": round(rope_flops / (scores_ms / 1e3) / 1e12 / bf16_peak, 4),
+                "given_score_split": {"avg_launch_ms": round(split_ms, 5),
+                                      "algorithmic_bytes_per_launch": gsplit_bytes,
+                                      "hbm_gbs": round(gsplit_bytes / (split_ms / 1e3) / 1e9, 1),
+                                      "frac_of_hbm": round(gsplit_bytes / (split_ms / 1e3) / 1e9 / peak, 4)},
+                "traffic": profiled_traffic(f"rope_scores_{name}", "rope_scores_tc_kernel",
+                                            ROPE_SCORE_SOURCES)}
+    else:
+        achieved = split_bytes / (split_ms / 1e3) / 1e9
+        roof = {"kernel": "decode split (factored scores + online softmax + value reductions)",
+                "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "frac_of_8TBs": round(achieved / NORTH_STAR_HBM_GBS, 4),
+                "algorithmic_bytes_per_launch": split_bytes,
+                "avg_launch_ms": round(split_ms, 5), "launches_timed": n_split,
+                "traffic": profiled_traffic(f"decode_split_{name}", "decode_split_fast_kernel",
+                                            DECODE_SPLIT_SOURCES)}
     res = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 cache, f16 mma inputs" if eb == 1 else "bf16", "data": "synthetic",
-        "config": {"workload": f"{name}: {WORKLOADS[name]}", "B": Bn, "d": d, "H": H, "d_h": d_h,
-                   "r": r, "groups": G, "seq_len": max_seq, "cached_rows": seq_total,
-                   "parallelism": f"replicas x{world} (requests are independent)",
-                   "l2": f"inputs larger than L2: the cache is rotated over {n_copies} copies "
-                         f"({n_copies * cache_bytes / 1e6:.0f} MB working set vs 129 MB L2); no flush",
-                   "step": ("lrkv_append (B new rows) + lrkv_decode_rope (B queries)" if rope else
-                            "lrkv_decode_step (append of the B new rows" +
-                            (", their reciprocal key norms" if norm else "") + ", decode of the B queries)")},
-        "roofline": ({"kernel": "rotary score kernel (tcgen05, f16/bf16 in, fp32 in tensor memory; C_j W_h private products, rotated shared term)",
-                      "bound": "tensor", "achieved": round(rope_flops / (scores_ms / 1e3) / 1e12, 2),
-                      "peak": bf16_peak, "unit": "TFLOP/s",
-                      "frac": round(rope_flops / (scores_ms / 1e3) / 1e12 / bf16_peak, 4),
-                      "peak_source": f"{bf16_kind} dense bf16 tensor throughput (f16 runs at the same rate)",
-                      "algorithmic_flops_per_launch": rope_flops,
-                      "algorithmic_bytes_per_launch": score_bytes,
-                      "hbm_gbs": round(score_bytes / (scores_ms / 1e3) / 1e9, 1),
-                      "avg_launch_ms": round(scores_ms, 5), "launches_timed": nl_s.value,
-                      "given_score_split": {"avg_launch_ms": round(split_ms, 5),
-                                            "algorithmic_bytes_per_launch": gsplit_bytes,
-                                            "hbm_gbs": round(gsplit_bytes / (split_ms / 1e3) / 1e9, 1),
-                                            "frac_of_hbm": round(gsplit_bytes / (split_ms / 1e3) / 1e9 / peak, 4)},
-                      "traffic": profiled_traffic(name, "rope_scores", files=ROPE_SCORE_SOURCES)} if rope else
-                     {"kernel": "decode split (factored scores + online softmax + value reductions)",
-                     "bound": "hbm", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "frac_of_8TBs": round(achieved / NORTH_STAR_HBM_GBS, 4),
-                     "algorithmic_bytes_per_launch": split_bytes,
-                     "avg_launch_ms": round(split_ms, 5), "launches_timed": nl.value,
-                     "traffic": profiled_traffic(name)}),
+        "value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(ms_step, 5),
+        "dtype": "e4m3 cache, f16 mma inputs" if eb == 1 else "bf16",
+        "config": describe(name, world),
+        "roofline": roof,
         "step_effective_gbs": round(step_bytes / (ms_step / 1e3) / 1e9, 1),
+        "step_frac_of_hbm": round(step_bytes / (ms_step / 1e3) / 1e9 / peak, 4),
         "breakdown_ms": {"split_kernel": round(split_ms, 5),
                          "rotary_score_kernel": None if scores_ms is None else round(scores_ms, 5),
                          "lrkv_append_alone": round(append_ms, 5),
                          "lrkv_decode_alone": round(decode_ms, 5),
                          "lrkv_append_then_lrkv_decode": None if separate_ms is None else round(separate_ms, 5)},
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "note": e2e_note},
         # per step: append, [key norms,] prologue, [rotary scores,] split, combine
         "gpu_launches": (4 + int(norm) + int(rope)) * K,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(name, args.cpu_pairs, args.cpu_workers)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    del caches, base
     return res
 
 
-def cpu_baseline(name, n_pairs, workers=0):
-    """The oracle on all host cores (the reported value), and once more on one
-    core over a proportionally smaller sample."""
-    from oracle.cpu_timing import time_oracle_decode
-    t = time_oracle_decode(name, n_pairs, workers=workers or None)
-    n1 = max(4, n_pairs // max(1, t["cores"]))
-    t1 = time_oracle_decode(name, n1, workers=1, seed=1)
-    return {"value": round(t["pairs"] / t["heads"] / t["wall_s"], 3), "unit": "tokens/s",
-            "cores": t["cores"], "nproc": os.cpu_count(), "kind": "oracle",
-            "sample": f"{t['pairs']} random (request, head) pairs of the {name} workload "
-                      f"({t['pairs'] / t['heads']:.0f} request-steps), float64 oracle "
-                      f"(gather, materialise K_h/V_h, textbook softmax), {t['cores']} single-"
-                      f"threaded processes, {t['cpu_s']:.1f} s CPU",
-            "single_core": {"value": round(t1["pairs"] / t1["heads"] / t1["wall_s"], 3),
-                            "unit": "tokens/s", "cores": 1,
-                            "sample": f"{t1['pairs']} random (request, head) pairs, one process"}}
-
-
-def cpu_baseline_prefill(name, workers=0, k_rows=8):
-    from oracle.cpu_timing import time_oracle_prefill
-    t = time_oracle_prefill(name, k_rows, workers=workers or None)
-    return {"value": round(t["tokens_per_s"], 3), "unit": "tokens/s", "cores": t["cores"],
-            "nproc": os.cpu_count(), "kind": "oracle",
-            "sample": f"{t['cores']} requests of the {name} workload, one per single-threaded "
-                      f"process: the float64 projection of the request's rows, then causal "
-                      f"attention of {k_rows} sampled rows (all heads), scaled to the full "
-                      f"request; {t['wall_s']:.1f} s wall"}
-
-
-def run_reference(args, rank, world):
-    """The float64 oracle timed on host cores: each step is one (request, head)
-    pair of the workload; tokens/s counts H pairs as one request-step."""
-    if rank != 0:
-        return None
-    from oracle.cpu_timing import time_oracle_decode
-    import lrkv_inputs as I
-    c = workload_shape(args.config)
-    if args.config == "prefill_2048":   # the prefill line's metric, on host cores
-        cb = cpu_baseline_prefill(args.config, args.cpu_workers)
-        v = cb["value"]
-        return {
-            "impl": "reference", "metric": "LRKV prefill tokens/s", "value": v, "unit": "tokens/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(c["B"] * c["T"] / v * 1e3, 1), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": c["B"],
-                       "d": c["d"], "H": c["H"], "d_h": c["d_h"], "r": c["r"], "seq_len": c["T"]},
-            "cpu_baseline": cb,
-            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        }
-    n = max(16, min(args.steps, 4096))   # bounded so the run ends within minutes
-    t = time_oracle_decode(args.config, n, workers=args.cpu_workers or None)
-    value = t["pairs"] / t["heads"] / t["wall_s"]
-    return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(t["wall_s"] / t["pairs"] * 1e3 * t["heads"], 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": c["B"],
-                   "H": c["H"], "d_h": c["d_h"], "r": c["r"]},
-        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": t["cores"],
-                         "kind": "oracle",
-                         "sample": f"{t['pairs']} (request, head) pairs (steps capped at 4096)"},
-        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
-
-
-def run_prefill(args, rank, world, local_rank):
-    """Prefill of fresh prompts: one step = lrkv_prefill over the whole batch."""
+# ----------------------------------------------------------------------------
+# our arm: prefill
+# ----------------------------------------------------------------------------
+def prefill_leg(lib, name, dev, world, local_rank, K, W, R, Ke):
+    """Step timing (one lrkv_prefill over the batch), the attention and
+    projection kernels' rooflines and the end-to-end rate of the prefill
+    workload."""
     import ctypes
     import numpy as np
     import torch
@@ -612,13 +627,7 @@ def run_prefill(args, rank, world, local_rank):
     from rank_kv_attention_gb300 import _abi
     from rank_kv_attention_gb300.api import PagedCache
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    lib = L.lib()
-    c = I.CONFIGS[args.config]
+    c = I.CONFIGS[name]
     Bq, d, H, d_h, r, T = c["B"], c["d"], c["H"], c["d_h"], c["r"], c["T"]
     n = Bq * T
     ac = I.make_append_case([T] * Bq, [0] * Bq, d, dtype="bf16", seed=c["seed"], shuffle=True)
@@ -641,10 +650,9 @@ def run_prefill(args, rank, world, local_rank):
     ws = L.workspace(L.prefill_workspace_bytes(Bq, n, H, d_h, r, T), dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(i=0):
         L.prefill(X, Qd, cu, sp, T, *Wt, cache, pt, out=out, ws=ws, stream=stream)
 
-    K, W = args.steps, args.warmup
     for _ in range(max(W, 3)):
         step()
     torch.cuda.synchronize()
@@ -663,16 +671,9 @@ def run_prefill(args, rank, world, local_rank):
     rank_barrier(world)
     clk = clocks.stop()
     total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    assert lib.lrkv_profile_enable(1) == 0
-    for _ in range(K):
-        step()
-    torch.cuda.synchronize()
-    res_k = {}
-    for which, name in ((0, "attention"), (1, "projection")):
-        tot, nl = ctypes.c_double(), ctypes.c_int32()
-        assert lib.lrkv_profile_read(which, ctypes.byref(tot), ctypes.byref(nl)) == 0
-        res_k[name] = tot.value / max(1, nl.value)
-    lib.lrkv_profile_enable(0)
+    prof = profile_pass(lib, step, R)
+    attn_ms, n_attn = prof[0]
+    proj_ms, n_proj = prof[1]
 
     # ---- end to end with host buffers: the step's rows X and queries Q from
     # pinned host memory, the output back to pinned host memory, the host
@@ -687,7 +688,6 @@ def run_prefill(args, rank, world, local_rank):
         hout.copy_(out, non_blocking=True)
         stream.synchronize()
 
-    Ke = max(3, min(K, 50))
     for _ in range(3):
         e2e_step()
     rank_barrier(world)
@@ -706,42 +706,152 @@ def run_prefill(args, rank, world, local_rank):
     ms = total_ms / K
     Ntot = 2 * d_h + 2 * H * r
     proj_flops = 2 * n * d * Ntot
-    peak, kind = measured_peaks("bf16_tflops", 1900.0)
+    peak, kind = measured_peaks("bf16_tflops", FALLBACK_BF16_TFLOPS)
     # attention: per (row, head) with v visible keys, scores and values cost
     # 2 v (d_h + r) each; p = q B_K[h] and the B_V[h] expansion 2 d_h r each
     visible = Bq * T * (T + 1) // 2
     attn_flops = H * (4 * visible * (d_h + r) + 4 * n * d_h * r)
-    attn_tf = attn_flops / (res_k["attention"] / 1e3) / 1e12
-    proj_tf = proj_flops / (res_k["projection"] / 1e3) / 1e12
+    attn_tf = attn_flops / (attn_ms / 1e3) / 1e12
+    proj_tf = proj_flops / (proj_ms / 1e3) / 1e12
     res = {
-        "metric": "LRKV prefill tokens/s", "value": round(world * n / (ms / 1e3), 1), "unit": "tokens/s",
-        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": Bq, "d": d, "H": H,
-                   "d_h": d_h, "r": r, "seq_len": T, "rows": n,
-                   "l2": "no flush: one step's working set (~0.3 GB) exceeds L2"},
+        "value": round(world * n / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "dtype": "bf16", "config": describe(name, world),
         "roofline": {"kernel": "prefill_tc_kernel (causal attention, tcgen05)", "bound": "tensor",
                      "achieved": round(attn_tf, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(attn_tf / peak, 4), "peak_source": f"{kind} bf16 GEMM (burst)",
-                     "flops_per_launch": attn_flops, "avg_launch_ms": round(res_k["attention"], 4),
-                     "traffic": profiled_traffic(args.config, "prefill_attention", PREFILL_SOURCES)},
+                     "flops_per_launch": attn_flops, "avg_launch_ms": round(attn_ms, 5),
+                     "launches_timed": n_attn,
+                     "traffic": profiled_traffic(f"prefill_attention_{name}", "prefill_tc_kernel",
+                                                 PREFILL_SOURCES)},
         "projection": {"kernel": "append_tc_kernel (X.[W_S_K|W_S_V|U_K|U_V], tcgen05)",
-                       "achieved": round(proj_tf, 1), "unit": "TFLOP/s", "frac": round(proj_tf / peak, 4),
-                       "flops_per_launch": proj_flops, "avg_launch_ms": round(res_k["projection"], 4)},
-        "breakdown_ms": {"projection": round(res_k["projection"], 4),
-                         "attention": round(res_k["attention"], 4)},
+                       "bound": "tensor", "achieved": round(proj_tf, 1), "peak": peak,
+                       "unit": "TFLOP/s", "frac": round(proj_tf / peak, 4),
+                       "flops_per_launch": proj_flops, "avg_launch_ms": round(proj_ms, 5),
+                       "launches_timed": n_proj,
+                       "traffic": profiled_traffic(f"prefill_attention_{name}", "append_tc_kernel",
+                                                   PREFILL_SOURCES)},
+        "breakdown_ms": {"projection": round(proj_ms, 5), "attention": round(attn_ms, 5)},
         "e2e": {"value": round(world * n / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "note": "pinned host X and Q copied in, lrkv_prefill, out copied back and "
                         "synchronised every step"},
         # per step: row metadata, the projection, the attention (tiled path)
         "gpu_launches": 3 * K if tiled else None,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline_prefill(args.config, args.cpu_workers)
     return res
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import rank_kv_attention_gb300 as L
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    lib = L.lib()
+    K, W, R = args.steps, args.warmup, max(1, args.roofline_launches)
+    Ke = args.e2e_steps or max(50, min(K, 2000))
+    name = args.config
+    if name == "prefill_2048":
+        head = prefill_leg(lib, name, dev, world, local_rank, K, W, R, args.e2e_steps or max(3, min(K, 50)))
+    else:
+        head = decode_leg(lib, name, dev, world, local_rank, K, W, R, Ke, True)
+    res = {"metric": PREFILL_METRIC if name == "prefill_2048" else METRIC, "value": head["value"],
+           "unit": head["unit"], "n_gpus": world, "steps": K, "warmup": W,
+           "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic"}
+    res.update({k: v for k, v in head.items() if k not in res})
+    extras = [x for x in (args.extra_configs or "").split(",") if x and x != name]
+    if extras:
+        res["configs"] = {}
+        for x in extras:
+            torch.cuda.empty_cache()
+            if x == "prefill_2048":
+                leg = prefill_leg(lib, x, dev, world, local_rank, max(3, args.extra_steps // 6), 5,
+                                  R, 20)
+            else:
+                leg = decode_leg(lib, x, dev, world, local_rank, args.extra_steps, 10, R, 200, False)
+            res["configs"][x] = {"metric": PREFILL_METRIC if x == "prefill_2048" else METRIC, **leg}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = (cpu_baseline_prefill(name, args.cpu_workers) if name == "prefill_2048"
+                               else cpu_baseline(name, args.cpu_pairs, args.cpu_workers))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return res
+
+
+# ----------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def oracle_decode_sample(name, n_pairs, workers=0):
+    """The float64 oracle on ``n_pairs`` seeded (request, head) pairs of a
+    decode workload, on all host cores: the one sample both the line's
+    cpu_baseline and the reference arm report."""
+    from oracle.cpu_timing import time_oracle_decode
+    t = time_oracle_decode(name, n_pairs, workers=workers or None)
+    return {"value": round(t["pairs"] / t["heads"] / t["wall_s"], 3), "unit": "tokens/s",
+            "cores": t["cores"], "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"{t['pairs']} seeded random (request, head) pairs of the {name} workload "
+                      f"({t['pairs'] / t['heads']:.0f} request-steps), float64 oracle "
+                      f"(gather, materialise K_h/V_h, textbook softmax), {t['cores']} single-"
+                      f"threaded processes (spawned and warmed before timing), "
+                      f"{t['cpu_s']:.1f} s CPU, {t['wall_s']:.2f} s wall",
+            "wall_s": t["wall_s"]}
+
+
+def cpu_baseline(name, n_pairs, workers=0):
+    """The oracle on all host cores (the reported value), and once more on one
+    core over a proportionally smaller sample."""
+    from oracle.cpu_timing import time_oracle_decode
+    out = oracle_decode_sample(name, n_pairs, workers)
+    n1 = max(4, n_pairs // max(1, out["cores"]))
+    t1 = time_oracle_decode(name, n1, workers=1, seed=1)
+    out.pop("wall_s")
+    out["single_core"] = {"value": round(t1["pairs"] / t1["heads"] / t1["wall_s"], 3),
+                          "unit": "tokens/s", "cores": 1,
+                          "sample": f"{t1['pairs']} random (request, head) pairs, one process"}
+    return out
+
+
+def cpu_baseline_prefill(name, workers=0, k_rows=8):
+    from oracle.cpu_timing import time_oracle_prefill
+    t = time_oracle_prefill(name, k_rows, workers=workers or None)
+    return {"value": round(t["tokens_per_s"], 3), "unit": "tokens/s", "cores": t["cores"],
+            "nproc": os.cpu_count(), "kind": "oracle",
+            "sample": f"{t['cores']} requests of the {name} workload, one per single-threaded "
+                      f"process: the float64 projection of the request's rows, then causal "
+                      f"attention of {k_rows} sampled rows (all heads), scaled to the full "
+                      f"request; {t['wall_s']:.1f} s wall"}
+
+
+def run_reference(args, rank, world):
+    """The float64 oracle timed on host cores, on the same workload, config
+    and sample as our line's cpu_baseline (rank 0 alone; other ranks exit)."""
+    if rank != 0:
+        return None
+    c = workload_shape(args.config)
+    if args.config == "prefill_2048":   # the prefill line's metric, on host cores
+        cb = cpu_baseline_prefill(args.config, args.cpu_workers)
+        v = cb["value"]
+        metric, ms = PREFILL_METRIC, c["B"] * c["T"] / v * 1e3
+    else:
+        cb = oracle_decode_sample(args.config, args.cpu_pairs, args.cpu_workers)
+        v = cb["value"]
+        metric, ms = METRIC, c["B"] / v * 1e3
+        cb.pop("wall_s")
+    return {
+        "impl": "reference", "metric": metric, "value": v, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": describe(args.config, world),
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
 
 
 def main():
@@ -749,8 +859,6 @@ def main():
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world)
-    elif args.config == "prefill_2048":
-        res = run_prefill(args, rank, world, local_rank)
     else:
         res = run_ours(args, rank, world, local_rank)
     if rank == 0 and res is not None:

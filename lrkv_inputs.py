@@ -196,13 +196,19 @@ class DecodeCase:
 def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
                      shuffle=False, spare_pages=0, page_size=PAGE_SIZE,
                      q_std=1.0, cache_std=1.0, base_std=None,
-                     max_pages=None, fp8_scale=None, groups=1) -> DecodeCase:
+                     max_pages=None, fp8_scale=None, groups=1, device=None) -> DecodeCase:
     """Decode inputs: a filled paged cache plus one query row per request.
 
     Queries and cache rows ~ N(0, q_std^2 / cache_std^2); bases ~ N(0, 1/r)
     unless ``base_std`` is given.  With dtype "fp8" the pools hold 8-bit codes
     of value / scale (``fp8_scale``: one scale, or one per pool S_K, S_V, R_K,
     R_V; default FP8_SCALE) and the queries and bases are bf16.
+
+    ``device`` (bf16 only; for timing runs on large workloads): the four pools
+    are drawn on that torch device instead, from torch's generator seeded with
+    ``seed`` (same distribution, other values, slots past a request's length
+    left as drawn), and returned as bf16 torch tensors; lengths, page table,
+    queries and bases are the host case's own.
     """
     rng = np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32).reshape(B)
@@ -221,6 +227,13 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
     B_V = _draw(rng, (H, d_h, r), base_std, adt)
     # groups > 1: one shared row per group of heads, [pages, page_size, G, d_h]
     s_shape = (num_pages, page_size, d_h) if groups == 1 else (num_pages, page_size, groups, d_h)
+    if device is not None:
+        if dtype != "bf16":
+            raise ValueError("device-drawn pools are bf16")
+        pools = _device_pools(device, seed, [s_shape, s_shape, (num_pages, page_size, H, r),
+                                             (num_pages, page_size, H, r)], cache_std)
+        return DecodeCase(B, H, d_h, r, dtype, page_size, seq_lens, pt, num_pages,
+                          q, *pools, B_K, B_V, sc)
     S_K = _draw_chunked(rng, s_shape, cache_std, dtype, scale=sc[0])
     S_V = _draw_chunked(rng, s_shape, cache_std, dtype, scale=sc[1])
     R_K = _draw_chunked(rng, (num_pages, page_size, H, r), cache_std, dtype, scale=sc[2])
@@ -229,6 +242,27 @@ def make_decode_case(B, H, d_h, r, seq_lens, dtype="bf16", seed=0,
         poison_tail_slots(pool, pt, seq_lens, page_size, dtype)
     return DecodeCase(B, H, d_h, r, dtype, page_size, seq_lens, pt, num_pages,
                       q, S_K, S_V, R_K, R_V, B_K, B_V, sc)
+
+
+def _device_pools(device, seed, shapes, std):
+    """bf16 pools ~ N(0, std^2) drawn on a torch device (seeded generator, in
+    chunks that bound the float32 temporary)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) + 15485863)
+    out = []
+    for shape in shapes:
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = t.view(-1)
+        step = 1 << 26
+        for a in range(0, flat.numel(), step):
+            n = min(step, flat.numel() - a)
+            x = torch.randn(n, generator=g, device=device, dtype=torch.float32)
+            if std != 1.0:
+                x.mul_(std)
+            flat[a:a + n].copy_(x)
+        out.append(t)
+    return out
 
 
 def ragged_lengths(B, lo, hi, seed):
@@ -353,9 +387,10 @@ CONFIGS = {
 }
 
 
-def config_decode_case(name, seed=None, scale_T=None) -> DecodeCase:
+def config_decode_case(name, seed=None, scale_T=None, device=None) -> DecodeCase:
     """Decode inputs of one of the named decode workloads (optionally with a
-    shorter history ``scale_T`` for quick parity runs)."""
+    shorter history ``scale_T`` for quick parity runs; ``device``: pools drawn
+    on that torch device, see make_decode_case)."""
     c = CONFIGS[name]
     s = c["seed"] if seed is None else seed
     if name == "ragged_paged":
@@ -363,7 +398,8 @@ def config_decode_case(name, seed=None, scale_T=None) -> DecodeCase:
         if scale_T is not None:
             lens = np.maximum(1, (lens.astype(np.int64) * scale_T) // c["hi"]).astype(np.int32)
         return make_decode_case(c["B"], c["H"], c["d_h"], c["r"], lens, c["dtype"],
-                                s, shuffle=True, spare_pages=3)
+                                s, shuffle=True, spare_pages=3, device=device)
     T = c["T"] if scale_T is None else scale_T
     return make_decode_case(c["B"], c["H"], c["d_h"], c["r"], [T] * c["B"],
-                            c["dtype"], s, shuffle=False, groups=c.get("groups", 1))
+                            c["dtype"], s, shuffle=False, groups=c.get("groups", 1),
+                            device=device)

@@ -59,7 +59,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
            "--impl", "reference", "--gpus", "2", "--steps", "16", "--warmup", "3",
-           "--cpu-workers", "1"]
+           "--cpu-workers", "1", "--cpu-pairs", "48"]
     p = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert p.returncode == 0, p.stderr[-2000:]
     lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
@@ -67,3 +67,24 @@ def test_reference_arm_under_torchrun_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["cores"] == 1 and d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same config object our arm prints, and the same sample as its cpu_baseline
+    sys.path.insert(0, ROOT)
+    import bench
+    assert d["config"] == bench.describe("decode_T4096", 2)
+    assert d["cpu_baseline"]["sample"].startswith("48 seeded random (request, head) pairs")
+
+
+def test_profile_summary_sections(tmp_path):
+    """Each kernel's figures are read from its own section of an ncu summary:
+    a later kernel's DRAM bytes never stand in for an earlier one's."""
+    sys.path.insert(0, ROOT)
+    import bench
+    p = tmp_path / "s.md"
+    p.write_text("# title\n\n- kernel_source_sha256_16: `abc`\n\n## first\n\n"
+                 "- kernel: `prefill_tc_kernel`\n- dram_bytes_per_full_launch: 201862400\n\n"
+                 "## second\n\n- kernel: `append_tc_kernel`\n"
+                 "- dram_bytes_per_full_launch: 92373504  (the projection)\n")
+    head, sec = bench.summary_sections(str(p))
+    assert head == {"kernel_source_sha256_16": "abc"}
+    assert sec["prefill_tc_kernel"]["dram_bytes_per_full_launch"] == "201862400"
+    assert sec["append_tc_kernel"]["dram_bytes_per_full_launch"] == "92373504"

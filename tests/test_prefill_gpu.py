@@ -215,9 +215,12 @@ def test_prefill_2048_pools_full():
     (16384 rows, d = 2048, 128 x 7 output tiles of the persistent projection)
     against the float64 projection placed by the oracle: every written slot
     within the bf16 tolerance and, tighter, equal to the oracle's value
-    rounded to bf16 except for rare rounding-boundary cases one bf16 unit
-    apart (fp32 accumulation can land on the other side of a tie); spare
-    pages keep their NaN canary."""
+    rounded to bf16 except for rare cases where fp32 accumulation lands on
+    the other side of a rounding boundary: those are within one bf16 unit
+    of |ref| (2^-7 relative) plus 1e-6 absolute (projections are ~0.02 in
+    magnitude; the floor covers values that cancel to near zero, where
+    fp32 and float64 may even round to opposite signs); spare pages keep
+    their NaN canary."""
     c = I.CONFIGS["prefill_2048"]
     Bq, d, H, d_h, r, T = c["B"], c["d"], c["H"], c["d_h"], c["r"], c["T"]
     ac = I.make_append_case([T] * Bq, [0] * Bq, d, dtype="bf16", seed=c["seed"], shuffle=True,
@@ -239,8 +242,9 @@ def test_prefill_2048_pools_full():
         got_bits = host_bits(t)
         got = I.bf16_bits_to_f64(got_bits)
         assert_close(got[touched], want[k][touched], "bf16", f"pool {k}")
-        want_bits = I.f32_to_bf16_bits(want[k][touched].astype(np.float32)).astype(np.int32)
-        diff = np.abs(got_bits[touched].astype(np.int32) - want_bits)
-        assert diff.max() <= 1, f"pool {k}: a value more than one bf16 unit from the oracle"
-        assert np.count_nonzero(diff) <= 1e-4 * diff.size, f"pool {k}: {np.count_nonzero(diff)} off"
+        ref = want[k][touched]
+        off = got_bits[touched] != I.f32_to_bf16_bits(ref.astype(np.float32))
+        assert np.count_nonzero(off) <= 1e-4 * off.size, f"pool {k}: {np.count_nonzero(off)} off"
+        e = np.abs(got[touched][off] - ref[off])
+        assert np.all(e <= 2.0 ** -7 * np.abs(ref[off]) + 1e-6), f"pool {k}: worst {e.max():.3e}"
         assert np.all(got_bits[~touched] == I.BF16_NAN_BITS), f"pool {k} canary"
