@@ -580,7 +580,8 @@ def decode_leg(lib, name, dev, world, local_rank, K, W, R, Ke, headline):
                                             ROPE_SCORE_SOURCES)}
     else:
         achieved = split_bytes / (split_ms / 1e3) / 1e9
-        roof = {"kernel": "decode split (factored scores + online softmax + value reductions)",
+        roof = {"kernel": "decode split (factored scores, online softmax, value reductions; its "
+                          "last phase merges each request's segments and expands by B_V)",
                 "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": f"{peak_kind} HBM copy bandwidth",
@@ -604,8 +605,9 @@ def decode_leg(lib, name, dev, world, local_rank, K, W, R, Ke, headline):
         "e2e": {"value": round(world * Bn * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "note": e2e_note},
-        # per step: append, [key norms,] prologue, [rotary scores,] split, combine
-        "gpu_launches": (4 + int(norm) + int(rope)) * K,
+        # per step: append, [key norms,] prologue, [rotary scores,] split (the
+        # split kernel's last phase merges the segments; no combine launch)
+        "gpu_launches": (3 + int(norm) + int(rope)) * K,
         "clocks": clk,
     }
     del caches, base

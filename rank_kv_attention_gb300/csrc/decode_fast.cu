@@ -83,6 +83,10 @@ struct FastCfg {
     static constexpr int OFF_PLAN = OFF_CUR + 64;    // local plan: scan scratch + request offsets
     static constexpr int OFF_PEND = OFF_PLAN + 512;  // given scores: rows of the first copies
     static constexpr int SMEM = OFF_PEND + 64 + 1024;  // + alignment slack
+    // registers per thread: at most 224 leaves room for a 128-thread prologue
+    // block of up to 48 registers on the same SM, so the split CTAs do not
+    // wait for the prologue to leave; the widest private rows need more
+    static constexpr int MAXREG = H * R >= 1024 ? 255 : 224;
 
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
@@ -113,6 +117,10 @@ struct FastParams {
     const uint16_t *qb;
     const float *wsc;
     float *sc_out;
+    // the merge phase: expansion bases and the output
+    const __nv_bfloat16 *B_K;
+    const __nv_bfloat16 *B_V;
+    __nv_bfloat16 *out;
 };
 
 struct FastMaps {
@@ -278,7 +286,7 @@ template <class C>
 __device__ __forceinline__ void q8_segment_setup(const FastParams &P, int b, int warp, int gq,
                                                  int tq, uint32_t (&qb)[8][2],
                                                  uint32_t (&pb)[C::KSP][2], float (&fS)[2],
-                                                 float (&fR)[2]) {
+                                                 float (&fR)[2], const float *pw) {
     // column n = gq of the B fragments is head warp*HPW + n (n < HPW), else 0;
     // contraction index k of k-step ks in slot order is 16 ks + 4 tq + e
     const bool own = gq < C::HPW;
@@ -296,8 +304,7 @@ __device__ __forceinline__ void q8_segment_setup(const FastParams &P, int b, int
         for (int e = 0; e < 4; ++e) mq = fmaxf(mq, fabsf(qv[ks][e]));
     }
     // blockdiag(p)^T: entry (k, n) is p[head n][k - n R] when k lies in head
-    // n's columns of the warp, else 0
-    const float *pw = P.ws.p + ((size_t)b * C::H + warp * C::HPW) * C::R;
+    // n's columns of the warp, else 0 (pw: the warp's heads' p, R apart)
 #pragma unroll
     for (int ks = 0; ks < C::KSP; ++ks)
 #pragma unroll
@@ -475,6 +482,7 @@ struct CtaRange {
     int32_t start, end;
     const int32_t *off;  // off[b] for the CTA's requests
     bool local;
+    int32_t chunk;       // rows per CTA: CTA g covers [g chunk, (g + 1) chunk)
 };
 
 
@@ -511,12 +519,30 @@ __device__ __forceinline__ CtaRange cta_range(const FastParams &P, int g, int G,
     chunk = max(chunk, kPlanTileAlign);
     chunk = (chunk + kPlanTileAlign - 1) / kPlanTileAlign * kPlanTileAlign;
     CtaRange rg;
+    rg.chunk = chunk;
     rg.start = g * chunk;
     rg.end = min(total, rg.start + chunk);
     rg.b0 = 0;
     rg.off = nullptr;
     rg.local = true;
-    if (rg.start >= rg.end) return rg;
+    // a batch of at most kLocalReq requests: every CTA (with rows or not)
+    // keeps the whole offset table, off[b] at pl[16 + b]
+    const bool all_local = Bn <= kLocalReq;
+    if (all_local) {
+        int32_t o = base_t;
+        for (int bb = lo; bb < hi; ++bb) {
+            pl[16 + bb] = o;
+            o += len_at(bb);
+        }
+        if (hi == Bn) pl[16 + Bn] = o;  // off[B] = total
+    }
+    if (rg.start >= rg.end) {  // the whole CTA takes this path
+        if (all_local) {
+            __syncthreads();
+            rg.off = pl + 16;
+        }
+        return rg;
+    }
     {
         int32_t o = base_t;
         for (int bb = lo; bb < hi; ++bb) {
@@ -535,6 +561,10 @@ __device__ __forceinline__ CtaRange cta_range(const FastParams &P, int g, int G,
     }
     __syncthreads();
     rg.b0 = pl[0];
+    if (all_local) {
+        rg.off = pl + 16;
+        return rg;
+    }
     rg.local = pl[1] + 1 - rg.b0 <= kLocalReq;
     if (rg.local) {
         int32_t o = base_t;
@@ -550,8 +580,41 @@ __device__ __forceinline__ CtaRange cta_range(const FastParams &P, int g, int G,
     return rg;
 }
 
+__device__ __forceinline__ uint32_t u4w(const uint4 &v, int w) {
+    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Bounded wait until the workspace counter reaches the grid size (every CTA
+// has written its partial states).  After ~2 s it flags LRKV_STATUS_TIMEOUT
+// and returns false; the caller goes on without the data it waited for
+// (wrong values, flagged, but nothing out of bounds).
+__device__ __forceinline__ bool wait_grid_count(const FastParams &P) {
+    const int32_t *c = P.ws.cnt;
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+        if (v >= (int32_t)gridDim.x) return true;
+        if (it == 0) t0 = globaltimer_ns();
+        else if ((it & 63u) == 63u && globaltimer_ns() - t0 > 2000000000ull) {
+            status_or(P.status, LRKV_STATUS_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+}
+
 template <class C>
-__global__ void __launch_bounds__(C::NT, 1)
+__device__ __forceinline__ void stream_range(const FastMaps &M, const FastParams &P, const CtaRange &rg,
+                                             uint8_t *smem);
+template <class C>
+__device__ void merge_phase(const FastParams &P, const CtaRange &rg, const int32_t *off, int warp,
+                            int lane, float *scratch);
+
+template <class C>
+__global__ void __maxnreg__(C::MAXREG)
     decode_split_fast_kernel(const __grid_constant__ FastMaps M, const FastParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -586,15 +649,12 @@ __global__ void __launch_bounds__(C::NT, 1)
     int32_t *pl = reinterpret_cast<int32_t *>(smem + C::OFF_PLAN);
     const CtaRange rg = cta_range<C::NT>(P, g, (int)gridDim.x, pl);
     const int32_t start0 = rg.start, end = rg.end;
-    if (start0 >= end) {
-        pdl_wait();
-        return;
-    }
+    const bool has_rows = start0 < end;
     const int b0 = rg.b0;
     const bool local = rg.local;
     const int32_t *off = rg.off;  // off[b] for this CTA's requests
 
-    if (tid == 0) {
+    if (has_rows && tid == 0) {
         // given scores: two arrivals per phase, the cache rows' and the scores'
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], C::GS ? 2 : 1);
@@ -614,12 +674,35 @@ __global__ void __launch_bounds__(C::NT, 1)
     }
     __syncthreads();
     if (local) pdl_wait();  // the private queries (or the scores) come from the previous kernel
-    if (C::GS && tid == 0)  // the first tiles' score copies
+    if (has_rows && C::GS && tid == 0)  // the first tiles' score copies
         for (int k = 0; k < cur->issued; ++k)
             issue_scores<C>(smem + (k % C::STAGES) * C::STAGE, M, pend[k % C::STAGES],
                             &full[k % C::STAGES]);
     pdl_launch_dependents();
+    if (has_rows) stream_range<C>(M, P, rg, smem);
+    // every partial state of this CTA is written: count the CTA, then merge
+    // the (request, head) pairs that fall to it once every CTA is counted
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) atomicAdd(ws.cnt, 1);
+    merge_phase<C>(P, rg, off, warp, lane, reinterpret_cast<float *>(smem));
+}
 
+// The tiles of a CTA's range: scores, online softmax, value reductions; one
+// partial state per (request, CTA) segment.
+template <class C>
+__device__ __forceinline__ void stream_range(const FastMaps &M, const FastParams &P, const CtaRange &rg,
+                                             uint8_t *smem) {
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    int *cnt = reinterpret_cast<int *>(smem + C::OFF_CNT);
+    int *okf = reinterpret_cast<int *>(smem + C::OFF_OK);
+    IssueCursor *cur = reinterpret_cast<IssueCursor *>(smem + C::OFF_CUR);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.x;
+    const DecodeWs &ws = P.ws;
+    const int32_t start0 = rg.start, end = rg.end;
+    const int b0 = rg.b0;
+    const int32_t *off = rg.off;
     const int gq = lane >> 2, tq = lane & 3;  // mma fragment coordinates
     const int hl = lane >> 4, j = lane & 15;  // this lane's (head slot, tile row)
     // first 16-byte chunk of the shared group of this warp's heads
@@ -662,7 +745,8 @@ __global__ void __launch_bounds__(C::NT, 1)
         if constexpr (C::GS) {
             // the scores arrive with the tiles
         } else if constexpr (C::Q8) {
-            q8_segment_setup<C>(P, b, warp, gq, tq, qb, pbh, fS, fR);
+            q8_segment_setup<C>(P, b, warp, gq, tq, qb, pbh, fS, fR,
+                                ws.p + ((size_t)b * C::H + warp * C::HPW) * C::R);
         } else {
             // B fragments of Q^T: column n = head warp*HPW + n (n < HPW), else 0
             const bool own = gq < C::HPW;
@@ -880,11 +964,10 @@ __global__ void __launch_bounds__(C::NT, 1)
             }
             __syncwarp();
         }
-        if (timed_out) break;
-
         // -------- segment end: this warp's heads of partial slot b + g
         const size_t slot = (size_t)b + g;
         const size_t W = C::DH + C::R;
+        if (!timed_out) {  // (a timed-out warp leaves its partial unwritten)
 #pragma unroll
         for (int i = 0; i < C::NH; ++i) {
             if (j == 0) {
@@ -918,6 +1001,8 @@ __global__ void __launch_bounds__(C::NT, 1)
                     ws.acc[(slot * C::H + warp * C::HPW + n) * W + C::DH + (mm - n * C::R)] = accR[mt][e];
             }
         }
+        }  // !timed_out
+        if (timed_out) break;
         start = seg_end;
     }
 
@@ -927,6 +1012,169 @@ __global__ void __launch_bounds__(C::NT, 1)
     if (tid == 0) {
         const int issued = cur->issued;
         for (int k = (int)it; k < issued; ++k) mbar_wait(&full[k % C::STAGES], (k / C::STAGES) & 1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of a request's segment states into its output (section 3 after
+// Algorithm 2: one softmax over the whole sequence -- the segments' (m, l,
+// accS, accR) combine by the log-sum-exp rule -- and equation 7's expansion
+// by B_V[h], once, on the merged private accumulator):
+//     out[b, h] = accS / L + (accR / L) B_V[h]^T.
+// A (request, head) pair is merged by WP warps of one CTA: warp k of the
+// group takes segments k, k + WP, ... and keeps a running (M, L, acc) over
+// batches of eight segments whose loads are all in flight; lane i holds value
+// columns 2i, 2i + 1 and 64 + 2i, 65 + 2i of accS and, for 2i < r, columns
+// 2i, 2i + 1 of accR.  The group's first warp then combines the WP states in
+// warp order through shared memory and expands.  Partial states come from L2
+// (other CTAs wrote them).
+// ---------------------------------------------------------------------------
+struct MergeState {
+    float M, L;
+    float2 a0, a1, ar;
+};
+
+template <class C>
+__device__ __forceinline__ MergeState merge_segments(const FastParams &P, size_t s0, int first,
+                                                     int step, int nseg, int lane) {
+    constexpr int W = C::DH + C::R, U = 8;
+    const bool has_r = 2 * lane < C::R;
+    MergeState st{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    for (int s = first; s < nseg; s += U * step) {
+        float2 ml[U], v0[U], v1[U], vr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            ml[u] = make_float2(-INFINITY, 0.f);
+            v0[u] = v1[u] = vr[u] = make_float2(0.f, 0.f);
+            if (s + u * step < nseg) {
+                const size_t slot = s0 + (size_t)(s + u * step) * C::H;
+                const float *acc = P.ws.acc + slot * W;
+                ml[u] = __ldcg(reinterpret_cast<const float2 *>(P.ws.ml + slot * 2));
+                v0[u] = __ldcg(reinterpret_cast<const float2 *>(acc + 2 * lane));
+                v1[u] = __ldcg(reinterpret_cast<const float2 *>(acc + 64 + 2 * lane));
+                if (has_r) vr[u] = __ldcg(reinterpret_cast<const float2 *>(acc + C::DH + 2 * lane));
+            }
+        }
+        float Mb = st.M;
+#pragma unroll
+        for (int u = 0; u < U; ++u) Mb = fmaxf(Mb, ml[u].x);
+        if (Mb == -INFINITY) continue;  // nothing visible so far
+        const float sc = st.M == -INFINITY ? 0.f : exp2f(st.M - Mb);
+        st.L *= sc;
+        st.a0.x *= sc; st.a0.y *= sc; st.a1.x *= sc; st.a1.y *= sc; st.ar.x *= sc; st.ar.y *= sc;
+        st.M = Mb;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float w = (ml[u].x == -INFINITY) ? 0.f : exp2f(ml[u].x - Mb);
+            st.L = fmaf(w, ml[u].y, st.L);
+            st.a0.x = fmaf(w, v0[u].x, st.a0.x); st.a0.y = fmaf(w, v0[u].y, st.a0.y);
+            st.a1.x = fmaf(w, v1[u].x, st.a1.x); st.a1.y = fmaf(w, v1[u].y, st.a1.y);
+            st.ar.x = fmaf(w, vr[u].x, st.ar.x); st.ar.y = fmaf(w, vr[u].y, st.ar.y);
+        }
+    }
+    return st;
+}
+
+// Expansion and store of a merged state: out[b, h] = a / L + (ar / L) B_V[h]^T
+// (bvr: this lane's four B_V rows, loaded beforehand).
+template <class C>
+__device__ __forceinline__ void merge_store(const FastParams &P, int b, int h, const MergeState &st,
+                                            const uint4 (&bvr)[4][C::R / 8], int lane) {
+    const float inv = st.L > 0.f ? 1.f / st.L : 0.f;
+    float o[4] = {st.a0.x * inv, st.a0.y * inv, st.a1.x * inv, st.a1.y * inv};
+#pragma unroll
+    for (int k = 0; k < C::R / 8; ++k) {
+        float r[8];  // (accR / L)[8k .. 8k + 7], from lanes 4k .. 4k + 3
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            r[2 * e] = __shfl_sync(0xffffffffu, st.ar.x, 4 * k + e) * inv;
+            r[2 * e + 1] = __shfl_sync(0xffffffffu, st.ar.y, 4 * k + e) * inv;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t wd = u4w(bvr[i][k], e);
+                o[i] = fmaf(r[2 * e], bf16_lo(wd), o[i]);
+                o[i] = fmaf(r[2 * e + 1], bf16_hi(wd), o[i]);
+            }
+    }
+    __nv_bfloat16 *dst = P.out + ((size_t)b * C::H + h) * C::DH;
+    *reinterpret_cast<uint32_t *>(dst + 2 * lane) = pack_bf16(o[0], o[1]);
+    *reinterpret_cast<uint32_t *>(dst + 64 + 2 * lane) = pack_bf16(o[2], o[3]);
+}
+
+// The grid's last phase.  Once every CTA has written its partial states
+// (the workspace counter reaches the grid size; a bounded wait), CTA g merges the
+// (request, head) pairs g, g + G, ...: in rounds of up to eight pairs, each
+// pair on WP = 8 / (pairs in the round) warps (a power of two).  A request
+// of invalid length has no segment; its zero output was written by the
+// kernel that started the decode.  Offsets: the CTA's full table (batches of
+// at most kLocalReq requests) or the prologue's.  `scratch`: 8 KB of shared
+// memory no longer in use (the first ring stage).
+template <class C>
+__device__ void merge_phase(const FastParams &P, const CtaRange &rg, const int32_t *off, int warp,
+                            int lane, float *scratch) {
+    constexpr int NO = C::R / 8;
+    const int32_t *full_off = P.B <= kLocalReq ? off : P.ws.off;
+    const int npairs = P.B * C::H, G = (int)gridDim.x, g = blockIdx.x;
+    const int mine = npairs > g ? (npairs - g + G - 1) / G : 0;  // pairs of this CTA
+    if (mine == 0) return;
+    for (int r0 = 0; r0 < mine; r0 += C::NCW) {
+        const int nr = min(C::NCW, mine - r0);
+        const int wp = nr > 4 ? 1 : nr > 2 ? 2 : nr > 1 ? 4 : 8;  // warps per pair
+        const int slot = warp / wp, part = warp % wp;
+        const bool active = slot < nr;
+        int b = 0, h = 0, g_lo = 0, nseg = 0;
+        if (active) {
+            const int i = g + (r0 + slot) * G;
+            b = i / C::H;
+            h = i % C::H;
+            const int32_t o0 = full_off[b], o1 = full_off[b + 1];
+            if (o1 > o0) {
+                g_lo = o0 / rg.chunk;
+                nseg = (o1 - 1) / rg.chunk - g_lo + 1;
+            }
+        }
+        // the expanding warp's B_V rows, in flight across the wait
+        uint4 bvr[4][NO];
+        if (active && part == 0 && nseg > 0) {
+            const __nv_bfloat16 *bv = P.B_V + (size_t)h * C::DH * C::R;
+            const int dd[4] = {2 * lane, 2 * lane + 1, 64 + 2 * lane, 65 + 2 * lane};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int k = 0; k < NO; ++k)
+                    bvr[i][k] = __ldg(reinterpret_cast<const uint4 *>(bv + (size_t)dd[i] * C::R + 8 * k));
+        }
+        if (r0 == 0) wait_grid_count(P);  // (flagged on timeout; merges stale states)
+        MergeState st{-INFINITY, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if (active && nseg > 0)
+            st = merge_segments<C>(P, (size_t)(b + g_lo) * C::H + h, part, wp, nseg, lane);
+        if (wp > 1) {
+            // [warp][lane][8]: M, L, a0, a1, ar
+            float *my = scratch + (warp * 32 + lane) * 8;
+            reinterpret_cast<float4 *>(my)[0] = make_float4(st.M, st.L, st.a0.x, st.a0.y);
+            reinterpret_cast<float4 *>(my)[1] = make_float4(st.a1.x, st.a1.y, st.ar.x, st.ar.y);
+            __syncthreads();
+            if (active && part == 0 && nseg > 0) {
+                float M = st.M;
+                for (int k = 1; k < wp; ++k) M = fmaxf(M, scratch[((warp + k) * 32 + lane) * 8]);
+                MergeState t{M, 0.f, make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                if (M != -INFINITY)
+                    for (int k = 0; k < wp; ++k) {
+                        const float *o = scratch + ((warp + k) * 32 + lane) * 8;
+                        const float w = o[0] == -INFINITY ? 0.f : exp2f(o[0] - M);
+                        t.L = fmaf(w, o[1], t.L);
+                        t.a0.x = fmaf(w, o[2], t.a0.x); t.a0.y = fmaf(w, o[3], t.a0.y);
+                        t.a1.x = fmaf(w, o[4], t.a1.x); t.a1.y = fmaf(w, o[5], t.a1.y);
+                        t.ar.x = fmaf(w, o[6], t.ar.x); t.ar.y = fmaf(w, o[7], t.ar.y);
+                    }
+                st = t;
+            }
+            __syncthreads();  // the scratch is reused by the next round
+        }
+        if (active && part == 0 && nseg > 0) merge_store<C>(P, b, h, st, bvr, lane);
     }
 }
 
@@ -1563,6 +1811,9 @@ static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
     P.qb = a.rope_ws.qb;
     P.wsc = a.rope_ws.wsc;
     P.sc_out = a.rope_ws.sc;
+    P.B_K = static_cast<const __nv_bfloat16 *>(a.B_K);
+    P.B_V = static_cast<const __nv_bfloat16 *>(a.B_V);
+    P.out = static_cast<__nv_bfloat16 *>(a.out);
     return P;
 }
 

@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
                 for (int i = tid; i < H * d_h; i += blockDim.x)
                     Elem<T>::store(out + (size_t)(blockIdx.y * nrows + bb) * H * d_h + i, 0.f);
         if (blockIdx.y != 0) return;
+        // the tensor-core split kernel's counters
+        if (tid < kDecodeCounters) ws.cnt[tid] = 0;
         // --- plan: exclusive scan of validated lengths ---
         __shared__ int32_t part[NTHR];
         const int per = (B + blockDim.x - 1) / blockDim.x;

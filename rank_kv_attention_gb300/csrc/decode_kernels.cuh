@@ -72,6 +72,7 @@ cudaError_t launch_combine(const DecodeArgs &a, const DecodeWs &ws, int G);
 // (H, r) pairs).  `fast_decode_supported` says whether a shape is covered;
 // `fast_decode_grid` is its CTA count on this device.
 bool fast_decode_supported(int H, int d_h, int r, int page_size, int dtype, int groups = 1);
+
 int fast_decode_grid(int H, int r);
 cudaError_t launch_split_fast(const DecodeArgs &a, const DecodeWs &ws, int G);
 

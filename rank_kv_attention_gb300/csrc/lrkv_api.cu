@@ -151,7 +151,9 @@ static int run_decode(const DecodeArgs &a, void *workspace, size_t ws_bytes) {
             e = fast ? launch_split_fast(a, ws, G) : launch_split_generic<__nv_bfloat16>(a, ws, G);
             prof_after(LRKV_PROFILE_ATTENTION, a.stream);
         }
-        if (e == cudaSuccess) e = launch_combine<__nv_bfloat16>(a, ws, G);
+        // the tensor-core split kernel merges the requests itself; the generic
+        // one leaves that to the combine kernel
+        if (e == cudaSuccess && !fast) e = launch_combine<__nv_bfloat16>(a, ws, G);
     } else {
         e = launch_prologue<float>(a, ws, G, kPlanTileAlign, false);
         if (e == cudaSuccess) {

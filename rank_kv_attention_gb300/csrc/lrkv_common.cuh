@@ -31,12 +31,17 @@ struct DecodePlan {
 constexpr int kPlanTileAlign = 16;
 
 // Workspace layout of lrkv_decode (all offsets 256-byte aligned):
-//   [plan header + off[B+1]] [p: B*H*r f32] [ml: slots*H*2 f32]
+//   [plan header + off[B+1] + cnt[4]] [p: B*H*r f32] [ml: slots*H*2 f32]
 //   [acc: slots*H*(d_h+r) f32]
+// cnt[0] counts the CTAs of the tensor-core split kernel that have written
+// all their partial states (the merge phase starts when it reaches the grid
+// size); the prologue zeroes it.  cnt[1..3] are spare.
+constexpr int kDecodeCounters = 4;
 
 struct DecodeWs {
     DecodePlan *plan;
     int32_t *off;
+    int32_t *cnt;
     float *p;
     float *ml;
     float *acc;
@@ -56,7 +61,8 @@ __host__ __device__ inline DecodeWs decode_ws_layout(void *base, int B, int H, i
     size_t o = 0;
     w.plan = reinterpret_cast<DecodePlan *>(p + o);
     w.off = reinterpret_cast<int32_t *>(p + o + sizeof(DecodePlan));
-    o += align256(sizeof(DecodePlan) + sizeof(int32_t) * (size_t)(B + 1));
+    w.cnt = w.off + (B + 1);
+    o += align256(sizeof(DecodePlan) + sizeof(int32_t) * (size_t)(B + 1 + kDecodeCounters));
     w.p = reinterpret_cast<float *>(p + o);
     o += align256(sizeof(float) * (size_t)B * H * r);
     size_t slots = (size_t)B + G;
