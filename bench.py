@@ -74,7 +74,7 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode_T4096", choices=sorted(WORKLOADS))
     ap.add_argument("--extra-configs", default=EXTRA_CONFIGS,
-                    help="comma-separated workloads measured beside the headline ('' for none)")
+                    help="comma-separated workloads measured beside the headline ('none' for none)")
     ap.add_argument("--extra-steps", type=int, default=300,
                     help="timed steps of each extra workload")
     ap.add_argument("--roofline-launches", type=int, default=512,
@@ -766,7 +766,7 @@ def run_ours(args, rank, world, local_rank):
            "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic"}
     res.update({k: v for k, v in head.items() if k not in res})
-    extras = [x for x in (args.extra_configs or "").split(",") if x and x != name]
+    extras = [x for x in (args.extra_configs or "").split(",") if x and x not in (name, "none")]
     if extras:
         res["configs"] = {}
         for x in extras:
