@@ -117,6 +117,7 @@ struct FastParams {
     const uint16_t *qb;
     const float *wsc;
     float *sc_out;
+    int step_rows;  // a decode step: the append of the new rows may run beside this kernel's start
     // the merge phase: expansion bases and the output
     const __nv_bfloat16 *B_K;
     const __nv_bfloat16 *B_V;
@@ -207,11 +208,16 @@ __device__ __forceinline__ void issue_scores(uint8_t *st, const FastMaps &M, int
 // ordered before the copy's writes.
 // `pend` (given scores only): the scores do not exist yet; their plan row is
 // kept in pend[stage] and the copy issued after the dependency wait.
+// `pre_wait` (decode step): the append of the step's new rows may still be
+// running, so a tile that holds a request's new row (its last row) is not
+// copied yet; the call returns false and the caller issues it after the wait.
 template <class C>
-__device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
+__device__ bool issue_next(IssueCursor *cur, const FastParams &P, const FastMaps &M,
                            const int32_t *off, uint8_t *smem, uint64_t *full, int *okf,
-                           int32_t end, bool refill = true, int32_t *pend = nullptr) {
-    if (cur->done) return;
+                           int32_t end, bool refill = true, int32_t *pend = nullptr,
+                           bool pre_wait = false) {
+    if (cur->done) return true;
+    if (pre_wait && P.step_rows && cur->t + C::TS >= off[cur->b + 1] - off[cur->b]) return false;
     const int s = cur->issued % C::STAGES;
     const int row = cursor_row(cur, P, okf, s);
     uint8_t *st = smem + s * C::STAGE;
@@ -237,6 +243,7 @@ __device__ void issue_next(IssueCursor *cur, const FastParams &P, const FastMaps
         if (P.norm) tma_load_3d_hint(st + C::OFF_NK, &M.nk, 0, row, 0, &full[s], pol);
     }
     cursor_advance<C>(cur, off, end);
+    return true;
 }
 
 __device__ __forceinline__ uint32_t ld_u32(const __nv_bfloat16 *p) {
@@ -668,12 +675,17 @@ __global__ void __maxnreg__(C::MAXREG)
         cur->page_key = pl[2];
         cur->page_id = pl[3];
         cursor_begin_segment<C>(cur, off, end);
-        // the ring is untouched: no generic-proxy access precedes these copies
+        // the ring is untouched: no generic-proxy access precedes these copies;
+        // in a decode step the tiles that hold the step's new rows wait
         for (int s = 0; s < C::STAGES; ++s)
-            issue_next<C>(cur, P, M, off, smem, full, okf, end, false, C::GS ? pend : nullptr);
+            if (!issue_next<C>(cur, P, M, off, smem, full, okf, end, false, C::GS ? pend : nullptr,
+                               true))
+                break;
     }
     __syncthreads();
     if (local) pdl_wait();  // the private queries (or the scores) come from the previous kernel
+    if (has_rows && P.step_rows && tid == 0)  // the tiles held back above (their rows are written)
+        while (!cur->done && cur->issued < C::STAGES) issue_next<C>(cur, P, M, off, smem, full, okf, end, false);
     if (has_rows && C::GS && tid == 0)  // the first tiles' score copies
         for (int k = 0; k < cur->issued; ++k)
             issue_scores<C>(smem + (k % C::STAGES) * C::STAGE, M, pend[k % C::STAGES],
@@ -1811,6 +1823,7 @@ static FastParams fast_params(const DecodeArgs &a, const DecodeWs &ws) {
     P.qb = a.rope_ws.qb;
     P.wsc = a.rope_ws.wsc;
     P.sc_out = a.rope_ws.sc;
+    P.step_rows = a.early;
     P.B_K = static_cast<const __nv_bfloat16 *>(a.B_K);
     P.B_V = static_cast<const __nv_bfloat16 *>(a.B_V);
     P.out = static_cast<__nv_bfloat16 *>(a.out);

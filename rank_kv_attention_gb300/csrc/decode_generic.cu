@@ -113,7 +113,12 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
     DecodeWs ws, int32_t *status, const float2 *__restrict__ rope_tab, RopeFastWs rf, bool early) {
     constexpr int nrows = (ROPE || NTHR == 128) ? 1 : kProRows;
     const int tid = threadIdx.x;
-    const PdlTail tail{early};  // early mode: the dependency wait runs as the block exits
+    // early mode: the split kernel may launch at once (its own early work
+    // reads none of this kernel's or the append's results, and it waits for
+    // this grid before using them), and this block waits for the append as
+    // it exits
+    if (early) pdl_launch_dependents();
+    const PdlWaitOnExit tail{early};
     if (!early && blockIdx.x < (unsigned)H) {
         // warm L2 with this block's B_K[h] and query rows while the
         // predecessor finishes: a prefetch reads nothing into the block, and
@@ -200,6 +205,49 @@ __global__ void __launch_bounds__(NTHR, NTHR == 128 ? 10 : 1) decode_prologue_ke
     // --- private queries of up to nrows requests for head h ---
     const int h = blockIdx.x, b0 = blockIdx.y * nrows;
     const int nb = min(nrows, B - b0);
+    if constexpr (!ROPE && NTHR == 128 && sizeof(T) == 2) {
+        if (d_h == 128 && (r & 7) == 0 && r <= 64) {
+            // p = q B_K[h] of one request with every load in flight: warp w
+            // sums channels 32 w .. 32 w + 31, lane o + 8 s (octet o < r/8 of
+            // columns, slice s < 4 of eight channels) loads its eight 16-byte
+            // B_K row slices and eight query values at once; xor-shuffles add
+            // the slices and shared memory the warps, in a fixed order
+            __shared__ float part[4][64];
+            const int w = tid >> 5, lane = tid & 31, o = lane & 7, sl = lane >> 3;
+            const int d0 = 32 * w + 8 * sl;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (8 * o < r) {
+                const uint4 qv = *reinterpret_cast<const uint4 *>(q + ((size_t)b0 * H + h) * 128 + d0);
+                uint4 bv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    bv[e] = *reinterpret_cast<const uint4 *>(B_K + ((size_t)h * 128 + d0 + e) * r + 8 * o);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t qw = (e >> 1) == 0 ? qv.x : (e >> 1) == 1 ? qv.y : (e >> 1) == 2 ? qv.z : qv.w;
+                    const float qf = __uint_as_float((e & 1) ? (qw & 0xffff0000u) : (qw << 16));
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t bw = c == 0 ? bv[e].x : c == 1 ? bv[e].y : c == 2 ? bv[e].z : bv[e].w;
+                        acc[2 * c] = fmaf(qf, __uint_as_float(bw << 16), acc[2 * c]);
+                        acc[2 * c + 1] = fmaf(qf, __uint_as_float(bw & 0xffff0000u), acc[2 * c + 1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 8);
+                acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
+            }
+            if (sl == 0 && 8 * o < r)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) part[w][8 * o + c] = acc[c];
+            __syncthreads();
+            if (tid < r)
+                ws.p[((size_t)b0 * H + h) * r + tid] = (part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid]);
+            return;
+        }
+    }
     extern __shared__ float sm[];
     float *bk = sm;                               // [d_h][r] when staged
     float *qs = bk + (staged ? d_h * r : 0);      // [nrows][d_h]

@@ -31,8 +31,11 @@ struct DecodeArgs {
     // The prologue's predecessor in the stream is the same call's append
     // (lrkv_decode_step), which writes none of q, B_K, seq_lens, out or the
     // workspace, and which let it launch only after passing its own wait: the
-    // prologue then does all its work first and waits for the append at its
-    // end, so the private queries overlap the append.
+    // prologue then lets the split kernel launch at once, does all its work
+    // and waits for the append at its end, so the private queries and the
+    // split kernel's first copies overlap the append.  The split kernel holds
+    // back the copies of tiles that hold a new row until its own wait (which
+    // the prologue's completion, and so the append's, releases).
     bool early = false;
 };
 

@@ -427,16 +427,14 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Scope guard of a kernel that works before its dependency wait: when on,
-// the wait (and the launch of dependents) runs as the thread leaves the
-// scope, on every return path.
-struct PdlTail {
+// Scope guard of a kernel that works before its dependency wait and has
+// already let its dependents launch: when on, the wait runs as the thread
+// leaves the scope, on every return path (the grid then completes only after
+// its predecessor has).
+struct PdlWaitOnExit {
     bool on;
-    __device__ ~PdlTail() {
-        if (on) {
-            pdl_wait();
-            pdl_launch_dependents();
-        }
+    __device__ ~PdlWaitOnExit() {
+        if (on) pdl_wait();
     }
 };
 
