@@ -85,8 +85,9 @@ struct FastCfg {
     static constexpr int SMEM = OFF_PEND + 64 + 1024;  // + alignment slack
     // registers per thread: at most 224 leaves room for a 128-thread prologue
     // block of up to 48 registers on the same SM, so the split CTAs do not
-    // wait for the prologue to leave; the widest private rows need more
-    static constexpr int MAXREG = H * R >= 1024 ? 255 : 224;
+    // wait for the prologue to leave; the widest private rows and the 8-bit
+    // tiles (whose code conversions want the registers) take all 255
+    static constexpr int MAXREG = (H * R >= 1024 || Q8) ? 255 : 224;
 
     static_assert(H == 16 || H == 32, "two or four heads per warp");
     static_assert(R % 8 == 0 && (H * R * EB) % 128 == 0, "private rows tile into 128-byte boxes");
