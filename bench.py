@@ -234,6 +234,94 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "sampled_after_region": after}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons of this process's GPU, read through the
+    driver's NVML library (ctypes; read-only queries) by a host thread every
+    ~0.2 ms.  The thread starts before the timed region; begin() and end()
+    mark the region on the host clock and only the samples between the marks
+    count, so that even a region of a few steps gets samples under load.
+    ``available`` is False where NVML cannot be loaded; the caller then uses
+    ClockSampler."""
+    # clock-event reason bits (NVML's documented values)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        import ctypes
+        import threading
+        import torch
+        self.ct, self.threading = ctypes, threading
+        self.available = False
+        self.samples, self.max_mhz = [], None  # (host time, MHz, reason bits)
+        self.t0 = self.t1 = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(cuda_index)
+            bus = None
+            if hasattr(props, "pci_bus_id"):
+                bus = (f"{getattr(props, 'pci_domain_id', 0):08x}:{props.pci_bus_id:02x}:"
+                       f"{getattr(props, 'pci_device_id', 0):02x}.0").encode()
+            if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+                    return
+            self.lib, self.h = lib, h
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1: SM clock
+                self.max_mhz = float(mx.value)
+            self.available = True
+        except Exception:
+            self.available = False
+
+    def _run(self):
+        ct = self.ct
+        mhz, bits = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag.is_set():
+            t = time.perf_counter()
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0:
+                b = 0
+                if self.reasons_fn is not None and self.reasons_fn(self.h, ct.byref(bits)) == 0:
+                    b = bits.value
+                self.samples.append((t, float(mhz.value), b))
+            time.sleep(0.0002)
+
+    def start(self):
+        self.stop_flag = self.threading.Event()
+        self.thread = self.threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        time.sleep(0.01)  # the thread is polling before the region begins
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = self.t1 if self.t1 is not None else math.inf
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        bits = 0
+        for x in inside:
+            bits |= x[2]
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        return {"sm_mhz": statistics.median(x[1] for x in inside) if inside else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "sampled_after_region": False, "source": "nvml, in-process, ~0.2 ms period"}
+
+
+def clock_sampler(cuda_index):
+    """The in-process NVML sampler where NVML loads, else nvidia-smi."""
+    s = NvmlClockSampler(cuda_index)
+    return s if s.available else ClockSampler(cuda_index)
+
+
 # ----------------------------------------------------------------------------
 # committed ncu summaries
 # ----------------------------------------------------------------------------
@@ -427,19 +515,26 @@ def decode_leg(lib, name, dev, world, local_rank, K, W, R, Ke, headline):
         step(i)
     torch.cuda.synchronize()
     barrier()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    time.sleep(0.25)
+    clocks = clock_sampler(local_rank)
+    if isinstance(clocks, ClockSampler):  # nvidia-smi needs a moment to start sampling
+        clocks.start()
+        time.sleep(0.25)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nvml = not isinstance(clocks, ClockSampler)
+    if nvml:
+        clocks.start()
+        clocks.begin()
     e0.record(stream)
     for i in range(K):
         step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier()
+    if nvml:
+        clocks.end()
     clk = clocks.stop()
+    barrier()
     total_ms = ranks_max(e0.elapsed_time(e1))
 
     # ---- live breakdown: the calls of a step on their own
@@ -659,19 +754,26 @@ def prefill_leg(lib, name, dev, world, local_rank, K, W, R, Ke):
         step()
     torch.cuda.synchronize()
     rank_barrier(world)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    time.sleep(0.25)
+    clocks = clock_sampler(local_rank)
+    if isinstance(clocks, ClockSampler):  # nvidia-smi needs a moment to start sampling
+        clocks.start()
+        time.sleep(0.25)
     torch.cuda.synchronize()
     rank_barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nvml = not isinstance(clocks, ClockSampler)
+    if nvml:
+        clocks.start()
+        clocks.begin()
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    rank_barrier(world)
+    if nvml:
+        clocks.end()
     clk = clocks.stop()
+    rank_barrier(world)
     total_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     prof = profile_pass(lib, step, R)
     attn_ms, n_attn = prof[0]

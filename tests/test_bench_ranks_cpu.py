@@ -88,3 +88,47 @@ def test_profile_summary_sections(tmp_path):
     assert head == {"kernel_source_sha256_16": "abc"}
     assert sec["prefill_tc_kernel"]["dram_bytes_per_full_launch"] == "201862400"
     assert sec["append_tc_kernel"]["dram_bytes_per_full_launch"] == "92373504"
+
+
+def test_nvml_clock_sampler_reads_and_decodes():
+    """The in-process clock sampler: without NVML (this host) the bench falls
+    back to nvidia-smi; with a fake NVML it polls the SM clock and decodes the
+    clock-event reason bits (read-only queries)."""
+    import ctypes
+    import bench
+    s = bench.clock_sampler(0)
+    if not torch.cuda.is_available():
+        assert isinstance(s, bench.ClockSampler)
+
+    class FakeNvml:
+        def __init__(self):
+            self.n = 0
+
+        def nvmlDeviceGetClockInfo(self, h, kind, out):
+            assert kind == 1  # SM clock
+            self.n += 1
+            ctypes.cast(out, ctypes.POINTER(ctypes.c_uint))[0] = 1900 if self.n % 2 else 2000
+            return 0
+
+    fake = FakeNvml()
+    smp = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    import threading
+    smp.ct, smp.threading = ctypes, threading
+    smp.samples, smp.max_mhz, smp.t0, smp.t1 = [], 2070.0, None, None
+    smp.lib, smp.h = fake, None
+
+    def reasons(h, out):
+        ctypes.cast(out, ctypes.POINTER(ctypes.c_ulonglong))[0] = 0x4 | 0x40  # power cap, hw thermal
+        return 0
+    smp.reasons_fn = reasons
+    smp.start()
+    import time
+    smp.begin()
+    time.sleep(0.02)
+    smp.end()
+    time.sleep(0.01)  # samples after the region do not count
+    r = smp.stop()
+    assert r["samples"] >= 5 and r["samples"] < len(smp.samples)
+    assert 1900.0 <= r["sm_mhz"] <= 2000.0 and r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert r["sampled_after_region"] is False
