@@ -66,7 +66,10 @@ constexpr float kPfLazyMax = 8.f;                    // log2 units
 
 struct PfBars {
     uint64_t q_full, pre_done, qa_ready, bv_full, ex_ready, ex_done, fin;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    // a key (value) stage is free once the scores (values) of its tile are
+    // complete: s_full[k] (pv_done[k]) of the tile's parity, so the
+    // producers wait on those (stage k and buffer k share the index)
+    uint64_t k_full[2], v_full[2];
     uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t pair[4];  // per lane quadrant: both softmax warps posted their half (64 arrivals)
     uint64_t out_ready;  // all 256 softmax threads staged their output row halves
@@ -150,9 +153,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         mbar_init(&bar.fin, 1);
         for (int k = 0; k < 2; ++k) {
             mbar_init(&bar.k_full[k], 1);
-            mbar_init(&bar.k_empty[k], 1);
             mbar_init(&bar.v_full[k], 1);
-            mbar_init(&bar.v_empty[k], 1);
             mbar_init(&bar.s_full[k], 1);
             mbar_init(&bar.pv_done[k], 1);
             mbar_init(&bar.p_full[k], 2 * PF_BM);  // ... and arrivals of the 256 softmax threads
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const CUtensorMap *m_s = kprod ? &maps.sk : &maps.sv;
             const CUtensorMap *m_r = kprod ? &maps.rk : &maps.rv;
             uint64_t *full = kprod ? bar.k_full : bar.v_full;
-            uint64_t *empty = kprod ? bar.k_empty : bar.v_empty;
+            uint64_t *empty = kprod ? bar.s_full : bar.pv_done;
             uint8_t *ring = smem + (kprod ? PF_OFF_K : PF_OFF_V);
             int n_iss = 0;
             int ya = slice_row(0, 0), yb = slice_row(0, 1);
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bool bv_issued = false;
             if (kprod && ok) {
                 const int st = nkt & 1;
-                if (nkt >= 2 && !mbar_wait(&bar.k_empty[st], ((nkt >> 1) - 1) & 1)) {
+                if (nkt >= 2 && !mbar_wait(&bar.s_full[st], ((nkt >> 1) - 1) & 1)) {
                     ok = false;
                 } else {
                     uint8_t *kb = smem + PF_OFF_K + st * PF_STAGE;
@@ -323,7 +324,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 tc_fence_after();
                 scores(0);
                 tc_commit(&bar.s_full[0]);
-                tc_commit(&bar.k_empty[0]);
             }
             for (int kt = 0; kt < nkt && ok; ++kt) {
                 const int st = kt & 1;
@@ -336,7 +336,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     tc_fence_after();
                     scores(kt + 1);
                     tc_commit(&bar.s_full[s1]);
-                    tc_commit(&bar.k_empty[s1]);
                 }
                 if (!mbar_wait(&bar.p_full[st], (kt >> 1) & 1) ||
                     !mbar_wait(&bar.v_full[st], (kt >> 1) & 1)) {
@@ -350,7 +349,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 for (int kk = 0; kk < 8; ++kk)  // 16 keys (8 packed columns) per instruction
                     tc_mma_ts_lo(tmem, pa + 8 * kk, vb + 128 * kk, id_pv, (kt | kk) != 0);
                 tc_commit(&bar.pv_done[st]);
-                tc_commit(&bar.v_empty[st]);
             }
             // E = (O_R / l)_hi B_V[h]^T + (O_R / l)_lo B_V[h]^T into score buffer 0
             if (ok) ok = mbar_wait(&bar.ex_ready, 0) && mbar_wait(&bar.bv_full, 0);
