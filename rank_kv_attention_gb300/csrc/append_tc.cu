@@ -5,13 +5,19 @@
 // each row's four blocks are stored at its token position (page table,
 // same page id in all four pools).  The projection is a dense
 // [n x d] . [d x (2 d_h + 2 H r)] GEMM, run here with tcgen05 by a persistent
-// grid (one CTA per SM walking the output tiles):
+// grid (one CTA per SM walking the output tiles) of CTA pairs (clusters of 2):
 //   * output tiles are 128 rows x 256 columns: two 128-column blocks of the
 //     concatenated output, each block inside one of the four segments (its
 //     own weight tensor map and column offset);
-//   * warp 0 (one thread) streams 128 x 64 K-major tiles of X and the two
-//     128 x 64 weight boxes by TMA (128-byte swizzle) through a 4-stage ring
-//     that runs on across tiles;
+//   * the two CTAs of a cluster take vertically adjacent row tiles of the
+//     same column tile, so they share its weight boxes: CTA rank c copies
+//     weight block c once, multicast into the same stage of both CTAs, which
+//     halves the weight copies each SM issues (the stage stream, not the
+//     tensor core, bounds a CTA that copies all 48 KB of a stage itself);
+//   * warp 0 (one thread) streams 128 x 64 K-major tiles of X and its weight
+//     box by TMA (128-byte swizzle) through a 4-stage ring that runs on
+//     across tiles; a stage is refilled once the products of both CTAs have
+//     read it (each MMA issuer releases it in both CTAs);
 //   * warp 1 (one thread) issues tcgen05.mma (kind::f16, M = 128, N = 256,
 //     bf16 in, fp32 accumulate) into one of two 256-column accumulators in
 //     tensor memory, so a tile's epilogue overlaps the next tile's products;
@@ -46,20 +52,23 @@ struct TcMaps {
 // column col[k]; tile j pairs blocks 2j and 2j + 1 (the last may be alone).
 constexpr int TC_MAX_BLOCKS = 32;
 struct TcBlocks {
-    int nblocks, ncoltiles, nrowtiles, ntiles;
+    int nblocks, ncoltiles, nrowtiles, npairs;  // npairs: (row-tile pair, column tile) items
     int seg[TC_MAX_BLOCKS];
     int col[TC_MAX_BLOCKS];
     int width[4];
 };
 
-__device__ __forceinline__ void tc_tile_of(const TcBlocks &t, int tile, int &m0, int &b0, int &nb) {
-    const int rt = tile / t.ncoltiles, ct = tile % t.ncoltiles;
-    m0 = rt * TC_BM;
+// Item `pt` of a cluster: row tile 2 (pt / ncoltiles) + rank (possibly past
+// the last row: its rows read as zeros and are not stored), column tile
+// pt % ncoltiles.
+__device__ __forceinline__ void tc_tile_of(const TcBlocks &t, int pt, int rank, int &m0, int &b0, int &nb) {
+    const int rp = pt / t.ncoltiles, ct = pt % t.ncoltiles;
+    m0 = (2 * rp + rank) * TC_BM;
     b0 = 2 * ct;
     nb = min(2, t.nblocks - b0);
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     append_tc_kernel(const __grid_constant__ TcMaps maps, const AppendArgsT<__nv_bfloat16> a,
                      const __grid_constant__ TcBlocks tb) {
     extern __shared__ uint8_t tc_smem_raw[];
@@ -75,11 +84,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nk = a.d / TC_BK;
+    const int rank = (int)cluster_ctarank();
+    const int pt0 = blockIdx.x >> 1, pstep = gridDim.x >> 1;  // this cluster's items
 
     if (tid == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);  // the MMA issuers of both CTAs
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&acc_full[k], 1);
@@ -90,8 +101,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int k = 0; k < 4; ++k) prefetch_tensormap(&maps.w[k]);
     }
     if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
+    // both CTAs' barriers are initialised before either copies into the other
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool ok = true;
@@ -100,9 +112,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0 && lane == 0) {
         // ---- producer
         int it = 0;
-        for (int tile = blockIdx.x; tile < tb.ntiles && ok; tile += gridDim.x) {
+        for (int pt = pt0; pt < tb.npairs && ok; pt += pstep) {
             int m0, b0, nb;
-            tc_tile_of(tb, tile, m0, b0, nb);
+            tc_tile_of(tb, pt, rank, m0, b0, nb);
             for (int kt = 0; kt < nk; ++kt, ++it) {
                 const int s = it % TC_STAGES;
                 if (it >= TC_STAGES && !mbar_wait(&empty[s], ((it / TC_STAGES) - 1) & 1)) {
@@ -112,9 +124,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 uint8_t *st = smem + s * TC_STAGE;
                 mbar_arrive_expect_tx(&full[s], TC_A_BYTES + nb * TC_B_BYTES);
                 tma_load_2d(st, &maps.x, kt * TC_BK, m0, &full[s]);
-                for (int k = 0; k < nb; ++k)
-                    tma_load_2d(st + TC_A_BYTES + k * TC_B_BYTES, &maps.w[tb.seg[b0 + k]], kt * TC_BK,
-                                tb.col[b0 + k], &full[s]);
+                if (rank < nb)  // weight block `rank` of the tile, into both CTAs
+                    tma_load_2d_multicast(st + TC_A_BYTES + rank * TC_B_BYTES, &maps.w[tb.seg[b0 + rank]],
+                                          kt * TC_BK, tb.col[b0 + rank], &full[s], 0x3);
                 issued = it + 1;
             }
         }
@@ -122,9 +134,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- MMA issuer
         const uint32_t idesc2 = tc_idesc_bf16(TC_BM, 2 * TC_BN), idesc1 = tc_idesc_bf16(TC_BM, TC_BN);
         int it = 0, i = 0;
-        for (int tile = blockIdx.x; tile < tb.ntiles && ok; tile += gridDim.x, ++i) {
+        for (int pt = pt0; pt < tb.npairs && ok; pt += pstep, ++i) {
             int m0, b0, nb;
-            tc_tile_of(tb, tile, m0, b0, nb);
+            tc_tile_of(tb, pt, rank, m0, b0, nb);
             const int acc = i & 1;
             // the epilogue has drained this accumulator's previous tile
             if (i >= 2 && !mbar_wait(&acc_empty[acc], ((i >> 1) - 1) & 1)) {
@@ -146,7 +158,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int kk = 0; kk < TC_BK / 16; ++kk)  // K = 16 per instruction: +32 bytes
                     tc_mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
                                nb == 2 ? idesc2 : idesc1, (kt | kk) != 0);
-                tc_commit(&empty[s]);  // stage free once these products have read it
+                tc_commit_multicast(&empty[s], 0x3);  // these products have read the stage
             }
             if (!ok) break;
             tc_commit(&acc_full[acc]);  // accumulator complete
@@ -155,9 +167,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---- epilogue: thread = tile row = tensor-memory lane of its quadrant
         const int q = warp & 3, row = 32 * q + lane;
         int i = 0;
-        for (int tile = blockIdx.x; tile < tb.ntiles; tile += gridDim.x, ++i) {
+        for (int pt = pt0; pt < tb.npairs; pt += pstep, ++i) {
             int m0, b0, nb;
-            tc_tile_of(tb, tile, m0, b0, nb);
+            tc_tile_of(tb, pt, rank, m0, b0, nb);
             // destination pool row while the products run
             int64_t dr = -1;
             {
@@ -250,8 +262,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0 && lane == 0 && !ok)
         for (int k = max(0, issued - TC_STAGES); k < issued; ++k)
             mbar_wait(&full[k % TC_STAGES], (k / TC_STAGES) & 1);
+    // neither CTA leaves while the other may still copy into it or release
+    // its stages
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TC_TMEM_COLS);
@@ -291,7 +305,7 @@ static bool tc_blocks(const AppendArgsT<__nv_bfloat16> &a, TcBlocks &t) {
     }
     t.ncoltiles = (t.nblocks + 1) / 2;
     t.nrowtiles = (a.n + TC_BM - 1) / TC_BM;
-    t.ntiles = t.ncoltiles * t.nrowtiles;
+    t.npairs = t.ncoltiles * ((t.nrowtiles + 1) / 2);
     return true;
 }
 
@@ -313,7 +327,7 @@ cudaError_t launch_append_tc(const AppendArgsT<__nv_bfloat16> &a) {
     if (!tc_blocks(a, t)) return cudaErrorInvalidValue;
     cudaError_t e = smem_limit_once(append_tc_kernel, TC_SMEM);
     if (e != cudaSuccess) return e;
-    const int grid = std::min(t.ntiles, device_sm_count());
+    const int grid = 2 * std::min(t.npairs, device_sm_count() / 2);
     return launch_pdl(append_tc_kernel, dim3(grid), dim3(TC_THREADS), TC_SMEM, a.stream, maps, a, t);
 }
 

@@ -172,6 +172,37 @@ __host__ __device__ constexpr uint32_t tc_idesc_bf16_bmn(int M, int N) {
 }
 
 // ---------------------------------------------------------------------------
+// Clusters: rank, cluster-wide barrier, multicast copies and commits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// all threads of every CTA of the cluster (release / acquire at cluster scope)
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// 2-D tiled TMA load delivered to the same shared-memory offset of every CTA
+// in `mask`, each completing `bytes` on its own mbarrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map, int x, int y,
+                                                      uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// tc_commit arriving on the mbarrier at `bar`'s offset in every CTA of `mask`
+__device__ __forceinline__ void tc_commit_multicast(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Host side: tensor maps through the driver entry point (no -lcuda needed)
 // ---------------------------------------------------------------------------
 typedef CUresult (*TcEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
