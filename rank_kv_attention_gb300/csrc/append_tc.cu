@@ -5,22 +5,24 @@
 // each row's four blocks are stored at its token position (page table,
 // same page id in all four pools).  The projection is a dense
 // [n x d] . [d x (2 d_h + 2 H r)] GEMM, run here with tcgen05 by a persistent
-// grid (one CTA per SM walking the output tiles) of CTA pairs (clusters of 2):
-//   * output tiles are 128 rows x 256 columns: two 128-column blocks of the
+// grid (one CTA per SM walking the output tiles) of CTA pairs (clusters of 2,
+// tcgen05 cta_group::2):
+//   * output tiles are 256 rows x 256 columns: two 128-column blocks of the
 //     concatenated output, each block inside one of the four segments (its
-//     own weight tensor map and column offset);
-//   * the two CTAs of a cluster take vertically adjacent row tiles of the
-//     same column tile, so they share its weight boxes: CTA rank c copies
-//     weight block c once, multicast into the same stage of both CTAs, which
-//     halves the weight copies each SM issues (the stage stream, not the
-//     tensor core, bounds a CTA that copies all 48 KB of a stage itself);
-//   * warp 0 (one thread) streams 128 x 64 K-major tiles of X and its weight
-//     box by TMA (128-byte swizzle) through a 4-stage ring that runs on
-//     across tiles; a stage is refilled once the products of both CTAs have
-//     read it (each MMA issuer releases it in both CTAs);
-//   * warp 1 (one thread) issues tcgen05.mma (kind::f16, M = 128, N = 256,
-//     bf16 in, fp32 accumulate) into one of two 256-column accumulators in
-//     tensor memory, so a tile's epilogue overlaps the next tile's products;
+//     own weight tensor map and column offset); CTA rank c owns rows
+//     [128 c, 128 c + 128) of the tile and holds weight block c (for a tile
+//     of one block, its rows [64 c, 64 c + 64)), so each SM receives 32 KB
+//     per K step instead of 48 (the stage stream into shared memory, not the
+//     tensor core, bounds a CTA that receives all of a 128 x 256 step);
+//   * warp 0 (one thread) of each CTA streams its 128 x 64 K-major tile of X
+//     and its weight box by TMA (128-byte swizzle) through a 6-stage ring
+//     that runs on across tiles; both CTAs' copies complete on the stage
+//     barrier of rank 0;
+//   * warp 1 (one thread) of rank 0 issues tcgen05.mma (kind::f16, M = 256,
+//     N = 256, bf16 in, fp32 accumulate) into one of two 256-column
+//     accumulators in both CTAs' tensor memory, so a tile's epilogue overlaps
+//     the next tile's products; stage and accumulator completions are
+//     signalled in both CTAs;
 //   * warps 2-5 read an accumulator back (tcgen05.ld, one row per thread),
 //     round to bf16 (or 8-bit codes) and store each row's columns straight
 //     into its page slot; the destination rows of a tile are looked up while
@@ -33,10 +35,10 @@
 
 namespace lrkv {
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 4;
-constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB
-constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 16 KB per 128-column block
-constexpr int TC_STAGE = TC_A_BYTES + 2 * TC_B_BYTES;
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64, TC_STAGES = 6;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;  // 16 KB: this CTA's 128 rows of X
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;  // 16 KB: this CTA's 128-row weight box
+constexpr int TC_STAGE = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_OFF_BAR = TC_STAGES * TC_STAGE;  // full[S], empty[S], acc_full[2], acc_empty[2]
 constexpr int TC_OFF_TMEM = TC_OFF_BAR + 8 * (2 * TC_STAGES + 4);
 constexpr int TC_SMEM = TC_OFF_TMEM + 16 + 1024;  // + alignment slack
@@ -88,19 +90,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     const int pt0 = blockIdx.x >> 1, pstep = gridDim.x >> 1;  // this cluster's items
 
     if (tid == 0) {
+        // (full and acc_empty are used in rank 0 only)
         for (int s = 0; s < TC_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // the MMA issuers of both CTAs
+            mbar_init(&full[s], 1);   // rank 0's producer, plus both CTAs' bytes
+            mbar_init(&empty[s], 1);  // the pair's MMAs have read the stage
         }
         for (int k = 0; k < 2; ++k) {
             mbar_init(&acc_full[k], 1);
-            mbar_init(&acc_empty[k], 4);  // one arrival per epilogue warp
+            mbar_init(&acc_empty[k], 8);  // one arrival per epilogue warp of both CTAs
         }
         fence_barrier_init();
         prefetch_tensormap(&maps.x);
         for (int k = 0; k < 4; ++k) prefetch_tensormap(&maps.w[k]);
     }
-    if (warp == 1) tmem_alloc(tmem_slot, TC_TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(tmem_slot, TC_TMEM_COLS);
     // both CTAs' barriers are initialised before either copies into the other
     tc_fence_before();
     cluster_sync_all();
@@ -111,10 +114,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ---- producer
+        const uint32_t full0 = mapa_rank(&full[0], 0);
         int it = 0;
         for (int pt = pt0; pt < tb.npairs && ok; pt += pstep) {
             int m0, b0, nb;
             tc_tile_of(tb, pt, rank, m0, b0, nb);
+            // this CTA's half of B: block b0 + rank, or for a one-block tile
+            // that block's rows from 64 rank (the MMA reads 64 rows per CTA)
+            const int bb = nb == 2 ? b0 + rank : b0;
+            const int brow = tb.col[bb] + (nb == 2 ? 0 : 64 * rank);
+            const CUtensorMap *wm = &maps.w[tb.seg[bb]];
             for (int kt = 0; kt < nk; ++kt, ++it) {
                 const int s = it % TC_STAGES;
                 if (it >= TC_STAGES && !mbar_wait(&empty[s], ((it / TC_STAGES) - 1) & 1)) {
@@ -122,17 +131,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                     break;
                 }
                 uint8_t *st = smem + s * TC_STAGE;
-                mbar_arrive_expect_tx(&full[s], TC_A_BYTES + nb * TC_B_BYTES);
-                tma_load_2d(st, &maps.x, kt * TC_BK, m0, &full[s]);
-                if (rank < nb)  // weight block `rank` of the tile, into both CTAs
-                    tma_load_2d_multicast(st + TC_A_BYTES + rank * TC_B_BYTES, &maps.w[tb.seg[b0 + rank]],
-                                          kt * TC_BK, tb.col[b0 + rank], &full[s], 0x3);
+                const uint32_t fb = full0 + 8u * s;  // rank 0's stage barrier
+                if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * TC_STAGE);
+                tma_load_2d_pair(st, &maps.x, kt * TC_BK, m0, fb);
+                tma_load_2d_pair(st + TC_A_BYTES, wm, kt * TC_BK, brow, fb);
                 issued = it + 1;
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        const uint32_t idesc2 = tc_idesc_bf16(TC_BM, 2 * TC_BN), idesc1 = tc_idesc_bf16(TC_BM, TC_BN);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---- MMA issuer (the pair's rows, M = 256)
+        const uint32_t idesc2 = tc_idesc_bf16(2 * TC_BM, 2 * TC_BN), idesc1 = tc_idesc_bf16(2 * TC_BM, TC_BN);
         int it = 0, i = 0;
         for (int pt = pt0; pt < tb.npairs && ok; pt += pstep, ++i) {
             int m0, b0, nb;
@@ -156,12 +164,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
                 const uint64_t ad = sw128_kmajor_desc(sa), bd = sw128_kmajor_desc(sa + TC_A_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < TC_BK / 16; ++kk)  // K = 16 per instruction: +32 bytes
-                    tc_mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
-                               nb == 2 ? idesc2 : idesc1, (kt | kk) != 0);
-                tc_commit_multicast(&empty[s], 0x3);  // these products have read the stage
+                    tc2_mma_f16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2),
+                                nb == 2 ? idesc2 : idesc1, (kt | kk) != 0);
+                tc2_commit_both(&empty[s]);  // these products have read the stage
             }
             if (!ok) break;
-            tc_commit(&acc_full[acc]);  // accumulator complete
+            tc2_commit_both(&acc_full[acc]);  // accumulator complete
         }
     } else if (warp >= 2) {
         // ---- epilogue: thread = tile row = tensor-memory lane of its quadrant
@@ -253,13 +261,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
             // this warp has read its lanes of the accumulator
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (lane == 0) mbar_arrive_remote(mapa_rank(&acc_empty[acc], 0));
         }
     }
     if (!ok) status_or(a.status, LRKV_STATUS_TIMEOUT);
     // Never leave with copies in flight into this CTA's shared memory (only
     // possible after a timeout: normally the MMA issuer consumed every stage).
-    if (warp == 0 && lane == 0 && !ok)
+    // (rank 0's stage barriers count the copies of both CTAs)
+    if (warp == 0 && lane == 0 && !ok && rank == 0)
         for (int k = max(0, issued - TC_STAGES); k < issued; ++k)
             mbar_wait(&full[k % TC_STAGES], (k / TC_STAGES) & 1);
     // neither CTA leaves while the other may still copy into it or release
@@ -268,7 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(TC_THREADS, 1)
     cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, TC_TMEM_COLS);
+        tmem_dealloc_pair(tmem, TC_TMEM_COLS);
     }
 }
 
