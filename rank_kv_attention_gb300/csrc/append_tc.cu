@@ -42,6 +42,7 @@ constexpr int TC_STAGE = TC_A_BYTES + TC_B_BYTES;
 constexpr int TC_OFF_BAR = TC_STAGES * TC_STAGE;  // full[S], empty[S], acc_full[2], acc_empty[2]
 constexpr int TC_OFF_TMEM = TC_OFF_BAR + 8 * (2 * TC_STAGES + 4);
 constexpr int TC_SMEM = TC_OFF_TMEM + 16 + 1024;  // + alignment slack
+static_assert(TC_SMEM <= 232448, "shared memory budget");
 constexpr int TC_TMEM_COLS = 512;                 // two 256-column accumulators
 constexpr int TC_THREADS = 192;                   // producer, MMA, 4 epilogue warps
 
