@@ -326,7 +326,8 @@ def clock_sampler(cuda_index):
 # committed ncu summaries
 # ----------------------------------------------------------------------------
 DECODE_SPLIT_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh")
-PREFILL_SOURCES = ("prefill_tc.cu", "tc_common.cuh", "append_kernels.cuh", "lrkv_common.cuh")
+PREFILL_SOURCES = ("prefill_tc.cu", "append_tc.cu", "tc_common.cuh", "tc_pair.cuh", "append_kernels.cuh",
+                   "lrkv_common.cuh")
 ROPE_SCORE_SOURCES = ("decode_fast.cu", "decode_kernels.cuh", "lrkv_common.cuh", "tc_common.cuh")
 
 

@@ -31,7 +31,7 @@
 #include <algorithm>
 
 #include "append_kernels.cuh"
-#include "tc_common.cuh"
+#include "tc_pair.cuh"
 
 namespace lrkv {
 

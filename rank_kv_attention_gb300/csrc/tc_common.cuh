@@ -172,76 +172,6 @@ __host__ __device__ constexpr uint32_t tc_idesc_bf16_bmn(int M, int N) {
 }
 
 // ---------------------------------------------------------------------------
-// Clusters: rank, cluster-wide barrier, addresses and arrivals in another CTA
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// all threads of every CTA of the cluster (release / acquire at cluster scope)
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// shared::cluster address of the variable at `p` in the CTA of rank `rank`
-__device__ __forceinline__ uint32_t mapa_rank(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-// arrive on an mbarrier of another CTA of the cluster (shared::cluster address)
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cl_addr) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// CTA pairs (tcgen05 cta_group::2): one warp of each CTA of the pair
-// allocates together; the CTA of even rank issues each MMA for both, M = 256
-// rows (rows 0..127 from its own shared and tensor memory, 128..255 from its
-// peer's) with the N columns of B split in halves (the first from its own
-// shared memory, the second from the peer's, same offsets).  Every tcgen05
-// instruction of such a kernel uses cta_group::2.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc2_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.u32 p, %4, 0; "
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// arrive on the mbarrier at `bar`'s offset in both CTAs of the pair once all
-// pair MMAs issued so far by this thread are complete
-__device__ __forceinline__ void tc2_commit_both(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-        "[%0], %1;" ::"r"(smem_u32(bar)),
-        "h"((uint16_t)3)
-        : "memory");
-}
-// 2-D tiled TMA load into this CTA's shared memory whose completion is
-// counted on an mbarrier of either CTA of the pair (shared::cluster address)
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int x, int y,
-                                                 uint32_t cl_bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cl_bar)
-        : "memory");
-}
-
-// ---------------------------------------------------------------------------
 // Host side: tensor maps through the driver entry point (no -lcuda needed)
 // ---------------------------------------------------------------------------
 typedef CUresult (*TcEncodeFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
